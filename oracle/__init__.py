@@ -1,0 +1,242 @@
+"""CPU oracle for split-KV decode attention and FFD top-delta decode.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg import this package; the product path never does.
+It shares no code with the CUDA library: the arithmetic lives in
+``fd_oracle.c`` (binary64 attention, binary32 key encoding), compiled with gcc
+by ``oracle/build.py``.  This module only marshals numpy arrays.
+
+Functions (each follows the passage cited in ``fd_oracle.c``):
+  decode_dense        standard attention, "Flash Decoding" tutorial section 1
+  decode_dense_f64    the same with binary64 K/V (for reductions)
+  decode_split        per-chunk (m_i, l_i, O_i) + the section-2 merge
+  decode_paged        page gather + the dense definition (tutorial section 3)
+  quantize_keys       2-bit body + int8 residual encoding (FFD summary section 5)
+  dequantize_keys     k~ = deq2 (+ deq8) as binary64
+  decode_topdelta     FFD pipeline, Fig. 2 order (sections 3-5)
+  float_to_half       IEEE binary32 -> binary16, round to nearest even
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = _build.library_path()
+        if not os.path.exists(path) or _build.is_stale():
+            _build.build()
+        lib = ctypes.CDLL(path)
+        P = ctypes.c_void_p
+        I = ctypes.c_int
+        D = ctypes.c_double
+        lib.oracle_decode_dense.argtypes = [P, P, P, P, I, I, I, I, I, D, P, P, I]
+        lib.oracle_decode_dense_f64.argtypes = [P, P, P, P, I, I, I, I, I, D, P, P, I]
+        lib.oracle_decode_split.argtypes = [P, P, P, P, I, I, I, I, I, D, I, P, P, P, P, P, I]
+        lib.oracle_decode_paged.argtypes = [P, P, P, P, I, I, P, I, I, I, I, I, D, P, P, I]
+        lib.oracle_quantize_keys.argtypes = [P, P, I, I, I, I, P, P, P, P, I]
+        lib.oracle_dequantize_keys.argtypes = [P, P, P, P, P, I, I, I, I, I, P]
+        lib.oracle_decode_topdelta.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, D, D, I, I,
+                                               P, P, P, P, P, P, I]
+        lib.oracle_float_to_half.argtypes = [ctypes.c_float]
+        lib.oracle_float_to_half.restype = ctypes.c_uint16
+        lib.oracle_half_to_float.argtypes = [ctypes.c_uint16]
+        lib.oracle_half_to_float.restype = ctypes.c_float
+        lib.oracle_max_threads.argtypes = []
+        for name in ("oracle_decode_dense", "oracle_decode_dense_f64", "oracle_decode_split",
+                     "oracle_decode_paged", "oracle_quantize_keys", "oracle_dequantize_keys",
+                     "oracle_decode_topdelta", "oracle_max_threads"):
+            getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _u16(a):
+    """bf16 / fp16 bit patterns as a C-contiguous uint16 array.  Accepts numpy
+    uint16 arrays or torch bfloat16/float16 CPU tensors."""
+    if hasattr(a, "detach"):  # torch tensor
+        import torch
+        a = a.detach().cpu().contiguous()
+        if a.dtype in (torch.bfloat16, torch.float16):
+            a = a.view(torch.int16)
+        a = a.numpy().view(np.uint16)
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        if a.dtype == np.int16:
+            a = a.view(np.uint16)
+        else:
+            raise TypeError(f"expected 16-bit bit patterns, got {a.dtype}")
+    return a
+
+
+def _i32(a):
+    if a is None:
+        return None
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _check(rc, name):
+    if rc != 0:
+        raise ValueError(f"{name} rejected its arguments (code {rc})")
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def decode_dense(q, k, v, seq_lens, scale, n_threads=0):
+    """q [B,Hq,d], k/v [B,Hkv,L_max,d] (bf16 bits), seq_lens [B] or None.
+    Returns (out [B,Hq,d] f64, lse [B,Hq] f64)."""
+    q, k, v = _u16(q), _u16(k), _u16(v)
+    B, Hq, d = q.shape
+    _, Hkv, L_max, _ = k.shape
+    sl = _i32(seq_lens)
+    out = np.empty((B, Hq, d), np.float64)
+    lse = np.empty((B, Hq), np.float64)
+    rc = _load().oracle_decode_dense(_ptr(q), _ptr(k), _ptr(v), _ptr(sl), B, Hq, Hkv, L_max, d,
+                                     float(scale), _ptr(out), _ptr(lse), int(n_threads))
+    _check(rc, "decode_dense")
+    return out, lse
+
+
+def decode_dense_f64(q, k, v, seq_lens, scale, n_threads=0):
+    """Same as decode_dense with binary64 q, K, V."""
+    q = np.ascontiguousarray(q, np.float64)
+    k = np.ascontiguousarray(k, np.float64)
+    v = np.ascontiguousarray(v, np.float64)
+    B, Hq, d = q.shape
+    _, Hkv, L_max, _ = k.shape
+    sl = _i32(seq_lens)
+    out = np.empty((B, Hq, d), np.float64)
+    lse = np.empty((B, Hq), np.float64)
+    rc = _load().oracle_decode_dense_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(sl), B, Hq, Hkv, L_max, d,
+                                         float(scale), _ptr(out), _ptr(lse), int(n_threads))
+    _check(rc, "decode_dense_f64")
+    return out, lse
+
+
+def decode_split(q, k, v, seq_lens, scale, num_splits, n_threads=0):
+    """Split form.  Returns (out, lse, part_m [B,Hq,S], part_l [B,Hq,S], part_o [B,Hq,S,d])."""
+    q, k, v = _u16(q), _u16(k), _u16(v)
+    B, Hq, d = q.shape
+    _, Hkv, L_max, _ = k.shape
+    S = int(num_splits)
+    sl = _i32(seq_lens)
+    out = np.empty((B, Hq, d), np.float64)
+    lse = np.empty((B, Hq), np.float64)
+    pm = np.empty((B, Hq, S), np.float64)
+    pl = np.empty((B, Hq, S), np.float64)
+    po = np.empty((B, Hq, S, d), np.float64)
+    rc = _load().oracle_decode_split(_ptr(q), _ptr(k), _ptr(v), _ptr(sl), B, Hq, Hkv, L_max, d,
+                                     float(scale), S, _ptr(out), _ptr(lse), _ptr(pm), _ptr(pl),
+                                     _ptr(po), int(n_threads))
+    _check(rc, "decode_split")
+    return out, lse, pm, pl, po
+
+
+def decode_paged(q, k_pages, v_pages, page_table, num_pages, seq_lens, scale, n_threads=0):
+    """k_pages/v_pages [P,Hkv,page_size,d] (bf16 bits), page_table [B,max_pages] int32."""
+    q, kp, vp = _u16(q), _u16(k_pages), _u16(v_pages)
+    B, Hq, d = q.shape
+    _, Hkv, page_size, _ = kp.shape
+    pt = _i32(page_table)
+    sl = _i32(seq_lens)
+    max_pages = pt.shape[1]
+    out = np.empty((B, Hq, d), np.float64)
+    lse = np.empty((B, Hq), np.float64)
+    rc = _load().oracle_decode_paged(_ptr(q), _ptr(kp), _ptr(vp), _ptr(pt), max_pages,
+                                     int(num_pages), _ptr(sl), page_size, B, Hq, Hkv, d,
+                                     float(scale), _ptr(out), _ptr(lse), int(n_threads))
+    _check(rc, "decode_paged")
+    return out, lse
+
+
+def quantize_keys(k, seq_lens=None, n_threads=0):
+    """k [B,Hkv,L_max,d] bf16 bits.  Returns (codes u8 [B,Hkv,L_max,d/4],
+    mn_scale u16 [B,Hkv,L_max,d/32,2], res i8 [B,Hkv,L_max,d], res_scale u16 [B,Hkv,L_max,d/32]).
+    Rows past seq_lens[b] are zero (never written by the encoder)."""
+    k = _u16(k)
+    B, Hkv, L_max, d = k.shape
+    sl = _i32(seq_lens)
+    codes = np.zeros((B, Hkv, L_max, d // 4), np.uint8)
+    ms = np.zeros((B, Hkv, L_max, d // 32, 2), np.uint16)
+    res = np.zeros((B, Hkv, L_max, d), np.int8)
+    rs = np.zeros((B, Hkv, L_max, d // 32), np.uint16)
+    rc = _load().oracle_quantize_keys(_ptr(k), _ptr(sl), B, Hkv, L_max, d, _ptr(codes), _ptr(ms),
+                                      _ptr(res), _ptr(rs), int(n_threads))
+    _check(rc, "quantize_keys")
+    return codes, ms, res, rs
+
+
+def dequantize_keys(codes, mn_scale, res, res_scale, seq_lens=None, with_residual=True):
+    codes = np.ascontiguousarray(codes, np.uint8)
+    ms = np.ascontiguousarray(mn_scale, np.uint16)
+    res = np.ascontiguousarray(res, np.int8)
+    rs = np.ascontiguousarray(res_scale, np.uint16)
+    B, Hkv, L_max, d4 = codes.shape
+    d = d4 * 4
+    sl = _i32(seq_lens)
+    kt = np.empty((B, Hkv, L_max, d), np.float64)
+    rc = _load().oracle_dequantize_keys(_ptr(codes), _ptr(ms), _ptr(res), _ptr(rs), _ptr(sl), B, Hkv,
+                                        L_max, d, int(bool(with_residual)), _ptr(kt))
+    _check(rc, "dequantize_keys")
+    return kt
+
+
+def decode_topdelta(q, codes, mn_scale, res, res_scale, v, seq_lens, scale, delta,
+                    n_sink=4, window=64, want_scores=False, n_threads=0):
+    """Returns a dict with out [B,Hq,d], lse [B,Hq], sel_mask [B,Hq,ceil(L/32)] u32,
+    sel_count [B,Hq], m_hat [B,Hq] and (optionally) s_tilde [B,Hq,L_max]."""
+    q, v = _u16(q), _u16(v)
+    codes = np.ascontiguousarray(codes, np.uint8)
+    ms = np.ascontiguousarray(mn_scale, np.uint16)
+    res = np.ascontiguousarray(res, np.int8)
+    rs = np.ascontiguousarray(res_scale, np.uint16)
+    B, Hq, d = q.shape
+    _, Hkv, L_max, _ = v.shape
+    sl = _i32(seq_lens)
+    words = (L_max + 31) // 32
+    out = np.empty((B, Hq, d), np.float64)
+    lse = np.empty((B, Hq), np.float64)
+    mask = np.zeros((B, Hq, words), np.uint32)
+    cnt = np.zeros((B, Hq), np.int32)
+    mh = np.empty((B, Hq), np.float64)
+    st = np.full((B, Hq, L_max), np.nan, np.float64) if want_scores else None
+    dl = math.inf if delta is None else float(delta)
+    rc = _load().oracle_decode_topdelta(_ptr(q), _ptr(codes), _ptr(ms), _ptr(res), _ptr(rs), _ptr(v),
+                                        _ptr(sl), B, Hq, Hkv, L_max, d, float(scale), dl,
+                                        int(n_sink), int(window), _ptr(out), _ptr(lse), _ptr(mask),
+                                        _ptr(cnt), _ptr(mh), _ptr(st), int(n_threads))
+    _check(rc, "decode_topdelta")
+    r = dict(out=out, lse=lse, sel_mask=mask, sel_count=cnt, m_hat=mh)
+    if want_scores:
+        r["s_tilde"] = st
+    return r
+
+
+def float_to_half(x) -> np.ndarray:
+    """Element-wise IEEE binary32 -> binary16 bits (round to nearest even)."""
+    lib = _load()
+    x = np.asarray(x, np.float32).ravel()
+    return np.array([lib.oracle_float_to_half(float(v)) for v in x], np.uint16)
+
+
+def half_to_float(h) -> np.ndarray:
+    lib = _load()
+    h = np.asarray(h, np.uint16).ravel()
+    return np.array([lib.oracle_half_to_float(int(v)) for v in h], np.float32)
