@@ -1,0 +1,558 @@
+"""Benchmark: decode-attention throughput of libfd on GB300.
+
+One step = one decode-attention call (every row of the hot path that the
+workload uses: split planning, the per-chunk partial pass, the merge; for the
+sparse workloads the fused 2-bit scan / top-delta / residual / attention pass)
+over one batch of synthetic inputs already resident in HBM.
+
+Default workload: MHA decode, B=1, Hq=Hkv=32, d=128, L=32768, bf16 KV cache
+(512 MiB of K+V per call, larger than the 129 MB L2, so no flush is needed
+between calls).  Other workloads: --workload tiny|mha32k|gqa_paged|million|
+ffd_dense|ffd_topdelta5|ffd_topdelta7.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fd|reference]
+
+With N > 1 (torchrun) every rank runs an independent replica of the
+workload on its own GPU (the path has no exchange step): weak scaling.
+--impl reference times the CPU oracle (the plain fp64 restatement) on the
+host cores, on a bounded sample of the same workload per step.
+Prints ONE JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode-attention tokens/s and µs/call at 1 GB300; achieved HBM GB/s vs 8 TB/s"
+NORTH_STAR_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+DEFAULT_STEPS = {"tiny": 20000, "mha32k": 20000, "gqa_paged": 3000, "million": 3000,
+                 "ffd_dense": 4000, "ffd_topdelta5": 4000, "ffd_topdelta7": 4000}
+
+
+# ----------------------------------------------------------------- helpers
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    for key in ("hbm_gbs", "hbm_GBps", "hbm_copy_gbs"):
+        if key in d:
+            return float(d[key]), d
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms in a thread."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.samples = []  # (t, sm, max_sm, reasons)
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm, mx = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            reasons = [n for n, v in zip(names, parts[5:9]) if v.lower() == "active"]
+            self.samples.append((time.time(), sm, mx, reasons))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        where = "timed region"
+        if not inside:
+            inside = self.samples
+            where = "whole run (timed region shorter than the 200 ms sampling period)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        reasons = sorted({r for s in inside for r in s[3]})
+        return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": max(s[2] for s in inside),
+                "reasons": reasons, "samples": len(inside), "window": where}
+
+
+# --------------------------------------------------------------- workloads
+
+class Workload:
+    """Resident inputs plus a `call()` that runs one decode through the C ABI."""
+
+    def __init__(self, name, seed, device):
+        import torch
+
+        import long_context_decode_split_gb300 as fd
+        import workloads as W
+
+        self.name = name
+        self.fd = fd
+        self.device = device
+        self.topdelta = None
+        if name == "tiny":
+            p = W.tiny(seed=seed, device=device)
+        elif name == "mha32k":
+            p = W.mha32k(seed=seed, device=device)
+        elif name == "million":
+            p = W.million(seed=seed, device=device)
+        elif name == "gqa_paged":
+            p = W.gqa_paged(seed=seed, device=device)
+        elif name.startswith("ffd"):
+            p = W.ffd(seed=seed, device=device)
+            if name != "ffd_dense":
+                self.topdelta = 5.0 if name.endswith("5") else 7.0
+        else:
+            raise ValueError(name)
+        self.p = p
+        self.paged = p.paged
+        self.out_dtype = p.out_dtype
+        B, Hq, Hkv, d = p.B, p.Hq, p.Hkv, p.d
+        self.out = torch.empty((B, Hq, d), device=device,
+                               dtype=torch.float32 if p.out_dtype == "f32" else torch.bfloat16)
+        self.lse = torch.empty((B, Hq), device=device, dtype=torch.float32)
+        if self.topdelta is not None:
+            self.qk = fd.fd_quantize_keys(p.k, p.seq_lens)
+            need = fd.fd_topdelta_workspace_size(B, Hq, Hkv, p.L_max, d, p.num_splits)
+            self.splits = None
+        else:
+            need = fd.fd_decode_workspace_size(B, Hq, Hkv, p.L_max, d, p.num_splits, self.paged)
+            self.splits = fd.fd_num_splits(B, Hq, Hkv, p.L_max, d, p.num_splits, self.paged)
+        self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+        self.kv_tokens = p.kv_tokens()
+
+    def call(self, stream=None):
+        p, fd = self.p, self.fd
+        if self.topdelta is not None:
+            c, ms, r, rs = self.qk
+            fd.fd_decode_topdelta(p.q, c, ms, r, rs, p.v, p.seq_lens, p.scale, self.topdelta, 4, 64,
+                                  p.num_splits, out=self.out, lse=self.lse, out_dtype=self.out_dtype,
+                                  workspace=self.ws, stream=stream)
+        elif self.paged:
+            fd.fd_decode_paged(p.q, p.k_pages, p.v_pages, p.page_table, p.num_pages, p.seq_lens, p.scale,
+                               p.num_splits, out=self.out, lse=self.lse, out_dtype=self.out_dtype,
+                               workspace=self.ws, stream=stream)
+        else:
+            fd.fd_decode_dense(p.q, p.k, p.v, None, p.scale, p.num_splits, out=self.out, lse=self.lse,
+                               out_dtype=self.out_dtype, workspace=self.ws, stream=stream)
+
+    def launches_per_call(self):
+        if self.topdelta is not None:
+            return 2  # fused pass + merge
+        return 1 if self.splits == 1 else 2
+
+    def algorithmic_bytes(self, topdelta_union=None):
+        """HBM bytes the method must move per call (K/V or 2-bit body + residual + V,
+        plus q in and out/lse out)."""
+        p = self.p
+        B, Hq, Hkv, d = p.B, p.Hq, p.Hkv, p.d
+        io = B * Hq * d * 2 + B * Hq * d * (4 if p.out_dtype == "f32" else 2) + B * Hq * 4
+        if self.topdelta is None:
+            return self.kv_tokens * Hkv * d * 2 * 2 + io
+        scan = self.kv_tokens * Hkv * (d // 4 + (d // 32) * 4)
+        detail = (topdelta_union if topdelta_union is not None else self.kv_tokens * Hkv) * (d + (d // 32) * 2 + d * 2)
+        return scan + detail + io
+
+    def config(self):
+        p = self.p
+        c = {"workload": self.name, "B": p.B, "Hq": p.Hq, "Hkv": p.Hkv, "d": p.d,
+             "L": p.L_max if not self.paged else "ragged", "kv_tokens": self.kv_tokens,
+             "num_splits": self.splits if self.splits is not None else p.num_splits,
+             "cache": "paged-64" if self.paged else "contiguous", "out_dtype": p.out_dtype}
+        if self.topdelta is not None:
+            c.update(delta=self.topdelta, n_sink=4, window=64)
+        return c
+
+
+# ------------------------------------------------------------------ timing
+
+def time_device(wl, steps, warmup, dist_ctx):
+    import torch
+
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        wl.call()
+    torch.cuda.synchronize()
+    dist_ctx.barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for _ in range(steps):
+        wl.call()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    dist_ctx.barrier()
+    ms = ev0.elapsed_time(ev1)
+    return dist_ctx.max(ms), (t_wall0, t_wall1)
+
+
+def time_e2e(wl, steps, warmup, dist_ctx):
+    """Same call through the public API, with this step's new inputs copied
+    from pinned host memory (the query and the newest token's K/V rows) and
+    the result (out, lse) read back, inside the timed region."""
+    import torch
+
+    p = wl.p
+    dev = wl.device
+    q_h = p.q.detach().cpu().pin_memory()
+    if wl.paged:
+        # newest token of every sequence: its row inside its last page
+        lens = p.seq_lens.cpu().tolist()
+        tgt = [(int(p.page_table[b, (L - 1) // 64]), (L - 1) % 64) for b, L in enumerate(lens) if L > 0]
+        k_rows = torch.stack([p.k_pages[pg, :, r] for pg, r in tgt]).cpu().pin_memory()
+        v_rows = torch.stack([p.v_pages[pg, :, r] for pg, r in tgt]).cpu().pin_memory()
+    else:
+        L = p.L_max
+        k_rows = p.k[:, :, L - 1].contiguous().cpu().pin_memory()
+        v_rows = p.v[:, :, L - 1].contiguous().cpu().pin_memory()
+        tgt = None
+    k_dev = torch.empty(k_rows.shape, dtype=k_rows.dtype, device=dev)
+    v_dev = torch.empty(v_rows.shape, dtype=v_rows.dtype, device=dev)
+    out_h = torch.empty(wl.out.shape, dtype=wl.out.dtype).pin_memory()
+    lse_h = torch.empty(wl.lse.shape, dtype=wl.lse.dtype).pin_memory()
+    h2d = q_h.numel() * 2 + k_rows.numel() * 2 + v_rows.numel() * 2
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
+
+    def step():
+        p.q.copy_(q_h, non_blocking=True)
+        k_dev.copy_(k_rows, non_blocking=True)
+        v_dev.copy_(v_rows, non_blocking=True)
+        if wl.paged:
+            for i, (pg, r) in enumerate(tgt):
+                p.k_pages[pg, :, r] = k_dev[i]
+                p.v_pages[pg, :, r] = v_dev[i]
+        else:
+            p.k[:, :, p.L_max - 1] = k_dev
+            p.v[:, :, p.L_max - 1] = v_dev
+        wl.call()
+        out_h.copy_(wl.out, non_blocking=True)
+        lse_h.copy_(wl.lse, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    dist_ctx.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    dist_ctx.barrier()
+    return dist_ctx.max((t1 - t0) * 1e3), h2d, d2h
+
+
+# ------------------------------------------------------------ CPU oracle
+
+FULL_SHAPES = {"tiny": (1, 1, 1, 1024, 64), "mha32k": (1, 32, 32, 32768, 128),
+               "million": (1, 32, 8, 1 << 20, 128), "gqa_paged": (8, 64, 8, 73728, 128),
+               "ffd_dense": (4, 32, 8, 131072, 128), "ffd_topdelta5": (4, 32, 8, 131072, 128),
+               "ffd_topdelta7": (4, 32, 8, 131072, 128)}
+
+
+class OracleSample:
+    """A bounded slice of a workload for the CPU oracle: the first `heads` KV
+    heads (with their query groups) and the first `Ls` tokens of every
+    sequence.  `frac` is the slice's share of one full call's work.  For the
+    ragged paged batch the full call is taken at the mean length."""
+
+    def __init__(self, name, seed, target_s):
+        import numpy as np
+        import torch
+
+        import oracle
+        import workloads as W
+
+        self.name = name
+        self.oracle = oracle
+        B, Hq, Hkv, L, d = FULL_SHAPES[name]
+        G = Hq // Hkv
+        self.B = B
+        self.delta = None
+        if name.startswith("ffd_top"):
+            self.delta = 5.0 if name.endswith("5") else 7.0
+
+        def bits(t):
+            return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+        heads, Ls = 1, min(L, 2048)
+        while True:
+            if name.startswith("ffd"):
+                p = W.ffd(seed=seed, B=B, L=Ls, Hq=heads * G, Hkv=heads, d=d)
+            else:
+                p = W.random_problem(B, heads * G, heads, Ls, d, seed=seed)
+            self.args = (bits(p.q), bits(p.k), bits(p.v), p.scale)
+            if self.delta is not None:
+                self.enc = oracle.quantize_keys(self.args[1])
+            t0 = time.perf_counter()
+            self.run()
+            dt = time.perf_counter() - t0
+            if dt >= target_s / 2 or (heads == Hkv and Ls == L):
+                break
+            grow = max(2, min(8, int(target_s / max(dt, 1e-4))))
+            if Ls < L:
+                Ls = min(L, Ls * grow)
+            else:
+                heads = min(Hkv, heads * 2)
+        self.frac = (heads / Hkv) * (Ls / L)
+        self.desc = (f"{heads} of {Hkv} KV heads (with their query heads) x first {Ls} of {L} tokens, "
+                     f"B={B}, d={d}: {self.frac:.4g} of one full call")
+        self.threads = oracle.max_threads()
+
+    def run(self):
+        q, k, v, scale = self.args
+        if self.delta is not None:
+            c, ms, r, rs = self.enc
+            self.oracle.decode_topdelta(q, c, ms, r, rs, v, None, scale, self.delta)
+        else:
+            self.oracle.decode_dense(q, k, v, None, scale)
+
+
+def time_oracle(sample, steps, warmup):
+    """Returns (tokens/s of full calls, seconds per step)."""
+    for _ in range(warmup):
+        sample.run()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        sample.run()
+    dt = time.perf_counter() - t0
+    per_call = dt / steps / sample.frac
+    return sample.B / per_call, dt / steps
+
+
+# ---------------------------------------------------------------- context
+
+class DistCtx:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch.distributed as dist
+
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, x):
+        if self.pg is None:
+            return x
+        import torch
+
+        t = torch.tensor([float(x)], device="cuda" if torch.cuda.is_available() else "cpu")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, x):
+        if self.pg is None:
+            return x
+        import torch
+
+        t = torch.tensor([float(x)], device="cuda" if torch.cuda.is_available() else "cpu")
+        self.pg.all_reduce(t)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+# ------------------------------------------------------------------- main
+
+def run_reference(args, ctx):
+    """The oracle as it stands, on the host cores: W warm-up and K timed
+    steps, each one bounded sample of the workload; value in the fd arm's unit."""
+    if ctx.rank != 0:
+        return
+    per_step = max(0.002, min(2.0, 90.0 / max(1, args.steps + args.warmup)))
+    sample = OracleSample(args.workload, args.seed, per_step)
+    value, s_per_step = time_oracle(sample, args.steps, args.warmup)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": s_per_step * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": args.workload},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": sample.threads, "kind": "oracle",
+                             "sample": sample.desc + " per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["fd", "reference"], default="fd")
+    ap.add_argument("--workload", default="mha32k",
+                    choices=["tiny", "mha32k", "gqa_paged", "million", "ffd_dense", "ffd_topdelta5",
+                             "ffd_topdelta7"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    args = ap.parse_args()
+    if args.steps is None:
+        args.steps = DEFAULT_STEPS[args.workload]
+    args.warmup = max(3, args.warmup)
+
+    ctx = DistCtx()
+    if args.impl == "reference":
+        ctx.init("gloo")
+        run_reference(args, ctx)
+        ctx.close()
+        return
+
+    import torch
+
+    torch.cuda.set_device(ctx.local_rank)
+    ctx.init("nccl")
+    import long_context_decode_split_gb300 as fd
+
+    fd.load()
+    dev = f"cuda:{ctx.local_rank}"
+    wl = Workload(args.workload, args.seed + ctx.rank, dev)
+
+    sampler = ClockSampler(ctx.local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    ms, (tw0, tw1) = time_device(wl, args.steps, args.warmup, ctx)
+    sampler_summary = sampler.summary(tw0, tw1)
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = max(3, min(args.steps, 2000))
+        ms_e2e, h2d, d2h = time_e2e(wl, e2e_steps, args.warmup, ctx)
+    sampler.stop()
+
+    status = fd.fd_device_status(clear=True)
+    B = wl.p.B
+    n = ctx.world
+    per_call_s = ms / 1e3 / args.steps
+    value = n * B * args.steps / (ms / 1e3)
+    algo = wl.algorithmic_bytes()
+    achieved_gbs = algo / per_call_s / 1e9
+    peak = measured_peaks()
+    if peak is not None:
+        peak_gbs, peak_src = peak[0], "measured (MEASURED_PEAKS.json hbm copy)"
+    else:
+        peak_gbs, peak_src = FALLBACK_HBM_GBS, "fallback (6.8 TB/s, no MEASURED_PEAKS.json)"
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tfile):
+        try:
+            with open(tfile) as f:
+                tj = json.load(f)
+            ent = tj.get(args.workload)
+            if ent and ent.get("source_sha") == source_digest():
+                traffic = ent.get("dram_bytes_per_launch")
+        except (OSError, ValueError):
+            traffic = None
+    if not args.no_e2e:
+        e2e = {"value": n * B * e2e_steps / (ms_e2e / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+               "note": "per step: query + newest token's K/V rows host->device, out + lse device->host"}
+    cpu = None
+    if ctx.rank == 0 and n == 1 and not args.no_cpu_baseline:
+        sample = OracleSample(args.workload, args.seed, 1.0)
+        t0 = time.perf_counter()
+        sample.run()
+        reps = max(1, int(args.cpu_budget / max(time.perf_counter() - t0, 1e-3)))
+        v, s_rep = time_oracle(sample, reps, 1)
+        cpu = {"value": v, "unit": "tokens/s", "cores": sample.threads, "kind": "oracle",
+               "sample": f"{sample.desc}; {reps} timed runs of {s_rep * 1e3:.1f} ms"}
+    if ctx.rank == 0:
+        cfg = wl.config()
+        cfg["l2"] = ("inputs larger than L2" if algo > L2_BYTES else "inputs smaller than L2 (no flush)")
+        cfg["parallelism"] = f"replicas x{n}"
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": n, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "kv_dtype": "bf16",
+            "data": "synthetic", "config": cfg,
+            "us_per_call": per_call_s * 1e6,
+            "kv_tokens_per_s": wl.kv_tokens * n / per_call_s,
+            "achieved_hbm_gbs": achieved_gbs,
+            "frac_of_8tbs": achieved_gbs / NORTH_STAR_HBM_GBS,
+            "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak_gbs, "unit": "GB/s",
+                         "frac": achieved_gbs / peak_gbs, "traffic": traffic, "peak_source": peak_src,
+                         "kernel": "split partial pass + merge (whole call)",
+                         "algorithmic_bytes_per_launch": algo},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps * wl.launches_per_call(),
+            "clocks": sampler_summary,
+            "device_status": fd.fd_status_string(status),
+        }
+        print(json.dumps(line), flush=True)
+    ctx.close()
+
+
+def source_digest():
+    import hashlib
+
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "long_context_decode_split_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+if __name__ == "__main__":
+    main()

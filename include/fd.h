@@ -1,0 +1,194 @@
+/*
+ * fd.h -- C ABI of libfd: split-KV decode attention for long KV caches on
+ * NVIDIA GB300 (sm_103a), with an opt-in sparse top-delta path.
+ *
+ * Sources of the operations declared here:
+ *   [FD]  "Flash Decoding" tutorial (aiqz.cc/article/flash-decoding.html):
+ *         section 1 (standard attention and its four steps), section 2 (the
+ *         sequence split into chunks, per-chunk m_i, l_i, O_i, and the merge
+ *         O = sum_i e^{m_i-m} l_i O_i / sum_j e^{m_j-m} l_j, m = max_i m_i),
+ *         section 3 (KV cache cut into fixed-size pages), section 6 and the
+ *         misconceptions section (how many chunks to use).
+ *   [FFD] "Faster Than Flash: Exploiting Attention Sparsity for Efficient
+ *         Long-Context Decoding" summary (PaperDaily): section 3 (top-delta
+ *         rule s_ij >= m_i - delta), section 4 (pseudo-max from attention
+ *         sinks and the local window), section 5 (2-bit body for the full
+ *         scan, 8-bit residual loaded for candidates only), section 6 and
+ *         Fig. 2 (one fused kernel: scan, select, correct, attend, aggregate).
+ *
+ * Conventions shared by every entry point
+ *   - Every data pointer is a DEVICE pointer owned by the caller, 16-byte
+ *     aligned, to a C-contiguous (row-major) array.  bf16 and fp16 values are
+ *     passed as their 16-bit patterns.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     only enqueue work on it: they never synchronise and never allocate
+ *     memory.  Scratch memory is the caller's `workspace`.
+ *   - Return value: an fd_status.  Arguments are checked on the host before
+ *     anything is enqueued; a call that returns anything but FD_OK has
+ *     enqueued nothing, except FD_ERR_CUDA, which reports a launch failure.
+ *   - Faults found by the kernels themselves (a page id outside the pool, a
+ *     pipeline wait that exceeded its time limit) do not stop the stream;
+ *     they set a per-process device status word read by fd_device_status().
+ *   - Softmax runs in natural-log units of the scaled score s = scale*<q,k>.
+ *     lse[b,hq] = log sum_j exp(s_j) over the attended keys.  A sequence of
+ *     length 0 yields out = 0 and lse = -inf.
+ *   - Head grouping: query head hq reads KV head hq / (Hq / Hkv).
+ *   - Supported shapes: d in {64, 128}; 1 <= Hq/Hkv <= 8; page_size == 64.
+ *   - Results are deterministic for fixed inputs, shapes and num_splits.
+ */
+#ifndef FD_H
+#define FD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FD_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define FD_API __attribute__((visibility("default")))
+#else
+#define FD_API
+#endif
+
+typedef enum fd_status {
+    FD_OK = 0,
+    FD_ERR_INVALID_ARG = 1,          /* null/misaligned pointer, bad size or relation */
+    FD_ERR_UNSUPPORTED = 2,          /* valid but not implemented: d, group size, page size */
+    FD_ERR_WORKSPACE_TOO_SMALL = 3,  /* workspace_bytes below the *_workspace_size() value */
+    FD_ERR_BAD_PAGE_TABLE = 4,       /* (device status) a page id outside [0, num_pages) */
+    FD_ERR_CUDA = 5,                 /* a CUDA launch or query failed */
+    FD_ERR_DEVICE_TIMEOUT = 6        /* (device status) a pipeline wait hit its time limit */
+} fd_status;
+
+typedef enum fd_out_dtype {
+    FD_OUT_F32 = 0,                  /* out is float32 */
+    FD_OUT_BF16 = 1                  /* out is bf16, rounded to nearest even */
+} fd_out_dtype;
+
+/* Version of this ABI (FD_ABI_VERSION of the built library). */
+FD_API int fd_abi_version(void);
+
+/* Static, human-readable name of a status code (never NULL). */
+FD_API const char* fd_status_string(int status);
+
+/* Number of chunks per sequence ("num_splits", [FD] section 2) that the
+ * decode entry points will use on the CURRENT device for these sizes.
+ * num_splits > 0 is honoured as the chunk count: chunk = ceil(L_b/num_splits)
+ * rounded up to a multiple of 64 tokens (so trailing chunks may be empty).
+ * num_splits == 0 lets the planner choose from the device's SM count
+ * ([FD] section 6: fill every SM, chunks of at least a few hundred tokens).
+ * `ragged` != 0 says sequence lengths may differ (paged batches).
+ * Returns the chunk count (>= 1), or -FD_ERR_* on bad arguments. */
+FD_API int fd_num_splits(int B, int Hq, int Hkv, int L_max, int d, int num_splits, int ragged);
+
+/* Bytes of workspace the dense and paged decode need for these sizes on the
+ * current device (same arguments as fd_num_splits).  0 when no
+ * workspace is needed (one chunk).  Returns 0 on bad arguments too. */
+FD_API size_t fd_decode_workspace_size(int B, int Hq, int Hkv, int L_max, int d,
+                                int num_splits, int ragged);
+
+/* Dense split-KV decode ([FD] sections 1-2): one new query token per
+ * sequence attends to that sequence's whole contiguous KV cache.
+ *   q         [B, Hq, d]          bf16
+ *   k, v      [B, Hkv, L_max, d]  bf16
+ *   seq_lens  [B] int32 in [0, L_max], or NULL: every sequence has L_max
+ *   scale     softmax scale (usually 1/sqrt(d))
+ *   num_splits 0 = planner, > 0 = chunk count (see fd_num_splits)
+ *   out       [B, Hq, d] in out_dtype;  lse [B, Hq] float32, or NULL
+ *   workspace fd_decode_workspace_size(B, Hq, Hkv, L_max, d, num_splits,
+ *             seq_lens != NULL) bytes; may be NULL when that size is 0.
+ * Tokens t >= seq_lens[b] are never read. */
+FD_API int fd_decode_dense(const void* q, const void* k, const void* v,
+                    const int32_t* seq_lens,
+                    int B, int Hq, int Hkv, int L_max, int d,
+                    float scale, int num_splits,
+                    void* out, int out_dtype, float* lse,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* Paged split-KV decode ([FD] section 3 with sections 1-2): the cache is a
+ * pool of fixed-size pages.
+ *   k_pages, v_pages [num_pages, Hkv, page_size, d] bf16
+ *   page_table [B, max_pages] int32: token t of sequence b is row
+ *              t % page_size of page page_table[b * max_pages + t / page_size]
+ *   seq_lens   [B] int32 in [0, max_pages * page_size] (required)
+ *   page_size  must be 64
+ * Other arguments as fd_decode_dense, with L_max = max_pages * page_size for
+ * the workspace size (ragged = 1).  Only the first ceil(seq_lens[b]/64)
+ * entries of a table row are read; an entry outside [0, num_pages) is not
+ * dereferenced: its tokens are skipped and the device status records
+ * FD_ERR_BAD_PAGE_TABLE. */
+FD_API int fd_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                    const int32_t* page_table, int max_pages, int num_pages,
+                    const int32_t* seq_lens, int page_size,
+                    int B, int Hq, int Hkv, int d,
+                    float scale, int num_splits,
+                    void* out, int out_dtype, float* lse,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* Key encoder for the sparse path ([FFD] section 5): per token and per
+ * group of 32 channels, a 2-bit asymmetric body and an int8 symmetric
+ * residual.  With x the group's bf16 values, in IEEE binary32 arithmetic:
+ *   mn16 = fp16(min x), s16 = fp16((max x - min x) / 3)
+ *   code = clamp(rint((x - mn16) / s16), 0, 3)      (0 when s16 == 0)
+ *   deq2 = mn16 + code * s16,  r = x - deq2
+ *   rs16 = fp16(max |r| / 127)
+ *   rq   = clamp(rint(r / rs16), -127, 127)         (0 when rs16 == 0)
+ * fp16() and rint() round to nearest, ties to even.  Keys must lie within
+ * the fp16 range.  Layouts (row = (b * Hkv + h) * L_max + t):
+ *   k          [B, Hkv, L_max, d] bf16 (input)
+ *   codes      [row, d/4]     uint8: channel c in byte c/4, bits 2*(c%4)+{0,1}
+ *   mn_scale   [row, d/32, 2] fp16 (mn16, s16)
+ *   res        [row, d]       int8
+ *   res_scale  [row, d/32]    fp16 (rs16)
+ * Rows with t >= seq_lens[b] (seq_lens may be NULL) are not written.
+ * d must be 64 or 128. */
+FD_API int fd_quantize_keys(const void* k, const int32_t* seq_lens,
+                     int B, int Hkv, int L_max, int d,
+                     uint8_t* codes, void* mn_scale, int8_t* res, void* res_scale,
+                     void* stream);
+
+/* Bytes of workspace fd_decode_topdelta needs (0 when none). */
+FD_API size_t fd_topdelta_workspace_size(int B, int Hq, int Hkv, int L_max, int d,
+                                  int num_splits);
+
+/* Top-delta sparse decode ([FFD] sections 3-6, Fig. 2), one fused pass per
+ * chunk of the cache.  For each (b, query head):
+ *   1. s~_j  = scale * <q, deq2_j>   for every cached token (2-bit body only)
+ *   2. m^    = max of s~ over the anchors {0..n_sink-1} U {L-window..L-1}
+ *   3. Sel   = { j : s~_j >= m^ - delta }       (delta = +inf keeps all)
+ *   4. s_j   = scale * <q, deq2_j + deq8_j>     for j in Sel (int8 residual)
+ *   5. out   = sum_{Sel} e^{s_j} v_j / sum_{Sel} e^{s_j}; lse over Sel.
+ * Inputs are fd_quantize_keys' outputs for the same cache, plus
+ *   q [B, Hq, d] bf16, v [B, Hkv, L_max, d] bf16, seq_lens [B] or NULL,
+ *   delta >= 0 (may be +inf), n_sink >= 0, window >= 0.
+ * Optional outputs for inspection (NULL to skip): sel_mask
+ * [B, Hq, ceil(L_max/32)] uint32 (bit j%32 of word j/32 set when j is in
+ * Sel) and sel_count [B, Hq] int32.  The residual and V of a token are read
+ * only when some query head of its KV group selects a token in the same
+ * 64-token tile.  workspace: fd_topdelta_workspace_size() bytes. */
+FD_API int fd_decode_topdelta(const void* q, const uint8_t* codes, const void* mn_scale,
+                       const int8_t* res, const void* res_scale, const void* v,
+                       const int32_t* seq_lens,
+                       int B, int Hq, int Hkv, int L_max, int d,
+                       float scale, float delta, int n_sink, int window,
+                       int num_splits,
+                       void* out, int out_dtype, float* lse,
+                       uint32_t* sel_mask, int32_t* sel_count,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream`, then reports the device status word of the current
+ * device: FD_ERR_DEVICE_TIMEOUT, FD_ERR_BAD_PAGE_TABLE, FD_ERR_INVALID_ARG (a
+ * seq_lens entry outside [0, L_max]; the kernels clamped it) or FD_OK, in
+ * that order of precedence (FD_ERR_CUDA if the synchronisation itself
+ * failed).  clear != 0 resets the word afterwards. */
+FD_API int fd_device_status(int clear, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FD_H */

@@ -1,0 +1,293 @@
+"""Python binding of libfd, the C-ABI split-KV decode attention library.
+
+Argument marshalling only: every function below checks tensor dtypes,
+shapes, devices and contiguity, allocates outputs and workspace with torch
+when the caller did not pass them, and calls the C entry point of the same
+name (declared in include/fd.h) on the current CUDA stream.  All arithmetic
+runs in the library's CUDA kernels; there is no fallback.  A missing or
+unloadable libfd.so raises an error.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+
+import torch
+
+__all__ = [
+    "FdError", "load", "open_library", "header_symbols", "fd_abi_version", "fd_status_string", "fd_num_splits",
+    "fd_decode_workspace_size", "fd_decode_dense", "fd_decode_paged", "fd_quantize_keys",
+    "fd_topdelta_workspace_size", "fd_decode_topdelta", "fd_device_status",
+    "FD_OK", "FD_ERR_INVALID_ARG", "FD_ERR_UNSUPPORTED", "FD_ERR_WORKSPACE_TOO_SMALL",
+    "FD_ERR_BAD_PAGE_TABLE", "FD_ERR_CUDA", "FD_ERR_DEVICE_TIMEOUT", "FD_OUT_F32", "FD_OUT_BF16",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfd.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "fd.h")
+
+FD_OK = 0
+FD_ERR_INVALID_ARG = 1
+FD_ERR_UNSUPPORTED = 2
+FD_ERR_WORKSPACE_TOO_SMALL = 3
+FD_ERR_BAD_PAGE_TABLE = 4
+FD_ERR_CUDA = 5
+FD_ERR_DEVICE_TIMEOUT = 6
+FD_OUT_F32 = 0
+FD_OUT_BF16 = 1
+
+_lib = None
+
+
+class FdError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        msg = fd_status_string(status) if _lib is not None else str(status)
+        super().__init__(f"{where}: {msg}")
+
+
+def load():
+    """The process-wide libfd handle (loaded on first use); raises if the
+    library has not been built."""
+    global _lib
+    if _lib is None:
+        _lib = open_library(LIB_PATH)
+    return _lib
+
+
+def open_library(path: str):
+    """Open libfd at `path` and declare its C signatures."""
+    if not os.path.exists(path):
+        raise ImportError(f"libfd.so not built at {path}; run long_context_decode_split_gb300._build.build()")
+    lib = ctypes.CDLL(path)
+    P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    sig = {
+        "fd_abi_version": (I, []),
+        "fd_status_string": (ctypes.c_char_p, [I]),
+        "fd_num_splits": (I, [I, I, I, I, I, I, I]),
+        "fd_decode_workspace_size": (S, [I, I, I, I, I, I, I]),
+        "fd_decode_dense": (I, [P, P, P, P, I, I, I, I, I, F, I, P, I, P, P, S, P]),
+        "fd_decode_paged": (I, [P, P, P, P, I, I, P, I, I, I, I, I, F, I, P, I, P, P, S, P]),
+        "fd_quantize_keys": (I, [P, P, I, I, I, I, P, P, P, P, P]),
+        "fd_topdelta_workspace_size": (S, [I, I, I, I, I, I]),
+        "fd_decode_topdelta": (I, [P, P, P, P, P, P, P, I, I, I, I, I, F, F, I, I, I, P, I, P, P, P, P, S, P]),
+        "fd_device_status": (I, [I, P]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+def header_symbols(path: str = HEADER):
+    """Names of the functions include/fd.h declares."""
+    with open(path) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^FD_API\s+[\w\s\*]+?\b(fd_\w+)\s*\(", text, flags=re.M)))
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(cond, what):
+    if not cond:
+        raise ValueError(what)
+
+
+def _check_cuda(t, name, dtype=None, shape=None):
+    _need(t.is_cuda, f"{name} must be a CUDA tensor")
+    _need(t.is_contiguous(), f"{name} must be contiguous")
+    if dtype is not None:
+        _need(t.dtype == dtype, f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None:
+        _need(tuple(t.shape) == tuple(shape), f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _raise(st, where):
+    if st != FD_OK:
+        raise FdError(st, where)
+
+
+def _out_code(out_dtype):
+    if out_dtype in ("bf16", torch.bfloat16, FD_OUT_BF16):
+        return FD_OUT_BF16, torch.bfloat16
+    if out_dtype in ("f32", "fp32", torch.float32, FD_OUT_F32):
+        return FD_OUT_F32, torch.float32
+    raise ValueError(f"out_dtype {out_dtype!r}")
+
+
+def fd_abi_version() -> int:
+    return int(load().fd_abi_version())
+
+
+def fd_status_string(status: int) -> str:
+    return load().fd_status_string(int(status)).decode()
+
+
+def fd_num_splits(B, Hq, Hkv, L_max, d, num_splits=0, ragged=False) -> int:
+    r = int(load().fd_num_splits(B, Hq, Hkv, L_max, d, num_splits, int(bool(ragged))))
+    if r < 0:
+        raise FdError(-r, "fd_num_splits")
+    return r
+
+
+def fd_decode_workspace_size(B, Hq, Hkv, L_max, d, num_splits=0, ragged=False) -> int:
+    return int(load().fd_decode_workspace_size(B, Hq, Hkv, L_max, d, num_splits, int(bool(ragged))))
+
+
+def fd_topdelta_workspace_size(B, Hq, Hkv, L_max, d, num_splits=0) -> int:
+    return int(load().fd_topdelta_workspace_size(B, Hq, Hkv, L_max, d, num_splits))
+
+
+def _workspace(nbytes, device, workspace):
+    if nbytes == 0:
+        return workspace
+    if workspace is None:
+        return torch.empty(nbytes, dtype=torch.uint8, device=device)
+    _check_cuda(workspace, "workspace")
+    _need(workspace.numel() * workspace.element_size() >= nbytes, "workspace too small")
+    return workspace
+
+
+def _outputs(B, Hq, d, device, out, lse, out_dtype, want_lse):
+    code, tdt = _out_code(out_dtype)
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=tdt, device=device)
+    _check_cuda(out, "out", tdt, (B, Hq, d))
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=device)
+    if lse is not None:
+        _check_cuda(lse, "lse", torch.float32, (B, Hq))
+    return code, out, lse
+
+
+def fd_decode_dense(q, k, v, seq_lens=None, scale=None, num_splits=0, out=None, lse=None,
+                    out_dtype="bf16", want_lse=True, workspace=None, stream=None):
+    """Dense split-KV decode.  q [B,Hq,d] bf16; k, v [B,Hkv,L_max,d] bf16;
+    seq_lens [B] int32 or None.  Returns (out [B,Hq,d], lse [B,Hq] or None)."""
+    lib = load()
+    _check_cuda(q, "q", torch.bfloat16)
+    B, Hq, d = q.shape
+    _check_cuda(k, "k", torch.bfloat16)
+    _need(k.dim() == 4 and k.shape[0] == B and k.shape[3] == d, "k must be [B, Hkv, L_max, d]")
+    _, Hkv, L_max, _ = k.shape
+    _check_cuda(v, "v", torch.bfloat16, k.shape)
+    if seq_lens is not None:
+        _check_cuda(seq_lens, "seq_lens", torch.int32, (B,))
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    code, out, lse = _outputs(B, Hq, d, q.device, out, lse, out_dtype, want_lse)
+    need = fd_decode_workspace_size(B, Hq, Hkv, L_max, d, num_splits, seq_lens is not None)
+    ws = _workspace(need, q.device, workspace)
+    st = lib.fd_decode_dense(_p(q), _p(k), _p(v), _p(seq_lens), B, Hq, Hkv, L_max, d, scale,
+                             int(num_splits), _p(out), code, _p(lse), _p(ws),
+                             0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
+    _raise(st, "fd_decode_dense")
+    return out, lse
+
+
+def fd_decode_paged(q, k_pages, v_pages, page_table, num_pages, seq_lens, scale=None, num_splits=0,
+                    out=None, lse=None, out_dtype="bf16", want_lse=True, workspace=None, stream=None):
+    """Paged split-KV decode.  k_pages/v_pages [P,Hkv,64,d] bf16,
+    page_table [B,max_pages] int32, seq_lens [B] int32."""
+    lib = load()
+    _check_cuda(q, "q", torch.bfloat16)
+    B, Hq, d = q.shape
+    _check_cuda(k_pages, "k_pages", torch.bfloat16)
+    _need(k_pages.dim() == 4 and k_pages.shape[3] == d, "k_pages must be [P, Hkv, page, d]")
+    _, Hkv, page_size, _ = k_pages.shape
+    _check_cuda(v_pages, "v_pages", torch.bfloat16, k_pages.shape)
+    _check_cuda(page_table, "page_table", torch.int32)
+    _need(page_table.dim() == 2 and page_table.shape[0] == B, "page_table must be [B, max_pages]")
+    max_pages = page_table.shape[1]
+    _check_cuda(seq_lens, "seq_lens", torch.int32, (B,))
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    code, out, lse = _outputs(B, Hq, d, q.device, out, lse, out_dtype, want_lse)
+    need = fd_decode_workspace_size(B, Hq, Hkv, max_pages * page_size, d, num_splits, True)
+    ws = _workspace(need, q.device, workspace)
+    st = lib.fd_decode_paged(_p(q), _p(k_pages), _p(v_pages), _p(page_table), max_pages, int(num_pages),
+                             _p(seq_lens), page_size, B, Hq, Hkv, d, scale, int(num_splits), _p(out), code,
+                             _p(lse), _p(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+                             _stream(stream))
+    _raise(st, "fd_decode_paged")
+    return out, lse
+
+
+def fd_quantize_keys(k, seq_lens=None, codes=None, mn_scale=None, res=None, res_scale=None, stream=None):
+    """Key encoder.  Returns (codes u8 [B,Hkv,L,d/4], mn_scale fp16 [B,Hkv,L,d/32,2],
+    res int8 [B,Hkv,L,d], res_scale fp16 [B,Hkv,L,d/32])."""
+    lib = load()
+    _check_cuda(k, "k", torch.bfloat16)
+    B, Hkv, L_max, d = k.shape
+    dev = k.device
+    if codes is None:
+        codes = torch.zeros((B, Hkv, L_max, d // 4), dtype=torch.uint8, device=dev)
+    if mn_scale is None:
+        mn_scale = torch.zeros((B, Hkv, L_max, d // 32, 2), dtype=torch.float16, device=dev)
+    if res is None:
+        res = torch.zeros((B, Hkv, L_max, d), dtype=torch.int8, device=dev)
+    if res_scale is None:
+        res_scale = torch.zeros((B, Hkv, L_max, d // 32), dtype=torch.float16, device=dev)
+    _check_cuda(codes, "codes", torch.uint8, (B, Hkv, L_max, d // 4))
+    _check_cuda(mn_scale, "mn_scale", torch.float16, (B, Hkv, L_max, d // 32, 2))
+    _check_cuda(res, "res", torch.int8, (B, Hkv, L_max, d))
+    _check_cuda(res_scale, "res_scale", torch.float16, (B, Hkv, L_max, d // 32))
+    if seq_lens is not None:
+        _check_cuda(seq_lens, "seq_lens", torch.int32, (B,))
+    st = lib.fd_quantize_keys(_p(k), _p(seq_lens), B, Hkv, L_max, d, _p(codes), _p(mn_scale), _p(res),
+                              _p(res_scale), _stream(stream))
+    _raise(st, "fd_quantize_keys")
+    return codes, mn_scale, res, res_scale
+
+
+def fd_decode_topdelta(q, codes, mn_scale, res, res_scale, v, seq_lens=None, scale=None, delta=5.0,
+                       n_sink=4, window=64, num_splits=0, out=None, lse=None, out_dtype="bf16",
+                       want_lse=True, sel_mask=None, sel_count=None, want_selection=False,
+                       workspace=None, stream=None):
+    """Top-delta sparse decode over fd_quantize_keys' outputs.  Returns
+    (out, lse, sel_mask or None, sel_count or None)."""
+    lib = load()
+    _check_cuda(q, "q", torch.bfloat16)
+    B, Hq, d = q.shape
+    _check_cuda(v, "v", torch.bfloat16)
+    _need(v.dim() == 4 and v.shape[0] == B and v.shape[3] == d, "v must be [B, Hkv, L_max, d]")
+    _, Hkv, L_max, _ = v.shape
+    _check_cuda(codes, "codes", torch.uint8, (B, Hkv, L_max, d // 4))
+    _check_cuda(mn_scale, "mn_scale", torch.float16, (B, Hkv, L_max, d // 32, 2))
+    _check_cuda(res, "res", torch.int8, (B, Hkv, L_max, d))
+    _check_cuda(res_scale, "res_scale", torch.float16, (B, Hkv, L_max, d // 32))
+    if seq_lens is not None:
+        _check_cuda(seq_lens, "seq_lens", torch.int32, (B,))
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    delta = math.inf if delta is None else float(delta)
+    code, out, lse = _outputs(B, Hq, d, q.device, out, lse, out_dtype, want_lse)
+    words = (L_max + 31) // 32
+    if want_selection and sel_mask is None:
+        sel_mask = torch.empty((B, Hq, words), dtype=torch.int32, device=q.device)
+    if want_selection and sel_count is None:
+        sel_count = torch.empty((B, Hq), dtype=torch.int32, device=q.device)
+    if sel_mask is not None:
+        _check_cuda(sel_mask, "sel_mask", torch.int32, (B, Hq, words))
+    if sel_count is not None:
+        _check_cuda(sel_count, "sel_count", torch.int32, (B, Hq))
+    need = fd_topdelta_workspace_size(B, Hq, Hkv, L_max, d, num_splits)
+    ws = _workspace(need, q.device, workspace)
+    st = lib.fd_decode_topdelta(_p(q), _p(codes), _p(mn_scale), _p(res), _p(res_scale), _p(v), _p(seq_lens),
+                                B, Hq, Hkv, L_max, d, scale, delta, int(n_sink), int(window), int(num_splits),
+                                _p(out), code, _p(lse), _p(sel_mask), _p(sel_count), _p(ws),
+                                0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
+    _raise(st, "fd_decode_topdelta")
+    return out, lse, sel_mask, sel_count
+
+
+def fd_device_status(clear=True, stream=None) -> int:
+    """Synchronises the stream and returns the device status (FD_OK or an FD_ERR_* code)."""
+    return int(load().fd_device_status(int(bool(clear)), _stream(stream)))

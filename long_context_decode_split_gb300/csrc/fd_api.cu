@@ -1,0 +1,304 @@
+// fd_api.cu -- the extern "C" entry points declared in include/fd.h: host-side
+// argument checks, the split planner and the dispatch to the kernels.  No
+// entry point allocates memory or synchronises (except fd_device_status).
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "fd.h"
+#include "fd_internal.h"
+
+namespace {
+
+using fd::kTile;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int current_sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return -1;
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    return n;
+}
+
+int check_shape(int B, int Hq, int Hkv, int L_max, int d) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || L_max < 0) return FD_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return FD_ERR_INVALID_ARG;
+    if (B > 65535 || Hkv > 65535 || L_max > (1 << 30)) return FD_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FD_ERR_UNSUPPORTED;
+    if (Hq / Hkv > 8) return FD_ERR_UNSUPPORTED;
+    return FD_OK;
+}
+
+// Chunk plan shared by the planner queries, the workspace sizes and the
+// launches.  `chunk_fixed` = 0 means per-sequence chunks of
+// ceil(L_b / splits) rounded up to 64 tokens.
+struct Plan {
+    int splits;
+    int chunk_fixed;
+};
+
+// The "Flash Decoding" tutorial (section 6, misconception 2) asks for a chunk
+// count that keeps every compute unit busy, chunks of at least a few hundred
+// tokens, and no more chunks than that: each costs merge work.  Here that is
+// a small cost model over whole 64-token tiles:
+//   time(S) ~ waves(S) * tiles_per_chunk(S) + merge(S)
+// with waves = ceil(units * S / resident CTAs).  Uniform batches take the
+// minimum exactly.  Ragged batches (lengths unknown on the host) take chunks
+// small enough that the longest sequences span many waves, so the hardware
+// block scheduler can even out the load.
+Plan plan(int B, int Hkv, int L_max, int requested, bool ragged, int ctas_per_sm, int sms) {
+    Plan pl{1, 0};
+    if (requested > 0) {
+        pl.splits = requested;
+        return pl;
+    }
+    const int tiles = (L_max + kTile - 1) / kTile;
+    if (tiles <= 4 || sms <= 0) return pl;
+    const long units = (long)B * Hkv;
+    const long slots = (long)sms * (ctas_per_sm > 0 ? ctas_per_sm : 1);
+    const int min_chunk_tiles = 4;  // 256 tokens
+    int best_chunk = tiles;
+    if (!ragged) {
+        double best = 1e300;
+        const int max_s = tiles / min_chunk_tiles;
+        for (int S = 1; S <= max_s; ++S) {
+            const int ct = (tiles + S - 1) / S;
+            const int s_eff = (tiles + ct - 1) / ct;
+            if (s_eff != S) continue;  // same chunk as a smaller S
+            const long waves = (units * s_eff + slots - 1) / slots;
+            const double cost = (double)waves * ct + (s_eff > 1 ? 2.0 : 0.0) + 0.02 * s_eff;
+            if (cost < best - 1e-9) {
+                best = cost;
+                best_chunk = ct;
+            }
+        }
+    } else {
+        // aim at ~16 waves for sequences of length L_max, chunks of 8..64 tiles
+        long ct = (units * tiles + 16 * slots - 1) / (16 * slots);
+        if (ct < 8) ct = 8;
+        if (ct > 64) ct = 64;
+        if (ct > tiles) ct = tiles;
+        best_chunk = (int)ct;
+    }
+    pl.chunk_fixed = best_chunk * kTile;
+    pl.splits = (L_max + pl.chunk_fixed - 1) / pl.chunk_fixed;
+    if (pl.splits <= 1) pl = Plan{1, 0};
+    return pl;
+}
+
+Plan decode_plan(int B, int Hq, int Hkv, int L_max, int d, int requested, bool ragged) {
+    const int sms = current_sm_count();
+    const int occ = requested > 0 ? 1 : fd::decode_ctas_per_sm(d, Hq / Hkv, ragged);
+    return plan(B, Hkv, L_max, requested, ragged, occ, sms);
+}
+
+Plan topdelta_plan(int B, int Hq, int Hkv, int L_max, int d, int requested) {
+    const int sms = current_sm_count();
+    const int occ = requested > 0 ? 1 : fd::topdelta_ctas_per_sm(d, Hq / Hkv);
+    return plan(B, Hkv, L_max, requested, false, occ, sms);
+}
+
+int to_status(cudaError_t e) { return e == cudaSuccess ? FD_OK : FD_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int fd_abi_version(void) { return FD_ABI_VERSION; }
+
+const char* fd_status_string(int status) {
+    switch (status) {
+        case FD_OK: return "FD_OK";
+        case FD_ERR_INVALID_ARG: return "FD_ERR_INVALID_ARG: invalid argument";
+        case FD_ERR_UNSUPPORTED: return "FD_ERR_UNSUPPORTED: shape not supported (d, group size or page size)";
+        case FD_ERR_WORKSPACE_TOO_SMALL: return "FD_ERR_WORKSPACE_TOO_SMALL: workspace smaller than required";
+        case FD_ERR_BAD_PAGE_TABLE: return "FD_ERR_BAD_PAGE_TABLE: a page id was outside the page pool";
+        case FD_ERR_CUDA: return "FD_ERR_CUDA: a CUDA call failed";
+        case FD_ERR_DEVICE_TIMEOUT: return "FD_ERR_DEVICE_TIMEOUT: a kernel pipeline wait hit its time limit";
+        default: return "unknown fd_status";
+    }
+}
+
+int fd_num_splits(int B, int Hq, int Hkv, int L_max, int d, int num_splits, int ragged) {
+    const int st = check_shape(B, Hq, Hkv, L_max, d);
+    if (st != FD_OK) return -st;
+    if (num_splits < 0) return -FD_ERR_INVALID_ARG;
+    return decode_plan(B, Hq, Hkv, L_max, d, num_splits, ragged != 0).splits;
+}
+
+size_t fd_decode_workspace_size(int B, int Hq, int Hkv, int L_max, int d, int num_splits, int ragged) {
+    if (check_shape(B, Hq, Hkv, L_max, d) != FD_OK || num_splits < 0) return 0;
+    const Plan pl = decode_plan(B, Hq, Hkv, L_max, d, num_splits, ragged != 0);
+    return fd::decode_workspace_bytes(B, Hq, d, pl.splits);
+}
+
+static int decode_common(fd::DecodeArgs& a, int num_splits, bool ragged, int out_dtype, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+    if (out_dtype != FD_OUT_F32 && out_dtype != FD_OUT_BF16) return FD_ERR_INVALID_ARG;
+    if (num_splits < 0 || !std::isfinite(a.scale)) return FD_ERR_INVALID_ARG;
+    if (a.B > 0 && (!a.q || !a.k || !a.v || !a.out)) return FD_ERR_INVALID_ARG;
+    if (!aligned16(a.q) || !aligned16(a.k) || !aligned16(a.v) || !aligned16(a.out)) return FD_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(a.lse) & 3u) || (reinterpret_cast<uintptr_t>(a.seq_lens) & 3u))
+        return FD_ERR_INVALID_ARG;
+    const Plan pl = decode_plan(a.B, a.Hq, a.Hkv, a.L_max, a.D, num_splits, ragged);
+    const size_t need = fd::decode_workspace_bytes(a.B, a.Hq, a.D, pl.splits);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return FD_ERR_WORKSPACE_TOO_SMALL;
+        if (!aligned16(workspace)) return FD_ERR_INVALID_ARG;
+    }
+    a.splits = pl.splits;
+    a.chunk_fixed = pl.chunk_fixed;
+    a.out_bf16 = out_dtype == FD_OUT_BF16;
+    float* ws = static_cast<float*>(workspace);
+    a.part_o = ws;
+    a.part_ml = ws ? ws + (size_t)a.B * a.Hq * pl.splits * a.D : nullptr;
+    return to_status(fd::launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+int fd_decode_dense(const void* q, const void* k, const void* v, const int32_t* seq_lens,
+                    int B, int Hq, int Hkv, int L_max, int d, float scale, int num_splits,
+                    void* out, int out_dtype, float* lse,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+    const int st = check_shape(B, Hq, Hkv, L_max, d);
+    if (st != FD_OK) return st;
+    fd::DecodeArgs a = {};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.seq_lens = seq_lens;
+    a.page_table = nullptr;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.L_max = L_max;
+    a.D = d;
+    a.scale = scale;
+    a.out = out;
+    a.lse = lse;
+    return decode_common(a, num_splits, seq_lens != nullptr, out_dtype, workspace, workspace_bytes, stream);
+}
+
+int fd_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                    const int32_t* page_table, int max_pages, int num_pages,
+                    const int32_t* seq_lens, int page_size,
+                    int B, int Hq, int Hkv, int d, float scale, int num_splits,
+                    void* out, int out_dtype, float* lse,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+    if (page_size != kTile) return page_size > 0 ? FD_ERR_UNSUPPORTED : FD_ERR_INVALID_ARG;
+    if (max_pages <= 0 || num_pages < 0 || max_pages > (1 << 24)) return FD_ERR_INVALID_ARG;
+    const int L_max = max_pages * page_size;
+    const int st = check_shape(B, Hq, Hkv, L_max, d);
+    if (st != FD_OK) return st;
+    if (B > 0 && (!page_table || !seq_lens)) return FD_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(page_table) & 3u) return FD_ERR_INVALID_ARG;
+    fd::DecodeArgs a = {};
+    a.q = q;
+    a.k = k_pages;
+    a.v = v_pages;
+    a.seq_lens = seq_lens;
+    a.page_table = page_table;
+    a.max_pages = max_pages;
+    a.num_pages = num_pages;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.L_max = L_max;
+    a.D = d;
+    a.scale = scale;
+    a.out = out;
+    a.lse = lse;
+    return decode_common(a, num_splits, true, out_dtype, workspace, workspace_bytes, stream);
+}
+
+int fd_quantize_keys(const void* k, const int32_t* seq_lens, int B, int Hkv, int L_max, int d,
+                     uint8_t* codes, void* mn_scale, int8_t* res, void* res_scale, void* stream) {
+    const int st = check_shape(B, Hkv, Hkv, L_max, d);
+    if (st != FD_OK) return st;
+    if (B > 0 && L_max > 0 && (!k || !codes || !mn_scale || !res || !res_scale)) return FD_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(codes) || !aligned16(mn_scale) || !aligned16(res) || !aligned16(res_scale))
+        return FD_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(seq_lens) & 3u) return FD_ERR_INVALID_ARG;
+    fd::QuantArgs a = {k, seq_lens, B, Hkv, L_max, d, codes, mn_scale, res, res_scale};
+    return to_status(fd::launch_quantize(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t fd_topdelta_workspace_size(int B, int Hq, int Hkv, int L_max, int d, int num_splits) {
+    if (check_shape(B, Hq, Hkv, L_max, d) != FD_OK || num_splits < 0) return 0;
+    const Plan pl = topdelta_plan(B, Hq, Hkv, L_max, d, num_splits);
+    return fd::decode_workspace_bytes(B, Hq, d, pl.splits);
+}
+
+int fd_decode_topdelta(const void* q, const uint8_t* codes, const void* mn_scale, const int8_t* res,
+                       const void* res_scale, const void* v, const int32_t* seq_lens,
+                       int B, int Hq, int Hkv, int L_max, int d, float scale, float delta,
+                       int n_sink, int window, int num_splits,
+                       void* out, int out_dtype, float* lse, uint32_t* sel_mask, int32_t* sel_count,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+    const int st = check_shape(B, Hq, Hkv, L_max, d);
+    if (st != FD_OK) return st;
+    if (out_dtype != FD_OUT_F32 && out_dtype != FD_OUT_BF16) return FD_ERR_INVALID_ARG;
+    if (num_splits < 0 || !std::isfinite(scale) || std::isnan(delta) || delta < 0.f) return FD_ERR_INVALID_ARG;
+    if (n_sink < 0 || window < 0) return FD_ERR_INVALID_ARG;
+    if (B > 0 && (!q || !codes || !mn_scale || !res || !res_scale || !v || !out)) return FD_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(codes) || !aligned16(mn_scale) || !aligned16(res) || !aligned16(res_scale) ||
+        !aligned16(v) || !aligned16(out))
+        return FD_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
+        (reinterpret_cast<uintptr_t>(sel_mask) & 3u) || (reinterpret_cast<uintptr_t>(sel_count) & 3u))
+        return FD_ERR_INVALID_ARG;
+    const Plan pl = topdelta_plan(B, Hq, Hkv, L_max, d, num_splits);
+    const size_t need = fd::decode_workspace_bytes(B, Hq, d, pl.splits);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return FD_ERR_WORKSPACE_TOO_SMALL;
+        if (!aligned16(workspace)) return FD_ERR_INVALID_ARG;
+    }
+    fd::TopDeltaArgs a = {};
+    a.q = q;
+    a.codes = codes;
+    a.mn_scale = mn_scale;
+    a.res = res;
+    a.res_scale = res_scale;
+    a.v = v;
+    a.seq_lens = seq_lens;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.L_max = L_max;
+    a.D = d;
+    a.scale = scale;
+    a.delta = delta;
+    a.n_sink = n_sink;
+    a.window = window;
+    a.splits = pl.splits;
+    a.chunk_fixed = pl.chunk_fixed;
+    a.out = out;
+    a.out_bf16 = out_dtype == FD_OUT_BF16;
+    a.lse = lse;
+    a.sel_mask = sel_mask;
+    a.sel_count = sel_count;
+    float* ws = static_cast<float*>(workspace);
+    a.part_o = ws;
+    a.part_ml = ws ? ws + (size_t)B * Hq * pl.splits * d : nullptr;
+    return to_status(fd::launch_topdelta(a, static_cast<cudaStream_t>(stream)));
+}
+
+int fd_device_status(int clear, void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FD_ERR_CUDA;
+    unsigned a = 0, b = 0;
+    if (fd::decode_status_read(&a, clear != 0) != cudaSuccess) return FD_ERR_CUDA;
+    if (fd::topdelta_status_read(&b, clear != 0) != cudaSuccess) return FD_ERR_CUDA;
+    const unsigned bits = a | b;
+    if (bits & 2u) return FD_ERR_DEVICE_TIMEOUT;
+    if (bits & 1u) return FD_ERR_BAD_PAGE_TABLE;
+    if (bits & 4u) return FD_ERR_INVALID_ARG;
+    return FD_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,555 @@
+// fd_decode.cu -- split-KV decode attention ("Flash Decoding" tutorial,
+// sections 1-3) for sm_103a: the per-chunk partial pass over a contiguous or
+// paged bf16 KV cache, and the exact log-sum-exp merge of the chunks.
+//
+// Partial pass, one CTA per (chunk, KV head, sequence):
+//   * warp CW (the producer) streams the chunk's K and V through a STAGES-deep
+//     ring of 64-token shared-memory tiles with bulk asynchronous copies
+//     (cp.async.bulk + mbarrier transaction counts).  A tile is one contiguous
+//     64-row slab in both layouts: a slice of [L, d] rows, or one cache page.
+//   * warps 0..CW-1 (the consumers) each own 64/CW rows of every tile and
+//     keep, for every query head of the GQA group, a running max m, exp-sum l
+//     and output accumulator o in registers (online softmax in base 2).  So
+//     every K/V byte is read from HBM once per KV head, whatever the group
+//     size.  Dot products run on packed fp32x2 FMAs; per-row partial sums are
+//     combined by a transposing butterfly (one shuffle per token per query).
+//   * at the end the consumer warps combine their states through shared
+//     memory and write either the final output (one chunk) or the chunk's
+//     (m_i, l_i, O_i / l_i) to the workspace.
+// Merge, one CTA per (sequence, query head): m = max_i m_i,
+//   w_i = 2^(m_i - m) l_i, out = sum_i w_i O_i / sum_i w_i, lse = m + log sum w.
+// The merge is launched with programmatic dependent launch so its launch
+// overlaps the tail of the partial pass.
+#include <cmath>
+#include <cstdio>
+
+#include "fd_device.cuh"
+#include "fd_internal.h"
+
+namespace fd {
+
+__device__ unsigned int g_status_decode;
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxDevices = 64;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Static geometry of the partial pass for head dim D, padded group GP and CW
+// consumer warps.
+template <int D, int GP, int CW>
+struct Geo {
+    static constexpr int LPR = D / 8;           // lanes per K/V row (16 B each)
+    static constexpr int RPI = 32 / LPR;        // rows per warp-wide load
+    static constexpr int TPW = kTile / CW;      // rows of a tile owned by one warp
+    static constexpr int NIT = TPW / RPI;       // loads per warp per tile
+    static constexpr int LOG_LPR = D == 128 ? 4 : 3;
+    static constexpr int LOG_NIT = NIT == 16 ? 4 : NIT == 8 ? 3 : NIT == 4 ? 2 : NIT == 2 ? 1 : 0;
+    static constexpr int SH = LOG_LPR - LOG_NIT;  // low lane bits that hold copies
+    static constexpr int TILE_BYTES = kTile * D * 2;
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K tile + V tile
+    static_assert(NIT >= 1 && NIT <= LPR, "bad warp split");
+    static_assert((1 << LOG_NIT) == NIT, "NIT must be a power of two");
+};
+
+template <int D>
+constexpr int stages_for() { return D == 128 ? 3 : 4; }
+
+template <int D, int GP, int CW, int STAGES>
+constexpr int partial_smem_bytes() {
+    // stage ring, then barriers and per-stage row counts
+    return STAGES * Geo<D, GP, CW>::STAGE_BYTES + STAGES * 16 + STAGES * 4 + 64;
+}
+
+// Chunk length in tokens for a sequence of length L.
+__device__ __forceinline__ int chunk_len(int L, int splits, int chunk_fixed) {
+    if (chunk_fixed > 0) return chunk_fixed;
+    int c = (L + splits - 1) / splits;
+    c = (c + kTile - 1) / kTile * kTile;
+    return c > 0 ? c : kTile;
+}
+
+// Butterfly over the LPR lanes of a row group that both sums the per-lane
+// partial dot products and transposes them: on entry lane l holds N partial
+// sums (one per row it touched), on exit it holds the full sum of the row
+// with index (l >> SH) & (N-1).
+template <int N, int LPR>
+__device__ __forceinline__ float transpose_reduce(float (&v)[N], int lane) {
+#pragma unroll
+    for (int n = N, o = LPR / 2; n > 1; n >>= 1, o >>= 1) {
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int k = 0; k < n / 2; ++k) {
+            const float send = upper ? v[k] : v[k + n / 2];
+            const float keep = upper ? v[k + n / 2] : v[k];
+            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    float r = v[0];
+#pragma unroll
+    for (int o = LPR / N / 2; o >= 1; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+    return r;
+}
+
+struct PartialParams {
+    const uint16_t* q;
+    const uint16_t* k;
+    const uint16_t* v;
+    const int32_t* seq_lens;
+    const int32_t* page_table;
+    int max_pages, num_pages;
+    int Hq, Hkv, L_max, G;
+    float scale_log2;
+    int splits, chunk_fixed;
+    float* part_o;
+    float* part_ml;
+    void* out;
+    int out_bf16;
+    float* lse;
+    int direct;  // one chunk: write the final output
+};
+
+template <int D, int GP, int CW, int STAGES, bool PAGED>
+__global__ void __launch_bounds__((CW + 1) * 32, 1)
+partial_kernel(const PartialParams p) {
+    using Gm = Geo<D, GP, CW>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * Gm::STAGE_BYTES);
+    uint64_t* empty = full + STAGES;
+    int* stage_rows = reinterpret_cast<int*>(empty + STAGES);
+
+    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int L = clamped_len(p.seq_lens, b, p.L_max, &g_status_decode);
+    const int chunk = chunk_len(L, p.splits, p.chunk_fixed);
+    const int t0 = split * chunk;
+    const int t1 = min(L, t0 + chunk);
+    const int hq0 = h * p.G;
+
+    if (t0 >= t1) {
+        pdl_launch_dependents();
+        // An empty chunk writes nothing, except that the only chunk of an
+        // empty sequence writes out = 0, lse = -inf.
+        if (p.direct && split == 0) {
+            for (int i = threadIdx.x; i < p.G * D; i += blockDim.x) {
+                const size_t o = (size_t)(b * p.Hq + hq0 + i / D) * D + (i % D);
+                if (p.out_bf16) static_cast<uint16_t*>(p.out)[o] = 0;
+                else static_cast<float*>(p.out)[o] = 0.f;
+            }
+            if (p.lse && threadIdx.x < p.G) p.lse[b * p.Hq + hq0 + threadIdx.x] = -INFINITY;
+        }
+        return;
+    }
+    const int ntiles = (t1 - t0 + kTile - 1) / kTile;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], CW);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == CW) {
+        // ---------------- producer: one lane issues all bulk copies --------
+        if (lane == 0) {
+            const uint64_t pol = l2_evict_first_policy();
+            const size_t head_rows = PAGED ? 0 : ((size_t)b * p.Hkv + h) * (size_t)p.L_max;
+            for (int t = 0; t < ntiles; ++t) {
+                const int s = t % STAGES;
+                const uint32_t ph = (uint32_t)(t / STAGES) & 1u;
+                if (!mbar_wait(&empty[s], ph ^ 1u)) {
+                    atomicOr(&g_status_decode, kStatusTimeout);
+                    break;
+                }
+                const int tok = t0 + t * kTile;
+                const int rows = min(kTile, t1 - tok);
+                size_t row0;
+                bool ok = true;
+                if (PAGED) {
+                    const int pg = p.page_table[(size_t)b * p.max_pages + tok / kTile];
+                    ok = pg >= 0 && pg < p.num_pages;
+                    row0 = ((size_t)(ok ? pg : 0) * p.Hkv + h) * kTile;
+                } else {
+                    row0 = head_rows + tok;
+                }
+                unsigned char* sk = smem + s * Gm::STAGE_BYTES;
+                if (ok) {
+                    stage_rows[s] = rows;
+                    const uint32_t bytes = (uint32_t)rows * D * 2;
+                    mbar_arrive_expect_tx(&full[s], 2 * bytes);
+                    bulk_g2s(sk, p.k + row0 * D, bytes, &full[s], pol);
+                    bulk_g2s(sk + Gm::TILE_BYTES, p.v + row0 * D, bytes, &full[s], pol);
+                } else {
+                    atomicOr(&g_status_decode, kStatusBadPage);
+                    stage_rows[s] = 0;
+                    mbar_arrive(&full[s]);
+                }
+            }
+        }
+        pdl_launch_dependents();
+        return;
+    }
+
+    // ------------------------ consumers ------------------------------------
+    const int c = lane % Gm::LPR;   // 16-byte column of a row
+    const int rg = lane / Gm::LPR;  // row group within a warp-wide load
+    // my token slot after the transposing reduction
+    const int my_i = (lane >> Gm::SH) & (Gm::NIT - 1);
+    const int my_row = warp * Gm::TPW + Gm::RPI * my_i + rg;
+    const bool my_dup = (lane & ((1 << Gm::SH) - 1)) != 0;
+
+    float2 qv[GP][4];
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+        if (g < p.G) {
+            const uint4 w = *reinterpret_cast<const uint4*>(p.q + (size_t)(b * p.Hq + hq0 + g) * D + c * 8);
+            qv[g][0] = bf16x2_to_float2(w.x);
+            qv[g][1] = bf16x2_to_float2(w.y);
+            qv[g][2] = bf16x2_to_float2(w.z);
+            qv[g][3] = bf16x2_to_float2(w.w);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) qv[g][e] = make_float2(0.f, 0.f);
+        }
+    }
+
+    float m_run[GP], l_lane[GP];
+    float2 o[GP][4];
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+        m_run[g] = -INFINITY;
+        l_lane[g] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[g][e] = make_float2(0.f, 0.f);
+    }
+
+    bool failed = false;
+    for (int t = 0; t < ntiles && !failed; ++t) {
+        const int s = t % STAGES;
+        const uint32_t ph = (uint32_t)(t / STAGES) & 1u;
+        if (!mbar_wait(&full[s], ph)) {
+            atomicOr(&g_status_decode, kStatusTimeout);
+            failed = true;
+            break;
+        }
+        const int rows = stage_rows[s];
+        const unsigned char* sk = smem + s * Gm::STAGE_BYTES;
+        const unsigned char* sv = sk + Gm::TILE_BYTES;
+
+        // ---- scores: partial dots over my 8 dims, then butterfly -----------
+        float part[GP][Gm::NIT];
+#pragma unroll
+        for (int i = 0; i < Gm::NIT; ++i) {
+            const int row = warp * Gm::TPW + Gm::RPI * i + rg;
+            const uint4 w = lds128(sk + (row * D + c * 8) * 2);
+            const float2 k0 = bf16x2_to_float2(w.x), k1 = bf16x2_to_float2(w.y);
+            const float2 k2 = bf16x2_to_float2(w.z), k3 = bf16x2_to_float2(w.w);
+#pragma unroll
+            for (int g = 0; g < GP; ++g) {
+                float2 acc = f2mul(qv[g][0], k0);
+                acc = f2fma(qv[g][1], k1, acc);
+                acc = f2fma(qv[g][2], k2, acc);
+                acc = f2fma(qv[g][3], k3, acc);
+                part[g][i] = acc.x + acc.y;
+            }
+        }
+        float sc[GP];
+        const bool my_valid = my_row < rows;
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+            const float sum = transpose_reduce<Gm::NIT, Gm::LPR>(part[g], lane);
+            sc[g] = my_valid ? sum * p.scale_log2 : -INFINITY;
+        }
+
+        // ---- online softmax update -----------------------------------------
+        float pr[GP];
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+            float mx = sc[g];
+#pragma unroll
+            for (int off = 16; off >= (1 << Gm::SH); off >>= 1)
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            const float m_new = fmaxf(m_run[g], mx);
+            if (m_new == -INFINITY) {  // nothing valid yet (warp-uniform)
+                pr[g] = 0.f;
+                continue;
+            }
+            const float alpha = exp2_approx(m_run[g] - m_new);
+            m_run[g] = m_new;
+            pr[g] = exp2_approx(sc[g] - m_new);
+            l_lane[g] = l_lane[g] * alpha + (my_dup ? 0.f : pr[g]);
+            const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[g][e] = f2mul(o[g][e], a2);
+        }
+
+        // ---- o += p * v over my rows --------------------------------------
+#pragma unroll
+        for (int i = 0; i < Gm::NIT; ++i) {
+            const int row = warp * Gm::TPW + Gm::RPI * i + rg;
+            const int src = rg * Gm::LPR + (i << Gm::SH);
+            float pi[GP];
+#pragma unroll
+            for (int g = 0; g < GP; ++g) pi[g] = __shfl_sync(0xffffffffu, pr[g], src);
+            if (row < rows) {
+                const uint4 w = lds128(sv + (row * D + c * 8) * 2);
+                const float2 v0 = bf16x2_to_float2(w.x), v1 = bf16x2_to_float2(w.y);
+                const float2 v2 = bf16x2_to_float2(w.z), v3 = bf16x2_to_float2(w.w);
+#pragma unroll
+                for (int g = 0; g < GP; ++g) {
+                    const float2 p2 = make_float2(pi[g], pi[g]);
+                    o[g][0] = f2fma(p2, v0, o[g][0]);
+                    o[g][1] = f2fma(p2, v1, o[g][1]);
+                    o[g][2] = f2fma(p2, v2, o[g][2]);
+                    o[g][3] = f2fma(p2, v3, o[g][3]);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    pdl_launch_dependents();
+
+    // ---- reduce within the warp: l over all lanes, o over row groups ------
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) l_lane[g] += __shfl_xor_sync(0xffffffffu, l_lane[g], off);
+#pragma unroll
+        for (int off = 16; off >= Gm::LPR; off >>= 1) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                o[g][e].x += __shfl_xor_sync(0xffffffffu, o[g][e].x, off);
+                o[g][e].y += __shfl_xor_sync(0xffffffffu, o[g][e].y, off);
+            }
+        }
+    }
+
+    // ---- combine the consumer warps through shared memory -----------------
+    named_barrier(1, CW * 32);  // every consumer is done with the stage ring
+    float* red_o = reinterpret_cast<float*>(smem);            // [CW][GP][D]
+    float* red_m = red_o + CW * GP * D;                       // [CW][GP]
+    float* red_l = red_m + CW * GP;                           // [CW][GP]
+    if (lane < Gm::LPR) {
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+            float4* dst = reinterpret_cast<float4*>(red_o + (warp * GP + g) * D + c * 8);
+            dst[0] = make_float4(o[g][0].x, o[g][0].y, o[g][1].x, o[g][1].y);
+            dst[1] = make_float4(o[g][2].x, o[g][2].y, o[g][3].x, o[g][3].y);
+        }
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+            red_m[warp * GP + g] = failed ? -INFINITY : m_run[g];
+            red_l[warp * GP + g] = failed ? 0.f : l_lane[g];
+        }
+    }
+    named_barrier(1, CW * 32);
+
+    const int nthr = CW * 32;
+    for (int idx = threadIdx.x; idx < p.G * D; idx += nthr) {
+        const int g = idx / D, dim = idx % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < CW; ++w) M = fmaxf(M, red_m[w * GP + g]);
+        float lsum = 0.f, acc = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < CW; ++w) {
+                const float mw = red_m[w * GP + g];
+                const float sc = mw == -INFINITY ? 0.f : exp2_approx(mw - M);
+                lsum += sc * red_l[w * GP + g];
+                acc += sc * red_o[(w * GP + g) * D + dim];
+            }
+        }
+        const int row = b * p.Hq + hq0 + g;
+        const float val = lsum > 0.f ? acc / lsum : 0.f;
+        if (p.direct) {
+            const size_t oi = (size_t)row * D + dim;
+            if (p.out_bf16) static_cast<uint16_t*>(p.out)[oi] = f32_to_bf16_bits(val);
+            else static_cast<float*>(p.out)[oi] = val;
+            if (dim == 0 && p.lse) p.lse[row] = lsum > 0.f ? (M + __log2f(lsum)) * kLn2 : -INFINITY;
+        } else {
+            const size_t pi = (size_t)row * p.splits + split;
+            p.part_o[pi * D + dim] = val;
+            if (dim == 0) {
+                p.part_ml[2 * pi + 0] = lsum > 0.f ? M : -INFINITY;
+                p.part_ml[2 * pi + 1] = lsum;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Merge: one CTA of D threads per (sequence, query head).
+template <int D>
+__global__ void __launch_bounds__(D)
+merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
+             const int32_t* __restrict__ seq_lens, int Hq, int L_max, int splits, int chunk_fixed,
+             void* __restrict__ out, int out_bf16, float* __restrict__ lse) {
+    pdl_wait_primary();
+    const int row = blockIdx.x;
+    const int b = row / Hq;
+    const int dim = threadIdx.x;
+    const int L = clamped_len(seq_lens, b, L_max, nullptr);
+    const int chunk = chunk_len(L, splits, chunk_fixed);
+    const int n = L > 0 ? min(splits, (L + chunk - 1) / chunk) : 0;
+    const float* ml = part_ml + (size_t)row * splits * 2;
+    float M = -INFINITY;
+    for (int i = 0; i < n; ++i) M = fmaxf(M, ml[2 * i]);
+    float wsum = 0.f, acc = 0.f;
+    if (M != -INFINITY) {
+        const float* po = part_o + (size_t)row * splits * D + dim;
+        for (int i = 0; i < n; ++i) {
+            const float mi = ml[2 * i];
+            if (mi == -INFINITY) continue;
+            const float w = exp2_approx(mi - M) * ml[2 * i + 1];
+            wsum += w;
+            acc += w * po[(size_t)i * D];
+        }
+    }
+    const float val = wsum > 0.f ? acc / wsum : 0.f;
+    const size_t oi = (size_t)row * D + dim;
+    if (out_bf16) static_cast<uint16_t*>(out)[oi] = f32_to_bf16_bits(val);
+    else static_cast<float*>(out)[oi] = val;
+    if (dim == 0 && lse) lse[row] = wsum > 0.f ? (M + __log2f(wsum)) * kLn2 : -INFINITY;
+}
+
+template <int D, int GP, bool PAGED>
+struct PartialLauncher {
+    // 8 consumer warps for groups of 8 keep each warp's partial sums in registers
+    static constexpr int CW = GP >= 8 ? 8 : 4;
+    static constexpr int STAGES = stages_for<D>();
+    static constexpr int SMEM = partial_smem_bytes<D, GP, CW, STAGES>();
+    static_assert(SMEM >= CW * GP * D * 4 + 2 * CW * GP * 4, "reduction scratch must fit in the ring");
+
+    // Per device: raise the dynamic shared-memory limit once, and remember
+    // the occupancy the planner sizes its grids with.
+    static cudaError_t prepare() {
+        static bool done[kMaxDevices] = {};
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < kMaxDevices && done[dev]) return cudaSuccess;
+        e = cudaFuncSetAttribute(partial_kernel<D, GP, CW, STAGES, PAGED>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+        if (e == cudaSuccess && dev < kMaxDevices) done[dev] = true;
+        return e;
+    }
+    static int ctas_per_sm() {
+        static int cache[kMaxDevices] = {};
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+        if (dev < kMaxDevices && cache[dev] > 0) return cache[dev];
+        if (prepare() != cudaSuccess) return 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, partial_kernel<D, GP, CW, STAGES, PAGED>,
+                                                          (CW + 1) * 32, SMEM) != cudaSuccess || n <= 0)
+            return 1;
+        if (dev < kMaxDevices) cache[dev] = n;
+        return n;
+    }
+    static cudaError_t launch(const PartialParams& pp, dim3 grid, cudaStream_t st) {
+        cudaError_t e = prepare();
+        if (e != cudaSuccess) return e;
+        partial_kernel<D, GP, CW, STAGES, PAGED><<<grid, (CW + 1) * 32, SMEM, st>>>(pp);
+        return cudaGetLastError();
+    }
+};
+
+template <int D, bool PAGED>
+int ctas_per_sm_dispatch(int G) {
+    if (G <= 1) return PartialLauncher<D, 1, PAGED>::ctas_per_sm();
+    if (G <= 2) return PartialLauncher<D, 2, PAGED>::ctas_per_sm();
+    if (G <= 4) return PartialLauncher<D, 4, PAGED>::ctas_per_sm();
+    return PartialLauncher<D, 8, PAGED>::ctas_per_sm();
+}
+
+template <int D, bool PAGED>
+cudaError_t launch_dispatch(int G, const PartialParams& pp, dim3 grid, cudaStream_t st) {
+    if (G <= 1) return PartialLauncher<D, 1, PAGED>::launch(pp, grid, st);
+    if (G <= 2) return PartialLauncher<D, 2, PAGED>::launch(pp, grid, st);
+    if (G <= 4) return PartialLauncher<D, 4, PAGED>::launch(pp, grid, st);
+    return PartialLauncher<D, 8, PAGED>::launch(pp, grid, st);
+}
+
+}  // namespace
+
+size_t decode_workspace_bytes(int B, int Hq, int D, int splits) {
+    if (splits <= 1) return 0;
+    const size_t rows = (size_t)B * Hq * splits;
+    return rows * D * sizeof(float) + rows * 2 * sizeof(float) + 256;
+}
+
+int decode_ctas_per_sm(int D, int G, bool paged) {
+    if (D == 128) return paged ? ctas_per_sm_dispatch<128, true>(G) : ctas_per_sm_dispatch<128, false>(G);
+    return paged ? ctas_per_sm_dispatch<64, true>(G) : ctas_per_sm_dispatch<64, false>(G);
+}
+
+cudaError_t launch_merge(const float* part_o, const float* part_ml, const int32_t* seq_lens,
+                         int B, int Hq, int L_max, int D, int splits, int chunk_fixed,
+                         void* out, int out_bf16, float* lse, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(B * Hq));
+    cfg.blockDim = dim3((unsigned)D);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (D == 128)
+        return cudaLaunchKernelEx(&cfg, merge_kernel<128>, part_o, part_ml, seq_lens, Hq, L_max, splits,
+                                  chunk_fixed, out, out_bf16, lse);
+    return cudaLaunchKernelEx(&cfg, merge_kernel<64>, part_o, part_ml, seq_lens, Hq, L_max, splits,
+                              chunk_fixed, out, out_bf16, lse);
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+    if (a.B == 0) return cudaSuccess;
+    PartialParams pp;
+    pp.q = static_cast<const uint16_t*>(a.q);
+    pp.k = static_cast<const uint16_t*>(a.k);
+    pp.v = static_cast<const uint16_t*>(a.v);
+    pp.seq_lens = a.seq_lens;
+    pp.page_table = a.page_table;
+    pp.max_pages = a.max_pages;
+    pp.num_pages = a.num_pages;
+    pp.Hq = a.Hq;
+    pp.Hkv = a.Hkv;
+    pp.L_max = a.L_max;
+    pp.G = a.Hq / a.Hkv;
+    pp.scale_log2 = a.scale * kLog2e;
+    pp.splits = a.splits;
+    pp.chunk_fixed = a.chunk_fixed;
+    pp.part_o = a.part_o;
+    pp.part_ml = a.part_ml;
+    pp.out = a.out;
+    pp.out_bf16 = a.out_bf16;
+    pp.lse = a.lse;
+    pp.direct = a.splits == 1 ? 1 : 0;
+    const dim3 grid((unsigned)a.splits, (unsigned)a.Hkv, (unsigned)a.B);
+    const bool paged = a.page_table != nullptr;
+    cudaError_t e;
+    if (a.D == 128) e = paged ? launch_dispatch<128, true>(pp.G, pp, grid, stream)
+                              : launch_dispatch<128, false>(pp.G, pp, grid, stream);
+    else e = paged ? launch_dispatch<64, true>(pp.G, pp, grid, stream)
+                   : launch_dispatch<64, false>(pp.G, pp, grid, stream);
+    if (e != cudaSuccess || a.splits == 1) return e;
+    return launch_merge(a.part_o, a.part_ml, a.seq_lens, a.B, a.Hq, a.L_max, a.D, a.splits, a.chunk_fixed,
+                        a.out, a.out_bf16, a.lse, stream);
+}
+
+cudaError_t decode_status_read(unsigned* bits, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(bits, g_status_decode, sizeof(unsigned));
+    if (e != cudaSuccess || !clear) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_status_decode, &zero, sizeof(unsigned));
+}
+
+}  // namespace fd

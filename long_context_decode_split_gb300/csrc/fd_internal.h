@@ -1,0 +1,84 @@
+// fd_internal.h -- host-side interface between the C-ABI layer (fd_api.cu)
+// and the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fd {
+
+constexpr int kTile = 64;  // tokens per pipeline stage; also the page size
+
+// Inputs and outputs of one split-KV decode launch (dense or paged).
+struct DecodeArgs {
+    const void* q;            // [B, Hq, D] bf16
+    const void* k;            // contiguous [B, Hkv, L_max, D] or pool [P, Hkv, 64, D]
+    const void* v;
+    const int32_t* seq_lens;  // [B] or null (= L_max)
+    const int32_t* page_table;// [B, max_pages] when paged, else null
+    int max_pages, num_pages;
+    int B, Hq, Hkv, L_max, D;
+    float scale;
+    int splits;               // chunks per sequence = grid.x
+    int chunk_fixed;          // > 0: every sequence uses this chunk (tokens)
+    void* out;                // [B, Hq, D]
+    int out_bf16;
+    float* lse;               // [B, Hq] or null
+    float* part_o;            // workspace: [B, Hq, splits, D]
+    float* part_ml;           // workspace: [B, Hq, splits, 2]
+};
+
+// Workspace bytes for `splits` chunks (0 when splits == 1).
+size_t decode_workspace_bytes(int B, int Hq, int D, int splits);
+
+// Occupancy (resident CTAs per SM) of the partial-pass kernel for this shape.
+int decode_ctas_per_sm(int D, int G, bool paged);
+
+// Enqueue the partial pass (+ merge when splits > 1).  Returns a cudaError_t.
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+// Device status words, one per translation unit that owns kernels.
+cudaError_t decode_status_read(unsigned* bits, bool clear);
+
+struct QuantArgs {
+    const void* k;            // [B, Hkv, L_max, D] bf16
+    const int32_t* seq_lens;
+    int B, Hkv, L_max, D;
+    uint8_t* codes;
+    void* mn_scale;
+    int8_t* res;
+    void* res_scale;
+};
+cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream);
+
+struct TopDeltaArgs {
+    const void* q;
+    const uint8_t* codes;
+    const void* mn_scale;
+    const int8_t* res;
+    const void* res_scale;
+    const void* v;
+    const int32_t* seq_lens;
+    int B, Hq, Hkv, L_max, D;
+    float scale, delta;
+    int n_sink, window;
+    int splits, chunk_fixed;
+    void* out;
+    int out_bf16;
+    float* lse;
+    uint32_t* sel_mask;
+    int32_t* sel_count;
+    float* part_o;
+    float* part_ml;
+};
+int topdelta_ctas_per_sm(int D, int G);
+cudaError_t launch_topdelta(const TopDeltaArgs& a, cudaStream_t stream);
+cudaError_t topdelta_status_read(unsigned* bits, bool clear);
+
+// Merge of per-chunk partials (shared by the dense and top-delta paths).
+cudaError_t launch_merge(const float* part_o, const float* part_ml, const int32_t* seq_lens,
+                         int B, int Hq, int L_max, int D, int splits, int chunk_fixed,
+                         void* out, int out_bf16, float* lse, cudaStream_t stream);
+
+}  // namespace fd

@@ -199,9 +199,32 @@ int oracle_decode_dense_f64(const double* q, const double* K, const double* V,
     return bad ? -3 : 0;
 }
 
-/* Widen one (b, kv-head) slab of bf16 rows to binary64. */
+/* Widen bf16 rows to binary64. */
 static void widen_rows(const uint16_t* src, size_t n, double* dst) {
     for (size_t i = 0; i < n; ++i) dst[i] = bf16_value(src[i]);
+}
+
+/* attend_row with bf16 K and V rows, widened exactly as they are read. */
+static void attend_row_bf16(const double* q, const uint16_t* K, const uint16_t* V,
+                            int L, int d, double scale, double* sc,
+                            double* out, double* lse) {
+    for (int c = 0; c < d; ++c) out[c] = 0.0;
+    if (L <= 0) { *lse = -INFINITY; return; }
+    double m = -INFINITY;
+    for (int j = 0; j < L; ++j) {
+        double dot = 0.0;
+        for (int c = 0; c < d; ++c) dot += q[c] * bf16_value(K[(size_t)j * d + c]);
+        sc[j] = scale * dot;
+        if (sc[j] > m) m = sc[j];
+    }
+    double Z = 0.0;
+    for (int j = 0; j < L; ++j) {
+        double w = exp(sc[j] - m);
+        Z += w;
+        for (int c = 0; c < d; ++c) out[c] += w * bf16_value(V[(size_t)j * d + c]);
+    }
+    for (int c = 0; c < d; ++c) out[c] /= Z;
+    *lse = m + log(Z);
 }
 
 /* Dense decode with bf16 inputs (the library's contiguous-cache problem).
@@ -214,38 +237,29 @@ int oracle_decode_dense(const uint16_t* q, const uint16_t* k, const uint16_t* v,
     if (seq_lens) for (int b = 0; b < B; ++b) if (seq_lens[b] < 0 || seq_lens[b] > L_max) return -2;
     int G = Hq / Hkv;
     int nt = pick_threads(n_threads);
-    int units = B * Hkv;
+    int rows = B * Hq;
     int bad = 0;
-    /* one (b, kv head) at a time per thread: widen its K and V, then attend the G queries */
     #pragma omp parallel num_threads(nt)
     {
-        size_t slab = (size_t)(L_max > 0 ? L_max : 1) * d;
-        double* Kd = (double*)malloc(sizeof(double) * slab);
-        double* Vd = (double*)malloc(sizeof(double) * slab);
         double* sc = (double*)malloc(sizeof(double) * (size_t)(L_max > 0 ? L_max : 1));
         double* qd = (double*)malloc(sizeof(double) * (size_t)d);
-        int ok = Kd && Vd && sc && qd;
+        int ok = sc && qd;
         if (!ok) {
             #pragma omp atomic write
             bad = 1;
         }
         {
             #pragma omp for schedule(dynamic, 1)
-            for (int u = 0; u < units; ++u) {
+            for (int r = 0; r < rows; ++r) {
                 if (!ok) continue;
-                int b = u / Hkv, h = u % Hkv;
+                int b = r / Hq, hq = r % Hq, h = hq / G;
                 int L = seq_lens ? seq_lens[b] : L_max;
                 size_t kv = ((size_t)b * Hkv + h) * (size_t)L_max * d;
-                widen_rows(k + kv, (size_t)L * d, Kd);
-                widen_rows(v + kv, (size_t)L * d, Vd);
-                for (int g = 0; g < G; ++g) {
-                    int r = b * Hq + h * G + g;
-                    widen_rows(q + (size_t)r * d, (size_t)d, qd);
-                    attend_row(qd, Kd, Vd, L, d, scale, sc, out + (size_t)r * d, lse + r);
-                }
+                widen_rows(q + (size_t)r * d, (size_t)d, qd);
+                attend_row_bf16(qd, k + kv, v + kv, L, d, scale, sc, out + (size_t)r * d, lse + r);
             }
         }
-        free(Kd); free(Vd); free(sc); free(qd);
+        free(sc); free(qd);
     }
     return bad ? -3 : 0;
 }
@@ -390,11 +404,11 @@ int oracle_decode_paged(const uint16_t* q, const uint16_t* k_pages, const uint16
     int bad = 0;
     #pragma omp parallel num_threads(nt)
     {
-        double* Kd = (double*)malloc(sizeof(double) * (size_t)Lcap * d);
-        double* Vd = (double*)malloc(sizeof(double) * (size_t)Lcap * d);
+        uint16_t* Kg = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)Lcap * d);
+        uint16_t* Vg = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)Lcap * d);
         double* sc = (double*)malloc(sizeof(double) * (size_t)Lcap);
         double* qd = (double*)malloc(sizeof(double) * (size_t)d);
-        int ok = Kd && Vd && sc && qd;
+        int ok = Kg && Vg && sc && qd;
         if (!ok) {
             #pragma omp atomic write
             bad = 1;
@@ -408,17 +422,17 @@ int oracle_decode_paged(const uint16_t* q, const uint16_t* k_pages, const uint16
                 for (int t = 0; t < L; ++t) {
                     int id = page_table[(size_t)b * max_pages + t / page_size];
                     size_t row = (((size_t)id * Hkv + h) * page_size + (t % page_size)) * d;
-                    widen_rows(k_pages + row, (size_t)d, Kd + (size_t)t * d);
-                    widen_rows(v_pages + row, (size_t)d, Vd + (size_t)t * d);
+                    memcpy(Kg + (size_t)t * d, k_pages + row, sizeof(uint16_t) * (size_t)d);
+                    memcpy(Vg + (size_t)t * d, v_pages + row, sizeof(uint16_t) * (size_t)d);
                 }
                 for (int g = 0; g < G; ++g) {
                     int r = b * Hq + h * G + g;
                     widen_rows(q + (size_t)r * d, (size_t)d, qd);
-                    attend_row(qd, Kd, Vd, L, d, scale, sc, out + (size_t)r * d, lse + r);
+                    attend_row_bf16(qd, Kg, Vg, L, d, scale, sc, out + (size_t)r * d, lse + r);
                 }
             }
         }
-        free(Kd); free(Vd); free(sc); free(qd);
+        free(Kg); free(Vg); free(sc); free(qd);
     }
     return bad ? -3 : 0;
 }
