@@ -180,6 +180,34 @@ FD_API int fd_decode_topdelta(const void* q, const uint8_t* codes, const void* m
                        uint32_t* sel_mask, int32_t* sel_count,
                        void* workspace, size_t workspace_bytes, void* stream);
 
+/* Size of the fixed device scratch array used by fd_decode_dense_noalloc. */
+#define FD_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* fd_decode_dense without a workspace argument, for callers that cannot
+ * allocate device memory: for example a plug-in inside a host engine that
+ * has reserved all device memory and exposes no allocator, or a decode loop
+ * that must not call cudaMalloc/cudaFree because they can synchronise the
+ * device.  The source pages have no counterpart of this entry point.
+ *   - Arguments, layouts and results are those of fd_decode_dense.
+ *   - Scratch comes from one static device array of FD_NOALLOC_SCRATCH_BYTES
+ *     (4 MiB) inside the library, held by every GPU that loads the library
+ *     until the process exits.  When the plan for these sizes needs more
+ *     (fd_decode_workspace_size(B, Hq, Hkv, L_max, d, num_splits,
+ *     seq_lens != NULL) > FD_NOALLOC_SCRATCH_BYTES) the call returns
+ *     FD_ERR_WORKSPACE_TOO_SMALL and enqueues nothing.
+ *   - The call allocates nothing.  Its first call on a device (with that
+ *     device current) looks up the array's device address; make that first
+ *     call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents
+ *     (nothing in it needs to start at zero: a call reads only what it wrote
+ *     earlier in the same call).  Calls that overlap on the GPU, e.g. on two
+ *     streams at once, race on it. */
+FD_API int fd_decode_dense_noalloc(const void* q, const void* k, const void* v,
+                                   const int32_t* seq_lens,
+                                   int B, int Hq, int Hkv, int L_max, int d,
+                                   float scale, int num_splits,
+                                   void* out, int out_dtype, float* lse, void* stream);
+
 /* Synchronises `stream`, then reports the device status word of the current
  * device: FD_ERR_DEVICE_TIMEOUT, FD_ERR_BAD_PAGE_TABLE, FD_ERR_INVALID_ARG (a
  * seq_lens entry outside [0, L_max]; the kernels clamped it) or FD_OK, in

@@ -19,7 +19,7 @@ import torch
 __all__ = [
     "FdError", "load", "open_library", "header_symbols", "fd_abi_version", "fd_status_string", "fd_num_splits",
     "fd_decode_workspace_size", "fd_decode_dense", "fd_decode_paged", "fd_quantize_keys",
-    "fd_topdelta_workspace_size", "fd_decode_topdelta", "fd_device_status",
+    "fd_topdelta_workspace_size", "fd_decode_topdelta", "fd_device_status", "fd_decode_dense_noalloc",
     "FD_OK", "FD_ERR_INVALID_ARG", "FD_ERR_UNSUPPORTED", "FD_ERR_WORKSPACE_TOO_SMALL",
     "FD_ERR_BAD_PAGE_TABLE", "FD_ERR_CUDA", "FD_ERR_DEVICE_TIMEOUT", "FD_OUT_F32", "FD_OUT_BF16",
 ]
@@ -74,6 +74,7 @@ def open_library(path: str):
         "fd_topdelta_workspace_size": (S, [I, I, I, I, I, I]),
         "fd_decode_topdelta": (I, [P, P, P, P, P, P, P, I, I, I, I, I, F, F, I, I, I, P, I, P, P, P, P, S, P]),
         "fd_device_status": (I, [I, P]),
+        "fd_decode_dense_noalloc": (I, [P, P, P, P, I, I, I, I, I, F, I, P, I, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -286,6 +287,32 @@ def fd_decode_topdelta(q, codes, mn_scale, res, res_scale, v, seq_lens=None, sca
                                 0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
     _raise(st, "fd_decode_topdelta")
     return out, lse, sel_mask, sel_count
+
+
+def fd_decode_dense_noalloc(q, k, v, out, seq_lens=None, scale=None, num_splits=0, lse=None, stream=None):
+    """fd_decode_dense for callers that cannot allocate: the library's fixed
+    device scratch array stands in for the workspace, and this wrapper
+    allocates nothing either (the caller passes `out` and, optionally,
+    `lse`).  Raises FdError(FD_ERR_WORKSPACE_TOO_SMALL) when the plan needs
+    more than FD_NOALLOC_SCRATCH_BYTES of scratch."""
+    lib = load()
+    _check_cuda(q, "q", torch.bfloat16)
+    B, Hq, d = q.shape
+    _check_cuda(k, "k", torch.bfloat16)
+    _need(k.dim() == 4 and k.shape[0] == B and k.shape[3] == d, "k must be [B, Hkv, L_max, d]")
+    _, Hkv, L_max, _ = k.shape
+    _check_cuda(v, "v", torch.bfloat16, k.shape)
+    if seq_lens is not None:
+        _check_cuda(seq_lens, "seq_lens", torch.int32, (B,))
+    code, _ = _out_code(out.dtype)
+    _check_cuda(out, "out", None, (B, Hq, d))
+    if lse is not None:
+        _check_cuda(lse, "lse", torch.float32, (B, Hq))
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = lib.fd_decode_dense_noalloc(_p(q), _p(k), _p(v), _p(seq_lens), B, Hq, Hkv, L_max, d, scale,
+                                     int(num_splits), _p(out), code, _p(lse), _stream(stream))
+    _raise(st, "fd_decode_dense_noalloc")
+    return out, lse
 
 
 def fd_device_status(clear=True, stream=None) -> int:
