@@ -128,7 +128,7 @@ class ClockSampler:
 class Workload:
     """Resident inputs plus a `call()` that runs one decode through the C ABI."""
 
-    def __init__(self, name, seed, device):
+    def __init__(self, name, seed, device, batch=None, seq_len=None):
         import torch
 
         import long_context_decode_split_gb300 as fd
@@ -138,16 +138,24 @@ class Workload:
         self.fd = fd
         self.device = device
         self.topdelta = None
+        over = {}
+        if seq_len is not None:
+            over["L"] = seq_len
         if name == "tiny":
             p = W.tiny(seed=seed, device=device)
         elif name == "mha32k":
-            p = W.mha32k(seed=seed, device=device)
+            p = W.mha32k(seed=seed, device=device, **over)
         elif name == "million":
-            p = W.million(seed=seed, device=device)
+            p = W.million(seed=seed, device=device, **over)
         elif name == "gqa_paged":
-            p = W.gqa_paged(seed=seed, device=device)
+            kw = {"B": batch} if batch is not None else {}
+            if seq_len is not None:
+                kw.update(L_min=max(64, seq_len // 8), L_max=seq_len)
+            p = W.gqa_paged(seed=seed, device=device, **kw)
         elif name.startswith("ffd"):
-            p = W.ffd(seed=seed, device=device)
+            if batch is not None:
+                over["B"] = batch
+            p = W.ffd(seed=seed, device=device, **over)
             if name != "ffd_dense":
                 self.topdelta = 5.0 if name.endswith("5") else 7.0
         else:
@@ -444,6 +452,8 @@ def main():
                     choices=["tiny", "mha32k", "gqa_paged", "million", "ffd_dense", "ffd_topdelta5",
                              "ffd_topdelta7"])
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--batch", type=int, default=None, help="override B (gqa_paged, ffd_*)")
+    ap.add_argument("--seq-len", type=int, default=None, help="override L (L_max for gqa_paged)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
@@ -467,7 +477,7 @@ def main():
 
     fd.load()
     dev = f"cuda:{ctx.local_rank}"
-    wl = Workload(args.workload, args.seed + ctx.rank, dev)
+    wl = Workload(args.workload, args.seed + ctx.rank, dev, batch=args.batch, seq_len=args.seq_len)
 
     sampler = ClockSampler(ctx.local_rank)
     sampler.start()

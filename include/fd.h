@@ -132,7 +132,8 @@ FD_API int fd_decode_paged(const void* q, const void* k_pages, const void* v_pag
 /* Key encoder for the sparse path ([FFD] section 5): per token and per
  * group of 32 channels, a 2-bit asymmetric body and an int8 symmetric
  * residual.  With x the group's bf16 values, in IEEE binary32 arithmetic:
- *   mn16 = fp16(min x), s16 = fp16((max x - min x) / 3)
+ *   mn16 = fp16(min x), s16 = fp16((max x - min x) / 3)  (a zero min or
+ *          max counts as +0)
  *   code = clamp(rint((x - mn16) / s16), 0, 3)      (0 when s16 == 0)
  *   deq2 = mn16 + code * s16,  r = x - deq2
  *   rs16 = fp16(max |r| / 127)
@@ -169,7 +170,8 @@ FD_API size_t fd_topdelta_workspace_size(int B, int Hq, int Hkv, int L_max, int 
  * [B, Hq, ceil(L_max/32)] uint32 (bit j%32 of word j/32 set when j is in
  * Sel) and sel_count [B, Hq] int32.  The residual and V of a token are read
  * only when some query head of its KV group selects a token in the same
- * 64-token tile.  workspace: fd_topdelta_workspace_size() bytes. */
+ * 64-token tile.  L_max must be a multiple of 4 (FD_ERR_UNSUPPORTED
+ * otherwise).  workspace: fd_topdelta_workspace_size() bytes. */
 FD_API int fd_decode_topdelta(const void* q, const uint8_t* codes, const void* mn_scale,
                        const int8_t* res, const void* res_scale, const void* v,
                        const int32_t* seq_lens,

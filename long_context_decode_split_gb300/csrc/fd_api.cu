@@ -246,6 +246,7 @@ int fd_decode_topdelta(const void* q, const uint8_t* codes, const void* mn_scale
     if (out_dtype != FD_OUT_F32 && out_dtype != FD_OUT_BF16) return FD_ERR_INVALID_ARG;
     if (num_splits < 0 || !std::isfinite(scale) || std::isnan(delta) || delta < 0.f) return FD_ERR_INVALID_ARG;
     if (n_sink < 0 || window < 0) return FD_ERR_INVALID_ARG;
+    if (L_max % 4 != 0) return FD_ERR_UNSUPPORTED;  // keeps every tile copy 16-byte aligned
     if (B > 0 && (!q || !codes || !mn_scale || !res || !res_scale || !v || !out)) return FD_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(codes) || !aligned16(mn_scale) || !aligned16(res) || !aligned16(res_scale) ||
         !aligned16(v) || !aligned16(out))

@@ -32,9 +32,7 @@ __device__ unsigned int g_status_decode;
 
 namespace {
 
-constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxDevices = 64;
-constexpr float kLn2 = 0.6931471805599453f;
 
 // Static geometry of the partial pass for head dim D, padded group GP and CW
 // consumer warps.
@@ -68,28 +66,6 @@ __device__ __forceinline__ int chunk_len(int L, int splits, int chunk_fixed) {
     int c = (L + splits - 1) / splits;
     c = (c + kTile - 1) / kTile * kTile;
     return c > 0 ? c : kTile;
-}
-
-// Butterfly over the LPR lanes of a row group that both sums the per-lane
-// partial dot products and transposes them: on entry lane l holds N partial
-// sums (one per row it touched), on exit it holds the full sum of the row
-// with index (l >> SH) & (N-1).
-template <int N, int LPR>
-__device__ __forceinline__ float transpose_reduce(float (&v)[N], int lane) {
-#pragma unroll
-    for (int n = N, o = LPR / 2; n > 1; n >>= 1, o >>= 1) {
-        const bool upper = (lane & o) != 0;
-#pragma unroll
-        for (int k = 0; k < n / 2; ++k) {
-            const float send = upper ? v[k] : v[k + n / 2];
-            const float keep = upper ? v[k + n / 2] : v[k];
-            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-        }
-    }
-    float r = v[0];
-#pragma unroll
-    for (int o = LPR / N / 2; o >= 1; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
-    return r;
 }
 
 struct PartialParams {
@@ -230,7 +206,7 @@ partial_kernel(const PartialParams p) {
     for (int t = 0; t < ntiles && !failed; ++t) {
         const int s = t % STAGES;
         const uint32_t ph = (uint32_t)(t / STAGES) & 1u;
-        if (!mbar_wait(&full[s], ph)) {
+        if (!warp_wait(&full[s], ph)) {
             atomicOr(&g_status_decode, kStatusTimeout);
             failed = true;
             break;
@@ -313,75 +289,16 @@ partial_kernel(const PartialParams p) {
     }
     pdl_launch_dependents();
 
-    // ---- reduce within the warp: l over all lanes, o over row groups ------
-#pragma unroll
-    for (int g = 0; g < GP; ++g) {
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) l_lane[g] += __shfl_xor_sync(0xffffffffu, l_lane[g], off);
-#pragma unroll
-        for (int off = 16; off >= Gm::LPR; off >>= 1) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                o[g][e].x += __shfl_xor_sync(0xffffffffu, o[g][e].x, off);
-                o[g][e].y += __shfl_xor_sync(0xffffffffu, o[g][e].y, off);
-            }
-        }
-    }
-
-    // ---- combine the consumer warps through shared memory -----------------
-    named_barrier(1, CW * 32);  // every consumer is done with the stage ring
-    float* red_o = reinterpret_cast<float*>(smem);            // [CW][GP][D]
-    float* red_m = red_o + CW * GP * D;                       // [CW][GP]
-    float* red_l = red_m + CW * GP;                           // [CW][GP]
-    if (lane < Gm::LPR) {
-#pragma unroll
-        for (int g = 0; g < GP; ++g) {
-            float4* dst = reinterpret_cast<float4*>(red_o + (warp * GP + g) * D + c * 8);
-            dst[0] = make_float4(o[g][0].x, o[g][0].y, o[g][1].x, o[g][1].y);
-            dst[1] = make_float4(o[g][2].x, o[g][2].y, o[g][3].x, o[g][3].y);
-        }
-    }
-    if (lane == 0) {
-#pragma unroll
-        for (int g = 0; g < GP; ++g) {
-            red_m[warp * GP + g] = failed ? -INFINITY : m_run[g];
-            red_l[warp * GP + g] = failed ? 0.f : l_lane[g];
-        }
-    }
-    named_barrier(1, CW * 32);
-
-    const int nthr = CW * 32;
-    for (int idx = threadIdx.x; idx < p.G * D; idx += nthr) {
-        const int g = idx / D, dim = idx % D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < CW; ++w) M = fmaxf(M, red_m[w * GP + g]);
-        float lsum = 0.f, acc = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < CW; ++w) {
-                const float mw = red_m[w * GP + g];
-                const float sc = mw == -INFINITY ? 0.f : exp2_approx(mw - M);
-                lsum += sc * red_l[w * GP + g];
-                acc += sc * red_o[(w * GP + g) * D + dim];
-            }
-        }
-        const int row = b * p.Hq + hq0 + g;
-        const float val = lsum > 0.f ? acc / lsum : 0.f;
-        if (p.direct) {
-            const size_t oi = (size_t)row * D + dim;
-            if (p.out_bf16) static_cast<uint16_t*>(p.out)[oi] = f32_to_bf16_bits(val);
-            else static_cast<float*>(p.out)[oi] = val;
-            if (dim == 0 && p.lse) p.lse[row] = lsum > 0.f ? (M + __log2f(lsum)) * kLn2 : -INFINITY;
-        } else {
-            const size_t pi = (size_t)row * p.splits + split;
-            p.part_o[pi * D + dim] = val;
-            if (dim == 0) {
-                p.part_ml[2 * pi + 0] = lsum > 0.f ? M : -INFINITY;
-                p.part_ml[2 * pi + 1] = lsum;
-            }
-        }
-    }
+    StoreTarget st;
+    st.out = p.out;
+    st.out_bf16 = p.out_bf16;
+    st.lse = p.lse;
+    st.part_o = p.part_o;
+    st.part_ml = p.part_ml;
+    st.direct = p.direct;
+    st.splits = p.splits;
+    combine_warps_and_store<D, GP, CW>(smem, warp, lane, p.G, b * p.Hq + hq0, split, m_run, l_lane, o,
+                                       failed, st);
 }
 
 // ---------------------------------------------------------------------------

@@ -10,6 +10,9 @@
 
 namespace fd {
 
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
 // Device status bits (see fd_device_status in fd.h).
 constexpr unsigned kStatusBadPage = 1u;
 constexpr unsigned kStatusTimeout = 2u;
@@ -87,6 +90,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     return false;
 }
 
+// mbar_wait for all 32 lanes of a warp, with one verdict for the whole warp
+// (so a time-out can never split the warp before its shuffles).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
+    const bool ok = mbar_wait(bar, parity);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // L2 policy for data that is streamed exactly once.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     uint64_t pol;
@@ -144,6 +154,119 @@ __device__ __forceinline__ float2 f2fma(float2 a, float2 b, float2 c) { return _
 
 __device__ __forceinline__ unsigned short f32_to_bf16_bits(float x) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+// Butterfly over the LPR lanes of a row group that both sums the per-lane
+// partial dot products and transposes them: on entry lane l holds N partial
+// sums (one per row it touched), on exit it holds the full sum of the row
+// with index (l >> SH) & (N-1).
+template <int N, int LPR>
+__device__ __forceinline__ float transpose_reduce(float (&v)[N], int lane) {
+#pragma unroll
+    for (int n = N, o = LPR / 2; n > 1; n >>= 1, o >>= 1) {
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int k = 0; k < n / 2; ++k) {
+            const float send = upper ? v[k] : v[k + n / 2];
+            const float keep = upper ? v[k + n / 2] : v[k];
+            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    float r = v[0];
+#pragma unroll
+    for (int o = LPR / N / 2; o >= 1; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+    return r;
+}
+
+
+// Where a CTA's combined result goes: the final output (one chunk per
+// sequence) or its chunk's slot of the merge workspace.
+struct StoreTarget {
+    void* out;
+    int out_bf16;
+    float* lse;
+    float* part_o;   // [rows, splits, D]: O_i / l_i
+    float* part_ml;  // [rows, splits, 2]: (m_i in log2 units, l_i)
+    int direct;
+    int splits;
+};
+
+// End of a partial pass: every consumer warp holds, per query g of the
+// group, a running max m (log2 units, warp-uniform), a per-lane share of the
+// exp-sum l and, in the lanes of each row group, the output accumulator for
+// 8 columns.  Sum l over the warp and o over row groups, combine the CW warps
+// through shared memory (the stage ring is reused, after a barrier over the
+// consumer warps) and store.  row0 = b * Hq + first query head of the group.
+template <int D, int GP, int CW>
+__device__ __forceinline__ void combine_warps_and_store(unsigned char* smem, int warp, int lane, int G, int row0,
+                                                        int split, const float (&m_run)[GP], float (&l_lane)[GP],
+                                                        float2 (&o)[GP][4], bool failed, const StoreTarget& st) {
+    constexpr int LPR = D / 8;
+    const int c = lane % LPR;
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) l_lane[g] += __shfl_xor_sync(0xffffffffu, l_lane[g], off);
+#pragma unroll
+        for (int off = 16; off >= LPR; off >>= 1) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                o[g][e].x += __shfl_xor_sync(0xffffffffu, o[g][e].x, off);
+                o[g][e].y += __shfl_xor_sync(0xffffffffu, o[g][e].y, off);
+            }
+        }
+    }
+    named_barrier(1, CW * 32);  // every consumer is done with the stage rings
+    float* red_o = reinterpret_cast<float*>(smem);  // [CW][GP][D]
+    float* red_m = red_o + CW * GP * D;             // [CW][GP]
+    float* red_l = red_m + CW * GP;                 // [CW][GP]
+    if (lane < LPR) {
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+            float4* dst = reinterpret_cast<float4*>(red_o + (warp * GP + g) * D + c * 8);
+            dst[0] = make_float4(o[g][0].x, o[g][0].y, o[g][1].x, o[g][1].y);
+            dst[1] = make_float4(o[g][2].x, o[g][2].y, o[g][3].x, o[g][3].y);
+        }
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+            red_m[warp * GP + g] = failed ? -INFINITY : m_run[g];
+            red_l[warp * GP + g] = failed ? 0.f : l_lane[g];
+        }
+    }
+    named_barrier(1, CW * 32);
+    for (int idx = warp * 32 + lane; idx < G * D; idx += CW * 32) {
+        const int g = idx / D, dim = idx % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < CW; ++w) M = fmaxf(M, red_m[w * GP + g]);
+        float lsum = 0.f, acc = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < CW; ++w) {
+                const float mw = red_m[w * GP + g];
+                const float sc = mw == -INFINITY ? 0.f : exp2_approx(mw - M);
+                lsum += sc * red_l[w * GP + g];
+                acc += sc * red_o[(w * GP + g) * D + dim];
+            }
+        }
+        const int row = row0 + g;
+        const float val = lsum > 0.f ? acc / lsum : 0.f;
+        if (st.direct) {
+            const size_t oi = (size_t)row * D + dim;
+            if (st.out_bf16) static_cast<uint16_t*>(st.out)[oi] = f32_to_bf16_bits(val);
+            else static_cast<float*>(st.out)[oi] = val;
+            if (dim == 0 && st.lse) st.lse[row] = lsum > 0.f ? (M + __log2f(lsum)) * kLn2 : -INFINITY;
+        } else {
+            const size_t pi = (size_t)row * st.splits + split;
+            st.part_o[pi * D + dim] = val;
+            if (dim == 0) {
+                st.part_ml[2 * pi + 0] = lsum > 0.f ? M : -INFINITY;
+                st.part_ml[2 * pi + 1] = lsum;
+            }
+        }
+    }
 }
 
 }  // namespace fd

@@ -445,7 +445,8 @@ int oracle_decode_paged(const uint16_t* q, const uint16_t* k_pages, const uint16
  * body (read for the full scan) and an 8-bit residual (read only for the
  * candidates).  The page gives no formulas; the encoding below is the one
  * this library defines, per token and per group of 32 channels:
- *   mn  = min x,  mx = max x                       (exact bf16 values)
+ *   mn  = min x,  mx = max x                       (exact bf16 values; a zero
+ *                                                   extreme is taken as +0)
  *   mn16 = half(mn),  s16 = half((mx - mn) / 3)    (binary32 ops, then RNE to fp16)
  *   code = clamp(rint((x - mn16) / s16), 0, 3)     (all codes 0 when s16 == 0)
  *   deq2 = mn16 + code * s16                       (binary32, two roundings)
@@ -485,6 +486,9 @@ int oracle_quantize_keys(const uint16_t* k, const int32_t* seq_lens,
                 if (xv[c] < mn) mn = xv[c];
                 if (xv[c] > mx) mx = xv[c];
             }
+            /* min and max are values: a zero extreme is +0 whatever its sign */
+            mn = mn + 0.0f;
+            mx = mx + 0.0f;
             float diff = mx - mn;
             float third = diff / 3.0f;
             uint16_t mn16 = oracle_float_to_half(mn);

@@ -102,6 +102,14 @@ def test_encode_ties_round_to_even(oracle):
     assert list(rs.ravel()) == [0x1C08]
 
 
+@pytest.mark.parametrize("x", [[-0.0] * 32, [-0.0, 0.0] * 16, [0.0, -0.0] * 16])
+def test_encode_signed_zero_group(oracle, x):
+    # a zero extreme is +0 whatever its sign: mn16 = +0 (0x0000), s16 = +0, codes 0, residual 0
+    codes, ms, res, rs = encode_group(oracle, x)
+    assert list(ms.ravel()) == [0x0000, 0x0000]
+    assert not codes.any() and not res.any() and rs.ravel()[0] == 0
+
+
 def test_encoder_leaves_rows_past_the_end(oracle):
     p = W.random_problem(2, 2, 2, 40, 64, seed=1, seq_lens=[40, 7])
     codes, ms, res, rs = oracle.quantize_keys(bits(p.k), p.seq_lens)
