@@ -33,7 +33,9 @@
  *     lse[b,hq] = log sum_j exp(s_j) over the attended keys.  A sequence of
  *     length 0 yields out = 0 and lse = -inf.
  *   - Head grouping: query head hq reads KV head hq / (Hq / Hkv).
- *   - Supported shapes: d in {64, 128}; 1 <= Hq/Hkv <= 8; page_size == 64.
+ *   - Supported shapes: d in {64, 128}; 1 <= Hq/Hkv <= 8; page_size == 64;
+ *     at most 2^31 - 1 cache rows (B * Hkv * L_max, or num_pages * Hkv * 64)
+ *     for the dense and paged decode (FD_ERR_UNSUPPORTED otherwise).
  *   - Results are deterministic for fixed inputs, shapes and num_splits.
  */
 #ifndef FD_H

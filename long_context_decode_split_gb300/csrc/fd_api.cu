@@ -147,6 +147,10 @@ static int decode_common(fd::DecodeArgs& a, int num_splits, bool ragged, int out
     if (!aligned16(a.q) || !aligned16(a.k) || !aligned16(a.v) || !aligned16(a.out)) return FD_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(a.lse) & 3u) || (reinterpret_cast<uintptr_t>(a.seq_lens) & 3u))
         return FD_ERR_INVALID_ARG;
+    // tile copies address cache rows with 32-bit coordinates
+    const long long cache_rows = a.page_table ? (long long)a.num_pages * a.Hkv * kTile
+                                              : (long long)a.B * a.Hkv * a.L_max;
+    if (cache_rows > 0x7fffffffLL) return FD_ERR_UNSUPPORTED;
     const Plan pl = decode_plan(a.B, a.Hq, a.Hkv, a.L_max, a.D, num_splits, ragged);
     const size_t need = fd::decode_workspace_bytes(a.B, a.Hq, a.D, pl.splits);
     if (need > 0) {

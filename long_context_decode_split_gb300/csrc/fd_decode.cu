@@ -25,6 +25,7 @@
 
 #include "fd_device.cuh"
 #include "fd_internal.h"
+#include "fd_tma.h"
 
 namespace fd {
 
@@ -45,20 +46,9 @@ struct Geo {
     static constexpr int LOG_LPR = D == 128 ? 4 : 3;
     static constexpr int LOG_NIT = NIT == 16 ? 4 : NIT == 8 ? 3 : NIT == 4 ? 2 : NIT == 2 ? 1 : 0;
     static constexpr int SH = LOG_LPR - LOG_NIT;  // low lane bits that hold copies
-    static constexpr int TILE_BYTES = kTile * D * 2;
-    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K tile + V tile
     static_assert(NIT >= 1 && NIT <= LPR, "bad warp split");
     static_assert((1 << LOG_NIT) == NIT, "NIT must be a power of two");
 };
-
-template <int D>
-constexpr int stages_for() { return D == 128 ? 3 : 4; }
-
-template <int D, int GP, int CW, int STAGES>
-constexpr int partial_smem_bytes() {
-    // stage ring, then barriers and per-stage row counts
-    return STAGES * Geo<D, GP, CW>::STAGE_BYTES + STAGES * 16 + STAGES * 4 + 64;
-}
 
 // Chunk length in tokens for a sequence of length L.
 __device__ __forceinline__ int chunk_len(int L, int splits, int chunk_fixed) {
@@ -70,28 +60,100 @@ __device__ __forceinline__ int chunk_len(int L, int splits, int chunk_fixed) {
 
 struct PartialParams {
     const uint16_t* q;
-    const uint16_t* k;
-    const uint16_t* v;
     const int32_t* seq_lens;
     const int32_t* page_table;
     int max_pages, num_pages;
     int Hq, Hkv, L_max, G;
     float scale_log2;
     int splits, chunk_fixed;
-    float* part_o;
-    float* part_ml;
-    void* out;
-    int out_bf16;
-    float* lse;
-    int direct;  // one chunk: write the final output
+    StoreTarget st;
 };
 
-template <int D, int GP, int CW, int STAGES, bool PAGED>
-__global__ void __launch_bounds__((CW + 1) * 32, 1)
-partial_kernel(const PartialParams p) {
+// Tensor-core consumer, one warp, 16 rows of a 64-token tile (queries padded
+// to 8; rows 8-15 of the m16 A operand are zero):
+//   S[q][t]  = Q K^T   m16n8k16, A = Q fragments held in registers, B = K rows
+//                      loaded with ldmatrix from the swizzled tile
+//   online softmax per query (quad = the 4 lanes holding one query's row)
+//   O^T[d][q] += V^T P^T  A = V^T via ldmatrix.trans, B = P^T taken straight
+//                      from the S accumulators, P split into bf16 hi + lo.
+template <int D>
+struct MmaWarpState {
+    uint32_t qa0[D / 16], qa2[D / 16];  // A fragments of Q (rows gid), k-steps of 16 dims
+    float o[D / 16][4];                 // O^T accumulators
+    float m_run, l_run;                 // query gid: running max (log2 units), exp-sum share
+};
+
+template <int D>
+__device__ __forceinline__ void mma_consume_tile(MmaWarpState<D>& ws, uint32_t ks, uint32_t vs, unsigned char* vgen,
+                                                 int warp, int lane, int rows, float scale_log2) {
+    const int tig = lane & 3;
+    const int mi = lane >> 3;
+    const int ld_row = warp * 16 + 8 * (mi >> 1) + (lane & 7);  // row this lane addresses for ldmatrix
+    float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        uint32_t b00, b01, b10, b11;
+        ldsm_x4(ks + swz(ld_row, 2 * kk + (mi & 1)), b00, b01, b10, b11);
+        mma_bf16(sacc[0], ws.qa0[kk], 0u, ws.qa2[kk], 0u, b00, b01);
+        mma_bf16(sacc[1], ws.qa0[kk], 0u, ws.qa2[kk], 0u, b10, b11);
+    }
+    // rows of this warp past the valid ones: masked scores, zeroed V rows
+    const int r0 = warp * 16 + 2 * tig;
+    float sc[4];
+    sc[0] = r0 < rows ? sacc[0][0] * scale_log2 : -INFINITY;
+    sc[1] = r0 + 1 < rows ? sacc[0][1] * scale_log2 : -INFINITY;
+    sc[2] = r0 + 8 < rows ? sacc[1][0] * scale_log2 : -INFINITY;
+    sc[3] = r0 + 9 < rows ? sacc[1][1] * scale_log2 : -INFINITY;
+    if (warp * 16 + 16 > rows) {
+        // the tile's tail: clear V rows >= rows so 0 * (stale data) cannot make NaN
+        for (int i = lane; i < 16 * (D / 8); i += 32) {
+            const int r = warp * 16 + i / (D / 8);
+            if (r >= rows) *reinterpret_cast<uint4*>(vgen + swz(r, i % (D / 8))) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        // order these generic stores before the tile copy that later refills the stage
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+    }
+    float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float m_new = fmaxf(ws.m_run, mx);
+    const bool none = m_new == -INFINITY;
+    const float alpha = none ? 1.f : exp2_approx(ws.m_run - m_new);
+    float pr[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) pr[i] = none ? 0.f : exp2_approx(sc[i] - m_new);
+    ws.m_run = m_new;
+    ws.l_run = ws.l_run * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
+    uint32_t h0, l0, h1, l1;
+    split_bf16(pr[0], pr[1], h0, l0);
+    split_bf16(pr[2], pr[3], h1, l1);
+    // rescale: accumulator columns are queries 2*tig and 2*tig+1
+    const float a_even = __shfl_sync(0xffffffffu, alpha, 8 * tig);
+    const float a_odd = __shfl_sync(0xffffffffu, alpha, 8 * tig + 4);
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+        ws.o[mt][0] *= a_even;
+        ws.o[mt][1] *= a_odd;
+        ws.o[mt][2] *= a_even;
+        ws.o[mt][3] *= a_odd;
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(vs + swz(ld_row, 2 * mt + (mi & 1)), a0, a1, a2, a3);
+        mma_bf16(ws.o[mt], a0, a1, a2, a3, h0, h1);
+        mma_bf16(ws.o[mt], a0, a1, a2, a3, l0, l1);
+    }
+}
+
+template <int D, int GP, int CW, int STAGES, bool PAGED, bool MMA>
+__global__ void __launch_bounds__((CW + 1) * 32, (MMA || GP < 8) ? 2 : 1)
+partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+               const PartialParams p) {
     using Gm = Geo<D, GP, CW>;
-    extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * Gm::STAGE_BYTES);
+    constexpr int BOXES = D / 64;                // boxes per K (or V) tile
+    constexpr int STAGE = 2 * BOXES * kBoxBytes;  // K tile + V tile
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE);
     uint64_t* empty = full + STAGES;
     int* stage_rows = reinterpret_cast<int*>(empty + STAGES);
 
@@ -107,13 +169,13 @@ partial_kernel(const PartialParams p) {
         pdl_launch_dependents();
         // An empty chunk writes nothing, except that the only chunk of an
         // empty sequence writes out = 0, lse = -inf.
-        if (p.direct && split == 0) {
+        if (p.st.direct && split == 0) {
             for (int i = threadIdx.x; i < p.G * D; i += blockDim.x) {
                 const size_t o = (size_t)(b * p.Hq + hq0 + i / D) * D + (i % D);
-                if (p.out_bf16) static_cast<uint16_t*>(p.out)[o] = 0;
-                else static_cast<float*>(p.out)[o] = 0.f;
+                if (p.st.out_bf16) static_cast<uint16_t*>(p.st.out)[o] = 0;
+                else static_cast<float*>(p.st.out)[o] = 0.f;
             }
-            if (p.lse && threadIdx.x < p.G) p.lse[b * p.Hq + hq0 + threadIdx.x] = -INFINITY;
+            if (p.st.lse && threadIdx.x < p.G) p.st.lse[b * p.Hq + hq0 + threadIdx.x] = -INFINITY;
         }
         return;
     }
@@ -129,10 +191,12 @@ partial_kernel(const PartialParams p) {
     __syncthreads();
 
     if (warp == CW) {
-        // ---------------- producer: one lane issues all bulk copies --------
+        // ---------------- producer: one lane issues all tile copies --------
         if (lane == 0) {
+            prefetch_tmap(&tmk);
+            prefetch_tmap(&tmv);
             const uint64_t pol = l2_evict_first_policy();
-            const size_t head_rows = PAGED ? 0 : ((size_t)b * p.Hkv + h) * (size_t)p.L_max;
+            const int head_row0 = PAGED ? 0 : (b * p.Hkv + h) * p.L_max;
             for (int t = 0; t < ntiles; ++t) {
                 const int s = t % STAGES;
                 const uint32_t ph = (uint32_t)(t / STAGES) & 1u;
@@ -142,22 +206,24 @@ partial_kernel(const PartialParams p) {
                 }
                 const int tok = t0 + t * kTile;
                 const int rows = min(kTile, t1 - tok);
-                size_t row0;
+                int y;
                 bool ok = true;
                 if (PAGED) {
                     const int pg = p.page_table[(size_t)b * p.max_pages + tok / kTile];
                     ok = pg >= 0 && pg < p.num_pages;
-                    row0 = ((size_t)(ok ? pg : 0) * p.Hkv + h) * kTile;
+                    y = (pg * p.Hkv + h) * kTile;
                 } else {
-                    row0 = head_rows + tok;
+                    y = head_row0 + tok;
                 }
-                unsigned char* sk = smem + s * Gm::STAGE_BYTES;
+                unsigned char* sk = smem + s * STAGE;
                 if (ok) {
                     stage_rows[s] = rows;
-                    const uint32_t bytes = (uint32_t)rows * D * 2;
-                    mbar_arrive_expect_tx(&full[s], 2 * bytes);
-                    bulk_g2s(sk, p.k + row0 * D, bytes, &full[s], pol);
-                    bulk_g2s(sk + Gm::TILE_BYTES, p.v + row0 * D, bytes, &full[s], pol);
+                    mbar_arrive_expect_tx(&full[s], STAGE);
+#pragma unroll
+                    for (int bx = 0; bx < BOXES; ++bx) {
+                        tma_load_box(sk + bx * kBoxBytes, &tmk, 64 * bx, y, &full[s], pol);
+                        tma_load_box(sk + (BOXES + bx) * kBoxBytes, &tmv, 64 * bx, y, &full[s], pol);
+                    }
                 } else {
                     atomicOr(&g_status_decode, kStatusBadPage);
                     stage_rows[s] = 0;
@@ -169,7 +235,43 @@ partial_kernel(const PartialParams p) {
         return;
     }
 
-    // ------------------------ consumers ------------------------------------
+    bool failed = false;
+    if constexpr (MMA) {
+        // ------------------- tensor-core consumers (groups of 2..8) --------
+        const int gid = lane >> 2, tig = lane & 3;
+        MmaWarpState<D> ws;
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + (size_t)(b * p.Hq + hq0 + gid) * D);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            ws.qa0[kk] = gid < p.G ? qrow[8 * kk + tig] : 0u;
+            ws.qa2[kk] = gid < p.G ? qrow[8 * kk + 4 + tig] : 0u;
+        }
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) ws.o[mt][i] = 0.f;
+        ws.m_run = -INFINITY;
+        ws.l_run = 0.f;
+        for (int t = 0; t < ntiles; ++t) {
+            const int s = t % STAGES;
+            if (!warp_wait(&full[s], (uint32_t)(t / STAGES) & 1u)) {
+                atomicOr(&g_status_decode, kStatusTimeout);
+                failed = true;
+                break;
+            }
+            const int rows = stage_rows[s];
+            unsigned char* sk = smem + s * STAGE;
+            mma_consume_tile<D>(ws, smem_u32(sk), smem_u32(sk + BOXES * kBoxBytes), sk + BOXES * kBoxBytes, warp,
+                                lane, rows, p.scale_log2);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+        pdl_launch_dependents();
+        combine_mma_warps_and_store<D, 8, CW>(smem, warp, lane, p.G, b * p.Hq + hq0, split, ws.m_run, ws.l_run,
+                                              ws.o, failed, p.st);
+        return;
+    } else {
+    // ------------------------ CUDA-core consumers --------------------------
     const int c = lane % Gm::LPR;   // 16-byte column of a row
     const int rg = lane / Gm::LPR;  // row group within a warp-wide load
     // my token slot after the transposing reduction
@@ -202,8 +304,7 @@ partial_kernel(const PartialParams p) {
         for (int e = 0; e < 4; ++e) o[g][e] = make_float2(0.f, 0.f);
     }
 
-    bool failed = false;
-    for (int t = 0; t < ntiles && !failed; ++t) {
+    for (int t = 0; t < ntiles; ++t) {
         const int s = t % STAGES;
         const uint32_t ph = (uint32_t)(t / STAGES) & 1u;
         if (!warp_wait(&full[s], ph)) {
@@ -212,15 +313,15 @@ partial_kernel(const PartialParams p) {
             break;
         }
         const int rows = stage_rows[s];
-        const unsigned char* sk = smem + s * Gm::STAGE_BYTES;
-        const unsigned char* sv = sk + Gm::TILE_BYTES;
+        const unsigned char* sk = smem + s * STAGE;
+        const unsigned char* sv = sk + BOXES * kBoxBytes;
 
         // ---- scores: partial dots over my 8 dims, then butterfly -----------
         float part[GP][Gm::NIT];
 #pragma unroll
         for (int i = 0; i < Gm::NIT; ++i) {
             const int row = warp * Gm::TPW + Gm::RPI * i + rg;
-            const uint4 w = lds128(sk + (row * D + c * 8) * 2);
+            const uint4 w = lds128(sk + swz(row, c));
             const float2 k0 = bf16x2_to_float2(w.x), k1 = bf16x2_to_float2(w.y);
             const float2 k2 = bf16x2_to_float2(w.z), k3 = bf16x2_to_float2(w.w);
 #pragma unroll
@@ -271,7 +372,7 @@ partial_kernel(const PartialParams p) {
 #pragma unroll
             for (int g = 0; g < GP; ++g) pi[g] = __shfl_sync(0xffffffffu, pr[g], src);
             if (row < rows) {
-                const uint4 w = lds128(sv + (row * D + c * 8) * 2);
+                const uint4 w = lds128(sv + swz(row, c));
                 const float2 v0 = bf16x2_to_float2(w.x), v1 = bf16x2_to_float2(w.y);
                 const float2 v2 = bf16x2_to_float2(w.z), v3 = bf16x2_to_float2(w.w);
 #pragma unroll
@@ -288,17 +389,9 @@ partial_kernel(const PartialParams p) {
         if (lane == 0) mbar_arrive(&empty[s]);
     }
     pdl_launch_dependents();
-
-    StoreTarget st;
-    st.out = p.out;
-    st.out_bf16 = p.out_bf16;
-    st.lse = p.lse;
-    st.part_o = p.part_o;
-    st.part_ml = p.part_ml;
-    st.direct = p.direct;
-    st.splits = p.splits;
-    combine_warps_and_store<D, GP, CW>(smem, warp, lane, p.G, b * p.Hq + hq0, split, m_run, l_lane, o,
-                                       failed, st);
+    combine_warps_and_store<D, GP, CW>(smem, warp, lane, p.G, b * p.Hq + hq0, split, m_run, l_lane, o, failed,
+                                       p.st);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -338,11 +431,15 @@ merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml
 
 template <int D, int GP, bool PAGED>
 struct PartialLauncher {
-    // 8 consumer warps for groups of 8 keep each warp's partial sums in registers
-    static constexpr int CW = GP >= 8 ? 8 : 4;
-    static constexpr int STAGES = stages_for<D>();
-    static constexpr int SMEM = partial_smem_bytes<D, GP, CW, STAGES>();
-    static_assert(SMEM >= CW * GP * D * 4 + 2 * CW * GP * 4, "reduction scratch must fit in the ring");
+    // groups of 2..8 run on the tensor cores; single queries on CUDA cores
+    static constexpr bool MMA = GP >= 2;
+    static constexpr int CW = 4;
+    static constexpr int STAGES = D == 128 ? 3 : 4;
+    static constexpr int STAGE = 2 * (D / 64) * kBoxBytes;
+    static constexpr int SMEM = 1024 + STAGES * STAGE + STAGES * 16 + STAGES * 4 + 64;
+    static constexpr int RED = CW * 8 * D * 4 + 2 * CW * 8 * 4;
+    static_assert(STAGES * STAGE >= RED, "reduction scratch must fit in the ring");
+    static constexpr auto kernel = partial_kernel<D, MMA ? 8 : GP, CW, STAGES, PAGED, MMA>;
 
     // Per device: raise the dynamic shared-memory limit once, and remember
     // the occupancy the planner sizes its grids with.
@@ -352,8 +449,7 @@ struct PartialLauncher {
         cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
         if (dev < kMaxDevices && done[dev]) return cudaSuccess;
-        e = cudaFuncSetAttribute(partial_kernel<D, GP, CW, STAGES, PAGED>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
         if (e == cudaSuccess && dev < kMaxDevices) done[dev] = true;
         return e;
     }
@@ -364,16 +460,16 @@ struct PartialLauncher {
         if (dev < kMaxDevices && cache[dev] > 0) return cache[dev];
         if (prepare() != cudaSuccess) return 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, partial_kernel<D, GP, CW, STAGES, PAGED>,
-                                                          (CW + 1) * 32, SMEM) != cudaSuccess || n <= 0)
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, (CW + 1) * 32, SMEM) != cudaSuccess || n <= 0)
             return 1;
         if (dev < kMaxDevices) cache[dev] = n;
         return n;
     }
-    static cudaError_t launch(const PartialParams& pp, dim3 grid, cudaStream_t st) {
+    static cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const PartialParams& pp, dim3 grid,
+                              cudaStream_t st) {
         cudaError_t e = prepare();
         if (e != cudaSuccess) return e;
-        partial_kernel<D, GP, CW, STAGES, PAGED><<<grid, (CW + 1) * 32, SMEM, st>>>(pp);
+        kernel<<<grid, (CW + 1) * 32, SMEM, st>>>(tk, tv, pp);
         return cudaGetLastError();
     }
 };
@@ -381,17 +477,14 @@ struct PartialLauncher {
 template <int D, bool PAGED>
 int ctas_per_sm_dispatch(int G) {
     if (G <= 1) return PartialLauncher<D, 1, PAGED>::ctas_per_sm();
-    if (G <= 2) return PartialLauncher<D, 2, PAGED>::ctas_per_sm();
-    if (G <= 4) return PartialLauncher<D, 4, PAGED>::ctas_per_sm();
     return PartialLauncher<D, 8, PAGED>::ctas_per_sm();
 }
 
 template <int D, bool PAGED>
-cudaError_t launch_dispatch(int G, const PartialParams& pp, dim3 grid, cudaStream_t st) {
-    if (G <= 1) return PartialLauncher<D, 1, PAGED>::launch(pp, grid, st);
-    if (G <= 2) return PartialLauncher<D, 2, PAGED>::launch(pp, grid, st);
-    if (G <= 4) return PartialLauncher<D, 4, PAGED>::launch(pp, grid, st);
-    return PartialLauncher<D, 8, PAGED>::launch(pp, grid, st);
+cudaError_t launch_dispatch(int G, const CUtensorMap& tk, const CUtensorMap& tv, const PartialParams& pp, dim3 grid,
+                            cudaStream_t st) {
+    if (G <= 1) return PartialLauncher<D, 1, PAGED>::launch(tk, tv, pp, grid, st);
+    return PartialLauncher<D, 8, PAGED>::launch(tk, tv, pp, grid, st);
 }
 
 }  // namespace
@@ -429,10 +522,18 @@ cudaError_t launch_merge(const float* part_o, const float* part_ml, const int32_
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     if (a.B == 0) return cudaSuccess;
+    const bool paged = a.page_table != nullptr;
+    const uint64_t rows = paged ? (uint64_t)a.num_pages * a.Hkv * kTile : (uint64_t)a.B * a.Hkv * a.L_max;
+    CUtensorMap tk, tv;
+    if (rows == 0) {
+        // nothing can be read (an empty pool or cache): any well-formed map will do
+        if (!make_row_map(&tk, a.q, 1, (uint32_t)a.D * 2) || !make_row_map(&tv, a.q, 1, (uint32_t)a.D * 2))
+            return cudaErrorInvalidValue;
+    } else if (!make_row_map(&tk, a.k, rows, (uint32_t)a.D * 2) || !make_row_map(&tv, a.v, rows, (uint32_t)a.D * 2)) {
+        return cudaErrorInvalidValue;
+    }
     PartialParams pp;
     pp.q = static_cast<const uint16_t*>(a.q);
-    pp.k = static_cast<const uint16_t*>(a.k);
-    pp.v = static_cast<const uint16_t*>(a.v);
     pp.seq_lens = a.seq_lens;
     pp.page_table = a.page_table;
     pp.max_pages = a.max_pages;
@@ -444,19 +545,19 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     pp.scale_log2 = a.scale * kLog2e;
     pp.splits = a.splits;
     pp.chunk_fixed = a.chunk_fixed;
-    pp.part_o = a.part_o;
-    pp.part_ml = a.part_ml;
-    pp.out = a.out;
-    pp.out_bf16 = a.out_bf16;
-    pp.lse = a.lse;
-    pp.direct = a.splits == 1 ? 1 : 0;
+    pp.st.part_o = a.part_o;
+    pp.st.part_ml = a.part_ml;
+    pp.st.out = a.out;
+    pp.st.out_bf16 = a.out_bf16;
+    pp.st.lse = a.lse;
+    pp.st.direct = a.splits == 1 ? 1 : 0;
+    pp.st.splits = a.splits;
     const dim3 grid((unsigned)a.splits, (unsigned)a.Hkv, (unsigned)a.B);
-    const bool paged = a.page_table != nullptr;
     cudaError_t e;
-    if (a.D == 128) e = paged ? launch_dispatch<128, true>(pp.G, pp, grid, stream)
-                              : launch_dispatch<128, false>(pp.G, pp, grid, stream);
-    else e = paged ? launch_dispatch<64, true>(pp.G, pp, grid, stream)
-                   : launch_dispatch<64, false>(pp.G, pp, grid, stream);
+    if (a.D == 128) e = paged ? launch_dispatch<128, true>(pp.G, tk, tv, pp, grid, stream)
+                              : launch_dispatch<128, false>(pp.G, tk, tv, pp, grid, stream);
+    else e = paged ? launch_dispatch<64, true>(pp.G, tk, tv, pp, grid, stream)
+                   : launch_dispatch<64, false>(pp.G, tk, tv, pp, grid, stream);
     if (e != cudaSuccess || a.splits == 1) return e;
     return launch_merge(a.part_o, a.part_ml, a.seq_lens, a.B, a.Hq, a.L_max, a.D, a.splits, a.chunk_fixed,
                         a.out, a.out_bf16, a.lse, stream);

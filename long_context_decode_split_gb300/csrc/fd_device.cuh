@@ -40,6 +40,11 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// bf16x2 word -> two fp32 (exact: bf16 is the top half of binary32).
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
 __device__ __forceinline__ unsigned long long global_timer_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -115,6 +120,79 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
+// Tiled TMA load of one 64-row x 128-byte box (coordinates: x in 2-byte
+// units along the row, y = row) into `dst` (1024-byte aligned, 128-byte
+// swizzle as encoded in the tensor map).  Completion counts 8192 bytes on `bar`.
+__device__ __forceinline__ void tma_load_box(void* dst, const void* tmap, int x, int y, uint64_t* bar,
+                                             uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar)),
+        "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
+constexpr int kBoxBytes = 64 * 128;  // one TMA box: 64 rows x 128 bytes
+
+// Byte offset of 16-byte chunk `chunk` of row `row` in a tile stored as
+// consecutive 64x128-byte boxes with the 128-byte swizzle (chunk c of a row
+// lives in box c / 8 at position (c % 8) ^ (row % 8)).
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+    return (uint32_t)((chunk >> 3) * kBoxBytes + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+}
+
+// ldmatrix: four 8x8 b16 matrices; lanes 8j..8j+7 give the row addresses of matrix j.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+// D += A * B for one m16n8k16 tile, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Same with fp16 inputs.
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two fp32 -> packed bf16x2 (round to nearest even); `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Probability pair p -> bf16 hi part and bf16 remainder (p ~= hi + lo with
+// relative error ~2^-16), so the P.V product keeps fp32-level accuracy.
+__device__ __forceinline__ void split_bf16(float p0, float p1, uint32_t& hi, uint32_t& lo) {
+    hi = pack_bf16(p0, p1);
+    const float2 h = bf16x2_to_float2(hi);
+    lo = pack_bf16(p0 - h.x, p1 - h.y);
+}
+
 // Programmatic dependent launch: let the next kernel in the stream start its
 // prologue, and (in that kernel) wait for this grid's results.
 __device__ __forceinline__ void pdl_launch_dependents() {
@@ -138,10 +216,6 @@ __device__ __forceinline__ uint4 lds128(const void* p) {
     return v;
 }
 
-// bf16x2 word -> two fp32 (exact: bf16 is the top half of binary32).
-__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
-    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-}
 
 __device__ __forceinline__ float exp2_approx(float x) {
     float y;
@@ -191,6 +265,48 @@ struct StoreTarget {
     int splits;
 };
 
+// Final step of both combines: red_o/red_m/red_l hold every consumer warp's
+// (O, m, l) per query; merge the warps and write the CTA's result.
+template <int D, int GP, int CW>
+__device__ __forceinline__ void store_combined(unsigned char* smem, int tid, int G, int row0, int split,
+                                               const StoreTarget& st) {
+    const float* red_o = reinterpret_cast<const float*>(smem);
+    const float* red_m = red_o + CW * GP * D;
+    const float* red_l = red_m + CW * GP;
+    for (int idx = tid; idx < G * D; idx += CW * 32) {
+        const int g = idx / D, dim = idx % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < CW; ++w) M = fmaxf(M, red_m[w * GP + g]);
+        float lsum = 0.f, acc = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < CW; ++w) {
+                const float mw = red_m[w * GP + g];
+                const float sc = mw == -INFINITY ? 0.f : exp2_approx(mw - M);
+                lsum += sc * red_l[w * GP + g];
+                acc += sc * red_o[(w * GP + g) * D + dim];
+            }
+        }
+        const int row = row0 + g;
+        const float val = lsum > 0.f ? acc / lsum : 0.f;
+        if (st.direct) {
+            const size_t oi = (size_t)row * D + dim;
+            if (st.out_bf16) static_cast<uint16_t*>(st.out)[oi] = f32_to_bf16_bits(val);
+            else static_cast<float*>(st.out)[oi] = val;
+            if (dim == 0 && st.lse) st.lse[row] = lsum > 0.f ? (M + __log2f(lsum)) * kLn2 : -INFINITY;
+        } else {
+            const size_t pi = (size_t)row * st.splits + split;
+            st.part_o[pi * D + dim] = val;
+            if (dim == 0) {
+                st.part_ml[2 * pi + 0] = lsum > 0.f ? M : -INFINITY;
+                st.part_ml[2 * pi + 1] = lsum;
+            }
+        }
+    }
+}
+
+
 // End of a partial pass: every consumer warp holds, per query g of the
 // group, a running max m (log2 units, warp-uniform), a per-lane share of the
 // exp-sum l and, in the lanes of each row group, the output accumulator for
@@ -236,37 +352,42 @@ __device__ __forceinline__ void combine_warps_and_store(unsigned char* smem, int
         }
     }
     named_barrier(1, CW * 32);
-    for (int idx = warp * 32 + lane; idx < G * D; idx += CW * 32) {
-        const int g = idx / D, dim = idx % D;
-        float M = -INFINITY;
+    store_combined<D, GP, CW>(smem, warp * 32 + lane, G, row0, split, st);
+}
+
+// The same for the tensor-core consumers: a warp's output lives in O^T
+// accumulator fragments (o[mt][i] = O[query 2*tig + (i & 1)][dim 16*mt +
+// gid + 8*(i >> 1)], gid = lane / 4, tig = lane % 4), its running max m (log2
+// units) and exp-sum share l belong to query gid (each quad shares m; l is a
+// per-lane share).
+template <int D, int GP, int CW>
+__device__ __forceinline__ void combine_mma_warps_and_store(unsigned char* smem, int warp, int lane, int G, int row0,
+                                                            int split, float m_run, float l_run,
+                                                            float (&o)[D / 16][4], bool failed,
+                                                            const StoreTarget& st) {
+    static_assert(GP == 8, "tensor-core consumers hold 8 query columns");
+    const int gid = lane >> 2, tig = lane & 3;
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+    named_barrier(1, CW * 32);
+    float* red_o = reinterpret_cast<float*>(smem);  // [CW][GP][D]
+    float* red_m = red_o + CW * GP * D;             // [CW][GP]
+    float* red_l = red_m + CW * GP;                 // [CW][GP]
 #pragma unroll
-        for (int w = 0; w < CW; ++w) M = fmaxf(M, red_m[w * GP + g]);
-        float lsum = 0.f, acc = 0.f;
-        if (M != -INFINITY) {
+    for (int mt = 0; mt < D / 16; ++mt) {
 #pragma unroll
-            for (int w = 0; w < CW; ++w) {
-                const float mw = red_m[w * GP + g];
-                const float sc = mw == -INFINITY ? 0.f : exp2_approx(mw - M);
-                lsum += sc * red_l[w * GP + g];
-                acc += sc * red_o[(w * GP + g) * D + dim];
-            }
-        }
-        const int row = row0 + g;
-        const float val = lsum > 0.f ? acc / lsum : 0.f;
-        if (st.direct) {
-            const size_t oi = (size_t)row * D + dim;
-            if (st.out_bf16) static_cast<uint16_t*>(st.out)[oi] = f32_to_bf16_bits(val);
-            else static_cast<float*>(st.out)[oi] = val;
-            if (dim == 0 && st.lse) st.lse[row] = lsum > 0.f ? (M + __log2f(lsum)) * kLn2 : -INFINITY;
-        } else {
-            const size_t pi = (size_t)row * st.splits + split;
-            st.part_o[pi * D + dim] = val;
-            if (dim == 0) {
-                st.part_ml[2 * pi + 0] = lsum > 0.f ? M : -INFINITY;
-                st.part_ml[2 * pi + 1] = lsum;
-            }
+        for (int i = 0; i < 4; ++i) {
+            const int q = 2 * tig + (i & 1);
+            const int dim = 16 * mt + gid + 8 * (i >> 1);
+            red_o[(warp * GP + q) * D + dim] = o[mt][i];
         }
     }
+    if (tig == 0) {
+        red_m[warp * GP + gid] = failed ? -INFINITY : m_run;
+        red_l[warp * GP + gid] = failed ? 0.f : l_run;
+    }
+    named_barrier(1, CW * 32);
+    store_combined<D, GP, CW>(smem, warp * 32 + lane, G, row0, split, st);
 }
 
 }  // namespace fd

@@ -1,0 +1,51 @@
+// fd_tma.h -- host side of the tiled TMA copies: 2-D tensor maps over a row
+// matrix [rows, row_bytes] with 64-row x 128-byte boxes and the 128-byte
+// swizzle.  In shared memory a box is 64 rows of 128 bytes; the 16-byte chunk
+// c of row r sits at chunk position c ^ (r % 8) (box base 1024-byte aligned),
+// which spreads the 8 rows that one tensor-core fragment load touches over
+// all 32 banks.  The encoder is reached through the runtime's driver entry
+// point, so the library needs no link against libcuda.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+namespace fd {
+
+using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+inline EncodeTiledFn tensor_map_encoder() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        tried = true;
+    }
+    return fn;
+}
+
+// Tensor map for `rows` rows of `row_bytes` bytes (a multiple of 128), read
+// as boxes of 64 rows x 128 bytes.  Elements are taken as 16-bit values, so
+// the first coordinate counts 2-byte units; int8 rows work the same way.
+// Returns false when the encoder is unavailable or rejects the arguments.
+inline bool make_row_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t row_bytes) {
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (!enc || (row_bytes % 128) != 0 || rows == 0) return false;
+    const cuuint64_t dims[2] = {row_bytes / 2, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {64, 64};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace fd

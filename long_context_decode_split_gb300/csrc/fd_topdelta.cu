@@ -237,7 +237,8 @@ __device__ __forceinline__ void score_tile_rows(const uint8_t* codes, const uint
 }
 
 template <int D, int GP>
-__global__ void __launch_bounds__((CW + 1) * 32, 1)
+// two CTAs per SM (168 registers) up to groups of 4; groups of 8 need the registers of one
+__global__ void __launch_bounds__((CW + 1) * 32, GP >= 8 ? 1 : 2)
 topdelta_kernel(const TDParams p) {
     using Gm = TGeo<D>;
     using Ly = TLayout<D, GP>;
