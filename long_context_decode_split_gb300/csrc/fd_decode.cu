@@ -69,20 +69,9 @@ struct PartialParams {
     StoreTarget st;
 };
 
-// Tensor-core consumer, one warp, 16 rows of a 64-token tile (queries padded
-// to 8; rows 8-15 of the m16 A operand are zero):
-//   S[q][t]  = Q K^T   m16n8k16, A = Q fragments held in registers, B = K rows
-//                      loaded with ldmatrix from the swizzled tile
-//   online softmax per query (quad = the 4 lanes holding one query's row)
-//   O^T[d][q] += V^T P^T  A = V^T via ldmatrix.trans, B = P^T taken straight
-//                      from the S accumulators, P split into bf16 hi + lo.
-template <int D>
-struct MmaWarpState {
-    uint32_t qa0[D / 16], qa2[D / 16];  // A fragments of Q (rows gid), k-steps of 16 dims
-    float o[D / 16][4];                 // O^T accumulators
-    float m_run, l_run;                 // query gid: running max (log2 units), exp-sum share
-};
-
+// Tensor-core consumer, one warp, 16 rows of a 64-token tile: S = Q K^T on
+// mma.sync (A = Q fragments in registers, B = K rows by ldmatrix from the
+// swizzled tile), then the shared online-softmax / P.V step.
 template <int D>
 __device__ __forceinline__ void mma_consume_tile(MmaWarpState<D>& ws, uint32_t ks, uint32_t vs, unsigned char* vgen,
                                                  int warp, int lane, int rows, float scale_log2) {
@@ -97,51 +86,13 @@ __device__ __forceinline__ void mma_consume_tile(MmaWarpState<D>& ws, uint32_t k
         mma_bf16(sacc[0], ws.qa0[kk], 0u, ws.qa2[kk], 0u, b00, b01);
         mma_bf16(sacc[1], ws.qa0[kk], 0u, ws.qa2[kk], 0u, b10, b11);
     }
-    // rows of this warp past the valid ones: masked scores, zeroed V rows
     const int r0 = warp * 16 + 2 * tig;
     float sc[4];
     sc[0] = r0 < rows ? sacc[0][0] * scale_log2 : -INFINITY;
     sc[1] = r0 + 1 < rows ? sacc[0][1] * scale_log2 : -INFINITY;
     sc[2] = r0 + 8 < rows ? sacc[1][0] * scale_log2 : -INFINITY;
     sc[3] = r0 + 9 < rows ? sacc[1][1] * scale_log2 : -INFINITY;
-    if (warp * 16 + 16 > rows) {
-        // the tile's tail: clear V rows >= rows so 0 * (stale data) cannot make NaN
-        for (int i = lane; i < 16 * (D / 8); i += 32) {
-            const int r = warp * 16 + i / (D / 8);
-            if (r >= rows) *reinterpret_cast<uint4*>(vgen + swz(r, i % (D / 8))) = make_uint4(0u, 0u, 0u, 0u);
-        }
-        // order these generic stores before the tile copy that later refills the stage
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-    }
-    float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const float m_new = fmaxf(ws.m_run, mx);
-    const bool none = m_new == -INFINITY;
-    const float alpha = none ? 1.f : exp2_approx(ws.m_run - m_new);
-    float pr[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) pr[i] = none ? 0.f : exp2_approx(sc[i] - m_new);
-    ws.m_run = m_new;
-    ws.l_run = ws.l_run * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
-    uint32_t h0, l0, h1, l1;
-    split_bf16(pr[0], pr[1], h0, l0);
-    split_bf16(pr[2], pr[3], h1, l1);
-    // rescale: accumulator columns are queries 2*tig and 2*tig+1
-    const float a_even = __shfl_sync(0xffffffffu, alpha, 8 * tig);
-    const float a_odd = __shfl_sync(0xffffffffu, alpha, 8 * tig + 4);
-#pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt) {
-        ws.o[mt][0] *= a_even;
-        ws.o[mt][1] *= a_odd;
-        ws.o[mt][2] *= a_even;
-        ws.o[mt][3] *= a_odd;
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4_t(vs + swz(ld_row, 2 * mt + (mi & 1)), a0, a1, a2, a3);
-        mma_bf16(ws.o[mt], a0, a1, a2, a3, h0, h1);
-        mma_bf16(ws.o[mt], a0, a1, a2, a3, l0, l1);
-    }
+    mma_softmax_pv<D>(ws, sc, vs, vgen, warp, lane, rows);
 }
 
 template <int D, int GP, int CW, int STAGES, bool PAGED, bool MMA>

@@ -146,6 +146,22 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
     return (uint32_t)((chunk >> 3) * kBoxBytes + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
 }
 
+// The same for a box of 64-byte rows with the 64-byte swizzle (chunk c of
+// row r at position c ^ ((r / 2) % 4)).
+__device__ __forceinline__ uint32_t swz64(int row, int chunk) {
+    return (uint32_t)(row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4));
+}
+
+// TMA load of one box of 64 rows x 64 bytes (64-byte swizzle): 4096 bytes.
+__device__ __forceinline__ void tma_load_box64(void* dst, const void* tmap, int y, uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(0), "r"(y), "r"(smem_u32(bar)),
+        "l"(policy)
+        : "memory");
+}
+
 // ldmatrix: four 8x8 b16 matrices; lanes 8j..8j+7 give the row addresses of matrix j.
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -161,7 +177,7 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
 // D += A * B for one m16n8k16 tile, bf16 inputs, fp32 accumulate.
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -171,7 +187,7 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
 // Same with fp16 inputs.
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -252,6 +268,73 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[N], int lane) {
     return r;
 }
 
+
+// State of one tensor-core consumer warp (queries padded to 8; the warp
+// owns 16 rows of every 64-token tile).  gid = lane / 4 is the lane's query,
+// tig = lane % 4.
+template <int D>
+struct MmaWarpState {
+    uint32_t qa0[D / 16], qa2[D / 16];  // bf16 A fragments of Q (row gid), one pair per 16 dims
+    float o[D / 16][4];                 // O^T accumulators: [query 2*tig + (i&1)][dim 16*mt + gid + 8*(i>>1)]
+    float m_run, l_run;                 // query gid: running max (log2 units), per-lane exp-sum share
+};
+
+// Online softmax over one tile for the lane's query and O^T += V^T P^T.
+// sc[i] are the scores (log2 units; -inf = not attended) of the lane's rows
+// warp*16 + 2*tig + (i & 1) + 8*(i >> 1).  V rows at or past `rows` are
+// cleared first (they may hold anything; P is 0 there, but 0 * NaN is NaN).
+// P goes to the tensor cores as bf16 hi + lo, so the product keeps ~2^-16
+// relative accuracy; B = P^T comes straight from the lane's own scores.
+template <int D>
+__device__ __forceinline__ void mma_softmax_pv(MmaWarpState<D>& ws, const float (&sc)[4], uint32_t vs,
+                                               unsigned char* vgen, int warp, int lane, int rows) {
+    const int tig = lane & 3;
+    const int mi = lane >> 3;
+    const int ld_row = warp * 16 + 8 * (mi >> 1) + (lane & 7);
+    if (warp * 16 + 16 > rows) {
+        for (int i = lane; i < 16 * (D / 8); i += 32) {
+            const int r = warp * 16 + i / (D / 8);
+            if (r >= rows) *reinterpret_cast<uint4*>(vgen + swz(r, i % (D / 8))) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        // order these generic stores before the tile copy that later refills the stage
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+    }
+    float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float m_new = fmaxf(ws.m_run, mx);
+    const bool none = m_new == -INFINITY;
+    const float alpha = none ? 1.f : exp2_approx(ws.m_run - m_new);
+    float pr[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) pr[i] = none ? 0.f : exp2_approx(sc[i] - m_new);
+    ws.m_run = m_new;
+    ws.l_run = ws.l_run * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
+    uint32_t h0, l0, h1, l1;
+    split_bf16(pr[0], pr[1], h0, l0);
+    split_bf16(pr[2], pr[3], h1, l1);
+    // rescale only when some query's max moved (accumulator columns are
+    // queries 2*tig and 2*tig+1)
+    if (!__all_sync(0xffffffffu, alpha == 1.f)) {
+        const float a_even = __shfl_sync(0xffffffffu, alpha, 8 * tig);
+        const float a_odd = __shfl_sync(0xffffffffu, alpha, 8 * tig + 4);
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+            ws.o[mt][0] *= a_even;
+            ws.o[mt][1] *= a_odd;
+            ws.o[mt][2] *= a_even;
+            ws.o[mt][3] *= a_odd;
+        }
+    }
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(vs + swz(ld_row, 2 * mt + (mi & 1)), a0, a1, a2, a3);
+        mma_bf16(ws.o[mt], a0, a1, a2, a3, h0, h1);
+        mma_bf16(ws.o[mt], a0, a1, a2, a3, l0, l1);
+    }
+}
 
 // Where a CTA's combined result goes: the final output (one chunk per
 // sequence) or its chunk's slot of the merge workspace.

@@ -31,19 +31,24 @@ inline EncodeTiledFn tensor_map_encoder() {
     return fn;
 }
 
-// Tensor map for `rows` rows of `row_bytes` bytes (a multiple of 128), read
-// as boxes of 64 rows x 128 bytes.  Elements are taken as 16-bit values, so
-// the first coordinate counts 2-byte units; int8 rows work the same way.
+// Tensor map for `rows` rows of `row_bytes` bytes, read as boxes of 64 rows
+// x min(row_bytes, 128) bytes: row_bytes a multiple of 128 uses the 128-byte
+// swizzle, row_bytes == 64 the 64-byte swizzle (chunk c of row r at
+// position c ^ ((r / 2) % 4)).  Elements are taken as 16-bit values, so the
+// first coordinate counts 2-byte units; int8 rows work the same way.
 // Returns false when the encoder is unavailable or rejects the arguments.
 inline bool make_row_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t row_bytes) {
     EncodeTiledFn enc = tensor_map_encoder();
-    if (!enc || (row_bytes % 128) != 0 || rows == 0) return false;
+    if (!enc || rows == 0) return false;
+    if (row_bytes % 128 != 0 && row_bytes != 64) return false;
+    const uint32_t box_bytes = row_bytes >= 128 ? 128 : 64;
     const cuuint64_t dims[2] = {row_bytes / 2, rows};
     const cuuint64_t strides[1] = {row_bytes};
-    const cuuint32_t box[2] = {64, 64};
+    const cuuint32_t box[2] = {box_bytes / 2, 64};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }

@@ -28,6 +28,7 @@
 
 #include "fd_device.cuh"
 #include "fd_internal.h"
+#include "fd_tma.h"
 
 namespace fd {
 
@@ -132,42 +133,38 @@ quantize_kernel(const uint16_t* __restrict__ k, const int32_t* __restrict__ seq_
 
 template <int D>
 struct TGeo {
-    static constexpr int LPR = D / 8;      // lanes per row, 8 channels each
-    static constexpr int RPI = 32 / LPR;   // rows per warp-wide step
-    static constexpr int TPW = kTile / CW; // rows of a tile per warp
-    static constexpr int NIT = TPW / RPI;
-    static constexpr int LOG_LPR = D == 128 ? 4 : 3;
-    static constexpr int LOG_NIT = NIT == 8 ? 3 : NIT == 4 ? 2 : NIT == 2 ? 1 : 0;
-    static constexpr int SH = LOG_LPR - LOG_NIT;
-    static constexpr int CODES_ROW = D / 4;   // bytes
-    static constexpr int MS_ROW = D / 8;      // (mn16, s16) per 32 channels
+    static constexpr int NG = D / 32;          // 32-channel groups
+    static constexpr int KS = D / 16;          // 16-channel k-steps
+    static constexpr int CODES_ROW = D / 4;    // bytes per token row
+    static constexpr int MS_ROW = D / 8;       // (mn16, s16) per group
     static constexpr int RES_ROW = D;
-    static constexpr int RS_ROW = D / 16;     // rs16 per 32 channels
-    static constexpr int V_ROW = 2 * D;
+    static constexpr int RS_ROW = D / 16;      // rs16 per group
     static constexpr int SCAN_STAGE = kTile * (CODES_ROW + MS_ROW);
-    static constexpr int DET_STAGE = kTile * (RES_ROW + RS_ROW + V_ROW);
+    static constexpr int RES_BYTES = kTile * RES_ROW;        // one box
+    static constexpr int V_BYTES = kTile * 2 * D;            // D/64 boxes
+    static constexpr int RS_BYTES = kTile * RS_ROW;
+    static constexpr int DET_STAGE = (RES_BYTES + V_BYTES + RS_BYTES + 1023) / 1024 * 1024;
 };
 
-template <int D, int GP>
+template <int D>
 struct TLayout {
     using Gm = TGeo<D>;
-    static constexpr int SCAN_OFF = 0;
-    static constexpr int DET_OFF = SCAN_OFF + SS * Gm::SCAN_STAGE;
-    static constexpr int DEC_OFF = DET_OFF + DS * Gm::DET_STAGE;                // s~ [DS][64][GP] f32
-    static constexpr int FLAG_OFF = DEC_OFF + DS * kTile * GP * 4;              // need[DS][CW], loaded[DS], scan_rows[SS]
+    static constexpr int DET_OFF = 0;                                          // 1024-aligned boxes
+    static constexpr int SCAN_OFF = DET_OFF + DS * Gm::DET_STAGE;
+    static constexpr int DEC_OFF = SCAN_OFF + SS * Gm::SCAN_STAGE;             // s~ [DS][CW][32][4] f32
+    static constexpr int FLAG_OFF = DEC_OFF + DS * CW * 32 * 16;               // need[DS][CW], loaded[DS], scan_rows[SS]
     static constexpr int BAR_OFF = (FLAG_OFF + (DS * CW + DS + SS) * 4 + 15) / 16 * 16;
-    static constexpr int MH_OFF = BAR_OFF + (2 * SS + 3 * DS) * 8;               // anchor maxima [CW][GP]
-    static constexpr int BYTES = MH_OFF + CW * GP * 4;
-    static_assert(DEC_OFF >= CW * GP * D * 4 + 2 * CW * GP * 4, "epilogue scratch must fit in the rings");
+    static constexpr int MH_OFF = BAR_OFF + (2 * SS + 3 * DS) * 8;             // anchor maxima [CW][8]
+    static constexpr int BYTES = 1024 + MH_OFF + CW * 8 * 4;
+    static_assert(DS * Gm::DET_STAGE >= CW * 8 * D * 4 + 2 * CW * 8 * 4, "epilogue scratch must fit in the rings");
+    static_assert(Gm::DET_STAGE >= Gm::SCAN_STAGE, "anchor staging must fit in one detail stage");
 };
 
 struct TDParams {
     const uint16_t* q;
     const uint8_t* codes;
-    const uint16_t* mn_scale;
-    const int8_t* res;
-    const uint16_t* res_scale;
-    const uint16_t* v;
+    const uint8_t* mn_scale;
+    const uint8_t* res_scale;
     const int32_t* seq_lens;
     int Hq, Hkv, L_max, G;
     float scale, delta;
@@ -178,71 +175,174 @@ struct TDParams {
     StoreTarget st;
 };
 
-// The 2-bit score's contribution of one lane's 8 channels of one row, for
-// every query of the group: s * <q, code> + mn * sum(q) over those channels.
-// Codes are turned into floats exactly: (w & 3<<2i) | 0x4B000000 is the
-// binary32 value 2^23 + code * 4^i; subtracting 2^23 leaves code * 4^i, and
-// the query weights carry the matching 4^-i.  Every operation is an
-// explicitly rounded intrinsic, so all call sites round identically.
-template <int GP>
-__device__ __forceinline__ void scan_partial(uint32_t w16, uint32_t ms_bits, const float2 (&qs)[GP][4],
-                                             const float (&qsum)[GP], float (&out)[GP]) {
-    const float2 magic = make_float2(-8388608.f, -8388608.f);
-    float2 cf[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const uint32_t lo = (w16 & (3u << (4 * e))) | 0x4B000000u;
-        const uint32_t hi = (w16 & (3u << (4 * e + 2))) | 0x4B000000u;
-        cf[e] = __fadd2_rn(make_float2(__uint_as_float(lo), __uint_as_float(hi)), magic);
-    }
-    const float mn = __half2float(__ushort_as_half((unsigned short)(ms_bits & 0xffffu)));
-    const float sc = __half2float(__ushort_as_half((unsigned short)(ms_bits >> 16)));
-#pragma unroll
-    for (int g = 0; g < GP; ++g) {
-        float2 acc = __fmul2_rn(qs[g][0], cf[0]);
-        acc = __ffma2_rn(qs[g][1], cf[1], acc);
-        acc = __ffma2_rn(qs[g][2], cf[2], acc);
-        acc = __ffma2_rn(qs[g][3], cf[3], acc);
-        out[g] = __fmaf_rn(sc, __fadd_rn(acc.x, acc.y), __fmul_rn(mn, qsum[g]));
-    }
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t f16x2_from_f32(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
 }
 
-// Scores s~ (natural-log units) of the warp's 16 rows of one tile.  `codes`
-// and `ms` point at the tile's first row, in shared or global memory;
-// rows >= `rows` are not read when `guard` is set.  On return lane l holds
-// the score of row warp*16 + RPI*((l >> SH) & (NIT-1)) + l / LPR.
-template <int D, int GP>
-__device__ __forceinline__ void score_tile_rows(const uint8_t* codes, const uint16_t* ms, int warp, int lane,
-                                                int rows, bool guard, const float2 (&qs)[GP][4],
-                                                const float (&qsum)[GP], float scale, float (&s)[GP]) {
+// Query fragments of one lane (row gid of the m16 A operand), per 16-channel
+// k-step.  The k order inside a step is permuted to match how the B
+// operands are unpacked (the same permutation on both sides leaves every dot
+// product unchanged):
+//   2-bit codes: k = 2t, 2t+1, 8+2t, 9+2t <-> channels 2t, 2t+8, 2t+1, 2t+9,
+//                the last two unpacked as 4 * code and weighted by q / 4
+//   int8 residual (ldmatrix of 16-byte chunks): k = 2t, 2t+1, 8+2t, 9+2t <->
+//   channels 4t, 4t+1, 4t+2, 4t+3          (t = tig, relative to 16*kk)
+template <int D>
+struct TDQuery {
+    uint32_t qc0[D / 16], qc2[D / 16];  // bf16, for the 2-bit scan
+    uint32_t qr0[D / 16], qr2[D / 16];  // fp16, for the residual
+    float qsum[D / 32];                 // sum of the query over each 32-channel group
+};
+
+// Scores s~ (natural-log units) of the warp's 16 rows of a tile whose codes
+// and (mn16, s16) rows sit in shared memory (plain row-major).  st[i] is the
+// score of row warp*16 + 2*tig + (i & 1) + 8*(i >> 1) for the lane's query.
+//   s~ = scale * sum_g ( s_g * <q, code>_g + mn_g * sum_g(q) )
+// The per-group dots run on the tensor cores with the codes as exact bf16
+// (0x4300 | c is 128 + c; one subtraction leaves c); the group sums are
+// combined with explicitly rounded operations in a fixed order.
+template <int D>
+__device__ __forceinline__ void scan_tile(const unsigned char* codes, const unsigned char* ms, int warp, int lane,
+                                          const TDQuery<D>& tq, float scale, float (&st)[4]) {
     using Gm = TGeo<D>;
-    const int c = lane % Gm::LPR;
-    const int rg = lane / Gm::LPR;
-    float part[GP][Gm::NIT];
+    const int gid = lane >> 2, tig = lane & 3;
+    float acc[Gm::NG][2][4];
 #pragma unroll
-    for (int i = 0; i < Gm::NIT; ++i) {
-        const int row = warp * Gm::TPW + Gm::RPI * i + rg;
-        uint32_t w16 = 0, msb = 0;
-        if (!guard || row < rows) {
-            w16 = *reinterpret_cast<const uint16_t*>(codes + row * Gm::CODES_ROW + c * 2);
-            msb = *reinterpret_cast<const uint32_t*>(ms + row * (Gm::MS_ROW / 2) + (c / 4) * 2);
+    for (int g = 0; g < Gm::NG; ++g)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[g][j][i] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const uint4* crow = reinterpret_cast<const uint4*>(codes + (warp * 16 + 8 * j + gid) * Gm::CODES_ROW);
+#pragma unroll
+        for (int kq = 0; kq < Gm::KS / 4; ++kq) {
+            const uint4 w4 = crow[kq];
+            const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int kk = 4 * kq + e;
+                const uint32_t w = wv[e] >> (4 * tig);
+                const uint32_t b0 = bf16x2_sub((w & 0x00030003u) | 0x43004300u, 0x43004300u);
+                // codes of the odd pair stay at bits 2-3: 4 * code (exact); qc2 carries the 1/4
+                const uint32_t b1 = bf16x2_sub((w & 0x000C000Cu) | 0x43004300u, 0x43004300u);
+                mma_bf16(acc[kk >> 1][j], tq.qc0[kk], 0u, tq.qc2[kk], 0u, b0, b1);
+            }
         }
-        float pg[GP];
-        scan_partial<GP>(w16, msb, qs, qsum, pg);
-#pragma unroll
-        for (int g = 0; g < GP; ++g) part[g][i] = pg[g];
     }
+    // per lane: two rows per n-tile (columns 2*tig, 2*tig+1), combined pairwise
 #pragma unroll
-    for (int g = 0; g < GP; ++g) s[g] = __fmul_rn(transpose_reduce<Gm::NIT, Gm::LPR>(part[g], lane), scale);
+    for (int j = 0; j < 2; ++j) {
+        const int row = warp * 16 + 8 * j + 2 * tig;
+        uint32_t ma[Gm::NG], mb[Gm::NG];
+        if constexpr (Gm::NG == 4) {
+            const uint4 a = *reinterpret_cast<const uint4*>(ms + row * Gm::MS_ROW);
+            const uint4 bq = *reinterpret_cast<const uint4*>(ms + (row + 1) * Gm::MS_ROW);
+            ma[0] = a.x; ma[1] = a.y; ma[2] = a.z; ma[3] = a.w;
+            mb[0] = bq.x; mb[1] = bq.y; mb[2] = bq.z; mb[3] = bq.w;
+        } else {
+            const uint2 a = *reinterpret_cast<const uint2*>(ms + row * Gm::MS_ROW);
+            const uint2 bq = *reinterpret_cast<const uint2*>(ms + (row + 1) * Gm::MS_ROW);
+            ma[0] = a.x; ma[1] = a.y;
+            mb[0] = bq.x; mb[1] = bq.y;
+        }
+        float2 v = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int g = 0; g < Gm::NG; ++g) {
+            const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&ma[g]));  // (mn, s) of row
+            const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&mb[g]));  // (mn, s) of row + 1
+            const float2 mn2 = make_float2(fa.x, fb.x), s2 = make_float2(fa.y, fb.y);
+            const float2 t = __ffma2_rn(s2, make_float2(acc[g][j][0], acc[g][j][1]),
+                                        __fmul2_rn(mn2, make_float2(tq.qsum[g], tq.qsum[g])));
+            v = __fadd2_rn(v, t);
+        }
+        st[2 * j] = __fmul_rn(v.x, scale);
+        st[2 * j + 1] = __fmul_rn(v.y, scale);
+    }
 }
 
-template <int D, int GP>
-// two CTAs per SM (168 registers) up to groups of 4; groups of 8 need the registers of one
-__global__ void __launch_bounds__((CW + 1) * 32, GP >= 8 ? 1 : 2)
-topdelta_kernel(const TDParams p) {
+// Residual term sum_g rs_g * <q, rq>_g of the warp's 16 rows (same row
+// order as scan_tile).  The int8 residual tile is one swizzled box; each
+// lane's ldmatrix word holds 4 consecutive bytes, turned into exact fp16 by
+// prmt with 0x64 high bytes (1152 + x) and one subtraction.
+template <int D>
+__device__ __forceinline__ void residual_tile(uint32_t res_s, const unsigned char* rs, int warp, int lane,
+                                              const TDQuery<D>& tq, float (&rt)[4]) {
     using Gm = TGeo<D>;
-    using Ly = TLayout<D, GP>;
-    extern __shared__ __align__(128) unsigned char smem[];
+    const int tig = lane & 3;
+    const int mi = lane >> 3;
+    const int ld_row = warp * 16 + 8 * (mi >> 1) + (lane & 7);
+    float acc[Gm::NG][2][4];
+#pragma unroll
+    for (int g = 0; g < Gm::NG; ++g)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[g][j][i] = 0.f;
+#pragma unroll
+    for (int g = 0; g < Gm::NG; ++g) {
+        const int chunk = 2 * g + (mi & 1);
+        const uint32_t addr = res_s + (D == 128 ? swz(ld_row, chunk) : swz64(ld_row, chunk));
+        uint32_t r[4];
+        ldsm_x4(addr, r[0], r[1], r[2], r[3]);  // (n-tile 0, kk 2g), (0, 2g+1), (1, 2g), (1, 2g+1)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const uint32_t u = r[m] ^ 0x80808080u;
+            const uint32_t b0 = f16x2_sub(__byte_perm(u, 0x64646464u, 0x4140), 0x64806480u);
+            const uint32_t b1 = f16x2_sub(__byte_perm(u, 0x64646464u, 0x4342), 0x64806480u);
+            const int kk = 2 * g + (m & 1);
+            mma_f16(acc[g][m >> 1], tq.qr0[kk], 0u, tq.qr2[kk], 0u, b0, b1);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int row = warp * 16 + 8 * j + 2 * tig;
+        float2 v = make_float2(0.f, 0.f);
+        if constexpr (Gm::NG == 4) {
+            const uint2 a = *reinterpret_cast<const uint2*>(rs + row * Gm::RS_ROW);
+            const uint2 bq = *reinterpret_cast<const uint2*>(rs + (row + 1) * Gm::RS_ROW);
+            const float2 a01 = __half22float2(*reinterpret_cast<const __half2*>(&a.x));
+            const float2 a23 = __half22float2(*reinterpret_cast<const __half2*>(&a.y));
+            const float2 b01 = __half22float2(*reinterpret_cast<const __half2*>(&bq.x));
+            const float2 b23 = __half22float2(*reinterpret_cast<const __half2*>(&bq.y));
+            v = __ffma2_rn(make_float2(a01.x, b01.x), make_float2(acc[0][j][0], acc[0][j][1]), v);
+            v = __ffma2_rn(make_float2(a01.y, b01.y), make_float2(acc[1][j][0], acc[1][j][1]), v);
+            v = __ffma2_rn(make_float2(a23.x, b23.x), make_float2(acc[2][j][0], acc[2][j][1]), v);
+            v = __ffma2_rn(make_float2(a23.y, b23.y), make_float2(acc[3][j][0], acc[3][j][1]), v);
+        } else {
+            const uint32_t a = *reinterpret_cast<const uint32_t*>(rs + row * Gm::RS_ROW);
+            const uint32_t bq = *reinterpret_cast<const uint32_t*>(rs + (row + 1) * Gm::RS_ROW);
+            const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&a));
+            const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&bq));
+            v = __ffma2_rn(make_float2(fa.x, fb.x), make_float2(acc[0][j][0], acc[0][j][1]), v);
+            v = __ffma2_rn(make_float2(fa.y, fb.y), make_float2(acc[1][j][0], acc[1][j][1]), v);
+        }
+        rt[2 * j] = v.x;
+        rt[2 * j + 1] = v.y;
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__((CW + 1) * 32, 2)
+topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant__ CUtensorMap tm_v,
+                const TDParams p) {
+    using Gm = TGeo<D>;
+    using Ly = TLayout<D>;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     float* dec_s = reinterpret_cast<float*>(smem + Ly::DEC_OFF);
     int* need = reinterpret_cast<int*>(smem + Ly::FLAG_OFF);
     int* loaded = need + DS * CW;
@@ -266,7 +366,7 @@ topdelta_kernel(const TDParams p) {
     const int t0 = split * chunk;
     const int t1 = min(L, t0 + chunk);
     const int hq0 = h * p.G;
-    const size_t head_row0 = ((size_t)b * p.Hkv + h) * (size_t)p.L_max;
+    const int head_row0 = (b * p.Hkv + h) * p.L_max;
 
     if (t0 >= t1) {
         pdl_launch_dependents();
@@ -299,20 +399,22 @@ topdelta_kernel(const TDParams p) {
     if (warp == CW) {
         // ----------------------------- producer --------------------------------
         if (lane == 0) {
+            prefetch_tmap(&tm_res);
+            prefetch_tmap(&tm_v);
             const uint64_t pol = l2_evict_first_policy();
             auto rows_of = [&](int t) { return min(kTile, t1 - (t0 + t * kTile)); };
             auto copy_rows = [&](int t) { return (rows_of(t) + 3) & ~3; };  // L_max % 4 == 0 keeps this in bounds
             auto issue_scan = [&](int k) -> bool {
                 const int s = k % SS;
                 if (!mbar_wait(&scan_empty[s], ((uint32_t)(k / SS) & 1u) ^ 1u)) return false;
-                const size_t row0 = head_row0 + t0 + (size_t)k * kTile;
+                const size_t row0 = (size_t)head_row0 + t0 + (size_t)k * kTile;
                 const uint32_t rc = (uint32_t)copy_rows(k);
                 unsigned char* dst = smem + Ly::SCAN_OFF + s * Gm::SCAN_STAGE;
                 scan_rows[s] = rows_of(k);
                 mbar_arrive_expect_tx(&scan_full[s], rc * (Gm::CODES_ROW + Gm::MS_ROW));
                 bulk_g2s(dst, p.codes + row0 * Gm::CODES_ROW, rc * Gm::CODES_ROW, &scan_full[s], pol);
-                bulk_g2s(dst + kTile * Gm::CODES_ROW, reinterpret_cast<const uint8_t*>(p.mn_scale) + row0 * Gm::MS_ROW,
-                         rc * Gm::MS_ROW, &scan_full[s], pol);
+                bulk_g2s(dst + kTile * Gm::CODES_ROW, p.mn_scale + row0 * Gm::MS_ROW, rc * Gm::MS_ROW, &scan_full[s],
+                         pol);
                 return true;
             };
             bool ok = true;
@@ -327,17 +429,18 @@ topdelta_kernel(const TDParams p) {
                 int any = 0;
                 for (int w = 0; w < CW; ++w) any |= need[s * CW + w];
                 if (any) {
-                    const size_t row0 = head_row0 + t0 + (size_t)t * kTile;
+                    const int y = head_row0 + t0 + t * kTile;
                     const uint32_t rc = (uint32_t)copy_rows(t);
                     unsigned char* dst = smem + Ly::DET_OFF + s * Gm::DET_STAGE;
                     loaded[s] = 1;
-                    mbar_arrive_expect_tx(&det_full[s], rc * (Gm::RES_ROW + Gm::RS_ROW + Gm::V_ROW));
-                    bulk_g2s(dst, p.res + row0 * Gm::RES_ROW, rc * Gm::RES_ROW, &det_full[s], pol);
-                    bulk_g2s(dst + kTile * Gm::RES_ROW,
-                             reinterpret_cast<const uint8_t*>(p.res_scale) + row0 * Gm::RS_ROW, rc * Gm::RS_ROW,
-                             &det_full[s], pol);
-                    bulk_g2s(dst + kTile * (Gm::RES_ROW + Gm::RS_ROW), p.v + row0 * D, rc * Gm::V_ROW, &det_full[s],
-                             pol);
+                    mbar_arrive_expect_tx(&det_full[s], Gm::RES_BYTES + Gm::V_BYTES + rc * Gm::RS_ROW);
+                    if (D == 128) tma_load_box(dst, &tm_res, 0, y, &det_full[s], pol);
+                    else tma_load_box64(dst, &tm_res, y, &det_full[s], pol);
+#pragma unroll
+                    for (int bx = 0; bx < D / 64; ++bx)
+                        tma_load_box(dst + Gm::RES_BYTES + bx * kBoxBytes, &tm_v, 64 * bx, y, &det_full[s], pol);
+                    bulk_g2s(dst + Gm::RES_BYTES + Gm::V_BYTES, p.res_scale + (size_t)y * Gm::RS_ROW,
+                             rc * Gm::RS_ROW, &det_full[s], pol);
                 } else {
                     loaded[s] = 0;
                     mbar_arrive(&det_full[s]);
@@ -351,98 +454,94 @@ topdelta_kernel(const TDParams p) {
     }
 
     // ------------------------------- consumers -----------------------------------
-    const int c = lane % Gm::LPR;
-    const int rg = lane / Gm::LPR;
-    const int my_i = (lane >> Gm::SH) & (Gm::NIT - 1);
-    const int my_row = warp * Gm::TPW + Gm::RPI * my_i + rg;
-    const bool my_dup = (lane & ((1 << Gm::SH) - 1)) != 0;
-
-    // query weights for my 8 channels: exact (for the residual and V passes)
-    // and scaled by 4^-i (for the 2-bit codes), plus their sum
-    float2 qv[GP][4], qs[GP][4];
-    float qsum[GP];
+    const int gid = lane >> 2, tig = lane & 3;
+    const bool q_real = gid < p.G;
+    TDQuery<D> tq;
+    MmaWarpState<D> ws;
+    {
+        const uint16_t* qrow = p.q + (size_t)(b * p.Hq + hq0 + gid) * D;
+        auto qf = [&](int c) { return q_real ? __uint_as_float((uint32_t)qrow[c] << 16) : 0.f; };
+        auto qb = [&](int c) { return q_real ? (uint32_t)qrow[c] : 0u; };
 #pragma unroll
-    for (int g = 0; g < GP; ++g) {
-        float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (g < p.G) {
-            const uint4 w = *reinterpret_cast<const uint4*>(p.q + (size_t)(b * p.Hq + hq0 + g) * D + c * 8);
-            const float2 a0 = bf16x2_to_float2(w.x), a1 = bf16x2_to_float2(w.y);
-            const float2 a2 = bf16x2_to_float2(w.z), a3 = bf16x2_to_float2(w.w);
-            f[0] = a0.x; f[1] = a0.y; f[2] = a1.x; f[3] = a1.y;
-            f[4] = a2.x; f[5] = a2.y; f[6] = a3.x; f[7] = a3.y;
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const int c0 = 16 * kk;
+            tq.qc0[kk] = qb(c0 + 2 * tig) | (qb(c0 + 2 * tig + 8) << 16);
+            tq.qc2[kk] = pack_bf16(0.25f * qf(c0 + 2 * tig + 1), 0.25f * qf(c0 + 2 * tig + 9));  // exact
+            tq.qr0[kk] = f16x2_from_f32(qf(c0 + 4 * tig), qf(c0 + 4 * tig + 1));
+            tq.qr2[kk] = f16x2_from_f32(qf(c0 + 4 * tig + 2), qf(c0 + 4 * tig + 3));
+            ws.qa0[kk] = 0u;
+            ws.qa2[kk] = 0u;
         }
-        float sum = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) sum = __fadd_rn(sum, f[i]);
-        qsum[g] = sum;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            qv[g][e] = make_float2(f[2 * e], f[2 * e + 1]);
-            // channel 2e at bits 4e: weight 4^-(2e); channel 2e+1 at bits 4e+2: 4^-(2e+1)
-            const float w0 = __int_as_float((127 - 4 * e) << 23);  // 4^-(2e), exact
-            const float w1 = __int_as_float((125 - 4 * e) << 23);  // 4^-(2e+1)
-            qs[g][e] = make_float2(__fmul_rn(f[2 * e], w0), __fmul_rn(f[2 * e + 1], w1));
+        for (int g = 0; g < D / 32; ++g) {
+            float sum = 0.f;
+            for (int c = 0; c < 32; ++c) sum = __fadd_rn(sum, qf(32 * g + c));
+            tq.qsum[g] = sum;
         }
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) ws.o[mt][i] = 0.f;
+        ws.m_run = -INFINITY;
+        ws.l_run = 0.f;
     }
 
     // ---------------- anchor pass: pseudo-max per query head --------------------
-    float mh[GP];
-#pragma unroll
-    for (int g = 0; g < GP; ++g) mh[g] = -INFINITY;
+    // Anchor tiles are staged in the first detail stage (untouched until the
+    // first tile is flagged) in the scan ring's layout and scored by the same
+    // code, so m^ equals the scan's s~ of the best anchor bit for bit.
+    float mh = -INFINITY;
     {
-        const int sink_end = min(p.n_sink, L);              // anchors [0, sink_end)
-        const int win_beg = max(0, L - p.window);            // anchors [win_beg, L)
-        const int ts_end = (sink_end + kTile - 1) / kTile;   // sink tiles [0, ts_end)
+        unsigned char* stage = smem + Ly::DET_OFF;
+        const int sink_end = min(p.n_sink, L);
+        const int win_beg = max(0, L - p.window);
+        const int ts_end = (sink_end + kTile - 1) / kTile;
         const int tw_beg = win_beg < L ? win_beg / kTile : (L + kTile - 1) / kTile;
-        const int tw_end = (L + kTile - 1) / kTile;          // window tiles [tw_beg, tw_end)
+        const int tw_end = (L + kTile - 1) / kTile;
+        const int tid = warp * 32 + lane;
         for (int T = 0; T < tw_end; ++T) {
             if (T >= ts_end && T < tw_beg) T = tw_beg;
             if (T >= tw_end) break;
             const int tb = T * kTile;
             const int rows = min(kTile, L - tb);
-            float s[GP];
-            score_tile_rows<D, GP>(p.codes + (head_row0 + tb) * Gm::CODES_ROW,
-                                   p.mn_scale + (head_row0 + tb) * (Gm::MS_ROW / 2), warp, lane, rows, true, qs,
-                                   qsum, p.scale, s);
-            const int j = tb + my_row;
-            const bool anchor = my_row < rows && (j < sink_end || j >= win_beg);
+            named_barrier(1, CW * 32);  // the staging area is free
+            constexpr int CV = kTile * Gm::CODES_ROW / 16, MV = kTile * Gm::MS_ROW / 16;
+            for (int i = tid; i < CV + MV; i += CW * 32) {
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (i < CV) {
+                    const int r = i * 16 / Gm::CODES_ROW;  // first row this 16-byte vector covers
+                    if (r < rows) v = reinterpret_cast<const uint4*>(p.codes + (size_t)(head_row0 + tb) * Gm::CODES_ROW)[i];
+                    reinterpret_cast<uint4*>(stage)[i] = v;
+                } else {
+                    const int k = i - CV;
+                    const int r = k * 16 / Gm::MS_ROW;  // first row this 16-byte vector covers
+                    if (r < rows) v = reinterpret_cast<const uint4*>(p.mn_scale + (size_t)(head_row0 + tb) * Gm::MS_ROW)[k];
+                    reinterpret_cast<uint4*>(stage + kTile * Gm::CODES_ROW)[k] = v;
+                }
+            }
+            named_barrier(1, CW * 32);
+            float st[4];
+            scan_tile<D>(stage, stage + kTile * Gm::CODES_ROW, warp, lane, tq, p.scale, st);
 #pragma unroll
-            for (int g = 0; g < GP; ++g)
-                if (anchor) mh[g] = fmaxf(mh[g], s[g]);
+            for (int i = 0; i < 4; ++i) {
+                const int r = warp * 16 + 2 * tig + (i & 1) + 8 * (i >> 1);
+                const int j = tb + r;
+                if (r < rows && (j < sink_end || j >= win_beg)) mh = fmaxf(mh, st[i]);
+            }
         }
-#pragma unroll
-        for (int g = 0; g < GP; ++g) {
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) mh[g] = fmaxf(mh[g], __shfl_xor_sync(0xffffffffu, mh[g], off));
-            if (lane == 0) mh_red[warp * GP + g] = mh[g];
-        }
+        mh = fmaxf(mh, __shfl_xor_sync(0xffffffffu, mh, 1));
+        mh = fmaxf(mh, __shfl_xor_sync(0xffffffffu, mh, 2));
+        if (tig == 0) mh_red[warp * 8 + gid] = mh;
+        // staging stores must be ordered before the tile copies that reuse the area
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         named_barrier(1, CW * 32);
 #pragma unroll
-        for (int g = 0; g < GP; ++g) {
-            float m = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < CW; ++w) m = fmaxf(m, mh_red[w * GP + g]);
-            mh[g] = m;
-        }
+        for (int w = 0; w < CW; ++w) mh = fmaxf(mh, mh_red[w * 8 + gid]);
     }
-    float thr[GP];
-#pragma unroll
-    for (int g = 0; g < GP; ++g) thr[g] = __fsub_rn(mh[g], p.delta);  // delta = inf keeps every key
-
-    float m_run[GP], l_lane[GP];
-    float2 o[GP][4];
-    int cnt[GP];
-#pragma unroll
-    for (int g = 0; g < GP; ++g) {
-        m_run[g] = -INFINITY;
-        l_lane[g] = 0.f;
-        cnt[g] = 0;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) o[g][e] = make_float2(0.f, 0.f);
-    }
+    const float thr = __fsub_rn(mh, p.delta);  // delta = inf keeps every key
+    int cnt = 0;
     bool failed = false;
 
-    // scan one tile: s~ to the decision slot, flag the tile if any key passes
     auto scan_step = [&](int k) {
         const int s = k % SS;
         if (!warp_wait(&scan_full[s], (uint32_t)(k / SS) & 1u)) {
@@ -451,15 +550,15 @@ topdelta_kernel(const TDParams p) {
         }
         const int rows = scan_rows[s];
         const unsigned char* base = smem + Ly::SCAN_OFF + s * Gm::SCAN_STAGE;
-        float sc[GP];
-        score_tile_rows<D, GP>(base, reinterpret_cast<const uint16_t*>(base + kTile * Gm::CODES_ROW), warp, lane,
-                               rows, false, qs, qsum, p.scale, sc);
+        float st[4];
+        scan_tile<D>(base, base + kTile * Gm::CODES_ROW, warp, lane, tq, p.scale, st);
         const int ds = k % DS;
+        reinterpret_cast<float4*>(dec_s)[(ds * CW + warp) * 32 + lane] = make_float4(st[0], st[1], st[2], st[3]);
         bool any = false;
 #pragma unroll
-        for (int g = 0; g < GP; ++g) {
-            if (!my_dup) dec_s[(ds * kTile + my_row) * GP + g] = sc[g];
-            any |= (g < p.G) && (my_row < rows) && (sc[g] >= thr[g]);
+        for (int i = 0; i < 4; ++i) {
+            const int r = warp * 16 + 2 * tig + (i & 1) + 8 * (i >> 1);
+            any |= q_real && r < rows && st[i] >= thr;
         }
         any = __any_sync(0xffffffffu, any);
         __syncwarp();
@@ -485,95 +584,28 @@ topdelta_kernel(const TDParams p) {
         if (loaded[ds]) {
             const int tok0 = t0 + t * kTile;
             const int rows = min(kTile, t1 - tok0);
-            const unsigned char* rb = smem + Ly::DET_OFF + ds * Gm::DET_STAGE;
-            const unsigned char* rsb = rb + kTile * Gm::RES_ROW;
-            const unsigned char* vb = rsb + kTile * Gm::RS_ROW;
-            // residual term per row: rs * <q, rq> over my 8 channels, then butterfly
-            float part[GP][Gm::NIT];
+            unsigned char* st_base = smem + Ly::DET_OFF + ds * Gm::DET_STAGE;
+            float rt[4];
+            residual_tile<D>(smem_u32(st_base), st_base + Gm::RES_BYTES + Gm::V_BYTES, warp, lane, tq, rt);
+            const float4 sv = reinterpret_cast<const float4*>(dec_s)[(ds * CW + warp) * 32 + lane];
+            const float stv[4] = {sv.x, sv.y, sv.z, sv.w};
+            float sc[4];
 #pragma unroll
-            for (int i = 0; i < Gm::NIT; ++i) {
-                const int row = warp * Gm::TPW + Gm::RPI * i + rg;
-                const uint2 w = *reinterpret_cast<const uint2*>(rb + row * Gm::RES_ROW + c * 8);
-                const float rsf = __half2float(__ushort_as_half(
-                    *reinterpret_cast<const unsigned short*>(rsb + row * Gm::RS_ROW + (c / 4) * 2)));
-                float2 rf[4];
-                rf[0] = make_float2((float)(int8_t)(w.x & 0xff), (float)(int8_t)((w.x >> 8) & 0xff));
-                rf[1] = make_float2((float)(int8_t)((w.x >> 16) & 0xff), (float)(int8_t)(w.x >> 24));
-                rf[2] = make_float2((float)(int8_t)(w.y & 0xff), (float)(int8_t)((w.y >> 8) & 0xff));
-                rf[3] = make_float2((float)(int8_t)((w.y >> 16) & 0xff), (float)(int8_t)(w.y >> 24));
-#pragma unroll
-                for (int g = 0; g < GP; ++g) {
-                    float2 acc = f2mul(qv[g][0], rf[0]);
-                    acc = f2fma(qv[g][1], rf[1], acc);
-                    acc = f2fma(qv[g][2], rf[2], acc);
-                    acc = f2fma(qv[g][3], rf[3], acc);
-                    part[g][i] = rsf * (acc.x + acc.y);
-                }
-            }
-            float sx[GP];
-            bool sel[GP];
-            const bool my_valid = my_row < rows;
-#pragma unroll
-            for (int g = 0; g < GP; ++g) {
-                const float rterm = transpose_reduce<Gm::NIT, Gm::LPR>(part[g], lane) * p.scale;
-                const float st = dec_s[(ds * kTile + my_row) * GP + g];
-                sel[g] = my_valid && (g < p.G) && (st >= thr[g]);
-                sx[g] = sel[g] ? (st + rterm) * kLog2e : -INFINITY;
-                if (sel[g] && !my_dup) {
-                    ++cnt[g];
+            for (int i = 0; i < 4; ++i) {
+                const int r = warp * 16 + 2 * tig + (i & 1) + 8 * (i >> 1);
+                const bool sel = q_real && r < rows && stv[i] >= thr;
+                sc[i] = sel ? fmaf(p.scale, rt[i], stv[i]) * kLog2e : -INFINITY;
+                if (sel) {
+                    ++cnt;
                     if (p.sel_mask) {
-                        const int j = tok0 + my_row;
+                        const int j = tok0 + r;
                         const int words = (p.L_max + 31) / 32;
-                        atomicOr(&p.sel_mask[(size_t)(b * p.Hq + hq0 + g) * words + j / 32], 1u << (j % 32));
+                        atomicOr(&p.sel_mask[(size_t)(b * p.Hq + hq0 + gid) * words + j / 32], 1u << (j % 32));
                     }
                 }
             }
-            // online softmax over the candidates of this tile
-            float pr[GP];
-#pragma unroll
-            for (int g = 0; g < GP; ++g) {
-                float mx = sx[g];
-#pragma unroll
-                for (int off = 16; off >= (1 << Gm::SH); off >>= 1)
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                const float m_new = fmaxf(m_run[g], mx);
-                if (m_new == -INFINITY) {
-                    pr[g] = 0.f;
-                    continue;
-                }
-                const float alpha = exp2_approx(m_run[g] - m_new);
-                m_run[g] = m_new;
-                pr[g] = exp2_approx(sx[g] - m_new);
-                l_lane[g] = l_lane[g] * alpha + (my_dup ? 0.f : pr[g]);
-                const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) o[g][e] = f2mul(o[g][e], a2);
-            }
-#pragma unroll
-            for (int i = 0; i < Gm::NIT; ++i) {
-                const int row = warp * Gm::TPW + Gm::RPI * i + rg;
-                const int src = rg * Gm::LPR + (i << Gm::SH);
-                float pi[GP];
-                bool anyp = false;
-#pragma unroll
-                for (int g = 0; g < GP; ++g) {
-                    pi[g] = __shfl_sync(0xffffffffu, pr[g], src);
-                    anyp |= pi[g] != 0.f;
-                }
-                if (row < rows && anyp) {
-                    const uint4 w = lds128(vb + (row * D + c * 8) * 2);
-                    const float2 v0 = bf16x2_to_float2(w.x), v1 = bf16x2_to_float2(w.y);
-                    const float2 v2 = bf16x2_to_float2(w.z), v3 = bf16x2_to_float2(w.w);
-#pragma unroll
-                    for (int g = 0; g < GP; ++g) {
-                        const float2 p2 = make_float2(pi[g], pi[g]);
-                        o[g][0] = f2fma(p2, v0, o[g][0]);
-                        o[g][1] = f2fma(p2, v1, o[g][1]);
-                        o[g][2] = f2fma(p2, v2, o[g][2]);
-                        o[g][3] = f2fma(p2, v3, o[g][3]);
-                    }
-                }
-            }
+            mma_softmax_pv<D>(ws, sc, smem_u32(st_base + Gm::RES_BYTES), st_base + Gm::RES_BYTES, warp, lane,
+                              rows);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&det_empty[ds]);
@@ -582,28 +614,24 @@ topdelta_kernel(const TDParams p) {
     pdl_launch_dependents();
 
     if (p.sel_count) {
-#pragma unroll
-        for (int g = 0; g < GP; ++g) {
-            int n = cnt[g];
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
-            if (lane == 0 && g < p.G && n) atomicAdd(&p.sel_count[b * p.Hq + hq0 + g], n);
-        }
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, 1);
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, 2);
+        if (tig == 0 && q_real && cnt) atomicAdd(&p.sel_count[b * p.Hq + hq0 + gid], cnt);
     }
-    combine_warps_and_store<D, GP, CW>(smem, warp, lane, p.G, b * p.Hq + hq0, split, m_run, l_lane, o, failed,
-                                       p.st);
+    combine_mma_warps_and_store<D, 8, CW>(smem, warp, lane, p.G, b * p.Hq + hq0, split, ws.m_run, ws.l_run, ws.o,
+                                          failed, p.st);
 }
 
-template <int D, int GP>
+template <int D>
 struct TDLauncher {
-    static constexpr int SMEM = TLayout<D, GP>::BYTES;
+    static constexpr int SMEM = TLayout<D>::BYTES;
     static cudaError_t prepare() {
         static bool done[kMaxDevices] = {};
         int dev = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
         if (dev < kMaxDevices && done[dev]) return cudaSuccess;
-        e = cudaFuncSetAttribute(topdelta_kernel<D, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+        e = cudaFuncSetAttribute(topdelta_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
         if (e == cudaSuccess && dev < kMaxDevices) done[dev] = true;
         return e;
     }
@@ -614,40 +642,25 @@ struct TDLauncher {
         if (dev < kMaxDevices && cache[dev] > 0) return cache[dev];
         if (prepare() != cudaSuccess) return 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, topdelta_kernel<D, GP>, (CW + 1) * 32, SMEM) !=
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, topdelta_kernel<D>, (CW + 1) * 32, SMEM) !=
                 cudaSuccess ||
             n <= 0)
             return 1;
         if (dev < kMaxDevices) cache[dev] = n;
         return n;
     }
-    static cudaError_t launch(const TDParams& pp, dim3 grid, cudaStream_t st) {
+    static cudaError_t launch(const CUtensorMap& tr, const CUtensorMap& tv, const TDParams& pp, dim3 grid,
+                              cudaStream_t st) {
         cudaError_t e = prepare();
         if (e != cudaSuccess) return e;
-        topdelta_kernel<D, GP><<<grid, (CW + 1) * 32, SMEM, st>>>(pp);
+        topdelta_kernel<D><<<grid, (CW + 1) * 32, SMEM, st>>>(tr, tv, pp);
         return cudaGetLastError();
     }
 };
 
-template <int D>
-int td_ctas(int G) {
-    if (G <= 1) return TDLauncher<D, 1>::ctas_per_sm();
-    if (G <= 2) return TDLauncher<D, 2>::ctas_per_sm();
-    if (G <= 4) return TDLauncher<D, 4>::ctas_per_sm();
-    return TDLauncher<D, 8>::ctas_per_sm();
-}
-
-template <int D>
-cudaError_t td_launch(int G, const TDParams& pp, dim3 grid, cudaStream_t st) {
-    if (G <= 1) return TDLauncher<D, 1>::launch(pp, grid, st);
-    if (G <= 2) return TDLauncher<D, 2>::launch(pp, grid, st);
-    if (G <= 4) return TDLauncher<D, 4>::launch(pp, grid, st);
-    return TDLauncher<D, 8>::launch(pp, grid, st);
-}
-
 }  // namespace
 
-int topdelta_ctas_per_sm(int D, int G) { return D == 128 ? td_ctas<128>(G) : td_ctas<64>(G); }
+int topdelta_ctas_per_sm(int D, int) { return D == 128 ? TDLauncher<128>::ctas_per_sm() : TDLauncher<64>::ctas_per_sm(); }
 
 cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream) {
     const long long rows = (long long)a.B * a.Hkv * a.L_max;
@@ -679,13 +692,15 @@ cudaError_t launch_topdelta(const TopDeltaArgs& a, cudaStream_t stream) {
         e = cudaMemsetAsync(a.sel_count, 0, (size_t)a.B * a.Hq * sizeof(int32_t), stream);
         if (e != cudaSuccess) return e;
     }
+    const uint64_t rows = (uint64_t)a.B * a.Hkv * a.L_max;
+    CUtensorMap tr, tv;
+    if (!make_row_map(&tr, a.res, rows, (uint32_t)a.D) || !make_row_map(&tv, a.v, rows, (uint32_t)a.D * 2))
+        return cudaErrorInvalidValue;
     TDParams pp;
     pp.q = static_cast<const uint16_t*>(a.q);
     pp.codes = a.codes;
-    pp.mn_scale = static_cast<const uint16_t*>(a.mn_scale);
-    pp.res = a.res;
-    pp.res_scale = static_cast<const uint16_t*>(a.res_scale);
-    pp.v = static_cast<const uint16_t*>(a.v);
+    pp.mn_scale = static_cast<const uint8_t*>(a.mn_scale);
+    pp.res_scale = static_cast<const uint8_t*>(a.res_scale);
     pp.seq_lens = a.seq_lens;
     pp.Hq = a.Hq;
     pp.Hkv = a.Hkv;
@@ -707,7 +722,7 @@ cudaError_t launch_topdelta(const TopDeltaArgs& a, cudaStream_t stream) {
     pp.st.direct = a.splits == 1 ? 1 : 0;
     pp.st.splits = a.splits;
     const dim3 grid((unsigned)a.splits, (unsigned)a.Hkv, (unsigned)a.B);
-    e = a.D == 128 ? td_launch<128>(pp.G, pp, grid, stream) : td_launch<64>(pp.G, pp, grid, stream);
+    e = a.D == 128 ? TDLauncher<128>::launch(tr, tv, pp, grid, stream) : TDLauncher<64>::launch(tr, tv, pp, grid, stream);
     if (e != cudaSuccess || a.splits == 1) return e;
     return launch_merge(a.part_o, a.part_ml, a.seq_lens, a.B, a.Hq, a.L_max, a.D, a.splits, a.chunk_fixed, a.out,
                         a.out_bf16, a.lse, stream);
