@@ -167,15 +167,40 @@ class Workload:
         self.out = torch.empty((B, Hq, d), device=device,
                                dtype=torch.float32 if p.out_dtype == "f32" else torch.bfloat16)
         self.lse = torch.empty((B, Hq), device=device, dtype=torch.float32)
+        self.sel_stats = None
         if self.topdelta is not None:
             self.qk = fd.fd_quantize_keys(p.k, p.seq_lens)
             need = fd.fd_topdelta_workspace_size(B, Hq, Hkv, p.L_max, d, p.num_splits)
             self.splits = None
+            self.sel_stats = self._selection_stats()
         else:
             need = fd.fd_decode_workspace_size(B, Hq, Hkv, p.L_max, d, p.num_splits, self.paged)
             self.splits = fd.fd_num_splits(B, Hq, Hkv, p.L_max, d, p.num_splits, self.paged)
         self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
         self.kv_tokens = p.kv_tokens()
+
+    def _selection_stats(self):
+        """One inspection call: candidate counts per query head, their union per
+        KV head (what the method must read residual + V for) and the 64-token
+        tiles that hold any candidate (what the kernel actually loads)."""
+        import numpy as np
+
+        p, fd = self.p, self.fd
+        c, ms, r, rs = self.qk
+        _, _, mask, cnt = fd.fd_decode_topdelta(p.q, c, ms, r, rs, p.v, p.seq_lens, p.scale, self.topdelta, 4, 64,
+                                                p.num_splits, out_dtype=self.out_dtype, want_selection=True)
+        m = mask.cpu().numpy().view(np.uint32)
+        B, Hq, W_ = m.shape
+        G = Hq // p.Hkv
+        union = np.bitwise_or.reduce(m.reshape(B, p.Hkv, G, W_), axis=2)       # [B, Hkv, words]
+        ubits = np.unpackbits(union.view(np.uint8), bitorder="little").reshape(B, p.Hkv, -1)
+        pad = (-ubits.shape[-1]) % 64
+        tiles = np.pad(ubits, ((0, 0), (0, 0), (0, pad))).reshape(B, p.Hkv, -1, 64).any(axis=-1)
+        L = p.kv_tokens() / B
+        return {"selected_per_query": float(cnt.float().mean().item()) / L,
+                "union_per_kv_head": float(ubits.sum()) / (B * p.Hkv * L),
+                "union_tokens": int(ubits.sum()), "tiles_loaded": int(tiles.sum()),
+                "tiles_total": int(tiles.size)}
 
     def call(self, stream=None):
         p, fd = self.p, self.fd
@@ -206,7 +231,8 @@ class Workload:
         if self.topdelta is None:
             return self.kv_tokens * Hkv * d * 2 * 2 + io
         scan = self.kv_tokens * Hkv * (d // 4 + (d // 32) * 4)
-        detail = (topdelta_union if topdelta_union is not None else self.kv_tokens * Hkv) * (d + (d // 32) * 2 + d * 2)
+        union = topdelta_union if topdelta_union is not None else self.sel_stats["union_tokens"]
+        detail = union * (d + (d // 32) * 2 + d * 2)
         return scan + detail + io
 
     def config(self):
@@ -216,7 +242,8 @@ class Workload:
              "num_splits": self.splits if self.splits is not None else p.num_splits,
              "cache": "paged-64" if self.paged else "contiguous", "out_dtype": p.out_dtype}
         if self.topdelta is not None:
-            c.update(delta=self.topdelta, n_sink=4, window=64)
+            c.update(delta=self.topdelta, n_sink=4, window=64, selection=self.sel_stats,
+                     dense_equivalent_bytes=self.kv_tokens * p.Hkv * p.d * 4)
         return c
 
 
