@@ -128,7 +128,7 @@ class ClockSampler:
 class Workload:
     """Resident inputs plus a `call()` that runs one decode through the C ABI."""
 
-    def __init__(self, name, seed, device, batch=None, seq_len=None):
+    def __init__(self, name, seed, device, batch=None, seq_len=None, num_splits=None):
         import torch
 
         import long_context_decode_split_gb300 as fd
@@ -160,6 +160,8 @@ class Workload:
                 self.topdelta = 5.0 if name.endswith("5") else 7.0
         else:
             raise ValueError(name)
+        if num_splits is not None:
+            p.num_splits = num_splits
         self.p = p
         self.paged = p.paged
         self.out_dtype = p.out_dtype
@@ -481,6 +483,7 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--batch", type=int, default=None, help="override B (gqa_paged, ffd_*)")
     ap.add_argument("--seq-len", type=int, default=None, help="override L (L_max for gqa_paged)")
+    ap.add_argument("--num-splits", type=int, default=None, help="chunks per sequence (0 = planner)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
@@ -504,7 +507,8 @@ def main():
 
     fd.load()
     dev = f"cuda:{ctx.local_rank}"
-    wl = Workload(args.workload, args.seed + ctx.rank, dev, batch=args.batch, seq_len=args.seq_len)
+    wl = Workload(args.workload, args.seed + ctx.rank, dev, batch=args.batch, seq_len=args.seq_len,
+                  num_splits=args.num_splits)
 
     sampler = ClockSampler(ctx.local_rank)
     sampler.start()

@@ -47,13 +47,17 @@ struct Plan {
 // The "Flash Decoding" tutorial (section 6, misconception 2) asks for a chunk
 // count that keeps every compute unit busy, chunks of at least a few hundred
 // tokens, and no more chunks than that: each costs merge work.  Here that is
-// a small cost model over whole 64-token tiles:
-//   time(S) ~ waves(S) * tiles_per_chunk(S) + merge(S)
-// with waves = ceil(units * S / resident CTAs).  Uniform batches take the
-// minimum exactly.  Ragged batches (lengths unknown on the host) take chunks
-// small enough that the longest sequences span many waves, so the hardware
-// block scheduler can even out the load.
-Plan plan(int B, int Hkv, int L_max, int requested, bool ragged, int ctas_per_sm, int sms) {
+// a cost model over whole 64-token tiles, in units of one tile's bytes at
+// the GPU's full HBM bandwidth.  A wave of n CTAs with c tiles each takes
+//   c * max(n, r),
+// r being the number of CTAs whose copy pipelines together saturate HBM
+// (a lone CTA streams at about 1/r of the GPU's bandwidth); CTAs beyond
+// the resident slots form further waves; each wave and each chunk add a
+// small fixed cost.  So: few, long chunks while HBM stays saturated, and no
+// small trailing wave.  Ragged batches (lengths unknown on the host) take
+// chunks small enough that the longest sequences span many waves, so the
+// hardware block scheduler can even out the load.
+Plan plan(int B, int Hkv, int L_max, int requested, bool ragged, int ctas_per_sm, int sms, double r) {
     Plan pl{1, 0};
     if (requested > 0) {
         pl.splits = requested;
@@ -66,14 +70,18 @@ Plan plan(int B, int Hkv, int L_max, int requested, bool ragged, int ctas_per_sm
     const int min_chunk_tiles = 4;  // 256 tokens
     int best_chunk = tiles;
     if (!ragged) {
+        const double wave_cost = 400.0, split_cost = 20.0;
         double best = 1e300;
         const int max_s = tiles / min_chunk_tiles;
         for (int S = 1; S <= max_s; ++S) {
             const int ct = (tiles + S - 1) / S;
             const int s_eff = (tiles + ct - 1) / ct;
             if (s_eff != S) continue;  // same chunk as a smaller S
-            const long waves = (units * s_eff + slots - 1) / slots;
-            const double cost = (double)waves * ct + (s_eff > 1 ? 2.0 : 0.0) + 0.02 * s_eff;
+            const long ctas = units * s_eff;
+            const long full = ctas / slots, rest = ctas % slots;
+            double cost = (double)full * ct * (slots > r ? (double)slots : r);
+            if (rest) cost += (double)ct * (rest > r ? (double)rest : r);
+            cost += wave_cost * (double)(full + (rest ? 1 : 0)) + split_cost * s_eff * units / (double)slots;
             if (cost < best - 1e-9) {
                 best = cost;
                 best_chunk = ct;
@@ -93,16 +101,25 @@ Plan plan(int B, int Hkv, int L_max, int requested, bool ragged, int ctas_per_sm
     return pl;
 }
 
+// CTAs that saturate HBM.  On GB300 a CTA of the d=128 pass (3 stages of
+// 32 KiB in flight) streams ~64 GB/s alone, so ~110 would do in theory; one
+// CTA per SM is the measured safe point (a chunk-count sweep of the 32K and
+// 1M-token workloads has its optimum there).  The d=64 pass keeps 2/3 of the
+// bytes in flight, so it needs 1.5x as many.
+double saturating_ctas(int d, int sms) { return (d == 128 ? 1.0 : 1.5) * (sms > 0 ? sms : 1); }
+
 Plan decode_plan(int B, int Hq, int Hkv, int L_max, int d, int requested, bool ragged) {
     const int sms = current_sm_count();
     const int occ = requested > 0 ? 1 : fd::decode_ctas_per_sm(d, Hq / Hkv, ragged);
-    return plan(B, Hkv, L_max, requested, ragged, occ, sms);
+    return plan(B, Hkv, L_max, requested, ragged, occ, sms, saturating_ctas(d, sms));
 }
 
 Plan topdelta_plan(int B, int Hq, int Hkv, int L_max, int d, int requested) {
     const int sms = current_sm_count();
     const int occ = requested > 0 ? 1 : fd::topdelta_ctas_per_sm(d, Hq / Hkv);
-    return plan(B, Hkv, L_max, requested, false, occ, sms);
+    // the fused sparse pass is bound by its instruction issue, not by HBM: it
+    // needs every resident CTA slot busy to reach full speed
+    return plan(B, Hkv, L_max, requested, false, occ, sms, (double)occ * (sms > 0 ? sms : 1));
 }
 
 int to_status(cudaError_t e) { return e == cudaSuccess ? FD_OK : FD_ERR_CUDA; }
