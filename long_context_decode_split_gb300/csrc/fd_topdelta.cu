@@ -180,11 +180,6 @@ __device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
     asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
     return r;
 }
-__device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
 __device__ __forceinline__ uint32_t f16x2_from_f32(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -204,6 +199,7 @@ struct TDQuery {
     uint32_t qc0[D / 16], qc2[D / 16];  // bf16, for the 2-bit scan
     uint32_t qr0[D / 16], qr2[D / 16];  // fp16, for the residual
     float qsum[D / 32];                 // sum of the query over each 32-channel group
+    float qsumh[D / 32];                // the same over the fp16 values of the residual fragments
 };
 
 // Scores s~ (natural-log units) of the warp's 16 rows of a tile whose codes
@@ -276,8 +272,11 @@ __device__ __forceinline__ void scan_tile(const unsigned char* codes, const unsi
 
 // Residual term sum_g rs_g * <q, rq>_g of the warp's 16 rows (same row
 // order as scan_tile).  The int8 residual tile is one swizzled box; each
-// lane's ldmatrix word holds 4 consecutive bytes, turned into exact fp16 by
-// prmt with 0x64 high bytes (1152 + x) and one subtraction.
+// lane's ldmatrix word holds 4 consecutive bytes, which prmt with 0x64 high
+// bytes turns into the exact fp16 values 1152 + x.  The offset is removed
+// from the fp32 sums afterwards; its rounding error (~1e-3 in units of rq)
+// is scaled down by rs (~1e-2) and the softmax scale before it reaches a
+// score.
 template <int D>
 __device__ __forceinline__ void residual_tile(uint32_t res_s, const unsigned char* rs, int warp, int lane,
                                               const TDQuery<D>& tq, float (&rt)[4]) {
@@ -300,11 +299,22 @@ __device__ __forceinline__ void residual_tile(uint32_t res_s, const unsigned cha
         ldsm_x4(addr, r[0], r[1], r[2], r[3]);  // (n-tile 0, kk 2g), (0, 2g+1), (1, 2g), (1, 2g+1)
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
+            // fp16 0x64uu is 1024 + uu exactly; with uu = x + 128 the operand is 1152 + x and
+            // the offset leaves the sum as 1152 * (sum of q over the group), removed below
             const uint32_t u = r[m] ^ 0x80808080u;
-            const uint32_t b0 = f16x2_sub(__byte_perm(u, 0x64646464u, 0x4140), 0x64806480u);
-            const uint32_t b1 = f16x2_sub(__byte_perm(u, 0x64646464u, 0x4342), 0x64806480u);
+            const uint32_t b0 = __byte_perm(u, 0x64646464u, 0x4140);
+            const uint32_t b1 = __byte_perm(u, 0x64646464u, 0x4342);
             const int kk = 2 * g + (m & 1);
             mma_f16(acc[g][m >> 1], tq.qr0[kk], 0u, tq.qr2[kk], 0u, b0, b1);
+        }
+    }
+#pragma unroll
+    for (int g = 0; g < Gm::NG; ++g) {
+        const float off = 1152.f * tq.qsumh[g];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            acc[g][j][0] -= off;
+            acc[g][j][1] -= off;
         }
     }
 #pragma unroll
@@ -474,9 +484,13 @@ topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constan
         }
 #pragma unroll
         for (int g = 0; g < D / 32; ++g) {
-            float sum = 0.f;
-            for (int c = 0; c < 32; ++c) sum = __fadd_rn(sum, qf(32 * g + c));
+            float sum = 0.f, sumh = 0.f;
+            for (int c = 0; c < 32; ++c) {
+                sum = __fadd_rn(sum, qf(32 * g + c));
+                sumh += __half2float(__float2half_rn(qf(32 * g + c)));
+            }
             tq.qsum[g] = sum;
+            tq.qsumh[g] = sumh;
         }
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt)
