@@ -128,7 +128,7 @@ class ClockSampler:
 class Workload:
     """Resident inputs plus a `call()` that runs one decode through the C ABI."""
 
-    def __init__(self, name, seed, device, batch=None, seq_len=None, num_splits=None):
+    def __init__(self, name, seed, device, batch=None, seq_len=None, num_splits=None, n_sink=4, window=64):
         import torch
 
         import long_context_decode_split_gb300 as fd
@@ -138,6 +138,7 @@ class Workload:
         self.fd = fd
         self.device = device
         self.topdelta = None
+        self.n_sink, self.window = n_sink, window
         over = {}
         if seq_len is not None:
             over["L"] = seq_len
@@ -186,11 +187,18 @@ class Workload:
         KV head (what the method must read residual + V for) and the 64-token
         tiles that hold any candidate (what the kernel actually loads)."""
         import numpy as np
+        import torch
 
         p, fd = self.p, self.fd
         c, ms, r, rs = self.qk
-        _, _, mask, cnt = fd.fd_decode_topdelta(p.q, c, ms, r, rs, p.v, p.seq_lens, p.scale, self.topdelta, 4, 64,
-                                                p.num_splits, out_dtype=self.out_dtype, want_selection=True)
+        out_s, lse_s, mask, cnt = fd.fd_decode_topdelta(p.q, c, ms, r, rs, p.v, p.seq_lens, p.scale, self.topdelta,
+                                                        self.n_sink, self.window, p.num_splits,
+                                                        out_dtype=self.out_dtype, want_selection=True)
+        # quality proxy: the dense softmax mass the candidate set captures, exp(lse_sel - lse_dense),
+        # and the largest output deviation from dense attention over the bf16 keys
+        out_d, lse_d = fd.fd_decode_dense(p.q, p.k, p.v, p.seq_lens, p.scale, out_dtype=self.out_dtype)
+        mass = torch.exp(lse_s - lse_d)
+        dev = (out_s.float() - out_d.float()).abs().max().item()
         m = mask.cpu().numpy().view(np.uint32)
         B, Hq, W_ = m.shape
         G = Hq // p.Hkv
@@ -200,6 +208,8 @@ class Workload:
         tiles = np.pad(ubits, ((0, 0), (0, 0), (0, pad))).reshape(B, p.Hkv, -1, 64).any(axis=-1)
         L = p.kv_tokens() / B
         return {"selected_per_query": float(cnt.float().mean().item()) / L,
+                "captured_mass_min": float(mass.min().item()), "captured_mass_mean": float(mass.mean().item()),
+                "max_abs_dev_vs_dense": dev,
                 "union_per_kv_head": float(ubits.sum()) / (B * p.Hkv * L),
                 "union_tokens": int(ubits.sum()), "tiles_loaded": int(tiles.sum()),
                 "tiles_total": int(tiles.size)}
@@ -208,8 +218,8 @@ class Workload:
         p, fd = self.p, self.fd
         if self.topdelta is not None:
             c, ms, r, rs = self.qk
-            fd.fd_decode_topdelta(p.q, c, ms, r, rs, p.v, p.seq_lens, p.scale, self.topdelta, 4, 64,
-                                  p.num_splits, out=self.out, lse=self.lse, out_dtype=self.out_dtype,
+            fd.fd_decode_topdelta(p.q, c, ms, r, rs, p.v, p.seq_lens, p.scale, self.topdelta, self.n_sink,
+                                  self.window, p.num_splits, out=self.out, lse=self.lse, out_dtype=self.out_dtype,
                                   workspace=self.ws, stream=stream)
         elif self.paged:
             fd.fd_decode_paged(p.q, p.k_pages, p.v_pages, p.page_table, p.num_pages, p.seq_lens, p.scale,
@@ -244,7 +254,7 @@ class Workload:
              "num_splits": self.splits if self.splits is not None else p.num_splits,
              "cache": "paged-64" if self.paged else "contiguous", "out_dtype": p.out_dtype}
         if self.topdelta is not None:
-            c.update(delta=self.topdelta, n_sink=4, window=64, selection=self.sel_stats,
+            c.update(delta=self.topdelta, n_sink=self.n_sink, window=self.window, selection=self.sel_stats,
                      dense_equivalent_bytes=self.kv_tokens * p.Hkv * p.d * 4)
         return c
 
@@ -484,6 +494,8 @@ def main():
     ap.add_argument("--batch", type=int, default=None, help="override B (gqa_paged, ffd_*)")
     ap.add_argument("--seq-len", type=int, default=None, help="override L (L_max for gqa_paged)")
     ap.add_argument("--num-splits", type=int, default=None, help="chunks per sequence (0 = planner)")
+    ap.add_argument("--n-sink", type=int, default=4, help="top-delta: attention-sink anchors")
+    ap.add_argument("--window", type=int, default=64, help="top-delta: local-window anchors")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
@@ -508,7 +520,7 @@ def main():
     fd.load()
     dev = f"cuda:{ctx.local_rank}"
     wl = Workload(args.workload, args.seed + ctx.rank, dev, batch=args.batch, seq_len=args.seq_len,
-                  num_splits=args.num_splits)
+                  num_splits=args.num_splits, n_sink=args.n_sink, window=args.window)
 
     sampler = ClockSampler(ctx.local_rank)
     sampler.start()
