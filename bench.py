@@ -261,27 +261,48 @@ class Workload:
 
 # ------------------------------------------------------------------ timing
 
-def time_device(wl, steps, warmup, dist_ctx):
+def time_device(wl, steps, warmup, dist_ctx, graph=0):
+    """CUDA-event time of `steps` calls on the current stream.  With graph > 0
+    the calls are captured `graph` at a time into a CUDA graph and replayed,
+    so host-side overhead (Python, argument checks) leaves the measurement."""
     import torch
 
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
         wl.call()
     torch.cuda.synchronize()
+    g = None
+    if graph > 0:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                for _ in range(graph):
+                    wl.call()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        steps = max(graph, steps // graph * graph)
     dist_ctx.barrier()
     torch.cuda.synchronize()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     t_wall0 = time.time()
     ev0.record(stream)
-    for _ in range(steps):
-        wl.call()
+    if g is not None:
+        for _ in range(steps // graph):
+            g.replay()
+    else:
+        for _ in range(steps):
+            wl.call()
     ev1.record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.time()
     dist_ctx.barrier()
     ms = ev0.elapsed_time(ev1)
-    return dist_ctx.max(ms), (t_wall0, t_wall1)
+    return dist_ctx.max(ms), (t_wall0, t_wall1), steps
 
 
 def time_e2e(wl, steps, warmup, dist_ctx):
@@ -494,6 +515,7 @@ def main():
     ap.add_argument("--batch", type=int, default=None, help="override B (gqa_paged, ffd_*)")
     ap.add_argument("--seq-len", type=int, default=None, help="override L (L_max for gqa_paged)")
     ap.add_argument("--num-splits", type=int, default=None, help="chunks per sequence (0 = planner)")
+    ap.add_argument("--graph", type=int, default=0, help="replay calls from a CUDA graph of this many calls")
     ap.add_argument("--n-sink", type=int, default=4, help="top-delta: attention-sink anchors")
     ap.add_argument("--window", type=int, default=64, help="top-delta: local-window anchors")
     ap.add_argument("--no-e2e", action="store_true")
@@ -525,7 +547,7 @@ def main():
     sampler = ClockSampler(ctx.local_rank)
     sampler.start()
     time.sleep(0.3)
-    ms, (tw0, tw1) = time_device(wl, args.steps, args.warmup, ctx)
+    ms, (tw0, tw1), args.steps = time_device(wl, args.steps, args.warmup, ctx, graph=args.graph)
     sampler_summary = sampler.summary(tw0, tw1)
     e2e = None
     if not args.no_e2e:
@@ -573,6 +595,8 @@ def main():
         cfg = wl.config()
         cfg["l2"] = ("inputs larger than L2" if algo > L2_BYTES else "inputs smaller than L2 (no flush)")
         cfg["parallelism"] = f"replicas x{n}"
+        if args.graph:
+            cfg["timing"] = f"CUDA graph of {args.graph} calls, replayed"
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": n, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
