@@ -15,6 +15,9 @@ Functions (each follows the passage cited in ``fd_oracle.c``):
   dequantize_keys     k~ = deq2 (+ deq8) as binary64
   decode_topdelta     FFD pipeline, Fig. 2 order (sections 3-5)
   float_to_half       IEEE binary32 -> binary16, round to nearest even
+  quantize_kv_fp8     per-row scaled e4m3 KV cache encoding
+  dequantize_kv_fp8   its exact binary64 values
+  float_to_e4m3       binary32 -> e4m3 (RNE, saturating)
 """
 from __future__ import annotations
 
@@ -52,9 +55,16 @@ def _load():
         lib.oracle_half_to_float.argtypes = [ctypes.c_uint16]
         lib.oracle_half_to_float.restype = ctypes.c_float
         lib.oracle_max_threads.argtypes = []
+        lib.oracle_float_to_e4m3.argtypes = [ctypes.c_float]
+        lib.oracle_float_to_e4m3.restype = ctypes.c_uint8
+        lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_value.restype = ctypes.c_double
+        lib.oracle_quantize_kv_fp8.argtypes = [P, P, I, I, I, I, P, P, I]
+        lib.oracle_dequantize_kv_fp8.argtypes = [P, P, P, I, I, I, I, P]
         for name in ("oracle_decode_dense", "oracle_decode_dense_f64", "oracle_decode_split",
                      "oracle_decode_paged", "oracle_quantize_keys", "oracle_dequantize_keys",
-                     "oracle_decode_topdelta", "oracle_max_threads"):
+                     "oracle_decode_topdelta", "oracle_max_threads", "oracle_quantize_kv_fp8",
+                     "oracle_dequantize_kv_fp8"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -240,3 +250,52 @@ def half_to_float(h) -> np.ndarray:
     lib = _load()
     h = np.asarray(h, np.uint16).ravel()
     return np.array([lib.oracle_half_to_float(int(v)) for v in h], np.float32)
+
+
+def float_to_e4m3(x) -> np.ndarray:
+    """Element-wise binary32 -> e4m3 code (round to nearest even, saturating at 448)."""
+    lib = _load()
+    x = np.asarray(x, np.float32).ravel()
+    return np.array([lib.oracle_float_to_e4m3(float(v)) for v in x], np.uint8)
+
+
+def e4m3_value(c) -> np.ndarray:
+    lib = _load()
+    c = np.asarray(c, np.uint8).ravel()
+    return np.array([lib.oracle_e4m3_value(int(v)) for v in c], np.float64)
+
+
+def quantize_kv_fp8(x, seq_lens=None, n_threads=0):
+    """x [B,H,L_max,d] bf16 bits -> (codes u8 [B,H,L_max,d], scales f32 [B,H,L_max]);
+    rows past seq_lens[b] are zero."""
+    x = _u16(x)
+    B, H, L_max, d = x.shape
+    sl = _i32(seq_lens)
+    codes = np.zeros((B, H, L_max, d), np.uint8)
+    scales = np.zeros((B, H, L_max), np.float32)
+    rc = _load().oracle_quantize_kv_fp8(_ptr(x), _ptr(sl), B, H, L_max, d, _ptr(codes), _ptr(scales),
+                                        int(n_threads))
+    _check(rc, "quantize_kv_fp8")
+    return codes, scales
+
+
+def dequantize_kv_fp8(codes, scales, seq_lens=None):
+    codes = np.ascontiguousarray(codes, np.uint8)
+    scales = np.ascontiguousarray(scales, np.float32)
+    B, H, L_max, d = codes.shape
+    sl = _i32(seq_lens)
+    out = np.empty((B, H, L_max, d), np.float64)
+    rc = _load().oracle_dequantize_kv_fp8(_ptr(codes), _ptr(scales), _ptr(sl), B, H, L_max, d, _ptr(out))
+    _check(rc, "dequantize_kv_fp8")
+    return out
+
+
+def decode_dense_fp8(q, k_codes, k_scales, v_codes, v_scales, seq_lens, scale, n_threads=0):
+    """Attention over an fp8 cache: the dense definition (tutorial section 1)
+    evaluated in binary64 on the dequantized K~ = e4m3(code) * s rows.
+    q [B,Hq,d] bf16 bits; codes [B,Hkv,L_max,d] u8; scales [B,Hkv,L_max] f32."""
+    q = _u16(q)
+    qf = (q.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    kt = dequantize_kv_fp8(k_codes, k_scales, seq_lens)
+    vt = dequantize_kv_fp8(v_codes, v_scales, seq_lens)
+    return decode_dense_f64(qf, kt, vt, seq_lens, scale, n_threads)

@@ -17,6 +17,9 @@
  *   "Flash Decoding" tutorial (aiqz.cc/article/flash-decoding.html):
  *     section 1 (standard attention, steps 1-4), section 2 (two-stage max
  *     merge equation and its steps 1-4), section 3 (paged KV cache).
+ *   Benchmarking blog on a hosted 1M-context model (xxmr.cn), section 1:
+ *     an 8-bit-or-narrower KV cache as the lever on decode bytes (the fp8
+ *     cache encoding below is this library's definition).
  *   "Faster Than Flash / Faster Flash Decoding" summary (PaperDaily):
  *     section 3 (top-delta rule s >= m - delta), section 4 (pseudo-max from
  *     attention-sink and local-window anchors), section 5 (2-bit body scan,
@@ -707,4 +710,107 @@ int oracle_decode_topdelta(const uint16_t* q, const uint8_t* codes, const uint16
         free(st); free(sx); free(sel); free(qd); free(d2); free(d8);
     }
     return bad ? -3 : 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* fp8 (e4m3) KV cache encoding                                             */
+/* ------------------------------------------------------------------------ */
+
+/* IEEE-style e4m3 ("fn" variant: 1 sign, 4 exponent bits with bias 7, 3
+ * mantissa bits, subnormals m * 2^-9, largest finite 448 = 0x7E, 0x7F NaN, no
+ * infinity).  Round to nearest, ties to even; magnitudes beyond 448 saturate
+ * to 448.  Written from that format definition. */
+uint8_t oracle_float_to_e4m3(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint8_t sign = (uint8_t)((u >> 24) & 0x80u);
+    float a = fabsf(f);
+    if (a != a) return (uint8_t)(sign | 0x7f);           /* NaN */
+    if (a >= 448.0f) return (uint8_t)(sign | 0x7e);      /* saturate */
+    /* the representable magnitudes are k * 2^(e-3) for normals (e >= -6) and
+     * k * 2^-9 for subnormals; pick the quantum of a's binade and round */
+    int e;
+    (void)frexpf(a, &e);                                  /* a = m * 2^e, m in [0.5, 1) */
+    int ex = e - 1;                                       /* a in [2^ex, 2^(ex+1)) */
+    if (ex < -6) ex = -6;                                 /* subnormal quantum 2^-9 */
+    float quantum = ldexpf(1.0f, ex - 3);
+    float k = a / quantum;                                /* exact: power-of-two scaling */
+    float kr = nearbyintf(k);                             /* ties to even */
+    float r = kr * quantum;
+    if (r >= 448.0f) r = 448.0f;
+    /* encode r */
+    if (r == 0.0f) return sign;
+    int er;
+    (void)frexpf(r, &er);
+    int eb = er - 1;                                      /* r in [2^eb, 2^(eb+1)) */
+    if (eb < -6) {                                        /* subnormal: r = m * 2^-9 */
+        int m = (int)(r * 512.0f);
+        return (uint8_t)(sign | m);
+    }
+    int mant = (int)(r / ldexpf(1.0f, eb - 3)) - 8;       /* 3-bit fraction */
+    return (uint8_t)(sign | ((eb + 7) << 3) | mant);
+}
+
+/* Exact value of an e4m3 code. */
+double oracle_e4m3_value(uint8_t c) {
+    int sign = c & 0x80;
+    int ex = (c >> 3) & 0xf;
+    int m = c & 7;
+    double v;
+    if (ex == 0xf && m == 7) return NAN;
+    if (ex == 0) v = ldexp((double)m, -9);
+    else v = ldexp(1.0 + m / 8.0, ex - 7);
+    return sign ? -v : v;
+}
+
+/* Per row (token, head) of a bf16 cache [B, H, L_max, d]:
+ *   a = max_c |x_c|,  s = a / 448          (binary32 division)
+ *   code_c = e4m3(x_c / s)                  (binary32 division, RNE, saturating; 0 when s == 0)
+ * codes [B, H, L_max, d] u8, scales [B, H, L_max] binary32.  Rows past
+ * seq_lens[b] are not written.  The dequantized value is e4m3(code) * s. */
+int oracle_quantize_kv_fp8(const uint16_t* x, const int32_t* seq_lens, int B, int H, int L_max, int d,
+                           uint8_t* codes, float* scales, int n_threads) {
+    if (B < 0 || H <= 0 || L_max < 0 || d <= 0) return -1;
+    if (seq_lens) for (int b = 0; b < B; ++b) if (seq_lens[b] < 0 || seq_lens[b] > L_max) return -2;
+    int nt = pick_threads(n_threads);
+    long long rows = (long long)B * H * L_max;
+    #pragma omp parallel for num_threads(nt) schedule(static)
+    for (long long row = 0; row < rows; ++row) {
+        int b = (int)(row / ((long long)H * L_max));
+        int t = (int)(row % L_max);
+        int L = seq_lens ? seq_lens[b] : L_max;
+        if (t >= L) continue;
+        const uint16_t* xr = x + (size_t)row * d;
+        float a = 0.0f;
+        for (int c = 0; c < d; ++c) {
+            float v = fabsf(bf16_value_f(xr[c]));
+            if (v > a) a = v;
+        }
+        float sc = a / 448.0f;
+        scales[row] = sc;
+        for (int c = 0; c < d; ++c) {
+            uint8_t code = 0;
+            if (sc != 0.0f) {
+                float y = bf16_value_f(xr[c]) / sc;
+                code = oracle_float_to_e4m3(y);
+            }
+            codes[(size_t)row * d + c] = code;
+        }
+    }
+    return 0;
+}
+
+/* Dequantized cache as binary64 (exact products e4m3(code) * s); rows past
+ * seq_lens[b] are 0. */
+int oracle_dequantize_kv_fp8(const uint8_t* codes, const float* scales, const int32_t* seq_lens,
+                             int B, int H, int L_max, int d, double* out) {
+    if (B < 0 || H <= 0 || L_max < 0 || d <= 0) return -1;
+    for (long long row = 0; row < (long long)B * H * L_max; ++row) {
+        int b = (int)(row / ((long long)H * L_max));
+        int t = (int)(row % L_max);
+        int L = seq_lens ? seq_lens[b] : L_max;
+        for (int c = 0; c < d; ++c)
+            out[(size_t)row * d + c] = t < L ? oracle_e4m3_value(codes[(size_t)row * d + c]) * (double)scales[row] : 0.0;
+    }
+    return 0;
 }
