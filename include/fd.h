@@ -15,6 +15,10 @@
  *         sinks and the local window), section 5 (2-bit body for the full
  *         scan, 8-bit residual loaded for candidates only), section 6 and
  *         Fig. 2 (one fused kernel: scan, select, correct, attend, aggregate).
+ *   [KV8] Benchmarking blog on a hosted 1M-context model (xxmr.cn/news/240041),
+ *         section 1: a narrow floating-point KV cache as the lever on the
+ *         bytes a decode step reads.  The page gives no format; the fp8
+ *         encoding below is this library's definition.
  *
  * Conventions shared by every entry point
  *   - Every data pointer is a DEVICE pointer owned by the caller, 16-byte
@@ -183,6 +187,61 @@ FD_API int fd_decode_topdelta(const void* q, const uint8_t* codes, const void* m
                        void* out, int out_dtype, float* lse,
                        uint32_t* sel_mask, int32_t* sel_count,
                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* fp8 KV cache encoder ([KV8]).  For each cache row x (one token of one
+ * head, d bf16 values), in IEEE binary32 arithmetic:
+ *   s      = max_c |x_c| / 448
+ *   code_c = e4m3(x_c / s)        (0 for every c when s == 0)
+ * e4m3(): the OCP 8-bit float with 4 exponent bits (bias 7) and 3 mantissa
+ * bits, no infinities, largest finite 448; round to nearest, ties to even,
+ * magnitudes above 448 saturate to +-448.  The decoded value is
+ * e4m3(code) * s, within 2^-4 |x| + 2^-10 s of x.  Layouts
+ * (row = (b * H + h) * L_max + t):
+ *   x       [B, H, L_max, d] bf16 (input)
+ *   codes   [row, d] uint8 (output)
+ *   scales  [row]    float32 (output)
+ * Rows with t >= seq_lens[b] (seq_lens may be NULL) are not written.  Use
+ * it for K and for V of the same cache (H = Hkv).  d must be 64 or 128. */
+FD_API int fd_quantize_kv_fp8(const void* x, const int32_t* seq_lens,
+                              int B, int H, int L_max, int d,
+                              uint8_t* codes, float* scales, void* stream);
+
+/* fd_num_splits / fd_decode_workspace_size for the fp8 decode entry points
+ * (the planner counts the fp8 cache's bytes per tile). */
+FD_API int fd_num_splits_fp8(int B, int Hq, int Hkv, int L_max, int d, int num_splits, int ragged);
+FD_API size_t fd_decode_fp8_workspace_size(int B, int Hq, int Hkv, int L_max, int d,
+                                           int num_splits, int ragged);
+
+/* Split-KV decode ([FD] sections 1-2) over an fp8 cache written by
+ * fd_quantize_kv_fp8: the result is the attention of q over the decoded rows
+ * K~ = e4m3(k_codes) * k_scales, V~ = e4m3(v_codes) * v_scales (computed
+ * with fp16 tensor-core products and fp32 accumulation).
+ *   k_codes, v_codes    [B, Hkv, L_max, d] uint8
+ *   k_scales, v_scales  [B, Hkv, L_max]    float32
+ * All other arguments, outputs and the workspace contract are those of
+ * fd_decode_dense, with fd_decode_fp8_workspace_size() for the workspace. */
+FD_API int fd_decode_dense_fp8(const void* q, const uint8_t* k_codes, const float* k_scales,
+                               const uint8_t* v_codes, const float* v_scales,
+                               const int32_t* seq_lens,
+                               int B, int Hq, int Hkv, int L_max, int d,
+                               float scale, int num_splits,
+                               void* out, int out_dtype, float* lse,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/* The same over a paged fp8 cache ([FD] section 3): pages of 64 tokens,
+ *   k_pages, v_pages              [num_pages, Hkv, 64, d] uint8 codes
+ *   k_page_scales, v_page_scales  [num_pages, Hkv, 64] float32
+ * page_table, seq_lens and the remaining arguments as fd_decode_paged
+ * (workspace: fd_decode_fp8_workspace_size(..., L_max = max_pages * 64,
+ * ragged = 1)). */
+FD_API int fd_decode_paged_fp8(const void* q, const uint8_t* k_pages, const float* k_page_scales,
+                               const uint8_t* v_pages, const float* v_page_scales,
+                               const int32_t* page_table, int max_pages, int num_pages,
+                               const int32_t* seq_lens, int page_size,
+                               int B, int Hq, int Hkv, int d,
+                               float scale, int num_splits,
+                               void* out, int out_dtype, float* lse,
+                               void* workspace, size_t workspace_bytes, void* stream);
 
 /* Size of the fixed device scratch array used by fd_decode_dense_noalloc. */
 #define FD_NOALLOC_SCRATCH_BYTES (4u << 20)

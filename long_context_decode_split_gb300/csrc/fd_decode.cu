@@ -50,14 +50,6 @@ struct Geo {
     static_assert((1 << LOG_NIT) == NIT, "NIT must be a power of two");
 };
 
-// Chunk length in tokens for a sequence of length L.
-__device__ __forceinline__ int chunk_len(int L, int splits, int chunk_fixed) {
-    if (chunk_fixed > 0) return chunk_fixed;
-    int c = (L + splits - 1) / splits;
-    c = (c + kTile - 1) / kTile * kTile;
-    return c > 0 ? c : kTile;
-}
-
 struct PartialParams {
     const uint16_t* q;
     const int32_t* seq_lens;

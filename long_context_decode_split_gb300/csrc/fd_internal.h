@@ -10,11 +10,28 @@ namespace fd {
 
 constexpr int kTile = 64;  // tokens per pipeline stage; also the page size
 
+#ifdef __CUDACC__
+#define FD_HD __host__ __device__
+#else
+#define FD_HD
+#endif
+
+// Chunk length in tokens for a sequence of length L: `chunk_fixed` when the
+// plan fixed one, else ceil(L / splits) rounded up to whole 64-token tiles.
+FD_HD inline int chunk_len(int L, int splits, int chunk_fixed) {
+    if (chunk_fixed > 0) return chunk_fixed;
+    int c = (L + splits - 1) / splits;
+    c = (c + kTile - 1) / kTile * kTile;
+    return c > 0 ? c : kTile;
+}
+
 // Inputs and outputs of one split-KV decode launch (dense or paged).
 struct DecodeArgs {
     const void* q;            // [B, Hq, D] bf16
     const void* k;            // contiguous [B, Hkv, L_max, D] or pool [P, Hkv, 64, D]
     const void* v;
+    const float* k_scales;    // fp8 cache only: [rows] binary32 row scales of K and V
+    const float* v_scales;
     const int32_t* seq_lens;  // [B] or null (= L_max)
     const int32_t* page_table;// [B, max_pages] when paged, else null
     int max_pages, num_pages;
@@ -75,6 +92,20 @@ struct TopDeltaArgs {
 int topdelta_ctas_per_sm(int D, int G);
 cudaError_t launch_topdelta(const TopDeltaArgs& a, cudaStream_t stream);
 cudaError_t topdelta_status_read(unsigned* bits, bool clear);
+
+// fp8 (e4m3) KV cache: encoder and decode (DecodeArgs with k/v = codes,
+// k_scales/v_scales = row scales; same workspace layout as the bf16 path).
+struct Fp8QuantArgs {
+    const void* x;            // [B, H, L_max, D] bf16
+    const int32_t* seq_lens;
+    int B, H, L_max, D;
+    uint8_t* codes;           // [B, H, L_max, D]
+    float* scales;            // [B, H, L_max]
+};
+cudaError_t launch_quantize_fp8(const Fp8QuantArgs& a, cudaStream_t stream);
+int fp8_ctas_per_sm(int D, bool paged);
+cudaError_t launch_decode_fp8(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t fp8_status_read(unsigned* bits, bool clear);
 
 // Merge of per-chunk partials (shared by the dense and top-delta paths).
 cudaError_t launch_merge(const float* part_o, const float* part_ml, const int32_t* seq_lens,

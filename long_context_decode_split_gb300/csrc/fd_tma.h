@@ -53,4 +53,21 @@ inline bool make_row_map(CUtensorMap* map, const void* base, uint64_t rows, uint
     return r == CUDA_SUCCESS;
 }
 
+// Tensor map over a plain vector of `n` binary32 values, read as boxes of
+// `box` values (box * 4 a multiple of 16, box <= 256) without swizzle.  A
+// copy must start at an index that is a multiple of 4 (16 bytes); values
+// past the end read as zero.
+inline bool make_vec_map(CUtensorMap* map, const void* base, uint64_t n, uint32_t box) {
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (!enc || n == 0 || box == 0 || box > 256 || (box * 4) % 16 != 0) return false;
+    const cuuint64_t dims[1] = {n};
+    const cuuint64_t strides[1] = {n * 4};  // not read for a rank-1 map
+    const cuuint32_t boxd[1] = {box};
+    const cuuint32_t estr[1] = {1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, const_cast<void*>(base), dims, strides, boxd,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace fd

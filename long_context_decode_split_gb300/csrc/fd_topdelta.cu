@@ -180,11 +180,6 @@ __device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
     asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
     return r;
 }
-__device__ __forceinline__ uint32_t f16x2_from_f32(float lo, float hi) {
-    uint32_t r;
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
 
 // Query fragments of one lane (row gid of the m16 A operand), per 16-channel
 // k-step.  The k order inside a step is permuted to match how the B
@@ -477,8 +472,8 @@ topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constan
             const int c0 = 16 * kk;
             tq.qc0[kk] = qb(c0 + 2 * tig) | (qb(c0 + 2 * tig + 8) << 16);
             tq.qc2[kk] = pack_bf16(0.25f * qf(c0 + 2 * tig + 1), 0.25f * qf(c0 + 2 * tig + 9));  // exact
-            tq.qr0[kk] = f16x2_from_f32(qf(c0 + 4 * tig), qf(c0 + 4 * tig + 1));
-            tq.qr2[kk] = f16x2_from_f32(qf(c0 + 4 * tig + 2), qf(c0 + 4 * tig + 3));
+            tq.qr0[kk] = pack_f16(qf(c0 + 4 * tig), qf(c0 + 4 * tig + 1));
+            tq.qr2[kk] = pack_f16(qf(c0 + 4 * tig + 2), qf(c0 + 4 * tig + 3));
             ws.qa0[kk] = 0u;
             ws.qa2[kk] = 0u;
         }
