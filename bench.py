@@ -8,7 +8,8 @@ over one batch of synthetic inputs already resident in HBM.
 Default workload: MHA decode, B=1, Hq=Hkv=32, d=128, L=32768, bf16 KV cache
 (512 MiB of K+V per call, larger than the 129 MB L2, so no flush is needed
 between calls).  Other workloads: --workload tiny|mha32k|gqa_paged|million|
-ffd_dense|ffd_topdelta5|ffd_topdelta7.
+ffd_dense|ffd_topdelta5|ffd_topdelta7, and mha32k_fp8|million_fp8|ffd_dense_fp8|
+gqa_paged_fp8 (the same caches in the fp8 e4m3 encoding, per-row f32 scales).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fd|reference]
 
@@ -40,7 +41,9 @@ FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
 
 DEFAULT_STEPS = {"tiny": 20000, "mha32k": 20000, "gqa_paged": 3000, "million": 3000,
-                 "ffd_dense": 4000, "ffd_topdelta5": 4000, "ffd_topdelta7": 4000}
+                 "ffd_dense": 4000, "ffd_topdelta5": 4000, "ffd_topdelta7": 4000,
+                 "mha32k_fp8": 20000, "million_fp8": 4000, "ffd_dense_fp8": 6000, "gqa_paged_fp8": 4000}
+WORKLOADS = list(DEFAULT_STEPS)
 
 
 # ----------------------------------------------------------------- helpers
@@ -138,6 +141,9 @@ class Workload:
         self.fd = fd
         self.device = device
         self.topdelta = None
+        self.fp8 = name.endswith("_fp8")
+        if self.fp8:
+            name = name[:-4]
         self.n_sink, self.window = n_sink, window
         over = {}
         if seq_len is not None:
@@ -171,7 +177,16 @@ class Workload:
                                dtype=torch.float32 if p.out_dtype == "f32" else torch.bfloat16)
         self.lse = torch.empty((B, Hq), device=device, dtype=torch.float32)
         self.sel_stats = None
-        if self.topdelta is not None:
+        if self.fp8:
+            # encode the cache once (outside the timed region); keep the bf16 copy for e2e rows
+            if self.paged:
+                self.kv8 = fd.fd_quantize_kv_fp8(p.k_pages) + fd.fd_quantize_kv_fp8(p.v_pages)
+            else:
+                self.kv8 = fd.fd_quantize_kv_fp8(p.k) + fd.fd_quantize_kv_fp8(p.v)
+            torch.cuda.synchronize()
+            need = fd.fd_decode_fp8_workspace_size(B, Hq, Hkv, p.L_max, d, p.num_splits, self.paged)
+            self.splits = fd.fd_num_splits_fp8(B, Hq, Hkv, p.L_max, d, p.num_splits, self.paged)
+        elif self.topdelta is not None:
             self.qk = fd.fd_quantize_keys(p.k, p.seq_lens)
             need = fd.fd_topdelta_workspace_size(B, Hq, Hkv, p.L_max, d, p.num_splits)
             self.splits = None
@@ -216,7 +231,16 @@ class Workload:
 
     def call(self, stream=None):
         p, fd = self.p, self.fd
-        if self.topdelta is not None:
+        if self.fp8:
+            kc, ks, vc, vs = self.kv8
+            if self.paged:
+                fd.fd_decode_paged_fp8(p.q, kc, ks, vc, vs, p.page_table, p.num_pages, p.seq_lens, p.scale,
+                                       p.num_splits, out=self.out, lse=self.lse, out_dtype=self.out_dtype,
+                                       workspace=self.ws, stream=stream)
+            else:
+                fd.fd_decode_dense_fp8(p.q, kc, ks, vc, vs, None, p.scale, p.num_splits, out=self.out,
+                                       lse=self.lse, out_dtype=self.out_dtype, workspace=self.ws, stream=stream)
+        elif self.topdelta is not None:
             c, ms, r, rs = self.qk
             fd.fd_decode_topdelta(p.q, c, ms, r, rs, p.v, p.seq_lens, p.scale, self.topdelta, self.n_sink,
                                   self.window, p.num_splits, out=self.out, lse=self.lse, out_dtype=self.out_dtype,
@@ -240,6 +264,8 @@ class Workload:
         p = self.p
         B, Hq, Hkv, d = p.B, p.Hq, p.Hkv, p.d
         io = B * Hq * d * 2 + B * Hq * d * (4 if p.out_dtype == "f32" else 2) + B * Hq * 4
+        if self.fp8:
+            return self.kv_tokens * Hkv * (d + 4) * 2 + io  # K and V codes + their row scales
         if self.topdelta is None:
             return self.kv_tokens * Hkv * d * 2 * 2 + io
         scan = self.kv_tokens * Hkv * (d // 4 + (d // 32) * 4)
@@ -252,7 +278,8 @@ class Workload:
         c = {"workload": self.name, "B": p.B, "Hq": p.Hq, "Hkv": p.Hkv, "d": p.d,
              "L": p.L_max if not self.paged else "ragged", "kv_tokens": self.kv_tokens,
              "num_splits": self.splits if self.splits is not None else p.num_splits,
-             "cache": "paged-64" if self.paged else "contiguous", "out_dtype": p.out_dtype}
+             "cache": "paged-64" if self.paged else "contiguous", "out_dtype": p.out_dtype,
+             "kv_dtype": "e4m3 codes + f32 row scales" if self.fp8 else "bf16"}
         if self.topdelta is not None:
             c.update(delta=self.topdelta, n_sink=self.n_sink, window=self.window, selection=self.sel_stats,
                      dense_equivalent_bytes=self.kv_tokens * p.Hkv * p.d * 4)
@@ -312,6 +339,7 @@ def time_e2e(wl, steps, warmup, dist_ctx):
     import torch
 
     p = wl.p
+    fd = wl.fd
     dev = wl.device
     q_h = p.q.detach().cpu().pin_memory()
     if wl.paged:
@@ -327,6 +355,18 @@ def time_e2e(wl, steps, warmup, dist_ctx):
         tgt = None
     k_dev = torch.empty(k_rows.shape, dtype=k_rows.dtype, device=dev)
     v_dev = torch.empty(v_rows.shape, dtype=v_rows.dtype, device=dev)
+    if wl.fp8:
+        # the new rows are encoded on the device (fd_quantize_kv_fp8) and written into the fp8 cache
+        if wl.paged:  # rows [n, Hkv, d] -> n * Hkv cache rows of one token
+            k_new = k_dev.view(-1, 1, 1, k_dev.shape[-1])
+            v_new = v_dev.view(-1, 1, 1, v_dev.shape[-1])
+        else:         # rows [B, Hkv, d] -> token L_max - 1 of every head
+            k_new = k_dev.view(k_dev.shape[0], k_dev.shape[1], 1, -1)
+            v_new = v_dev.view(v_dev.shape[0], v_dev.shape[1], 1, -1)
+        kc_new = torch.empty(k_new.shape, dtype=torch.uint8, device=dev)
+        vc_new = torch.empty(v_new.shape, dtype=torch.uint8, device=dev)
+        ks_new = torch.empty(k_new.shape[:3], dtype=torch.float32, device=dev)
+        vs_new = torch.empty(v_new.shape[:3], dtype=torch.float32, device=dev)
     out_h = torch.empty(wl.out.shape, dtype=wl.out.dtype).pin_memory()
     lse_h = torch.empty(wl.lse.shape, dtype=wl.lse.dtype).pin_memory()
     h2d = q_h.numel() * 2 + k_rows.numel() * 2 + v_rows.numel() * 2
@@ -336,7 +376,23 @@ def time_e2e(wl, steps, warmup, dist_ctx):
         p.q.copy_(q_h, non_blocking=True)
         k_dev.copy_(k_rows, non_blocking=True)
         v_dev.copy_(v_rows, non_blocking=True)
-        if wl.paged:
+        if wl.fp8:
+            fd.fd_quantize_kv_fp8(k_new, codes=kc_new, scales=ks_new)
+            fd.fd_quantize_kv_fp8(v_new, codes=vc_new, scales=vs_new)
+            kc, ks, vc, vs = wl.kv8
+            if wl.paged:
+                H = k_dev.shape[1]
+                for i, (pg, r) in enumerate(tgt):
+                    kc[pg, :, r] = kc_new[i * H:(i + 1) * H, 0, 0]
+                    ks[pg, :, r] = ks_new[i * H:(i + 1) * H, 0, 0]
+                    vc[pg, :, r] = vc_new[i * H:(i + 1) * H, 0, 0]
+                    vs[pg, :, r] = vs_new[i * H:(i + 1) * H, 0, 0]
+            else:
+                kc[:, :, p.L_max - 1] = kc_new[:, :, 0]
+                ks[:, :, p.L_max - 1] = ks_new[:, :, 0]
+                vc[:, :, p.L_max - 1] = vc_new[:, :, 0]
+                vs[:, :, p.L_max - 1] = vs_new[:, :, 0]
+        elif wl.paged:
             for i, (pg, r) in enumerate(tgt):
                 p.k_pages[pg, :, r] = k_dev[i]
                 p.v_pages[pg, :, r] = v_dev[i]
@@ -367,6 +423,7 @@ FULL_SHAPES = {"tiny": (1, 1, 1, 1024, 64), "mha32k": (1, 32, 32, 32768, 128),
                "million": (1, 32, 8, 1 << 20, 128), "gqa_paged": (8, 64, 8, 73728, 128),
                "ffd_dense": (4, 32, 8, 131072, 128), "ffd_topdelta5": (4, 32, 8, 131072, 128),
                "ffd_topdelta7": (4, 32, 8, 131072, 128)}
+FULL_SHAPES.update({k + "_fp8": FULL_SHAPES[k] for k in ("mha32k", "million", "gqa_paged", "ffd_dense")})
 
 
 class OracleSample:
@@ -385,6 +442,7 @@ class OracleSample:
         self.name = name
         self.oracle = oracle
         B, Hq, Hkv, L, d = FULL_SHAPES[name]
+        self.fp8 = name.endswith("_fp8")
         G = Hq // Hkv
         self.B = B
         self.delta = None
@@ -403,6 +461,8 @@ class OracleSample:
             self.args = (bits(p.q), bits(p.k), bits(p.v), p.scale)
             if self.delta is not None:
                 self.enc = oracle.quantize_keys(self.args[1])
+            if self.fp8:
+                self.enc = oracle.quantize_kv_fp8(self.args[1]) + oracle.quantize_kv_fp8(self.args[2])
             t0 = time.perf_counter()
             self.run()
             dt = time.perf_counter() - t0
@@ -420,7 +480,10 @@ class OracleSample:
 
     def run(self):
         q, k, v, scale = self.args
-        if self.delta is not None:
+        if self.fp8:
+            kc, ks, vc, vs = self.enc
+            self.oracle.decode_dense_fp8(q, kc, ks, vc, vs, None, scale)
+        elif self.delta is not None:
             c, ms, r, rs = self.enc
             self.oracle.decode_topdelta(q, c, ms, r, rs, v, None, scale, self.delta)
         else:
@@ -508,9 +571,7 @@ def main():
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["fd", "reference"], default="fd")
-    ap.add_argument("--workload", default="mha32k",
-                    choices=["tiny", "mha32k", "gqa_paged", "million", "ffd_dense", "ffd_topdelta5",
-                             "ffd_topdelta7"])
+    ap.add_argument("--workload", default="mha32k", choices=WORKLOADS)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--batch", type=int, default=None, help="override B (gqa_paged, ffd_*)")
     ap.add_argument("--seq-len", type=int, default=None, help="override L (L_max for gqa_paged)")
@@ -574,7 +635,7 @@ def main():
             with open(tfile) as f:
                 tj = json.load(f)
             ent = tj.get(args.workload)
-            if ent and ent.get("source_sha") == source_digest():
+            if ent and ent.get("source_sha") == source_digest(args.workload):
                 traffic = ent.get("dram_bytes_per_launch")
         except (OSError, ValueError):
             traffic = None
@@ -600,7 +661,7 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": n, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "kv_dtype": "bf16",
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "kv_dtype": "e4m3" if wl.fp8 else "bf16",
             "data": "synthetic", "config": cfg,
             "us_per_call": per_call_s * 1e6,
             "kv_tokens_per_s": wl.kv_tokens * n / per_call_s,
@@ -620,12 +681,28 @@ def main():
     ctx.close()
 
 
-def source_digest():
+KERNEL_SOURCES = {"bf16": "fd_decode.cu", "topdelta": "fd_topdelta.cu", "fp8": "fd_fp8.cu"}
+
+
+def kernel_family(workload):
+    if workload.endswith("_fp8"):
+        return "fp8"
+    if workload.startswith("ffd_top"):
+        return "topdelta"
+    return "bf16"
+
+
+def source_digest(workload):
+    """Digest of the sources that define a workload's kernels and their launch
+    plan: the kernel's translation unit, the shared device/host headers and
+    the C-ABI layer (which picks the chunk count)."""
     import hashlib
 
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "long_context_decode_split_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    files = sorted(f for f in os.listdir(csrc) if f.endswith((".cuh", ".h")))
+    files += ["fd_api.cu", KERNEL_SOURCES[kernel_family(workload)]]
+    for f in files:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]

@@ -13,8 +13,9 @@
 // Partial pass, one CTA per (chunk, KV head, sequence), warp-specialised as
 // the bf16 pass: warp 4 issues the tile copies (two 64-row code boxes and two
 // 68-entry scale boxes per 64-token tile, through a STAGES-deep mbarrier
-// ring), warps 0..3 each own 16 tokens of every tile and run both products on
-// the tensor cores with fp16 operands (every e4m3 value is exact in fp16):
+// ring), warps 0..3 each own 16 tokens of every tile, take NT tiles per step
+// (one online-softmax update per step) and run both products on the tensor
+// cores with fp16 operands (every e4m3 value is exact in fp16):
 //   S = Q K^T   A = the query group (padded to 16 rows) in fp16, scaled per
 //               query by a power of two so that |q| < 1 (exact); B = K codes
 //               fetched by ldmatrix (4 bytes = 4 channels per lane) and
@@ -23,10 +24,10 @@
 //               dot products are unchanged.  The row scale of K and the
 //               power of two of Q are applied to the fp32 scores.
 //   O^T += V^T P^T
-//               A = V codes, four tokens' 4-byte words transposed by byte
-//               permutes and widened (the 16 output rows of an MMA tile are
-//               4 channels of 4 lane groups: channel 32u + 4*gid + 2j + r
-//               for tile 2u + j and row gid + 8r); B = P * s_V / s_ref in
+//               A = V codes: lane group gid reads channels D/8 * gid ..
+//               + D/8 - 1 of its four tokens in one shared load each, and
+//               byte permutes pair the tokens up before widening (row gid +
+//               8r of output tile j is channel D/8 * gid + 2j + r); B = P * s_V / s_ref in
 //               fp16, where s_ref, the largest V scale the warp has seen,
 //               keeps the operand in [0, 1]; a growing s_ref rescales O like
 //               a growing running max.  O is multiplied by s_ref at the end.
@@ -70,12 +71,6 @@ __device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi) {
         : "=r"(r)
         : "f"(hi), "f"(lo));
     return r;
-}
-
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-    return v;
 }
 
 // ---------------------------------------------------------------------------
@@ -142,7 +137,7 @@ __device__ __forceinline__ uint32_t code_off(int row, int ch) {
     else return swz64(row, ch);
 }
 
-template <int D, int STAGES, bool PAGED>
+template <int D, int STAGES, int NT, bool PAGED>
 __global__ void __launch_bounds__(5 * 32, 2)
 fp8_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                    const __grid_constant__ CUtensorMap tmks, const __grid_constant__ CUtensorMap tmvs,
@@ -288,67 +283,98 @@ fp8_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
     bool failed = false;
     const int ld_row = warp * 16 + 8 * (mi >> 1) + (lane & 7);  // row this lane addresses for ldmatrix
     const int r0 = warp * 16 + 2 * tig;                         // tokens r0, r0+1, r0+8, r0+9 are this lane's
-    const int vch = gid >> 2, vbyte = 4 * (gid & 3);            // V word: channels 32u + 4*gid .. +3
+    constexpr int VW = D / 32;                                  // V words per token and lane (D/8 channels)
+    // byte offset of this lane's V channels D/8 * gid .. within a code row
+    const uint32_t vofs_lo = D == 128 ? 0u : 8u * (uint32_t)(gid & 1);
+    const int vch = D == 128 ? gid : gid >> 1;
 
-    for (int t = 0; t < ntiles; ++t) {
-        const int s = t % STAGES;
-        if (!warp_wait(&full[s], (uint32_t)(t / STAGES) & 1u)) {
+    const int tok[4] = {r0, r0 + 1, r0 + 8, r0 + 9};
+    for (int t = 0; t < ntiles; t += NT) {
+        // NT consecutive stages per step; a step past the last tile reuses the
+        // first stage's buffers with no valid rows (everything masked)
+        int st[NT], rows[NT];
+        bool have[NT];
+#pragma unroll
+        for (int k = 0; k < NT; ++k) {
+            have[k] = t + k < ntiles;
+            st[k] = have[k] ? (t + k) % STAGES : t % STAGES;
+            rows[k] = 0;
+            if (have[k]) {
+                if (!warp_wait(&full[st[k]], (uint32_t)((t + k) / STAGES) & 1u)) failed = true;
+                else rows[k] = stage_rows[st[k]];
+            }
+        }
+        if (failed) {
             atomicOr(&g_status_fp8, kStatusTimeout);
-            failed = true;
             break;
         }
-        const int rows = stage_rows[s];
-        const uint32_t kt = smem_u32(smem + s * STAGE);
-        const uint32_t vt = kt + CB;
-        const float* ksc = reinterpret_cast<const float*>(scl + s * SSTAGE) + stage_off[s];
-        const float* vsc = reinterpret_cast<const float*>(scl + s * SSTAGE + kScaleSlot) + stage_off[s];
 
-        // ---- S = Q K^T over this warp's 16 tokens ---------------------------
-        float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        // ---- S = Q K^T over this warp's 16 tokens of each stage ---------------
+        float sacc[NT][2][4];
 #pragma unroll
-        for (int kk = 0; kk < D / 32; ++kk) {
-            uint32_t w0, w1, w2, w3, blo, bhi;
-            ldsm_x4(kt + code_off<D>(ld_row, 2 * kk + (mi & 1)), w0, w1, w2, w3);
-            e4m3x4_to_f16x4(w0, blo, bhi);
-            mma_f16(sacc[0], qa0[2 * kk], 0u, qa2[2 * kk], 0u, blo, bhi);
-            e4m3x4_to_f16x4(w1, blo, bhi);
-            mma_f16(sacc[0], qa0[2 * kk + 1], 0u, qa2[2 * kk + 1], 0u, blo, bhi);
-            e4m3x4_to_f16x4(w2, blo, bhi);
-            mma_f16(sacc[1], qa0[2 * kk], 0u, qa2[2 * kk], 0u, blo, bhi);
-            e4m3x4_to_f16x4(w3, blo, bhi);
-            mma_f16(sacc[1], qa0[2 * kk + 1], 0u, qa2[2 * kk + 1], 0u, blo, bhi);
+        for (int k = 0; k < NT; ++k) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) sacc[k][0][i] = sacc[k][1][i] = 0.f;
+            const uint32_t kt = smem_u32(smem + st[k] * STAGE);
+#pragma unroll
+            for (int kk = 0; kk < D / 32; ++kk) {
+                uint32_t w0, w1, w2, w3, blo, bhi;
+                ldsm_x4(kt + code_off<D>(ld_row, 2 * kk + (mi & 1)), w0, w1, w2, w3);
+                e4m3x4_to_f16x4(w0, blo, bhi);
+                mma_f16(sacc[k][0], qa0[2 * kk], 0u, qa2[2 * kk], 0u, blo, bhi);
+                e4m3x4_to_f16x4(w1, blo, bhi);
+                mma_f16(sacc[k][0], qa0[2 * kk + 1], 0u, qa2[2 * kk + 1], 0u, blo, bhi);
+                e4m3x4_to_f16x4(w2, blo, bhi);
+                mma_f16(sacc[k][1], qa0[2 * kk], 0u, qa2[2 * kk], 0u, blo, bhi);
+                e4m3x4_to_f16x4(w3, blo, bhi);
+                mma_f16(sacc[k][1], qa0[2 * kk + 1], 0u, qa2[2 * kk + 1], 0u, blo, bhi);
+            }
         }
-        const int tok[4] = {r0, r0 + 1, r0 + 8, r0 + 9};
-        const float raw[4] = {sacc[0][0], sacc[0][1], sacc[1][0], sacc[1][1]};
-        float sc[4], vs[4];
+        float sc[NT][4], vs[NT][4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const bool ok = tok[i] < rows;
-            sc[i] = ok ? raw[i] * ksc[tok[i]] * qmul : -INFINITY;
-            vs[i] = ok ? vsc[tok[i]] : 0.f;
+        for (int k = 0; k < NT; ++k) {
+            const float* ksc = reinterpret_cast<const float*>(scl + st[k] * SSTAGE) + stage_off[st[k]];
+            const float* vsc = reinterpret_cast<const float*>(scl + st[k] * SSTAGE + kScaleSlot) + stage_off[st[k]];
+            const float raw[4] = {sacc[k][0][0], sacc[k][0][1], sacc[k][1][0], sacc[k][1][1]};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const bool ok = tok[i] < rows[k];
+                sc[k][i] = ok ? raw[i] * ksc[tok[i]] * qmul : -INFINITY;
+                vs[k][i] = ok ? vsc[tok[i]] : 0.f;
+            }
         }
 
         // ---- online softmax and the V reference scale ------------------------
-        float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+        float mx = -INFINITY, vmax = 0.f;
+#pragma unroll
+        for (int k = 0; k < NT; ++k) {
+            mx = fmaxf(mx, fmaxf(fmaxf(sc[k][0], sc[k][1]), fmaxf(sc[k][2], sc[k][3])));
+            vmax = fmaxf(vmax, fmaxf(fmaxf(vs[k][0], vs[k][1]), fmaxf(vs[k][2], vs[k][3])));
+        }
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        float vmax = fmaxf(fmaxf(vs[0], vs[1]), fmaxf(vs[2], vs[3]));
         vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 1));
         vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
         const float vref_new = fmaxf(vref, vmax);
-        const float vinv = vref_new > 0.f ? 1.f / vref_new : 0.f;
+        const float vinv = vref_new > 0.f ? __fdividef(1.f, vref_new) : 0.f;
         const float vf = vref_new > 0.f ? vref * vinv : 1.f;
         vref = vref_new;
         const float m_new = fmaxf(m_run, mx);
         const bool none = m_new == -INFINITY;
         const float alpha = none ? 1.f : exp2_approx(m_run - m_new);
-        float pr[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) pr[i] = none ? 0.f : exp2_approx(sc[i] - m_new);
         m_run = m_new;
-        l_run = l_run * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
-        const uint32_t pb0 = pack_f16(pr[0] * (vs[0] * vinv), pr[1] * (vs[1] * vinv));
-        const uint32_t pb1 = pack_f16(pr[2] * (vs[2] * vinv), pr[3] * (vs[3] * vinv));
+        float lsum = 0.f;
+        uint32_t pb[NT][2];
+#pragma unroll
+        for (int k = 0; k < NT; ++k) {
+            float pr[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) pr[i] = none ? 0.f : exp2_approx(sc[k][i] - m_new);
+            lsum += (pr[0] + pr[1]) + (pr[2] + pr[3]);
+            pb[k][0] = pack_f16(pr[0] * (vs[k][0] * vinv), pr[1] * (vs[k][1] * vinv));
+            pb[k][1] = pack_f16(pr[2] * (vs[k][2] * vinv), pr[3] * (vs[k][3] * vinv));
+        }
+        l_run = l_run * alpha + lsum;
         if (!__all_sync(0xffffffffu, alpha == 1.f && vf == 1.f)) {
             // accumulator columns are queries 2*tig and 2*tig+1
             const float a_even = __shfl_sync(0xffffffffu, alpha, 8 * tig) * vf;
@@ -363,32 +389,43 @@ fp8_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
         }
 
         // ---- O^T += V^T P^T ----------------------------------------------------
-        const bool tail = warp * 16 + 16 > rows;  // warp-uniform
 #pragma unroll
-        for (int u = 0; u < D / 32; ++u) {
-            const uint32_t cofs = (uint32_t)vbyte;
-            uint32_t w0 = lds32(vt + code_off<D>(tok[0], 2 * u + vch) + cofs);
-            uint32_t w1 = lds32(vt + code_off<D>(tok[1], 2 * u + vch) + cofs);
-            uint32_t w8 = lds32(vt + code_off<D>(tok[2], 2 * u + vch) + cofs);
-            uint32_t w9 = lds32(vt + code_off<D>(tok[3], 2 * u + vch) + cofs);
-            if (tail) {  // rows past the tile's end may hold any bytes (0 * NaN = NaN)
-                w0 = tok[0] < rows ? w0 : 0u;
-                w1 = tok[1] < rows ? w1 : 0u;
-                w8 = tok[2] < rows ? w8 : 0u;
-                w9 = tok[3] < rows ? w9 : 0u;
+        for (int k = 0; k < NT; ++k) {
+            const uint32_t vt = smem_u32(smem + st[k] * STAGE) + CB;
+            uint32_t vw[4][VW];  // [token r0, r0+1, r0+8, r0+9][word]
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t a = vt + code_off<D>(tok[i], vch) + vofs_lo;
+                if constexpr (VW == 4) {
+                    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                                 : "=r"(vw[i][0]), "=r"(vw[i][1]), "=r"(vw[i][2]), "=r"(vw[i][3])
+                                 : "r"(a));
+                } else {
+                    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(vw[i][0]), "=r"(vw[i][1]) : "r"(a));
+                }
             }
-            uint32_t a0, a1, a2, a3;
-            // channels 32u + 4*gid + {0, 1}: tokens (r0, r0+1) and (r0+8, r0+9)
-            e4m3x4_to_f16x4(__byte_perm(w0, w1, 0x5140), a0, a1);
-            e4m3x4_to_f16x4(__byte_perm(w8, w9, 0x5140), a2, a3);
-            mma_f16(o[2 * u], a0, a1, a2, a3, pb0, pb1);
-            // channels 32u + 4*gid + {2, 3}
-            e4m3x4_to_f16x4(__byte_perm(w0, w1, 0x7362), a0, a1);
-            e4m3x4_to_f16x4(__byte_perm(w8, w9, 0x7362), a2, a3);
-            mma_f16(o[2 * u + 1], a0, a1, a2, a3, pb0, pb1);
+            if (warp * 16 + 16 > rows[k]) {  // rows past the tile's end may hold any bytes (0 * NaN = NaN)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int w = 0; w < VW; ++w) vw[i][w] = tok[i] < rows[k] ? vw[i][w] : 0u;
+            }
+#pragma unroll
+            for (int j = 0; j < D / 16; ++j) {
+                // channels D/8 * gid + 2j + {0, 1}: tokens (r0, r0+1) and (r0+8, r0+9)
+                const uint32_t sel = (j & 1) ? 0x7362u : 0x5140u;
+                uint32_t a0, a1, a2, a3;
+                e4m3x4_to_f16x4(__byte_perm(vw[0][j >> 1], vw[1][j >> 1], sel), a0, a1);
+                e4m3x4_to_f16x4(__byte_perm(vw[2][j >> 1], vw[3][j >> 1], sel), a2, a3);
+                mma_f16(o[j], a0, a1, a2, a3, pb[k][0], pb[k][1]);
+            }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+        if (lane == 0) {
+#pragma unroll
+            for (int k = 0; k < NT; ++k)
+                if (have[k]) mbar_arrive(&empty[st[k]]);
+        }
     }
     pdl_launch_dependents();
 
@@ -400,13 +437,14 @@ fp8_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
     float* red_m = red_o + CW * 8 * D;              // [CW][8]
     float* red_l = red_m + CW * 8;                  // [CW][8]
 #pragma unroll
-    for (int u = 0; u < D / 32; ++u) {
+    for (int jj = 0; jj < D / 32; ++jj) {
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
+            // query 2*tig + i, channels D/8 * gid + 4*jj .. + 3
             const int qi = 2 * tig + i;
-            float4 val = make_float4(o[2 * u][i] * vref, o[2 * u][i + 2] * vref, o[2 * u + 1][i] * vref,
-                                     o[2 * u + 1][i + 2] * vref);
-            *reinterpret_cast<float4*>(red_o + (warp * 8 + qi) * D + 32 * u + 4 * gid) = val;
+            const float4 val = make_float4(o[2 * jj][i] * vref, o[2 * jj][i + 2] * vref, o[2 * jj + 1][i] * vref,
+                                           o[2 * jj + 1][i + 2] * vref);
+            *reinterpret_cast<float4*>(red_o + (warp * 8 + qi) * D + (D / 8) * gid + 4 * jj) = val;
         }
     }
     if (tig == 0) {
@@ -419,12 +457,16 @@ fp8_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
 
 template <int D, bool PAGED>
 struct Fp8Launcher {
-    static constexpr int STAGES = 4;
+    // two stages per consumer step share the softmax bookkeeping and give each
+    // warp two independent MMA chains; six stages keep ~100 KiB per CTA in flight
+    static constexpr int STAGES = 6;
+    static constexpr int NT = 2;  // stages a consumer warp takes per step
+    static_assert(STAGES >= 2 * NT, "the producer needs stages to fill while NT are consumed");
     static constexpr int STAGE = 2 * 64 * D;
     static constexpr int SMEM = 1024 + STAGES * STAGE + STAGES * 2 * kScaleSlot + STAGES * 16 + STAGES * 8 + 64;
     static constexpr int RED = 4 * 8 * D * 4 + 2 * 4 * 8 * 4;
     static_assert(STAGES * STAGE >= RED, "reduction scratch must fit in the ring");
-    static constexpr auto kernel = fp8_partial_kernel<D, STAGES, PAGED>;
+    static constexpr auto kernel = fp8_partial_kernel<D, STAGES, NT, PAGED>;
 
     static cudaError_t prepare() {
         static bool done[kMaxDevices] = {};
