@@ -209,35 +209,11 @@ __device__ __forceinline__ void scan_tile(const unsigned char* codes, const unsi
                                           const TDQuery<D>& tq, float scale, float (&st)[4]) {
     using Gm = TGeo<D>;
     const int gid = lane >> 2, tig = lane & 3;
-    float acc[Gm::NG][2][4];
-#pragma unroll
-    for (int g = 0; g < Gm::NG; ++g)
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc[g][j][i] = 0.f;
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-        const uint4* crow = reinterpret_cast<const uint4*>(codes + (warp * 16 + 8 * j + gid) * Gm::CODES_ROW);
-#pragma unroll
-        for (int kq = 0; kq < Gm::KS / 4; ++kq) {
-            const uint4 w4 = crow[kq];
-            const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int kk = 4 * kq + e;
-                const uint32_t w = wv[e] >> (4 * tig);
-                const uint32_t b0 = bf16x2_sub((w & 0x00030003u) | 0x43004300u, 0x43004300u);
-                // codes of the odd pair stay at bits 2-3: 4 * code (exact); qc2 carries the 1/4
-                const uint32_t b1 = bf16x2_sub((w & 0x000C000Cu) | 0x43004300u, 0x43004300u);
-                mma_bf16(acc[kk >> 1][j], tq.qc0[kk], 0u, tq.qc2[kk], 0u, b0, b1);
-            }
-        }
-    }
-    // per lane: two rows per n-tile (columns 2*tig, 2*tig+1), combined pairwise
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        const int row = warp * 16 + 8 * j + 2 * tig;
+        const int crow = warp * 16 + 8 * j + gid;  // the token row this lane's code words come from
+        const int row = warp * 16 + 8 * j + 2 * tig;  // the two rows of this lane's accumulator columns
+        // (mn16, s16) of every group for rows `row` and `row + 1`
         uint32_t ma[Gm::NG], mb[Gm::NG];
         if constexpr (Gm::NG == 4) {
             const uint4 a = *reinterpret_cast<const uint4*>(ms + row * Gm::MS_ROW);
@@ -250,15 +226,33 @@ __device__ __forceinline__ void scan_tile(const unsigned char* codes, const unsi
             ma[0] = a.x; ma[1] = a.y;
             mb[0] = bq.x; mb[1] = bq.y;
         }
+        const uint4* cw = reinterpret_cast<const uint4*>(codes + crow * Gm::CODES_ROW);
         float2 v = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int g = 0; g < Gm::NG; ++g) {
-            const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&ma[g]));  // (mn, s) of row
-            const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&mb[g]));  // (mn, s) of row + 1
-            const float2 mn2 = make_float2(fa.x, fb.x), s2 = make_float2(fa.y, fb.y);
-            const float2 t = __ffma2_rn(s2, make_float2(acc[g][j][0], acc[g][j][1]),
-                                        __fmul2_rn(mn2, make_float2(tq.qsum[g], tq.qsum[g])));
-            v = __fadd2_rn(v, t);
+        for (int kq = 0; kq < Gm::KS / 4; ++kq) {
+            const uint4 w4 = cw[kq];
+            const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+            for (int hg = 0; hg < 2; ++hg) {  // the two 32-channel groups of this 16-byte word
+                const int g = 2 * kq + hg;
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int e2 = 0; e2 < 2; ++e2) {
+                    const int kk = 2 * g + e2;
+                    const uint32_t w = wv[2 * hg + e2] >> (4 * tig);
+                    const uint32_t b0 = bf16x2_sub((w & 0x00030003u) | 0x43004300u, 0x43004300u);
+                    // codes of the odd pair stay at bits 2-3: 4 * code (exact); qc2 carries the 1/4
+                    const uint32_t b1 = bf16x2_sub((w & 0x000C000Cu) | 0x43004300u, 0x43004300u);
+                    mma_bf16(acc, tq.qc0[kk], 0u, tq.qc2[kk], 0u, b0, b1);
+                }
+                // group g of rows (row, row + 1): s_g * <q, code>_g + mn_g * sum_g(q), added in g order
+                const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&ma[g]));  // (mn, s) of row
+                const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&mb[g]));  // (mn, s) of row + 1
+                const float2 mn2 = make_float2(fa.x, fb.x), s2 = make_float2(fa.y, fb.y);
+                const float2 t = __ffma2_rn(s2, make_float2(acc[0], acc[1]),
+                                            __fmul2_rn(mn2, make_float2(tq.qsum[g], tq.qsum[g])));
+                v = __fadd2_rn(v, t);
+            }
         }
         st[2 * j] = __fmul_rn(v.x, scale);
         st[2 * j + 1] = __fmul_rn(v.y, scale);
@@ -271,7 +265,8 @@ __device__ __forceinline__ void scan_tile(const unsigned char* codes, const unsi
 // bytes turns into the exact fp16 values 1152 + x.  The offset is removed
 // from the fp32 sums afterwards; its rounding error (~1e-3 in units of rq)
 // is scaled down by rs (~1e-2) and the softmax scale before it reaches a
-// score.
+// score.  Each group is folded into the running sum right after its two
+// k-steps, in group order.
 template <int D>
 __device__ __forceinline__ void residual_tile(uint32_t res_s, const unsigned char* rs, int warp, int lane,
                                               const TDQuery<D>& tq, float (&rt)[4]) {
@@ -279,19 +274,33 @@ __device__ __forceinline__ void residual_tile(uint32_t res_s, const unsigned cha
     const int tig = lane & 3;
     const int mi = lane >> 3;
     const int ld_row = warp * 16 + 8 * (mi >> 1) + (lane & 7);
-    float acc[Gm::NG][2][4];
+    // rs16 of every group for the lane's rows (row, row + 1) of both n-tiles
+    __half2 ra[2][Gm::NG / 2], rb[2][Gm::NG / 2];
 #pragma unroll
-    for (int g = 0; g < Gm::NG; ++g)
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc[g][j][i] = 0.f;
+    for (int j = 0; j < 2; ++j) {
+        const int row = warp * 16 + 8 * j + 2 * tig;
+        if constexpr (Gm::NG == 4) {
+            const uint2 a = *reinterpret_cast<const uint2*>(rs + row * Gm::RS_ROW);
+            const uint2 bq = *reinterpret_cast<const uint2*>(rs + (row + 1) * Gm::RS_ROW);
+            ra[j][0] = *reinterpret_cast<const __half2*>(&a.x);
+            ra[j][1] = *reinterpret_cast<const __half2*>(&a.y);
+            rb[j][0] = *reinterpret_cast<const __half2*>(&bq.x);
+            rb[j][1] = *reinterpret_cast<const __half2*>(&bq.y);
+        } else {
+            const uint32_t a = *reinterpret_cast<const uint32_t*>(rs + row * Gm::RS_ROW);
+            const uint32_t bq = *reinterpret_cast<const uint32_t*>(rs + (row + 1) * Gm::RS_ROW);
+            ra[j][0] = *reinterpret_cast<const __half2*>(&a);
+            rb[j][0] = *reinterpret_cast<const __half2*>(&bq);
+        }
+    }
+    float2 v[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
     for (int g = 0; g < Gm::NG; ++g) {
         const int chunk = 2 * g + (mi & 1);
         const uint32_t addr = res_s + (D == 128 ? swz(ld_row, chunk) : swz64(ld_row, chunk));
         uint32_t r[4];
         ldsm_x4(addr, r[0], r[1], r[2], r[3]);  // (n-tile 0, kk 2g), (0, 2g+1), (1, 2g), (1, 2g+1)
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
             // fp16 0x64uu is 1024 + uu exactly; with uu = x + 128 the operand is 1152 + x and
@@ -300,43 +309,20 @@ __device__ __forceinline__ void residual_tile(uint32_t res_s, const unsigned cha
             const uint32_t b0 = __byte_perm(u, 0x64646464u, 0x4140);
             const uint32_t b1 = __byte_perm(u, 0x64646464u, 0x4342);
             const int kk = 2 * g + (m & 1);
-            mma_f16(acc[g][m >> 1], tq.qr0[kk], 0u, tq.qr2[kk], 0u, b0, b1);
+            mma_f16(acc[m >> 1], tq.qr0[kk], 0u, tq.qr2[kk], 0u, b0, b1);
         }
-    }
-#pragma unroll
-    for (int g = 0; g < Gm::NG; ++g) {
         const float off = 1152.f * tq.qsumh[g];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            acc[g][j][0] -= off;
-            acc[g][j][1] -= off;
+            const float2 fa = __half22float2(ra[j][g >> 1]), fb = __half22float2(rb[j][g >> 1]);
+            const float2 rsg = (g & 1) ? make_float2(fa.y, fb.y) : make_float2(fa.x, fb.x);
+            v[j] = __ffma2_rn(rsg, make_float2(acc[j][0] - off, acc[j][1] - off), v[j]);
         }
     }
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-        const int row = warp * 16 + 8 * j + 2 * tig;
-        float2 v = make_float2(0.f, 0.f);
-        if constexpr (Gm::NG == 4) {
-            const uint2 a = *reinterpret_cast<const uint2*>(rs + row * Gm::RS_ROW);
-            const uint2 bq = *reinterpret_cast<const uint2*>(rs + (row + 1) * Gm::RS_ROW);
-            const float2 a01 = __half22float2(*reinterpret_cast<const __half2*>(&a.x));
-            const float2 a23 = __half22float2(*reinterpret_cast<const __half2*>(&a.y));
-            const float2 b01 = __half22float2(*reinterpret_cast<const __half2*>(&bq.x));
-            const float2 b23 = __half22float2(*reinterpret_cast<const __half2*>(&bq.y));
-            v = __ffma2_rn(make_float2(a01.x, b01.x), make_float2(acc[0][j][0], acc[0][j][1]), v);
-            v = __ffma2_rn(make_float2(a01.y, b01.y), make_float2(acc[1][j][0], acc[1][j][1]), v);
-            v = __ffma2_rn(make_float2(a23.x, b23.x), make_float2(acc[2][j][0], acc[2][j][1]), v);
-            v = __ffma2_rn(make_float2(a23.y, b23.y), make_float2(acc[3][j][0], acc[3][j][1]), v);
-        } else {
-            const uint32_t a = *reinterpret_cast<const uint32_t*>(rs + row * Gm::RS_ROW);
-            const uint32_t bq = *reinterpret_cast<const uint32_t*>(rs + (row + 1) * Gm::RS_ROW);
-            const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&a));
-            const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&bq));
-            v = __ffma2_rn(make_float2(fa.x, fb.x), make_float2(acc[0][j][0], acc[0][j][1]), v);
-            v = __ffma2_rn(make_float2(fa.y, fb.y), make_float2(acc[1][j][0], acc[1][j][1]), v);
-        }
-        rt[2 * j] = v.x;
-        rt[2 * j + 1] = v.y;
+        rt[2 * j] = v[j].x;
+        rt[2 * j + 1] = v[j].y;
     }
 }
 
