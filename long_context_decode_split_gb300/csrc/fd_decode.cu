@@ -18,8 +18,10 @@
 //     (m_i, l_i, O_i / l_i) to the workspace.
 // Merge, one CTA per (sequence, query head): m = max_i m_i,
 //   w_i = 2^(m_i - m) l_i, out = sum_i w_i O_i / sum_i w_i, lse = m + log sum w.
-// The merge is launched with programmatic dependent launch so its launch
-// overlaps the tail of the partial pass.
+// Both kernels are launched with programmatic dependent launch: the merge's
+// launch overlaps the tail of the partial pass, and the next call's partial
+// pass is scheduled while this call's merge runs (each waits on the grid
+// dependency before its first global memory access).
 #include <cmath>
 #include <cstdio>
 
@@ -102,6 +104,7 @@ partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
 
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait_primary();  // the previous kernel in the stream may still be running
     const int L = clamped_len(p.seq_lens, b, p.L_max, &g_status_decode);
     const int chunk = chunk_len(L, p.splits, p.chunk_fixed);
     const int t0 = split * chunk;
@@ -345,6 +348,7 @@ merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml
              const int32_t* __restrict__ seq_lens, int Hq, int L_max, int splits, int chunk_fixed,
              void* __restrict__ out, int out_bf16, float* __restrict__ lse) {
     pdl_wait_primary();
+    pdl_launch_dependents();  // the next call's partial pass waits for this grid before reading
     const int row = blockIdx.x;
     const int b = row / Hq;
     const int dim = threadIdx.x;
@@ -412,8 +416,7 @@ struct PartialLauncher {
                               cudaStream_t st) {
         cudaError_t e = prepare();
         if (e != cudaSuccess) return e;
-        kernel<<<grid, (CW + 1) * 32, SMEM, st>>>(tk, tv, pp);
-        return cudaGetLastError();
+        return launch_pdl(kernel, grid, dim3((CW + 1) * 32), SMEM, st, tk, tv, pp);
     }
 };
 
@@ -446,21 +449,12 @@ int decode_ctas_per_sm(int D, int G, bool paged) {
 cudaError_t launch_merge(const float* part_o, const float* part_ml, const int32_t* seq_lens,
                          int B, int Hq, int L_max, int D, int splits, int chunk_fixed,
                          void* out, int out_bf16, float* lse, cudaStream_t stream) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(B * Hq));
-    cfg.blockDim = dim3((unsigned)D);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    const dim3 grid((unsigned)(B * Hq)), block((unsigned)D);
     if (D == 128)
-        return cudaLaunchKernelEx(&cfg, merge_kernel<128>, part_o, part_ml, seq_lens, Hq, L_max, splits,
-                                  chunk_fixed, out, out_bf16, lse);
-    return cudaLaunchKernelEx(&cfg, merge_kernel<64>, part_o, part_ml, seq_lens, Hq, L_max, splits,
-                              chunk_fixed, out, out_bf16, lse);
+        return launch_pdl(merge_kernel<128>, grid, block, 0, stream, part_o, part_ml, seq_lens, Hq, L_max, splits,
+                          chunk_fixed, out, out_bf16, lse);
+    return launch_pdl(merge_kernel<64>, grid, block, 0, stream, part_o, part_ml, seq_lens, Hq, L_max, splits,
+                      chunk_fixed, out, out_bf16, lse);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {

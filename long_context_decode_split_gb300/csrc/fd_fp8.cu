@@ -156,6 +156,7 @@ fp8_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
 
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait_primary();  // the previous kernel in the stream may still be running
     const int L = clamped_len(p.seq_lens, b, p.L_max, &g_status_fp8);
     const int chunk = chunk_len(L, p.splits, p.chunk_fixed);
     const int t0 = split * chunk;
@@ -494,8 +495,7 @@ struct Fp8Launcher {
                               const CUtensorMap& tvs, const Fp8Params& pp, dim3 grid, cudaStream_t st) {
         cudaError_t e = prepare();
         if (e != cudaSuccess) return e;
-        kernel<<<grid, 5 * 32, SMEM, st>>>(tk, tv, tks, tvs, pp);
-        return cudaGetLastError();
+        return launch_pdl(kernel, grid, dim3(5 * 32), SMEM, st, tk, tv, tks, tvs, pp);
     }
 };
 

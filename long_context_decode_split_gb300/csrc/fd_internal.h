@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 namespace fd {
@@ -106,6 +107,26 @@ cudaError_t launch_quantize_fp8(const Fp8QuantArgs& a, cudaStream_t stream);
 int fp8_ctas_per_sm(int D, bool paged);
 cudaError_t launch_decode_fp8(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t fp8_status_read(unsigned* bits, bool clear);
+
+// Launch with programmatic stream serialization: the grid may be scheduled
+// while the previous kernel in the stream is still running, so the kernel
+// must execute griddepcontrol.wait before it touches global memory (every
+// kernel launched this way does so first).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Merge of per-chunk partials (shared by the dense and top-delta paths).
 cudaError_t launch_merge(const float* part_o, const float* part_ml, const int32_t* seq_lens,

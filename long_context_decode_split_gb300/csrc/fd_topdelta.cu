@@ -347,6 +347,7 @@ topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constan
 
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait_primary();  // the previous kernel in the stream may still be running
     const int L = clamped_len(p.seq_lens, b, p.L_max, &g_status_topdelta);
     int chunk = p.chunk_fixed;
     if (chunk <= 0) {
@@ -648,8 +649,7 @@ struct TDLauncher {
                               cudaStream_t st) {
         cudaError_t e = prepare();
         if (e != cudaSuccess) return e;
-        topdelta_kernel<D><<<grid, (CW + 1) * 32, SMEM, st>>>(tr, tv, pp);
-        return cudaGetLastError();
+        return launch_pdl(topdelta_kernel<D>, grid, dim3((CW + 1) * 32), SMEM, st, tr, tv, pp);
     }
 };
 
