@@ -18,6 +18,9 @@ Functions (each follows the passage cited in ``fd_oracle.c``):
   quantize_kv_fp8     per-row scaled e4m3 KV cache encoding
   dequantize_kv_fp8   its exact binary64 values
   float_to_e4m3       binary32 -> e4m3 (RNE, saturating)
+  quantize_kv_fp4     e2m1 codes with power-of-two scales per 32-channel block
+  dequantize_kv_fp4   its exact binary64 values
+  decode_dense_fp8/4  the dense definition over the decoded cache
 """
 from __future__ import annotations
 
@@ -61,10 +64,18 @@ def _load():
         lib.oracle_e4m3_value.restype = ctypes.c_double
         lib.oracle_quantize_kv_fp8.argtypes = [P, P, I, I, I, I, P, P, I]
         lib.oracle_dequantize_kv_fp8.argtypes = [P, P, P, I, I, I, I, P]
+        lib.oracle_e2m1_value.argtypes = [ctypes.c_uint8]
+        lib.oracle_e2m1_value.restype = ctypes.c_double
+        lib.oracle_double_to_e2m1.argtypes = [ctypes.c_double]
+        lib.oracle_double_to_e2m1.restype = ctypes.c_uint8
+        lib.oracle_fp4_block_exponent.argtypes = [ctypes.c_double]
+        lib.oracle_fp4_block_exponent.restype = ctypes.c_int
+        lib.oracle_quantize_kv_fp4.argtypes = [P, P, I, I, I, I, P, P, I]
+        lib.oracle_dequantize_kv_fp4.argtypes = [P, P, P, I, I, I, I, P]
         for name in ("oracle_decode_dense", "oracle_decode_dense_f64", "oracle_decode_split",
                      "oracle_decode_paged", "oracle_quantize_keys", "oracle_dequantize_keys",
                      "oracle_decode_topdelta", "oracle_max_threads", "oracle_quantize_kv_fp8",
-                     "oracle_dequantize_kv_fp8"):
+                     "oracle_dequantize_kv_fp8", "oracle_quantize_kv_fp4", "oracle_dequantize_kv_fp4"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -298,4 +309,57 @@ def decode_dense_fp8(q, k_codes, k_scales, v_codes, v_scales, seq_lens, scale, n
     qf = (q.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     kt = dequantize_kv_fp8(k_codes, k_scales, seq_lens)
     vt = dequantize_kv_fp8(v_codes, v_scales, seq_lens)
+    return decode_dense_f64(qf, kt, vt, seq_lens, scale, n_threads)
+
+
+def e2m1_value(c) -> np.ndarray:
+    lib = _load()
+    c = np.asarray(c, np.uint8).ravel()
+    return np.array([lib.oracle_e2m1_value(int(v)) for v in c], np.float64)
+
+
+def to_e2m1(y) -> np.ndarray:
+    """Element-wise nearest e2m1 code (ties to even, saturating at 6)."""
+    lib = _load()
+    y = np.asarray(y, np.float64).ravel()
+    return np.array([lib.oracle_double_to_e2m1(float(v)) for v in y], np.uint8)
+
+
+def fp4_block_exponent(amax) -> int:
+    return int(_load().oracle_fp4_block_exponent(float(amax)))
+
+
+def quantize_kv_fp4(x, seq_lens=None, n_threads=0):
+    """x [B,H,L_max,d] bf16 bits -> (codes u8 [B,H,L_max,d/2], scales u8 [B,H,L_max,d/32]);
+    rows past seq_lens[b] are zero."""
+    x = _u16(x)
+    B, H, L_max, d = x.shape
+    sl = _i32(seq_lens)
+    codes = np.zeros((B, H, L_max, d // 2), np.uint8)
+    scales = np.zeros((B, H, L_max, d // 32), np.uint8)
+    rc = _load().oracle_quantize_kv_fp4(_ptr(x), _ptr(sl), B, H, L_max, d, _ptr(codes), _ptr(scales),
+                                        int(n_threads))
+    _check(rc, "quantize_kv_fp4")
+    return codes, scales
+
+
+def dequantize_kv_fp4(codes, scales, seq_lens=None):
+    codes = np.ascontiguousarray(codes, np.uint8)
+    scales = np.ascontiguousarray(scales, np.uint8)
+    B, H, L_max, d2 = codes.shape
+    d = 2 * d2
+    sl = _i32(seq_lens)
+    out = np.empty((B, H, L_max, d), np.float64)
+    rc = _load().oracle_dequantize_kv_fp4(_ptr(codes), _ptr(scales), _ptr(sl), B, H, L_max, d, _ptr(out))
+    _check(rc, "dequantize_kv_fp4")
+    return out
+
+
+def decode_dense_fp4(q, k_codes, k_scales, v_codes, v_scales, seq_lens, scale, n_threads=0):
+    """Attention over an fp4 cache: the dense definition (tutorial section 1)
+    in binary64 on the decoded rows e2m1(code) * 2^e of K and V."""
+    q = _u16(q)
+    qf = (q.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    kt = dequantize_kv_fp4(k_codes, k_scales, seq_lens)
+    vt = dequantize_kv_fp4(v_codes, v_scales, seq_lens)
     return decode_dense_f64(qf, kt, vt, seq_lens, scale, n_threads)

@@ -18,8 +18,8 @@
  *     section 1 (standard attention, steps 1-4), section 2 (two-stage max
  *     merge equation and its steps 1-4), section 3 (paged KV cache).
  *   Benchmarking blog on a hosted 1M-context model (xxmr.cn), section 1:
- *     an 8-bit-or-narrower KV cache as the lever on decode bytes (the fp8
- *     cache encoding below is this library's definition).
+ *     an 8-bit-or-narrower ("FP4") KV cache as the lever on decode bytes
+ *     (the fp8 and fp4 cache encodings below are this library's definitions).
  *   "Faster Than Flash / Faster Flash Decoding" summary (PaperDaily):
  *     section 3 (top-delta rule s >= m - delta), section 4 (pseudo-max from
  *     attention-sink and local-window anchors), section 5 (2-bit body scan,
@@ -811,6 +811,104 @@ int oracle_dequantize_kv_fp8(const uint8_t* codes, const float* scales, const in
         int L = seq_lens ? seq_lens[b] : L_max;
         for (int c = 0; c < d; ++c)
             out[(size_t)row * d + c] = t < L ? oracle_e4m3_value(codes[(size_t)row * d + c]) * (double)scales[row] : 0.0;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* fp4 (e2m1) KV cache encoding with power-of-two block scales               */
+/* ------------------------------------------------------------------------ */
+
+/* e2m1: 1 sign, 2 exponent bits (bias 1), 1 mantissa bit; magnitudes
+ * 0, 0.5, 1, 1.5, 2, 3, 4, 6 for codes 0..7, no infinity or NaN. */
+double oracle_e2m1_value(uint8_t c) {
+    int e = (c >> 1) & 3, m = c & 1;
+    double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return (c & 8) ? -v : v;
+}
+
+/* Nearest e2m1 code to y (ties to the even code, i.e. mantissa bit 0),
+ * magnitudes above 6 saturating to 6.  Written as a search over the eight
+ * magnitudes so that it can be checked against the table by eye. */
+uint8_t oracle_double_to_e2m1(double y) {
+    uint8_t sign = signbit(y) ? 8 : 0;
+    double a = fabs(y);
+    if (a >= 6.0) return (uint8_t)(sign | 7);
+    int best = 0;
+    double bd = a;  /* distance to code 0 */
+    for (int k = 1; k < 8; ++k) {
+        double dk = fabs(a - oracle_e2m1_value((uint8_t)k));
+        if (dk < bd || (dk == bd && (k & 1) == 0 && (best & 1) == 1)) {
+            best = k;
+            bd = dk;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+/* Block scale exponent: the smallest e in [-126, 127] with 6 * 2^e >= amax. */
+int oracle_fp4_block_exponent(double amax) {
+    int e = -126;
+    while (e < 127 && 6.0 * ldexp(1.0, e) < amax) ++e;
+    return e;
+}
+
+/* Per cache row (token, head) of a bf16 cache [B, H, L_max, d] and per
+ * 32-channel block b of it:
+ *   e_b  = oracle_fp4_block_exponent(max over the block of |x_c|)
+ *   code = e2m1(x_c * 2^-e_b)                       (exact product, RNE)
+ * codes [B, H, L_max, d/2] u8: channel c in byte c/2, the low nibble for even
+ * c; scales [B, H, L_max, d/32] u8: e_b + 127.  Rows past seq_lens[b] are
+ * not written.  The decoded value is e2m1(code) * 2^e_b. */
+int oracle_quantize_kv_fp4(const uint16_t* x, const int32_t* seq_lens, int B, int H, int L_max, int d,
+                           uint8_t* codes, uint8_t* scales, int n_threads) {
+    if (B < 0 || H <= 0 || L_max < 0 || d <= 0 || d % 32 != 0) return -1;
+    if (seq_lens) for (int b = 0; b < B; ++b) if (seq_lens[b] < 0 || seq_lens[b] > L_max) return -2;
+    int nt = pick_threads(n_threads);
+    long long rows = (long long)B * H * L_max;
+    #pragma omp parallel for num_threads(nt) schedule(static)
+    for (long long row = 0; row < rows; ++row) {
+        int b = (int)(row / ((long long)H * L_max));
+        int t = (int)(row % L_max);
+        int L = seq_lens ? seq_lens[b] : L_max;
+        if (t >= L) continue;
+        const uint16_t* xr = x + (size_t)row * d;
+        for (int blk = 0; blk < d / 32; ++blk) {
+            double amax = 0.0;
+            for (int c = 32 * blk; c < 32 * blk + 32; ++c) {
+                double v = fabs(bf16_value(xr[c]));
+                if (v > amax) amax = v;
+            }
+            int e = oracle_fp4_block_exponent(amax);
+            scales[(size_t)row * (d / 32) + blk] = (uint8_t)(e + 127);
+            for (int c = 32 * blk; c < 32 * blk + 32; c += 2) {
+                uint8_t lo = oracle_double_to_e2m1(bf16_value(xr[c]) * ldexp(1.0, -e));
+                uint8_t hi = oracle_double_to_e2m1(bf16_value(xr[c + 1]) * ldexp(1.0, -e));
+                codes[(size_t)row * (d / 2) + c / 2] = (uint8_t)(lo | (hi << 4));
+            }
+        }
+    }
+    return 0;
+}
+
+/* Decoded cache as binary64 (exact); rows past seq_lens[b] are 0. */
+int oracle_dequantize_kv_fp4(const uint8_t* codes, const uint8_t* scales, const int32_t* seq_lens,
+                             int B, int H, int L_max, int d, double* out) {
+    if (B < 0 || H <= 0 || L_max < 0 || d <= 0 || d % 32 != 0) return -1;
+    for (long long row = 0; row < (long long)B * H * L_max; ++row) {
+        int b = (int)(row / ((long long)H * L_max));
+        int t = (int)(row % L_max);
+        int L = seq_lens ? seq_lens[b] : L_max;
+        for (int c = 0; c < d; ++c) {
+            double v = 0.0;
+            if (t < L) {
+                uint8_t byte = codes[(size_t)row * (d / 2) + c / 2];
+                uint8_t code = (c & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+                int e = (int)scales[(size_t)row * (d / 32) + c / 32] - 127;
+                v = oracle_e2m1_value(code) * ldexp(1.0, e);
+            }
+            out[(size_t)row * d + c] = v;
+        }
     }
     return 0;
 }
