@@ -55,7 +55,7 @@ struct Plan {
 // the resident slots form further waves; each wave and each chunk add a
 // small fixed cost.  So: few, long chunks while HBM stays saturated, and no
 // small trailing wave.  Ragged batches (lengths unknown on the host) take
-// chunks small enough that the longest sequences span many waves, so the
+// chunks such that sequences of length L_max span about four waves, so the
 // hardware block scheduler can even out the load.
 Plan plan(int B, int Hkv, int L_max, int requested, bool ragged, int ctas_per_sm, int sms, double r) {
     Plan pl{1, 0};
@@ -88,10 +88,12 @@ Plan plan(int B, int Hkv, int L_max, int requested, bool ragged, int ctas_per_sm
             }
         }
     } else {
-        // aim at ~16 waves for sequences of length L_max, chunks of 8..64 tiles
-        long ct = (units * tiles + 16 * slots - 1) / (16 * slots);
+        // aim at ~4 waves for sequences of length L_max, chunks of 8..256 tiles
+        // (on a batch of lengths U[L_max/8, L_max] fewer, longer chunks win
+        // until about four waves; shorter sequences then fill the gaps)
+        long ct = (units * tiles + 4 * slots - 1) / (4 * slots);
         if (ct < 8) ct = 8;
-        if (ct > 64) ct = 64;
+        if (ct > 256) ct = 256;
         if (ct > tiles) ct = tiles;
         best_chunk = (int)ct;
     }
