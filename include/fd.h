@@ -176,8 +176,9 @@ FD_API size_t fd_topdelta_workspace_size(int B, int Hq, int Hkv, int L_max, int 
  * [B, Hq, ceil(L_max/32)] uint32 (bit j%32 of word j/32 set when j is in
  * Sel) and sel_count [B, Hq] int32.  The residual and V of a token are read
  * only when some query head of its KV group selects a token in the same
- * 64-token tile.  L_max must be a multiple of 4 (FD_ERR_UNSUPPORTED
- * otherwise).  workspace: fd_topdelta_workspace_size() bytes. */
+ * 64-token tile.  L_max must be a multiple of 4 and B * Hkv * L_max at most
+ * 2^31 - 1 (FD_ERR_UNSUPPORTED otherwise).  workspace:
+ * fd_topdelta_workspace_size() bytes. */
 FD_API int fd_decode_topdelta(const void* q, const uint8_t* codes, const void* mn_scale,
                        const int8_t* res, const void* res_scale, const void* v,
                        const int32_t* seq_lens,

@@ -364,6 +364,7 @@ int fd_decode_topdelta(const void* q, const uint8_t* codes, const void* mn_scale
     if (num_splits < 0 || !std::isfinite(scale) || std::isnan(delta) || delta < 0.f) return FD_ERR_INVALID_ARG;
     if (n_sink < 0 || window < 0) return FD_ERR_INVALID_ARG;
     if (L_max % 4 != 0) return FD_ERR_UNSUPPORTED;  // keeps every tile copy 16-byte aligned
+    if ((long long)B * Hkv * L_max > 0x7fffffffLL) return FD_ERR_UNSUPPORTED;  // 32-bit row coordinates
     if (B > 0 && (!q || !codes || !mn_scale || !res || !res_scale || !v || !out)) return FD_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(codes) || !aligned16(mn_scale) || !aligned16(res) || !aligned16(res_scale) ||
         !aligned16(v) || !aligned16(out))

@@ -69,6 +69,13 @@ def test_host_validation_codes(lib):
     assert lib.fd_decode_topdelta(*args, -1.0, 4, 64, *tail) == fd.FD_ERR_INVALID_ARG
     assert lib.fd_decode_topdelta(*args, float("nan"), 4, 64, *tail) == fd.FD_ERR_INVALID_ARG
     assert lib.fd_decode_topdelta(*args, 5.0, 4, -1, *tail) == fd.FD_ERR_INVALID_ARG
+    # L_max not a multiple of 4; more cache rows than 32-bit tile coordinates reach
+    bad_l = [a, a, a, a, a, a, None, 1, 8, 2, 130, 128, 0.1]
+    assert lib.fd_decode_topdelta(*bad_l, 5.0, 4, 64, *tail) == fd.FD_ERR_UNSUPPORTED
+    huge = [a, a, a, a, a, a, None, 40000, 8, 8, 1 << 16, 128, 0.1]
+    assert lib.fd_decode_topdelta(*huge, 5.0, 4, 64, *tail) == fd.FD_ERR_UNSUPPORTED
+    assert lib.fd_decode_dense(a, a, a, None, 40000, 8, 8, 1 << 16, 128, 0.1, 1, a, 1, None, None, 0,
+                               None) == fd.FD_ERR_UNSUPPORTED
 
 
 def test_binding_fails_loudly_without_library(tmp_path):
