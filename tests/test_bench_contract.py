@@ -1,0 +1,47 @@
+"""The benchmark's reference arm on CPU: one JSON line with the contract's
+keys, the oracle timed on the host cores, and the other ranks silent under
+torchrun.  (The GPU arm's line is checked on the GPU machine by running
+bench.py; here only what needs no GPU.)"""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def run_bench(args, env=None):
+    e = dict(os.environ)
+    e.update(env or {})
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT, env=e,
+                       capture_output=True, text=True, timeout=600)
+    return r
+
+
+@pytest.mark.timeout(600)
+@pytest.mark.parametrize("workload", ["tiny", "mha32k_fp8"])
+def test_reference_arm_json_line(workload):
+    r = run_bench(["--impl", "reference", "--workload", workload, "--steps", "3", "--warmup", "3"])
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["steps"] == 3 and d["warmup"] == 3 and d["higher_is_better"] is True
+    assert d["value"] > 0 and d["unit"] == "tokens/s" and d["config"]["workload"] == workload
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+@pytest.mark.timeout(600)
+def test_reference_arm_other_ranks_print_nothing():
+    r = run_bench(["--impl", "reference", "--workload", "tiny", "--steps", "3", "--warmup", "3"],
+                  env={"RANK": "1", "WORLD_SIZE": "1", "LOCAL_RANK": "1"})
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip() == ""
