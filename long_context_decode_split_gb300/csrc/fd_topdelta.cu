@@ -175,25 +175,27 @@ struct TDParams {
     StoreTarget st;
 };
 
-__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
 
 // Query fragments of one lane (row gid of the m16 A operand), per 16-channel
 // k-step.  The k order inside a step is permuted to match how the B
 // operands are unpacked (the same permutation on both sides leaves every dot
 // product unchanged):
 //   2-bit codes: k = 2t, 2t+1, 8+2t, 9+2t <-> channels 2t, 2t+8, 2t+1, 2t+9,
-//                the last two unpacked as 4 * code and weighted by q / 4
+//                the last two unpacked as 4 * code and weighted by q / 4; the
+//                codes enter as bf16 subnormals code * 2^-133 (the tensor
+//                cores keep subnormal operands), so qc0 / qc2 carry the query
+//                scaled by 2^(sq + 126), sq a per-query power of two with
+//                max |q| * 2^sq in [1, 2): every product is exact and the dot
+//                products are those of the plain codes times 2^(sq - 7) (up to
+//                the tensor cores' fp32 accumulation order).
 //   int8 residual (ldmatrix of 16-byte chunks): k = 2t, 2t+1, 8+2t, 9+2t <->
 //   channels 4t, 4t+1, 4t+2, 4t+3          (t = tig, relative to 16*kk)
 template <int D>
 struct TDQuery {
-    uint32_t qc0[D / 16], qc2[D / 16];  // bf16, for the 2-bit scan
+    uint32_t qc0[D / 16], qc2[D / 16];  // bf16, for the 2-bit scan (scaled, see above)
     uint32_t qr0[D / 16], qr2[D / 16];  // fp16, for the residual
-    float qsum[D / 32];                 // sum of the query over each 32-channel group
+    float qsum[D / 32];                 // sum of the query over each 32-channel group, times 2^(sq - 7)
+    float scan_scale;                   // softmax scale times 2^(7 - sq)
     float qsumh[D / 32];                // the same over the fp16 values of the residual fragments
 };
 
@@ -206,7 +208,7 @@ struct TDQuery {
 // combined with explicitly rounded operations in a fixed order.
 template <int D>
 __device__ __forceinline__ void scan_tile(const unsigned char* codes, const unsigned char* ms, int warp, int lane,
-                                          const TDQuery<D>& tq, float scale, float (&st)[4]) {
+                                          const TDQuery<D>& tq, float (&st)[4]) {
     using Gm = TGeo<D>;
     const int gid = lane >> 2, tig = lane & 3;
 #pragma unroll
@@ -240,9 +242,9 @@ __device__ __forceinline__ void scan_tile(const unsigned char* codes, const unsi
                 for (int e2 = 0; e2 < 2; ++e2) {
                     const int kk = 2 * g + e2;
                     const uint32_t w = wv[2 * hg + e2] >> (4 * tig);
-                    const uint32_t b0 = bf16x2_sub((w & 0x00030003u) | 0x43004300u, 0x43004300u);
-                    // codes of the odd pair stay at bits 2-3: 4 * code (exact); qc2 carries the 1/4
-                    const uint32_t b1 = bf16x2_sub((w & 0x000C000Cu) | 0x43004300u, 0x43004300u);
+                    const uint32_t b0 = w & 0x00030003u;  // bf16 subnormals code * 2^-133
+                    // codes of the odd pair stay at bits 2-3: 4 * code * 2^-133; qc2 carries the 1/4
+                    const uint32_t b1 = w & 0x000C000Cu;
                     mma_bf16(acc, tq.qc0[kk], 0u, tq.qc2[kk], 0u, b0, b1);
                 }
                 // group g of rows (row, row + 1): s_g * <q, code>_g + mn_g * sum_g(q), added in g order
@@ -254,8 +256,9 @@ __device__ __forceinline__ void scan_tile(const unsigned char* codes, const unsi
                 v = __fadd2_rn(v, t);
             }
         }
-        st[2 * j] = __fmul_rn(v.x, scale);
-        st[2 * j + 1] = __fmul_rn(v.y, scale);
+        // v is the group sum times 2^(sq - 7) exactly; scan_scale undoes the power of two
+        st[2 * j] = __fmul_rn(v.x, tq.scan_scale);
+        st[2 * j + 1] = __fmul_rn(v.y, tq.scan_scale);
     }
 }
 
@@ -453,12 +456,20 @@ topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constan
     {
         const uint16_t* qrow = p.q + (size_t)(b * p.Hq + hq0 + gid) * D;
         auto qf = [&](int c) { return q_real ? __uint_as_float((uint32_t)qrow[c] << 16) : 0.f; };
-        auto qb = [&](int c) { return q_real ? (uint32_t)qrow[c] : 0u; };
+        // sq: max |q| * 2^sq in [1, 2) over the query's channels (a quad shares a query)
+        float amax = 0.f;
+        for (int c = tig; c < D; c += 4) amax = fmaxf(amax, fabsf(qf(c)));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        int ex = 0;  // amax = m * 2^ex, m in [0.5, 1)
+        if (amax > 0.f && amax <= 3.4e38f) (void)frexpf(amax, &ex);
+        const int sq = 1 - ex;
+        auto qs = [&](int c) { return ldexpf(qf(c), sq + 126); };  // exact: |q| 2^(sq+126) < 2^127
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             const int c0 = 16 * kk;
-            tq.qc0[kk] = qb(c0 + 2 * tig) | (qb(c0 + 2 * tig + 8) << 16);
-            tq.qc2[kk] = pack_bf16(0.25f * qf(c0 + 2 * tig + 1), 0.25f * qf(c0 + 2 * tig + 9));  // exact
+            tq.qc0[kk] = pack_bf16(qs(c0 + 2 * tig), qs(c0 + 2 * tig + 8));                  // exact
+            tq.qc2[kk] = pack_bf16(0.25f * qs(c0 + 2 * tig + 1), 0.25f * qs(c0 + 2 * tig + 9));  // exact
             tq.qr0[kk] = pack_f16(qf(c0 + 4 * tig), qf(c0 + 4 * tig + 1));
             tq.qr2[kk] = pack_f16(qf(c0 + 4 * tig + 2), qf(c0 + 4 * tig + 3));
             ws.qa0[kk] = 0u;
@@ -471,9 +482,10 @@ topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constan
                 sum = __fadd_rn(sum, qf(32 * g + c));
                 sumh += __half2float(__float2half_rn(qf(32 * g + c)));
             }
-            tq.qsum[g] = sum;
+            tq.qsum[g] = ldexpf(sum, sq - 7);  // exact
             tq.qsumh[g] = sumh;
         }
+        tq.scan_scale = ldexpf(p.scale, 7 - sq);
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt)
 #pragma unroll
@@ -517,7 +529,7 @@ topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constan
             }
             named_barrier(1, CW * 32);
             float st[4];
-            scan_tile<D>(stage, stage + kTile * Gm::CODES_ROW, warp, lane, tq, p.scale, st);
+            scan_tile<D>(stage, stage + kTile * Gm::CODES_ROW, warp, lane, tq, st);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int r = warp * 16 + 2 * tig + (i & 1) + 8 * (i >> 1);
@@ -547,7 +559,7 @@ topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constan
         const int rows = scan_rows[s];
         const unsigned char* base = smem + Ly::SCAN_OFF + s * Gm::SCAN_STAGE;
         float st[4];
-        scan_tile<D>(base, base + kTile * Gm::CODES_ROW, warp, lane, tq, p.scale, st);
+        scan_tile<D>(base, base + kTile * Gm::CODES_ROW, warp, lane, tq, st);
         const int ds = k % DS;
         reinterpret_cast<float4*>(dec_s)[(ds * CW + warp) * 32 + lane] = make_float4(st[0], st[1], st[2], st[3]);
         bool any = false;
