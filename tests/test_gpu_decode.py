@@ -210,3 +210,22 @@ def test_full_gqa_paged(fd, oracle):
     assert_out_close(out, ref, BF16_TOL)
     assert_lse_close(lse, lref)
     assert fd.fd_device_status(clear=True) == fd.FD_OK
+
+
+def test_many_short_ragged_sequences(fd, oracle):
+    # thousands of sequences (grid z = B), lengths 0..200 including empty ones, planner's chunking
+    B = 3000
+    g = torch.Generator().manual_seed(12)
+    lens = torch.randint(0, 201, (B,), generator=g).tolist()
+    p = W.random_problem(B, 8, 2, 200, 64, seed=12, device=DEV, seq_lens=lens)
+    ref, lref = oracle_dense(oracle, p)
+    for ns in (0, 1, 3):
+        out, lse = run_dense(fd, p, num_splits=ns)
+        assert_out_close(out, ref, BF16_TOL)
+        assert_lse_close(lse, lref)
+    pp = W.to_paged(p, seed=5)
+    out, lse = fd.fd_decode_paged(pp.q, pp.k_pages, pp.v_pages, pp.page_table, pp.num_pages, pp.seq_lens,
+                                  pp.scale)
+    assert_out_close(out, ref, BF16_TOL)
+    assert_lse_close(lse, lref)
+    assert fd.fd_device_status(clear=True) == fd.FD_OK

@@ -267,3 +267,18 @@ def test_fp8_full_gqa_sampled(fd, oracle):
                                             vc[:, ks_].cpu().numpy(), vs[:, ks_].cpu().numpy(), None, p.scale)
         assert_out_close(out[:, qs], ref, BF16_TOL, what=f"kv head {h}")
         assert_lse_close(lse[:, qs], lref)
+
+
+def test_fp8_many_short_ragged_sequences(fd, oracle):
+    B = 3000
+    g = torch.Generator().manual_seed(13)
+    lens = torch.randint(0, 201, (B,), generator=g).tolist()
+    p = W.random_problem(B, 8, 2, 200, 128, seed=13, device=DEV, seq_lens=lens)
+    kc, ks = fd.fd_quantize_kv_fp8(p.k, p.seq_lens)
+    vc, vs = fd.fd_quantize_kv_fp8(p.v, p.seq_lens)
+    ref, lref = oracle_fp8(oracle, p, kc, ks, vc, vs)
+    for ns in (0, 2):
+        out, lse = fd.fd_decode_dense_fp8(p.q, kc, ks, vc, vs, p.seq_lens, p.scale, num_splits=ns)
+        assert_out_close(out, ref, BF16_TOL)
+        assert_lse_close(lse, lref)
+    assert fd.fd_device_status(clear=True) == fd.FD_OK
