@@ -9,7 +9,8 @@ Default workload: MHA decode, B=1, Hq=Hkv=32, d=128, L=32768, bf16 KV cache
 (512 MiB of K+V per call, larger than the 129 MB L2, so no flush is needed
 between calls).  Other workloads: --workload tiny|mha32k|gqa_paged|million|
 ffd_dense|ffd_topdelta5|ffd_topdelta7, and mha32k_fp8|million_fp8|ffd_dense_fp8|
-gqa_paged_fp8 (the same caches in the fp8 e4m3 encoding, per-row f32 scales).
+gqa_paged_fp8 (the same caches in the fp8 e4m3 encoding, per-row f32 scales) and
+the *_fp4 variants (e2m1 codes with power-of-two scales per 32 channels).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fd|reference]
 
@@ -42,7 +43,8 @@ L2_BYTES = 129 * 1024 * 1024
 
 DEFAULT_STEPS = {"tiny": 20000, "mha32k": 20000, "gqa_paged": 3000, "million": 3000,
                  "ffd_dense": 4000, "ffd_topdelta5": 4000, "ffd_topdelta7": 4000,
-                 "mha32k_fp8": 20000, "million_fp8": 4000, "ffd_dense_fp8": 6000, "gqa_paged_fp8": 4000}
+                 "mha32k_fp8": 20000, "million_fp8": 4000, "ffd_dense_fp8": 6000, "gqa_paged_fp8": 4000,
+                 "mha32k_fp4": 20000, "million_fp4": 4000, "ffd_dense_fp4": 6000, "gqa_paged_fp4": 4000}
 WORKLOADS = list(DEFAULT_STEPS)
 
 
@@ -142,7 +144,8 @@ class Workload:
         self.device = device
         self.topdelta = None
         self.fp8 = name.endswith("_fp8")
-        if self.fp8:
+        self.fp4 = name.endswith("_fp4")
+        if self.fp8 or self.fp4:
             name = name[:-4]
         self.n_sink, self.window = n_sink, window
         over = {}
@@ -177,15 +180,20 @@ class Workload:
                                dtype=torch.float32 if p.out_dtype == "f32" else torch.bfloat16)
         self.lse = torch.empty((B, Hq), device=device, dtype=torch.float32)
         self.sel_stats = None
-        if self.fp8:
+        if self.fp8 or self.fp4:
             # encode the cache once (outside the timed region); keep the bf16 copy for e2e rows
+            enc = fd.fd_quantize_kv_fp8 if self.fp8 else fd.fd_quantize_kv_fp4
             if self.paged:
-                self.kv8 = fd.fd_quantize_kv_fp8(p.k_pages) + fd.fd_quantize_kv_fp8(p.v_pages)
+                self.kv8 = enc(p.k_pages) + enc(p.v_pages)
             else:
-                self.kv8 = fd.fd_quantize_kv_fp8(p.k) + fd.fd_quantize_kv_fp8(p.v)
+                self.kv8 = enc(p.k) + enc(p.v)
             torch.cuda.synchronize()
-            need = fd.fd_decode_fp8_workspace_size(B, Hq, Hkv, p.L_max, d, p.num_splits, self.paged)
-            self.splits = fd.fd_num_splits_fp8(B, Hq, Hkv, p.L_max, d, p.num_splits, self.paged)
+            if self.fp8:
+                need = fd.fd_decode_fp8_workspace_size(B, Hq, Hkv, p.L_max, d, p.num_splits, self.paged)
+                self.splits = fd.fd_num_splits_fp8(B, Hq, Hkv, p.L_max, d, p.num_splits, self.paged)
+            else:
+                need = fd.fd_decode_fp4_workspace_size(B, Hq, Hkv, p.L_max, d, p.num_splits, self.paged)
+                self.splits = fd.fd_num_splits_fp4(B, Hq, Hkv, p.L_max, d, p.num_splits, self.paged)
         elif self.topdelta is not None:
             self.qk = fd.fd_quantize_keys(p.k, p.seq_lens)
             need = fd.fd_topdelta_workspace_size(B, Hq, Hkv, p.L_max, d, p.num_splits)
@@ -231,15 +239,16 @@ class Workload:
 
     def call(self, stream=None):
         p, fd = self.p, self.fd
-        if self.fp8:
+        if self.fp8 or self.fp4:
             kc, ks, vc, vs = self.kv8
             if self.paged:
-                fd.fd_decode_paged_fp8(p.q, kc, ks, vc, vs, p.page_table, p.num_pages, p.seq_lens, p.scale,
-                                       p.num_splits, out=self.out, lse=self.lse, out_dtype=self.out_dtype,
-                                       workspace=self.ws, stream=stream)
+                paged = fd.fd_decode_paged_fp8 if self.fp8 else fd.fd_decode_paged_fp4
+                paged(p.q, kc, ks, vc, vs, p.page_table, p.num_pages, p.seq_lens, p.scale, p.num_splits,
+                      out=self.out, lse=self.lse, out_dtype=self.out_dtype, workspace=self.ws, stream=stream)
             else:
-                fd.fd_decode_dense_fp8(p.q, kc, ks, vc, vs, None, p.scale, p.num_splits, out=self.out,
-                                       lse=self.lse, out_dtype=self.out_dtype, workspace=self.ws, stream=stream)
+                dense = fd.fd_decode_dense_fp8 if self.fp8 else fd.fd_decode_dense_fp4
+                dense(p.q, kc, ks, vc, vs, None, p.scale, p.num_splits, out=self.out, lse=self.lse,
+                      out_dtype=self.out_dtype, workspace=self.ws, stream=stream)
         elif self.topdelta is not None:
             c, ms, r, rs = self.qk
             fd.fd_decode_topdelta(p.q, c, ms, r, rs, p.v, p.seq_lens, p.scale, self.topdelta, self.n_sink,
@@ -266,6 +275,8 @@ class Workload:
         io = B * Hq * d * 2 + B * Hq * d * (4 if p.out_dtype == "f32" else 2) + B * Hq * 4
         if self.fp8:
             return self.kv_tokens * Hkv * (d + 4) * 2 + io  # K and V codes + their row scales
+        if self.fp4:
+            return self.kv_tokens * Hkv * (d // 2 + d // 32) * 2 + io  # codes + block exponents
         if self.topdelta is None:
             return self.kv_tokens * Hkv * d * 2 * 2 + io
         scan = self.kv_tokens * Hkv * (d // 4 + (d // 32) * 4)
@@ -279,7 +290,8 @@ class Workload:
              "L": p.L_max if not self.paged else "ragged", "kv_tokens": self.kv_tokens,
              "num_splits": self.splits if self.splits is not None else p.num_splits,
              "cache": "paged-64" if self.paged else "contiguous", "out_dtype": p.out_dtype,
-             "kv_dtype": "e4m3 codes + f32 row scales" if self.fp8 else "bf16"}
+             "kv_dtype": ("e4m3 codes + f32 row scales" if self.fp8 else
+                          "e2m1 codes + power-of-two scales per 32 channels" if self.fp4 else "bf16")}
         if self.topdelta is not None:
             c.update(delta=self.topdelta, n_sink=self.n_sink, window=self.window, selection=self.sel_stats,
                      dense_equivalent_bytes=self.kv_tokens * p.Hkv * p.d * 4)
@@ -355,18 +367,26 @@ def time_e2e(wl, steps, warmup, dist_ctx):
         tgt = None
     k_dev = torch.empty(k_rows.shape, dtype=k_rows.dtype, device=dev)
     v_dev = torch.empty(v_rows.shape, dtype=v_rows.dtype, device=dev)
-    if wl.fp8:
-        # the new rows are encoded on the device (fd_quantize_kv_fp8) and written into the fp8 cache
+    if wl.fp8 or wl.fp4:
+        # the new rows are encoded on the device (fd_quantize_kv_fp8/fp4) and written into the cache
         if wl.paged:  # rows [n, Hkv, d] -> n * Hkv cache rows of one token
             k_new = k_dev.view(-1, 1, 1, k_dev.shape[-1])
             v_new = v_dev.view(-1, 1, 1, v_dev.shape[-1])
         else:         # rows [B, Hkv, d] -> token L_max - 1 of every head
             k_new = k_dev.view(k_dev.shape[0], k_dev.shape[1], 1, -1)
             v_new = v_dev.view(v_dev.shape[0], v_dev.shape[1], 1, -1)
-        kc_new = torch.empty(k_new.shape, dtype=torch.uint8, device=dev)
-        vc_new = torch.empty(v_new.shape, dtype=torch.uint8, device=dev)
-        ks_new = torch.empty(k_new.shape[:3], dtype=torch.float32, device=dev)
-        vs_new = torch.empty(v_new.shape[:3], dtype=torch.float32, device=dev)
+        dd = k_new.shape[-1]
+        if wl.fp8:
+            kc_new = torch.empty(k_new.shape, dtype=torch.uint8, device=dev)
+            vc_new = torch.empty(v_new.shape, dtype=torch.uint8, device=dev)
+            ks_new = torch.empty(k_new.shape[:3], dtype=torch.float32, device=dev)
+            vs_new = torch.empty(v_new.shape[:3], dtype=torch.float32, device=dev)
+        else:
+            kc_new = torch.empty(k_new.shape[:3] + (dd // 2,), dtype=torch.uint8, device=dev)
+            vc_new = torch.empty(v_new.shape[:3] + (dd // 2,), dtype=torch.uint8, device=dev)
+            ks_new = torch.empty(k_new.shape[:3] + (dd // 32,), dtype=torch.uint8, device=dev)
+            vs_new = torch.empty(v_new.shape[:3] + (dd // 32,), dtype=torch.uint8, device=dev)
+        encode = fd.fd_quantize_kv_fp8 if wl.fp8 else fd.fd_quantize_kv_fp4
     out_h = torch.empty(wl.out.shape, dtype=wl.out.dtype).pin_memory()
     lse_h = torch.empty(wl.lse.shape, dtype=wl.lse.dtype).pin_memory()
     h2d = q_h.numel() * 2 + k_rows.numel() * 2 + v_rows.numel() * 2
@@ -376,9 +396,9 @@ def time_e2e(wl, steps, warmup, dist_ctx):
         p.q.copy_(q_h, non_blocking=True)
         k_dev.copy_(k_rows, non_blocking=True)
         v_dev.copy_(v_rows, non_blocking=True)
-        if wl.fp8:
-            fd.fd_quantize_kv_fp8(k_new, codes=kc_new, scales=ks_new)
-            fd.fd_quantize_kv_fp8(v_new, codes=vc_new, scales=vs_new)
+        if wl.fp8 or wl.fp4:
+            encode(k_new, codes=kc_new, scales=ks_new)
+            encode(v_new, codes=vc_new, scales=vs_new)
             kc, ks, vc, vs = wl.kv8
             if wl.paged:
                 H = k_dev.shape[1]
@@ -424,6 +444,7 @@ FULL_SHAPES = {"tiny": (1, 1, 1, 1024, 64), "mha32k": (1, 32, 32, 32768, 128),
                "ffd_dense": (4, 32, 8, 131072, 128), "ffd_topdelta5": (4, 32, 8, 131072, 128),
                "ffd_topdelta7": (4, 32, 8, 131072, 128)}
 FULL_SHAPES.update({k + "_fp8": FULL_SHAPES[k] for k in ("mha32k", "million", "gqa_paged", "ffd_dense")})
+FULL_SHAPES.update({k + "_fp4": FULL_SHAPES[k] for k in ("mha32k", "million", "gqa_paged", "ffd_dense")})
 
 
 class OracleSample:
@@ -443,6 +464,7 @@ class OracleSample:
         self.oracle = oracle
         B, Hq, Hkv, L, d = FULL_SHAPES[name]
         self.fp8 = name.endswith("_fp8")
+        self.fp4 = name.endswith("_fp4")
         G = Hq // Hkv
         self.B = B
         self.delta = None
@@ -463,6 +485,8 @@ class OracleSample:
                 self.enc = oracle.quantize_keys(self.args[1])
             if self.fp8:
                 self.enc = oracle.quantize_kv_fp8(self.args[1]) + oracle.quantize_kv_fp8(self.args[2])
+            if self.fp4:
+                self.enc = oracle.quantize_kv_fp4(self.args[1]) + oracle.quantize_kv_fp4(self.args[2])
             t0 = time.perf_counter()
             self.run()
             dt = time.perf_counter() - t0
@@ -483,6 +507,9 @@ class OracleSample:
         if self.fp8:
             kc, ks, vc, vs = self.enc
             self.oracle.decode_dense_fp8(q, kc, ks, vc, vs, None, scale)
+        elif self.fp4:
+            kc, ks, vc, vs = self.enc
+            self.oracle.decode_dense_fp4(q, kc, ks, vc, vs, None, scale)
         elif self.delta is not None:
             c, ms, r, rs = self.enc
             self.oracle.decode_topdelta(q, c, ms, r, rs, v, None, scale, self.delta)
@@ -661,7 +688,8 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": n, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "kv_dtype": "e4m3" if wl.fp8 else "bf16",
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "kv_dtype": "e4m3" if wl.fp8 else "e2m1" if wl.fp4 else "bf16",
             "data": "synthetic", "config": cfg,
             "us_per_call": per_call_s * 1e6,
             "kv_tokens_per_s": wl.kv_tokens * n / per_call_s,

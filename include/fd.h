@@ -244,6 +244,59 @@ FD_API int fd_decode_paged_fp8(const void* q, const uint8_t* k_pages, const floa
                                void* out, int out_dtype, float* lse,
                                void* workspace, size_t workspace_bytes, void* stream);
 
+/* fp4 KV cache encoder ([KV8] names an "FP4" cache; this format is this
+ * library's definition).  For each cache row x (one token of one head) and
+ * each 32-channel block b of it, in exact arithmetic:
+ *   e_b   = the smallest integer in [-126, 127] with 6 * 2^e_b >= max |x|
+ *           over the block (-126 for an all-zero block)
+ *   code  = e2m1(x * 2^-e_b)
+ * e2m1(): 1 sign, 2 exponent bits (bias 1), 1 mantissa bit, magnitudes
+ * 0, 0.5, 1, 1.5, 2, 3, 4, 6, round to nearest with ties to the even code.
+ * The decoded value is e2m1(code) * 2^e_b.  Layouts (row = (b*H + h)*L_max + t):
+ *   x       [B, H, L_max, d] bf16 (input)
+ *   codes   [row, d/2]  uint8: channel c in byte c/2, the low nibble for even c
+ *   scales  [row, d/32] uint8: e_b + 127
+ * Rows with t >= seq_lens[b] (seq_lens may be NULL) are not written; the
+ * sign of a code rounded to zero follows x.  d must be 64 or 128. */
+FD_API int fd_quantize_kv_fp4(const void* x, const int32_t* seq_lens,
+                              int B, int H, int L_max, int d,
+                              uint8_t* codes, uint8_t* scales, void* stream);
+
+/* fd_num_splits / fd_decode_workspace_size for the fp4 decode entry points. */
+FD_API int fd_num_splits_fp4(int B, int Hq, int Hkv, int L_max, int d, int num_splits, int ragged);
+FD_API size_t fd_decode_fp4_workspace_size(int B, int Hq, int Hkv, int L_max, int d,
+                                           int num_splits, int ragged);
+
+/* Split-KV decode ([FD] sections 1-2) over an fp4 cache written by
+ * fd_quantize_kv_fp4: the attention of q over the decoded rows (computed
+ * with fp16 tensor-core products and fp32 accumulation).
+ *   k_codes, v_codes    [B, Hkv, L_max, d/2]  uint8
+ *   k_scales, v_scales  [B, Hkv, L_max, d/32] uint8
+ * All other arguments, outputs and the workspace contract are those of
+ * fd_decode_dense, with fd_decode_fp4_workspace_size() for the workspace. */
+FD_API int fd_decode_dense_fp4(const void* q, const uint8_t* k_codes, const uint8_t* k_scales,
+                               const uint8_t* v_codes, const uint8_t* v_scales,
+                               const int32_t* seq_lens,
+                               int B, int Hq, int Hkv, int L_max, int d,
+                               float scale, int num_splits,
+                               void* out, int out_dtype, float* lse,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/* The same over a paged fp4 cache ([FD] section 3): pages of 64 tokens,
+ *   k_pages, v_pages              [num_pages, Hkv, 64, d/2]  uint8 codes
+ *   k_page_scales, v_page_scales  [num_pages, Hkv, 64, d/32] uint8
+ * page_table, seq_lens and the remaining arguments as fd_decode_paged
+ * (workspace: fd_decode_fp4_workspace_size(..., L_max = max_pages * 64,
+ * ragged = 1)). */
+FD_API int fd_decode_paged_fp4(const void* q, const uint8_t* k_pages, const uint8_t* k_page_scales,
+                               const uint8_t* v_pages, const uint8_t* v_page_scales,
+                               const int32_t* page_table, int max_pages, int num_pages,
+                               const int32_t* seq_lens, int page_size,
+                               int B, int Hq, int Hkv, int d,
+                               float scale, int num_splits,
+                               void* out, int out_dtype, float* lse,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
 /* Size of the fixed device scratch array used by fd_decode_dense_noalloc. */
 #define FD_NOALLOC_SCRATCH_BYTES (4u << 20)
 

@@ -21,7 +21,8 @@ __all__ = [
     "fd_decode_workspace_size", "fd_decode_dense", "fd_decode_paged", "fd_quantize_keys",
     "fd_topdelta_workspace_size", "fd_decode_topdelta", "fd_device_status", "fd_decode_dense_noalloc",
     "fd_quantize_kv_fp8", "fd_num_splits_fp8", "fd_decode_fp8_workspace_size", "fd_decode_dense_fp8",
-    "fd_decode_paged_fp8",
+    "fd_decode_paged_fp8", "fd_quantize_kv_fp4", "fd_num_splits_fp4", "fd_decode_fp4_workspace_size",
+    "fd_decode_dense_fp4", "fd_decode_paged_fp4",
     "FD_OK", "FD_ERR_INVALID_ARG", "FD_ERR_UNSUPPORTED", "FD_ERR_WORKSPACE_TOO_SMALL",
     "FD_ERR_BAD_PAGE_TABLE", "FD_ERR_CUDA", "FD_ERR_DEVICE_TIMEOUT", "FD_OUT_F32", "FD_OUT_BF16",
 ]
@@ -82,6 +83,11 @@ def open_library(path: str):
         "fd_decode_fp8_workspace_size": (S, [I, I, I, I, I, I, I]),
         "fd_decode_dense_fp8": (I, [P, P, P, P, P, P, I, I, I, I, I, F, I, P, I, P, P, S, P]),
         "fd_decode_paged_fp8": (I, [P, P, P, P, P, P, I, I, P, I, I, I, I, I, F, I, P, I, P, P, S, P]),
+        "fd_quantize_kv_fp4": (I, [P, P, I, I, I, I, P, P, P]),
+        "fd_num_splits_fp4": (I, [I, I, I, I, I, I, I]),
+        "fd_decode_fp4_workspace_size": (S, [I, I, I, I, I, I, I]),
+        "fd_decode_dense_fp4": (I, [P, P, P, P, P, P, I, I, I, I, I, F, I, P, I, P, P, S, P]),
+        "fd_decode_paged_fp4": (I, [P, P, P, P, P, P, I, I, P, I, I, I, I, I, F, I, P, I, P, P, S, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -408,6 +414,95 @@ def fd_decode_paged_fp8(q, k_pages, k_page_scales, v_pages, v_page_scales, page_
                                  d, scale, int(num_splits), _p(out), code, _p(lse), _p(ws),
                                  0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
     _raise(st, "fd_decode_paged_fp8")
+    return out, lse
+
+
+def fd_quantize_kv_fp4(x, seq_lens=None, codes=None, scales=None, stream=None):
+    """fp4 cache encoder.  x [B,H,L_max,d] bf16 -> (codes uint8 [B,H,L_max,d/2],
+    scales uint8 [B,H,L_max,d/32]).  Rows past seq_lens[b] are left as passed
+    (zero when this wrapper allocates them)."""
+    lib = load()
+    _check_cuda(x, "x", torch.bfloat16)
+    _need(x.dim() == 4, "x must be [B, H, L_max, d]")
+    B, H, L_max, d = x.shape
+    if codes is None:
+        codes = torch.zeros((B, H, L_max, d // 2), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.zeros((B, H, L_max, d // 32), dtype=torch.uint8, device=x.device)
+    _check_cuda(codes, "codes", torch.uint8, (B, H, L_max, d // 2))
+    _check_cuda(scales, "scales", torch.uint8, (B, H, L_max, d // 32))
+    if seq_lens is not None:
+        _check_cuda(seq_lens, "seq_lens", torch.int32, (B,))
+    st = lib.fd_quantize_kv_fp4(_p(x), _p(seq_lens), B, H, L_max, d, _p(codes), _p(scales), _stream(stream))
+    _raise(st, "fd_quantize_kv_fp4")
+    return codes, scales
+
+
+def fd_num_splits_fp4(B, Hq, Hkv, L_max, d, num_splits=0, ragged=False) -> int:
+    r = int(load().fd_num_splits_fp4(B, Hq, Hkv, L_max, d, num_splits, int(bool(ragged))))
+    if r < 0:
+        raise FdError(-r, "fd_num_splits_fp4")
+    return r
+
+
+def fd_decode_fp4_workspace_size(B, Hq, Hkv, L_max, d, num_splits=0, ragged=False) -> int:
+    return int(load().fd_decode_fp4_workspace_size(B, Hq, Hkv, L_max, d, num_splits, int(bool(ragged))))
+
+
+def fd_decode_dense_fp4(q, k_codes, k_scales, v_codes, v_scales, seq_lens=None, scale=None, num_splits=0,
+                        out=None, lse=None, out_dtype="bf16", want_lse=True, workspace=None, stream=None):
+    """Split-KV decode over an fp4 cache.  q [B,Hq,d] bf16; k_codes, v_codes
+    [B,Hkv,L_max,d/2] uint8; k_scales, v_scales [B,Hkv,L_max,d/32] uint8."""
+    lib = load()
+    _check_cuda(q, "q", torch.bfloat16)
+    B, Hq, d = q.shape
+    _check_cuda(k_codes, "k_codes", torch.uint8)
+    _need(k_codes.dim() == 4 and k_codes.shape[0] == B and k_codes.shape[3] * 2 == d,
+          "k_codes must be [B, Hkv, L_max, d/2]")
+    _, Hkv, L_max, _ = k_codes.shape
+    _check_cuda(v_codes, "v_codes", torch.uint8, k_codes.shape)
+    _check_cuda(k_scales, "k_scales", torch.uint8, (B, Hkv, L_max, d // 32))
+    _check_cuda(v_scales, "v_scales", torch.uint8, (B, Hkv, L_max, d // 32))
+    if seq_lens is not None:
+        _check_cuda(seq_lens, "seq_lens", torch.int32, (B,))
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    code, out, lse = _outputs(B, Hq, d, q.device, out, lse, out_dtype, want_lse)
+    need = fd_decode_fp4_workspace_size(B, Hq, Hkv, L_max, d, num_splits, seq_lens is not None)
+    ws = _workspace(need, q.device, workspace)
+    st = lib.fd_decode_dense_fp4(_p(q), _p(k_codes), _p(k_scales), _p(v_codes), _p(v_scales), _p(seq_lens),
+                                 B, Hq, Hkv, L_max, d, scale, int(num_splits), _p(out), code, _p(lse), _p(ws),
+                                 0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
+    _raise(st, "fd_decode_dense_fp4")
+    return out, lse
+
+
+def fd_decode_paged_fp4(q, k_pages, k_page_scales, v_pages, v_page_scales, page_table, num_pages, seq_lens,
+                        scale=None, num_splits=0, out=None, lse=None, out_dtype="bf16", want_lse=True,
+                        workspace=None, stream=None):
+    """Paged split-KV decode over an fp4 cache.  k_pages/v_pages [P,Hkv,64,d/2]
+    uint8, k_page_scales/v_page_scales [P,Hkv,64,d/32] uint8."""
+    lib = load()
+    _check_cuda(q, "q", torch.bfloat16)
+    B, Hq, d = q.shape
+    _check_cuda(k_pages, "k_pages", torch.uint8)
+    _need(k_pages.dim() == 4 and k_pages.shape[3] * 2 == d, "k_pages must be [P, Hkv, page, d/2]")
+    P, Hkv, page_size, _ = k_pages.shape
+    _check_cuda(v_pages, "v_pages", torch.uint8, k_pages.shape)
+    _check_cuda(k_page_scales, "k_page_scales", torch.uint8, (P, Hkv, page_size, d // 32))
+    _check_cuda(v_page_scales, "v_page_scales", torch.uint8, (P, Hkv, page_size, d // 32))
+    _check_cuda(page_table, "page_table", torch.int32)
+    _need(page_table.dim() == 2 and page_table.shape[0] == B, "page_table must be [B, max_pages]")
+    max_pages = page_table.shape[1]
+    _check_cuda(seq_lens, "seq_lens", torch.int32, (B,))
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    code, out, lse = _outputs(B, Hq, d, q.device, out, lse, out_dtype, want_lse)
+    need = fd_decode_fp4_workspace_size(B, Hq, Hkv, max_pages * page_size, d, num_splits, True)
+    ws = _workspace(need, q.device, workspace)
+    st = lib.fd_decode_paged_fp4(_p(q), _p(k_pages), _p(k_page_scales), _p(v_pages), _p(v_page_scales),
+                                 _p(page_table), max_pages, int(num_pages), _p(seq_lens), page_size, B, Hq, Hkv,
+                                 d, scale, int(num_splits), _p(out), code, _p(lse), _p(ws),
+                                 0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
+    _raise(st, "fd_decode_paged_fp4")
     return out, lse
 
 

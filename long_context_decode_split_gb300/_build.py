@@ -22,7 +22,7 @@ LIB = os.path.join(PKG, "libfd.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "-Xptxas", "-warn-spills", f"-I{INCLUDE}", f"-I{CSRC}"]
-SOURCES = ["fd_api.cu", "fd_decode.cu", "fd_topdelta.cu", "fd_fp8.cu", "fd_noalloc.cu"]
+SOURCES = ["fd_api.cu", "fd_decode.cu", "fd_topdelta.cu", "fd_fp8.cu", "fd_fp4.cu", "fd_noalloc.cu"]
 
 
 def nvcc() -> str:

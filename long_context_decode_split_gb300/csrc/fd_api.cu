@@ -124,6 +124,14 @@ Plan fp8_plan(int B, int Hq, int Hkv, int L_max, int d, int requested, bool ragg
     return plan(B, Hkv, L_max, requested, ragged, occ, sms, saturating_ctas(d / 2, sms));
 }
 
+// The fp4 cache moves d/2 + d/32 bytes per row and operand: a tile carries
+// about the bytes of a bf16 tile of a quarter of the head size.
+Plan fp4_plan(int B, int Hq, int Hkv, int L_max, int d, int requested, bool ragged) {
+    const int sms = current_sm_count();
+    const int occ = requested > 0 ? 1 : fd::fp4_ctas_per_sm(d, ragged);
+    return plan(B, Hkv, L_max, requested, ragged, occ, sms, saturating_ctas(d / 4, sms));
+}
+
 Plan topdelta_plan(int B, int Hq, int Hkv, int L_max, int d, int requested) {
     const int sms = current_sm_count();
     const int occ = requested > 0 ? 1 : fd::topdelta_ctas_per_sm(d, Hq / Hkv);
@@ -166,13 +174,16 @@ size_t fd_decode_workspace_size(int B, int Hq, int Hkv, int L_max, int d, int nu
     return fd::decode_workspace_bytes(B, Hq, d, pl.splits);
 }
 
+enum class Cache { BF16, FP8, FP4 };
+
 static int decode_common(fd::DecodeArgs& a, int num_splits, bool ragged, int out_dtype, void* workspace,
-                         size_t workspace_bytes, void* stream, bool fp8 = false) {
+                         size_t workspace_bytes, void* stream, Cache cache = Cache::BF16) {
+    const bool quantized = cache != Cache::BF16;  // scale arrays required
     if (out_dtype != FD_OUT_F32 && out_dtype != FD_OUT_BF16) return FD_ERR_INVALID_ARG;
     if (num_splits < 0 || !std::isfinite(a.scale)) return FD_ERR_INVALID_ARG;
     if (a.B > 0 && (!a.q || !a.k || !a.v || !a.out)) return FD_ERR_INVALID_ARG;
     if (!aligned16(a.q) || !aligned16(a.k) || !aligned16(a.v) || !aligned16(a.out)) return FD_ERR_INVALID_ARG;
-    if (fp8 && ((a.B > 0 && (!a.k_scales || !a.v_scales)) || !aligned16(a.k_scales) || !aligned16(a.v_scales)))
+    if (quantized && ((a.B > 0 && (!a.k_scales || !a.v_scales)) || !aligned16(a.k_scales) || !aligned16(a.v_scales)))
         return FD_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(a.lse) & 3u) || (reinterpret_cast<uintptr_t>(a.seq_lens) & 3u))
         return FD_ERR_INVALID_ARG;
@@ -180,8 +191,9 @@ static int decode_common(fd::DecodeArgs& a, int num_splits, bool ragged, int out
     const long long cache_rows = a.page_table ? (long long)a.num_pages * a.Hkv * kTile
                                               : (long long)a.B * a.Hkv * a.L_max;
     if (cache_rows > 0x7fffffffLL) return FD_ERR_UNSUPPORTED;
-    const Plan pl = fp8 ? fp8_plan(a.B, a.Hq, a.Hkv, a.L_max, a.D, num_splits, ragged)
-                        : decode_plan(a.B, a.Hq, a.Hkv, a.L_max, a.D, num_splits, ragged);
+    const Plan pl = cache == Cache::FP8 ? fp8_plan(a.B, a.Hq, a.Hkv, a.L_max, a.D, num_splits, ragged)
+                    : cache == Cache::FP4 ? fp4_plan(a.B, a.Hq, a.Hkv, a.L_max, a.D, num_splits, ragged)
+                                          : decode_plan(a.B, a.Hq, a.Hkv, a.L_max, a.D, num_splits, ragged);
     const size_t need = fd::decode_workspace_bytes(a.B, a.Hq, a.D, pl.splits);
     if (need > 0) {
         if (!workspace || workspace_bytes < need) return FD_ERR_WORKSPACE_TOO_SMALL;
@@ -193,8 +205,10 @@ static int decode_common(fd::DecodeArgs& a, int num_splits, bool ragged, int out
     float* ws = static_cast<float*>(workspace);
     a.part_o = ws;
     a.part_ml = ws ? ws + (size_t)a.B * a.Hq * pl.splits * a.D : nullptr;
-    return to_status(fp8 ? fd::launch_decode_fp8(a, static_cast<cudaStream_t>(stream))
-                         : fd::launch_decode(a, static_cast<cudaStream_t>(stream)));
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return to_status(cache == Cache::FP8   ? fd::launch_decode_fp8(a, st)
+                     : cache == Cache::FP4 ? fd::launch_decode_fp4(a, st)
+                                           : fd::launch_decode(a, st));
 }
 
 int fd_decode_dense(const void* q, const void* k, const void* v, const int32_t* seq_lens,
@@ -298,7 +312,8 @@ int fd_decode_dense_fp8(const void* q, const uint8_t* k_codes, const float* k_sc
     a.scale = scale;
     a.out = out;
     a.lse = lse;
-    return decode_common(a, num_splits, seq_lens != nullptr, out_dtype, workspace, workspace_bytes, stream, true);
+    return decode_common(a, num_splits, seq_lens != nullptr, out_dtype, workspace, workspace_bytes, stream,
+                         Cache::FP8);
 }
 
 int fd_decode_paged_fp8(const void* q, const uint8_t* k_pages, const float* k_page_scales, const uint8_t* v_pages,
@@ -331,7 +346,90 @@ int fd_decode_paged_fp8(const void* q, const uint8_t* k_pages, const float* k_pa
     a.scale = scale;
     a.out = out;
     a.lse = lse;
-    return decode_common(a, num_splits, true, out_dtype, workspace, workspace_bytes, stream, true);
+    return decode_common(a, num_splits, true, out_dtype, workspace, workspace_bytes, stream, Cache::FP8);
+}
+
+int fd_quantize_kv_fp4(const void* x, const int32_t* seq_lens, int B, int H, int L_max, int d,
+                       uint8_t* codes, uint8_t* scales, void* stream) {
+    const int st = check_shape(B, H, H, L_max, d);
+    if (st != FD_OK) return st;
+    if (B > 0 && L_max > 0 && (!x || !codes || !scales)) return FD_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(codes) || !aligned16(scales)) return FD_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(seq_lens) & 3u) return FD_ERR_INVALID_ARG;
+    fd::Fp4QuantArgs a = {x, seq_lens, B, H, L_max, d, codes, scales};
+    return to_status(fd::launch_quantize_fp4(a, static_cast<cudaStream_t>(stream)));
+}
+
+int fd_num_splits_fp4(int B, int Hq, int Hkv, int L_max, int d, int num_splits, int ragged) {
+    const int st = check_shape(B, Hq, Hkv, L_max, d);
+    if (st != FD_OK) return -st;
+    if (num_splits < 0) return -FD_ERR_INVALID_ARG;
+    return fp4_plan(B, Hq, Hkv, L_max, d, num_splits, ragged != 0).splits;
+}
+
+size_t fd_decode_fp4_workspace_size(int B, int Hq, int Hkv, int L_max, int d, int num_splits, int ragged) {
+    if (check_shape(B, Hq, Hkv, L_max, d) != FD_OK || num_splits < 0) return 0;
+    const Plan pl = fp4_plan(B, Hq, Hkv, L_max, d, num_splits, ragged != 0);
+    return fd::decode_workspace_bytes(B, Hq, d, pl.splits);
+}
+
+int fd_decode_dense_fp4(const void* q, const uint8_t* k_codes, const uint8_t* k_scales, const uint8_t* v_codes,
+                        const uint8_t* v_scales, const int32_t* seq_lens, int B, int Hq, int Hkv, int L_max, int d,
+                        float scale, int num_splits, void* out, int out_dtype, float* lse,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+    const int st = check_shape(B, Hq, Hkv, L_max, d);
+    if (st != FD_OK) return st;
+    fd::DecodeArgs a = {};
+    a.q = q;
+    a.k = k_codes;
+    a.v = v_codes;
+    a.k_scales = k_scales;
+    a.v_scales = v_scales;
+    a.seq_lens = seq_lens;
+    a.page_table = nullptr;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.L_max = L_max;
+    a.D = d;
+    a.scale = scale;
+    a.out = out;
+    a.lse = lse;
+    return decode_common(a, num_splits, seq_lens != nullptr, out_dtype, workspace, workspace_bytes, stream,
+                         Cache::FP4);
+}
+
+int fd_decode_paged_fp4(const void* q, const uint8_t* k_pages, const uint8_t* k_page_scales, const uint8_t* v_pages,
+                        const uint8_t* v_page_scales, const int32_t* page_table, int max_pages, int num_pages,
+                        const int32_t* seq_lens, int page_size, int B, int Hq, int Hkv, int d, float scale,
+                        int num_splits, void* out, int out_dtype, float* lse,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+    if (page_size != kTile) return page_size > 0 ? FD_ERR_UNSUPPORTED : FD_ERR_INVALID_ARG;
+    if (max_pages <= 0 || num_pages < 0 || max_pages > (1 << 24)) return FD_ERR_INVALID_ARG;
+    const int L_max = max_pages * page_size;
+    const int st = check_shape(B, Hq, Hkv, L_max, d);
+    if (st != FD_OK) return st;
+    if (B > 0 && (!page_table || !seq_lens)) return FD_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(page_table) & 3u) return FD_ERR_INVALID_ARG;
+    fd::DecodeArgs a = {};
+    a.q = q;
+    a.k = k_pages;
+    a.v = v_pages;
+    a.k_scales = k_page_scales;
+    a.v_scales = v_page_scales;
+    a.seq_lens = seq_lens;
+    a.page_table = page_table;
+    a.max_pages = max_pages;
+    a.num_pages = num_pages;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.L_max = L_max;
+    a.D = d;
+    a.scale = scale;
+    a.out = out;
+    a.lse = lse;
+    return decode_common(a, num_splits, true, out_dtype, workspace, workspace_bytes, stream, Cache::FP4);
 }
 
 int fd_quantize_keys(const void* k, const int32_t* seq_lens, int B, int Hkv, int L_max, int d,
@@ -410,11 +508,12 @@ int fd_decode_topdelta(const void* q, const uint8_t* codes, const void* mn_scale
 
 int fd_device_status(int clear, void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FD_ERR_CUDA;
-    unsigned a = 0, b = 0, c = 0;
+    unsigned a = 0, b = 0, c = 0, e = 0;
     if (fd::decode_status_read(&a, clear != 0) != cudaSuccess) return FD_ERR_CUDA;
     if (fd::topdelta_status_read(&b, clear != 0) != cudaSuccess) return FD_ERR_CUDA;
     if (fd::fp8_status_read(&c, clear != 0) != cudaSuccess) return FD_ERR_CUDA;
-    const unsigned bits = a | b | c;
+    if (fd::fp4_status_read(&e, clear != 0) != cudaSuccess) return FD_ERR_CUDA;
+    const unsigned bits = a | b | c | e;
     if (bits & 2u) return FD_ERR_DEVICE_TIMEOUT;
     if (bits & 1u) return FD_ERR_BAD_PAGE_TABLE;
     if (bits & 4u) return FD_ERR_INVALID_ARG;

@@ -1,0 +1,611 @@
+// fd_fp4.cu -- split-KV decode attention ("Flash Decoding" tutorial, sections
+// 1-3) over a 4-bit floating-point KV cache, and its encoder, for sm_103a.
+// The benchmarking blog on a hosted 1M-context model (section 1) names an
+// "FP4" KV cache; this file implements this library's definition of one:
+//
+//   per cache row (token, KV head) and 32-channel block b:
+//     e_b  = the smallest integer in [-126, 127] with 6 * 2^e_b >= max |x|
+//     code = e2m1(x * 2^-e_b)      (round to nearest even; |x * 2^-e_b| <= 6)
+//   codes two per byte (the low nibble holds the even channel), one byte
+//   e_b + 127 per block.
+//
+// A row costs d/2 + d/32 bytes per operand (68 at d = 128), a quarter of the
+// bf16 cache.  The partial pass has the shape of the fp8 pass (fd_fp8.cu):
+// warp 4 copies per 64-token tile one K and one V code box and two scale
+// boxes into a STAGES-deep ring; warps 0..3 each own 16 tokens of every tile.
+// Both products run on fp16 tensor cores (every e2m1 value is exact in fp16):
+//   S = Q K^T   one ldmatrix word per lane holds 8 channels of one block;
+//               each of its bytes widens (cvt.rn.f16x2.e2m1x2) to the B
+//               fragment of half a k-step, Q's channel order inside each
+//               block permuted alike; every block accumulates on its own and
+//               is scaled by 2^e_b of its token before the blocks are summed.
+//   O^T += V^T P^T
+//               the 16 output rows of tile j are 4 channels of 4 lane groups
+//               inside block j/2 (row gid + 8r of tile 2c + h is channel
+//               32c + 4*gid + 2h + r); the two token nibbles of a channel are
+//               interleaved into one byte and widened; P carries
+//               2^e_b(token) / s_ref, s_ref the largest V block scale the
+//               warp has seen, so each block has its own P operand.
+#include <cmath>
+#include <cstdio>
+
+#include "fd_device.cuh"
+#include "fd_internal.h"
+#include "fd_tma.h"
+
+namespace fd {
+
+__device__ unsigned int g_status_fp4;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kScaleSlot = 384;  // bytes reserved per scale copy in shared memory (128-byte multiple)
+
+// Geometry per head size: code bytes per row, scale bytes per row, and the
+// scale copy (elements of SB bytes, a 64-token tile plus alignment slack).
+template <int D>
+struct F4Geo {
+    static constexpr int RB = D / 2;                 // code bytes per row
+    static constexpr int NB = D / 32;                // blocks per row = scale bytes per row
+    static constexpr int SB = NB;                    // scale element: one row's scale bytes (4 or 2)
+    static constexpr int ALIGN = 16 / SB;            // rows per 16 bytes of scales
+    static constexpr int SBOX = 64 + ALIGN;          // scale elements per copy
+    static constexpr int CB = 64 * RB;               // bytes of one code tile
+    static_assert(SBOX * SB <= kScaleSlot, "scale copy must fit its slot");
+};
+
+// Byte offset of 16-byte chunk `ch` of code row `row` in a 64-row box
+// (64-byte rows: 64-byte swizzle; 32-byte rows: no swizzle).
+template <int D>
+__device__ __forceinline__ uint32_t code4_off(int row, int ch) {
+    if constexpr (D == 128) return swz64(row, ch);
+    else return (uint32_t)(row * 32 + ch * 16);
+}
+
+// Four bytes of e2m1 pairs -> four fp16x2 words (byte i -> h[i], the low
+// nibble in the low half).  Exact.
+__device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t w, uint32_t (&h)[4]) {
+    asm("{\n\t.reg .b8 a, b, c, d;\n\t"
+        "mov.b32 {a, b, c, d}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, a;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, c;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, d;\n\t}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w));
+}
+
+// Two fp32 -> one byte of e2m1 codes (round to nearest even, saturating to
+// +-6), `lo` in the low nibble.
+__device__ __forceinline__ uint32_t e2m1x2_from_f32(float lo, float hi) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+        "cvt.u32.u8 %0, t;\n\t}"
+        : "=r"(r)
+        : "f"(hi), "f"(lo));
+    return r;
+}
+
+// 2^(E - 127) for a scale byte E in [1, 254] (a normal binary32, exact).
+__device__ __forceinline__ float scale_value(uint32_t E) { return __uint_as_float(E << 23); }
+
+// The two 16-bit nibble rows w0 (token a) and w1 (token b) of 4 channels
+// -> 4 bytes, byte c = (channel c of b) << 4 | (channel c of a).
+__device__ __forceinline__ uint32_t interleave_nibbles(uint32_t w0, uint32_t w1) {
+    uint32_t u = __byte_perm(w0, w1, 0x5140);  // halves: (b.byte0 : a.byte0), (b.byte1 : a.byte1)
+    const uint32_t t = (u ^ (u >> 4)) & 0x00F000F0u;  // swap nibble positions 1 and 2 of each half
+    return u ^ t ^ (t << 4);
+}
+
+// ---------------------------------------------------------------------------
+// Encoder: one warp per cache row; lane l holds channels D/32 * l ...
+template <int D>
+__global__ void __launch_bounds__(256)
+fp4_quantize_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ seq_lens, int H, int L_max,
+                    long long rows, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+    constexpr int E = D / 32;       // channels per lane: 4 or 2
+    constexpr int LPB = 32 / E;     // lanes per 32-channel block: 8 or 16
+    const int lane = threadIdx.x & 31;
+    const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
+    for (long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows;
+         row += nwarps) {
+        const int t = (int)(row % L_max);
+        const int b = (int)(row / ((long long)H * L_max));
+        const int L = clamped_len(seq_lens, b, L_max, &g_status_fp4);
+        if (t >= L) continue;  // warp-uniform: rows past the sequence are not written
+        float v[E];
+        if constexpr (E == 4) {
+            const uint2 w = *reinterpret_cast<const uint2*>(x + row * D + lane * 4);
+            const float2 a = bf16x2_to_float2(w.x), c = bf16x2_to_float2(w.y);
+            v[0] = a.x; v[1] = a.y; v[2] = c.x; v[3] = c.y;
+        } else {
+            const float2 a = bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(x + row * D + lane * 2));
+            v[0] = a.x; v[1] = a.y;
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(v[e]));
+#pragma unroll
+        for (int off = LPB / 2; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        // smallest e with 6 * 2^e >= amax: amax = 1.m * 2^k needs k - 2 when 1.m <= 1.5, else k - 1
+        int eb = -126;
+        const uint32_t bits = __float_as_uint(amax);
+        if ((bits >> 23) != 0u) {
+            const int k = (int)(bits >> 23) - 127;
+            eb = max(-126, k - 2 + ((bits & 0x7fffffu) > 0x400000u ? 1 : 0));
+        }
+        const float inv = __uint_as_float((uint32_t)(127 - eb) << 23);  // 2^-eb, exact
+        uint32_t packed = 0;
+#pragma unroll
+        for (int e = 0; e < E; e += 2) packed |= e2m1x2_from_f32(v[e] * inv, v[e + 1] * inv) << (4 * e);
+        if constexpr (E == 4) *reinterpret_cast<uint16_t*>(codes + row * (D / 2) + lane * 2) = (uint16_t)packed;
+        else codes[row * (D / 2) + lane] = (uint8_t)packed;
+        if (lane % LPB == 0) scales[row * (D / 32) + lane / LPB] = (uint8_t)(eb + 127);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Partial pass.
+struct Fp4Params {
+    const uint16_t* q;
+    const int32_t* seq_lens;
+    const int32_t* page_table;
+    int max_pages, num_pages;
+    int Hq, Hkv, L_max, G;
+    float scale_log2;
+    int splits, chunk_fixed;
+    StoreTarget st;
+};
+
+template <int D, int STAGES, bool PAGED>
+__global__ void __launch_bounds__(5 * 32, 2)
+fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                   const __grid_constant__ CUtensorMap tmks, const __grid_constant__ CUtensorMap tmvs,
+                   const Fp4Params p) {
+    using Gm = F4Geo<D>;
+    constexpr int CW = 4;
+    constexpr int NT = 1;                 // stages a consumer warp takes per step (two spill registers)
+    constexpr int CB = Gm::CB;
+    constexpr int STAGE = 2 * CB;         // K tile + V tile
+    constexpr int SSTAGE = 2 * kScaleSlot;
+    constexpr int NB = Gm::NB;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    unsigned char* scl = smem + STAGES * STAGE;
+    uint64_t* full = reinterpret_cast<uint64_t*>(scl + STAGES * SSTAGE);
+    uint64_t* empty = full + STAGES;
+    int* stage_rows = reinterpret_cast<int*>(empty + STAGES);
+    int* stage_off = stage_rows + STAGES;
+
+    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait_primary();  // the previous kernel in the stream may still be running
+    const int L = clamped_len(p.seq_lens, b, p.L_max, &g_status_fp4);
+    const int chunk = chunk_len(L, p.splits, p.chunk_fixed);
+    const int t0 = split * chunk;
+    const int t1 = min(L, t0 + chunk);
+    const int hq0 = h * p.G;
+
+    if (t0 >= t1) {
+        pdl_launch_dependents();
+        if (p.st.direct && split == 0) {
+            for (int i = threadIdx.x; i < p.G * D; i += blockDim.x) {
+                const size_t o = (size_t)(b * p.Hq + hq0 + i / D) * D + (i % D);
+                if (p.st.out_bf16) static_cast<uint16_t*>(p.st.out)[o] = 0;
+                else static_cast<float*>(p.st.out)[o] = 0.f;
+            }
+            if (p.st.lse && threadIdx.x < p.G) p.st.lse[b * p.Hq + hq0 + threadIdx.x] = -INFINITY;
+        }
+        return;
+    }
+    const int ntiles = (t1 - t0 + kTile - 1) / kTile;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], CW);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == CW) {
+        // ---------------- producer: one lane issues all tile copies --------
+        if (lane == 0) {
+            prefetch_tmap(&tmk);
+            prefetch_tmap(&tmv);
+            prefetch_tmap(&tmks);
+            prefetch_tmap(&tmvs);
+            const uint64_t pol = l2_evict_first_policy();
+            const int head_row0 = PAGED ? 0 : (b * p.Hkv + h) * p.L_max;
+            for (int t = 0; t < ntiles; ++t) {
+                const int s = t % STAGES;
+                const uint32_t ph = (uint32_t)(t / STAGES) & 1u;
+                if (!mbar_wait(&empty[s], ph ^ 1u)) {
+                    atomicOr(&g_status_fp4, kStatusTimeout);
+                    break;
+                }
+                const int tok = t0 + t * kTile;
+                const int rows = min(kTile, t1 - tok);
+                int y;
+                bool ok = true;
+                if (PAGED) {
+                    const int pg = p.page_table[(size_t)b * p.max_pages + tok / kTile];
+                    ok = pg >= 0 && pg < p.num_pages;
+                    y = (pg * p.Hkv + h) * kTile;
+                } else {
+                    y = head_row0 + tok;
+                }
+                unsigned char* sk = smem + s * STAGE;
+                unsigned char* ss = scl + s * SSTAGE;
+                if (ok) {
+                    stage_rows[s] = rows;
+                    stage_off[s] = y & (Gm::ALIGN - 1);
+                    mbar_arrive_expect_tx(&full[s], STAGE + 2 * Gm::SBOX * Gm::SB);
+                    tma_load_box64(sk, &tmk, y, &full[s], pol);  // one box of 64 rows (x = 0)
+                    tma_load_box64(sk + CB, &tmv, y, &full[s], pol);
+                    // the scale copies start on the 16-byte boundary at or below the tile
+                    tma_load_1d(ss, &tmks, y & ~(Gm::ALIGN - 1), &full[s], pol);
+                    tma_load_1d(ss + kScaleSlot, &tmvs, y & ~(Gm::ALIGN - 1), &full[s], pol);
+                } else {
+                    atomicOr(&g_status_fp4, kStatusBadPage);
+                    stage_rows[s] = 0;
+                    stage_off[s] = 0;
+                    mbar_arrive(&full[s]);
+                }
+            }
+        }
+        pdl_launch_dependents();
+        return;
+    }
+
+    // ------------------------------ consumers ------------------------------
+    const int gid = lane >> 2, tig = lane & 3, mi = lane >> 3;
+    // Q fragments of query gid, per block c: qa[c][0] = channels 32c + 8*tig
+    // + {0,1}, [1] = {2,3}, [2] = {4,5}, [3] = {6,7}, as fp16 times 2^-e (e the
+    // exponent of the query's largest |q|; exact).
+    uint32_t qa[NB][4];
+    float qmul;
+    {
+        const uint16_t* qrow = p.q + (size_t)(b * p.Hq + hq0 + gid) * D;
+        float amax = 0.f;
+        uint4 qw[NB];
+#pragma unroll
+        for (int c = 0; c < NB; ++c) {
+            qw[c] = gid < p.G ? *reinterpret_cast<const uint4*>(qrow + 32 * c + 8 * tig) : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t wv[4] = {qw[c].x, qw[c].y, qw[c].z, qw[c].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = bf16x2_to_float2(wv[i]);
+                amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+        }
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        int ex = 0;
+        if (amax > 0.f && amax <= 3.4e38f) (void)frexpf(amax, &ex);
+#pragma unroll
+        for (int c = 0; c < NB; ++c) {
+            const uint32_t wv[4] = {qw[c].x, qw[c].y, qw[c].z, qw[c].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = bf16x2_to_float2(wv[i]);
+                qa[c][i] = pack_f16(ldexpf(f.x, -ex), ldexpf(f.y, -ex));
+            }
+        }
+        qmul = ldexpf(p.scale_log2, ex);
+    }
+
+    float o[D / 16][4];
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[mt][i] = 0.f;
+    float m_run = -INFINITY, l_run = 0.f, vref = 0.f;
+    bool failed = false;
+    const int ld_row = warp * 16 + 8 * (mi >> 1) + (lane & 7);  // row this lane addresses for ldmatrix
+    const int r0 = warp * 16 + 2 * tig;                         // tokens r0, r0+1, r0+8, r0+9 are this lane's
+    const int tok[4] = {r0, r0 + 1, r0 + 8, r0 + 9};
+
+    for (int t = 0; t < ntiles; t += NT) {
+        int st[NT], rows[NT];
+        bool have[NT];
+#pragma unroll
+        for (int k = 0; k < NT; ++k) {
+            have[k] = t + k < ntiles;
+            st[k] = have[k] ? (t + k) % STAGES : t % STAGES;
+            rows[k] = 0;
+            if (have[k]) {
+                if (!warp_wait(&full[st[k]], (uint32_t)((t + k) / STAGES) & 1u)) failed = true;
+                else rows[k] = stage_rows[st[k]];
+            }
+        }
+        if (failed) {
+            atomicOr(&g_status_fp4, kStatusTimeout);
+            break;
+        }
+
+        // ---- scores, block by block, and the block scales of V ---------------
+        float sc[NT][4];
+        uint32_t ve[NT][4];  // V scale bytes of the lane's four tokens (0 for rows past the tile)
+#pragma unroll
+        for (int k = 0; k < NT; ++k) {
+            const uint32_t kt = smem_u32(smem + st[k] * STAGE);
+            const unsigned char* ksc = scl + st[k] * SSTAGE + stage_off[st[k]] * Gm::SB;
+            const unsigned char* vsc = ksc + kScaleSlot;
+            uint32_t ke[4];  // the K scale bytes of the lane's four tokens
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if constexpr (NB == 4) {
+                    ke[i] = *reinterpret_cast<const uint32_t*>(ksc + 4 * tok[i]);
+                    ve[k][i] = *reinterpret_cast<const uint32_t*>(vsc + 4 * tok[i]);
+                } else {
+                    ke[i] = *reinterpret_cast<const uint16_t*>(ksc + 2 * tok[i]);
+                    ve[k][i] = *reinterpret_cast<const uint16_t*>(vsc + 2 * tok[i]);
+                }
+            }
+            float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int cp = 0; cp < NB / 2; ++cp) {
+                // (token block 0, block 2cp), (0, 2cp+1), (1, 2cp), (1, 2cp+1)
+                uint32_t w[4];
+                ldsm_x4(kt + code4_off<D>(ld_row, 2 * cp + (mi & 1)), w[0], w[1], w[2], w[3]);
+#pragma unroll
+                for (int hb = 0; hb < 2; ++hb) {
+                    const int c = 2 * cp + hb;
+                    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        uint32_t hf[4];
+                        e2m1x8_to_f16x8(w[2 * j + hb], hf);
+                        mma_f16(acc[j], qa[c][0], 0u, qa[c][1], 0u, hf[0], hf[1]);
+                        mma_f16(acc[j], qa[c][2], 0u, qa[c][3], 0u, hf[2], hf[3]);
+                    }
+                    const float a4[4] = {acc[0][0], acc[0][1], acc[1][0], acc[1][1]};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) s4[i] = fmaf(a4[i], scale_value((ke[i] >> (8 * c)) & 0xffu), s4[i]);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const bool ok = tok[i] < rows[k];
+                sc[k][i] = ok ? s4[i] * qmul : -INFINITY;
+                ve[k][i] = ok ? ve[k][i] : 0u;  // scale byte 0 decodes to 0
+            }
+        }
+
+        // ---- online softmax and the V reference scale ------------------------
+        float mx = -INFINITY;
+        uint32_t emax = 0u;  // per-byte maximum of the V scale bytes (a larger byte is a larger scale)
+#pragma unroll
+        for (int k = 0; k < NT; ++k) {
+            mx = fmaxf(mx, fmaxf(fmaxf(sc[k][0], sc[k][1]), fmaxf(sc[k][2], sc[k][3])));
+            emax = __vmaxu4(emax, __vmaxu4(__vmaxu4(ve[k][0], ve[k][1]), __vmaxu4(ve[k][2], ve[k][3])));
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        emax = __vmaxu4(emax, __shfl_xor_sync(0xffffffffu, emax, 1));
+        emax = __vmaxu4(emax, __shfl_xor_sync(0xffffffffu, emax, 2));
+        emax = max(max(emax & 0xffu, (emax >> 8) & 0xffu), max((emax >> 16) & 0xffu, emax >> 24));
+        const float vref_new = fmaxf(vref, scale_value(emax));
+        const float vinv = vref_new > 0.f ? __fdividef(1.f, vref_new) : 0.f;
+        const float vf = vref_new > 0.f ? vref * vinv : 1.f;
+        vref = vref_new;
+        const float m_new = fmaxf(m_run, mx);
+        const bool none = m_new == -INFINITY;
+        const float alpha = none ? 1.f : exp2_approx(m_run - m_new);
+        m_run = m_new;
+        float lsum = 0.f;
+        float pr[NT][4];  // p / s_ref of the lane's tokens
+#pragma unroll
+        for (int k = 0; k < NT; ++k) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                pr[k][i] = none ? 0.f : exp2_approx(sc[k][i] - m_new);
+                lsum += pr[k][i];
+                pr[k][i] *= vinv;
+            }
+        }
+        l_run = l_run * alpha + lsum;
+        if (!__all_sync(0xffffffffu, alpha == 1.f && vf == 1.f)) {
+            // accumulator columns are queries 2*tig and 2*tig+1
+            const float a_even = __shfl_sync(0xffffffffu, alpha, 8 * tig) * vf;
+            const float a_odd = __shfl_sync(0xffffffffu, alpha, 8 * tig + 4) * vf;
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                o[mt][0] *= a_even;
+                o[mt][1] *= a_odd;
+                o[mt][2] *= a_even;
+                o[mt][3] *= a_odd;
+            }
+        }
+
+        // ---- O^T += V^T P^T -------------------------------------------------
+#pragma unroll
+        for (int k = 0; k < NT; ++k) {
+            const unsigned char* vt = smem + st[k] * STAGE + CB;
+            const bool tail = warp * 16 + 16 > rows[k];  // warp-uniform
+#pragma unroll
+            for (int c = 0; c < NB; ++c) {
+                // channels 32c + 4*gid .. +3 of the lane's four tokens: two bytes each
+                uint32_t w[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    w[i] = *reinterpret_cast<const uint16_t*>(vt + code4_off<D>(tok[i], c) + 2 * gid);
+                    if (tail) w[i] = tok[i] < rows[k] ? w[i] : 0u;  // rows past the end may hold anything
+                }
+                // P^T of this stage for V block c: p * 2^e_c(token) / s_ref
+                float sv[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) sv[i] = pr[k][i] * scale_value((ve[k][i] >> (8 * c)) & 0xffu);
+                const uint32_t pb0 = pack_f16(sv[0], sv[1]), pb1 = pack_f16(sv[2], sv[3]);
+                uint32_t x01[4], x89[4];
+                e2m1x8_to_f16x8(interleave_nibbles(w[0], w[1]), x01);
+                e2m1x8_to_f16x8(interleave_nibbles(w[2], w[3]), x89);
+                mma_f16(o[2 * c], x01[0], x01[1], x89[0], x89[1], pb0, pb1);
+                mma_f16(o[2 * c + 1], x01[2], x01[3], x89[2], x89[3], pb0, pb1);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+            for (int k = 0; k < NT; ++k)
+                if (have[k]) mbar_arrive(&empty[st[k]]);
+        }
+    }
+    pdl_launch_dependents();
+
+    // ---- combine the consumer warps and store --------------------------------
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+    named_barrier(1, CW * 32);  // every consumer is done with the stage ring
+    float* red_o = reinterpret_cast<float*>(smem);  // [CW][8][D]
+    float* red_m = red_o + CW * 8 * D;              // [CW][8]
+    float* red_l = red_m + CW * 8;                  // [CW][8]
+#pragma unroll
+    for (int c = 0; c < NB; ++c) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            // query 2*tig + i, channels 32c + 4*gid .. + 3
+            const int qi = 2 * tig + i;
+            const float4 val = make_float4(o[2 * c][i] * vref, o[2 * c][i + 2] * vref, o[2 * c + 1][i] * vref,
+                                           o[2 * c + 1][i + 2] * vref);
+            *reinterpret_cast<float4*>(red_o + (warp * 8 + qi) * D + 32 * c + 4 * gid) = val;
+        }
+    }
+    if (tig == 0) {
+        red_m[warp * 8 + gid] = failed ? -INFINITY : m_run;
+        red_l[warp * 8 + gid] = failed ? 0.f : l_run;
+    }
+    named_barrier(1, CW * 32);
+    store_combined<D, 8, CW>(smem, threadIdx.x, p.G, b * p.Hq + hq0, split, p.st);
+}
+
+template <int D, bool PAGED>
+struct Fp4Launcher {
+    static constexpr int STAGES = 8;
+    static constexpr int STAGE = 2 * F4Geo<D>::CB;
+    static constexpr int SMEM = 1024 + STAGES * STAGE + STAGES * 2 * kScaleSlot + STAGES * 16 + STAGES * 8 + 64;
+    static constexpr int RED = 4 * 8 * D * 4 + 2 * 4 * 8 * 4;
+    static_assert(STAGES * STAGE >= RED, "reduction scratch must fit in the ring");
+    static constexpr auto kernel = fp4_partial_kernel<D, STAGES, PAGED>;
+
+    static cudaError_t prepare() {
+        static bool done[kMaxDevices] = {};
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < kMaxDevices && done[dev]) return cudaSuccess;
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+        if (e == cudaSuccess && dev < kMaxDevices) done[dev] = true;
+        return e;
+    }
+    static int ctas_per_sm() {
+        static int cache[kMaxDevices] = {};
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+        if (dev < kMaxDevices && cache[dev] > 0) return cache[dev];
+        if (prepare() != cudaSuccess) return 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, 5 * 32, SMEM) != cudaSuccess || n <= 0)
+            return 1;
+        if (dev < kMaxDevices) cache[dev] = n;
+        return n;
+    }
+    static cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tks,
+                              const CUtensorMap& tvs, const Fp4Params& pp, dim3 grid, cudaStream_t st) {
+        cudaError_t e = prepare();
+        if (e != cudaSuccess) return e;
+        return launch_pdl(kernel, grid, dim3(5 * 32), SMEM, st, tk, tv, tks, tvs, pp);
+    }
+};
+
+}  // namespace
+
+int fp4_ctas_per_sm(int D, bool paged) {
+    if (D == 128) return paged ? Fp4Launcher<128, true>::ctas_per_sm() : Fp4Launcher<128, false>::ctas_per_sm();
+    return paged ? Fp4Launcher<64, true>::ctas_per_sm() : Fp4Launcher<64, false>::ctas_per_sm();
+}
+
+cudaError_t launch_quantize_fp4(const Fp4QuantArgs& a, cudaStream_t stream) {
+    const long long rows = (long long)a.B * a.H * a.L_max;
+    if (rows == 0) return cudaSuccess;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const long long want = (rows + 7) / 8;  // 8 rows (warps) per block
+    const long long cap = (long long)sms * 8;
+    const unsigned grid = (unsigned)(want < cap ? want : cap);
+    const uint16_t* x = static_cast<const uint16_t*>(a.x);
+    if (a.D == 128)
+        fp4_quantize_kernel<128><<<grid, 256, 0, stream>>>(x, a.seq_lens, a.H, a.L_max, rows, a.codes, a.scales);
+    else
+        fp4_quantize_kernel<64><<<grid, 256, 0, stream>>>(x, a.seq_lens, a.H, a.L_max, rows, a.codes, a.scales);
+    return cudaGetLastError();
+}
+
+template <int D>
+static bool fp4_maps(const DecodeArgs& a, uint64_t rows, CUtensorMap& tk, CUtensorMap& tv, CUtensorMap& tks,
+                     CUtensorMap& tvs) {
+    using Gm = F4Geo<D>;
+    if (rows == 0) {
+        // nothing can be read (an empty pool or cache): any well-formed map will do
+        return make_row_map(&tk, a.q, 1, Gm::RB) && make_row_map(&tv, a.q, 1, Gm::RB) &&
+               make_vec_map(&tks, a.q, 1, Gm::SBOX, Gm::SB) && make_vec_map(&tvs, a.q, 1, Gm::SBOX, Gm::SB);
+    }
+    return make_row_map(&tk, a.k, rows, Gm::RB) && make_row_map(&tv, a.v, rows, Gm::RB) &&
+           make_vec_map(&tks, a.k_scales, rows, Gm::SBOX, Gm::SB) &&
+           make_vec_map(&tvs, a.v_scales, rows, Gm::SBOX, Gm::SB);
+}
+
+cudaError_t launch_decode_fp4(const DecodeArgs& a, cudaStream_t stream) {
+    if (a.B == 0) return cudaSuccess;
+    const bool paged = a.page_table != nullptr;
+    const uint64_t rows = paged ? (uint64_t)a.num_pages * a.Hkv * kTile : (uint64_t)a.B * a.Hkv * a.L_max;
+    CUtensorMap tk, tv, tks, tvs;
+    const bool ok = a.D == 128 ? fp4_maps<128>(a, rows, tk, tv, tks, tvs) : fp4_maps<64>(a, rows, tk, tv, tks, tvs);
+    if (!ok) return cudaErrorInvalidValue;
+    Fp4Params pp;
+    pp.q = static_cast<const uint16_t*>(a.q);
+    pp.seq_lens = a.seq_lens;
+    pp.page_table = a.page_table;
+    pp.max_pages = a.max_pages;
+    pp.num_pages = a.num_pages;
+    pp.Hq = a.Hq;
+    pp.Hkv = a.Hkv;
+    pp.L_max = a.L_max;
+    pp.G = a.Hq / a.Hkv;
+    pp.scale_log2 = a.scale * kLog2e;
+    pp.splits = a.splits;
+    pp.chunk_fixed = a.chunk_fixed;
+    pp.st.part_o = a.part_o;
+    pp.st.part_ml = a.part_ml;
+    pp.st.out = a.out;
+    pp.st.out_bf16 = a.out_bf16;
+    pp.st.lse = a.lse;
+    pp.st.direct = a.splits == 1 ? 1 : 0;
+    pp.st.splits = a.splits;
+    const dim3 grid((unsigned)a.splits, (unsigned)a.Hkv, (unsigned)a.B);
+    cudaError_t e;
+    if (a.D == 128)
+        e = paged ? Fp4Launcher<128, true>::launch(tk, tv, tks, tvs, pp, grid, stream)
+                  : Fp4Launcher<128, false>::launch(tk, tv, tks, tvs, pp, grid, stream);
+    else
+        e = paged ? Fp4Launcher<64, true>::launch(tk, tv, tks, tvs, pp, grid, stream)
+                  : Fp4Launcher<64, false>::launch(tk, tv, tks, tvs, pp, grid, stream);
+    if (e != cudaSuccess || a.splits == 1) return e;
+    return launch_merge(a.part_o, a.part_ml, a.seq_lens, a.B, a.Hq, a.L_max, a.D, a.splits, a.chunk_fixed,
+                        a.out, a.out_bf16, a.lse, stream);
+}
+
+cudaError_t fp4_status_read(unsigned* bits, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(bits, g_status_fp4, sizeof(unsigned));
+    if (e != cudaSuccess || !clear) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_status_fp4, &zero, sizeof(unsigned));
+}
+
+}  // namespace fd

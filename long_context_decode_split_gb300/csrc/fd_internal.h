@@ -31,8 +31,8 @@ struct DecodeArgs {
     const void* q;            // [B, Hq, D] bf16
     const void* k;            // contiguous [B, Hkv, L_max, D] or pool [P, Hkv, 64, D]
     const void* v;
-    const float* k_scales;    // fp8 cache only: [rows] binary32 row scales of K and V
-    const float* v_scales;
+    const void* k_scales;     // fp8 cache: [rows] binary32 row scales; fp4 cache: [rows, D/32] u8 block
+    const void* v_scales;     // exponents (of K and of V)
     const int32_t* seq_lens;  // [B] or null (= L_max)
     const int32_t* page_table;// [B, max_pages] when paged, else null
     int max_pages, num_pages;
@@ -107,6 +107,19 @@ cudaError_t launch_quantize_fp8(const Fp8QuantArgs& a, cudaStream_t stream);
 int fp8_ctas_per_sm(int D, bool paged);
 cudaError_t launch_decode_fp8(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t fp8_status_read(unsigned* bits, bool clear);
+
+// fp4 (e2m1, power-of-two block scales) KV cache: encoder and decode.
+struct Fp4QuantArgs {
+    const void* x;            // [B, H, L_max, D] bf16
+    const int32_t* seq_lens;
+    int B, H, L_max, D;
+    uint8_t* codes;           // [B, H, L_max, D/2]
+    uint8_t* scales;          // [B, H, L_max, D/32]
+};
+cudaError_t launch_quantize_fp4(const Fp4QuantArgs& a, cudaStream_t stream);
+int fp4_ctas_per_sm(int D, bool paged);
+cudaError_t launch_decode_fp4(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t fp4_status_read(unsigned* bits, bool clear);
 
 // Launch with programmatic stream serialization: the grid may be scheduled
 // while the previous kernel in the stream is still running, so the kernel
