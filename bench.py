@@ -709,12 +709,14 @@ def main():
     ctx.close()
 
 
-KERNEL_SOURCES = {"bf16": "fd_decode.cu", "topdelta": "fd_topdelta.cu", "fp8": "fd_fp8.cu"}
+KERNEL_SOURCES = {"bf16": "fd_decode.cu", "topdelta": "fd_topdelta.cu", "fp8": "fd_fp8.cu", "fp4": "fd_fp4.cu"}
 
 
 def kernel_family(workload):
     if workload.endswith("_fp8"):
         return "fp8"
+    if workload.endswith("_fp4"):
+        return "fp4"
     if workload.startswith("ffd_top"):
         return "topdelta"
     return "bf16"
