@@ -176,10 +176,15 @@ struct TDParams {
 };
 
 
-// Query fragments of one lane (row gid of the m16 A operand), per 16-channel
-// k-step.  The k order inside a step is permuted to match how the B
-// operands are unpacked (the same permutation on both sides leaves every dot
-// product unchanged):
+// Both dot stages run as S = K Q^T on m16n8k16: the 16 token rows of a
+// warp's slice are M, the (up to 8) query heads of the group are N, so every
+// accumulator a lane holds belongs to a real token.  Lane (gid, tig) holds
+// the B fragment of query gid and, in the accumulators, rows gid and gid + 8
+// (tokens) x columns 2 tig, 2 tig + 1 (queries).
+//
+// B fragments of query gid per 16-channel k-step.  The k order inside a
+// step is permuted to match how the A operands are unpacked (the same
+// permutation on both sides leaves every dot product unchanged):
 //   2-bit codes: k = 2t, 2t+1, 8+2t, 9+2t <-> channels 2t, 2t+8, 2t+1, 2t+9,
 //                the last two unpacked as 4 * code and weighted by q / 4; the
 //                codes enter as bf16 subnormals code * 2^-133 (the tensor
@@ -190,142 +195,219 @@ struct TDParams {
 //                the tensor cores' fp32 accumulation order).
 //   int8 residual (ldmatrix of 16-byte chunks): k = 2t, 2t+1, 8+2t, 9+2t <->
 //   channels 4t, 4t+1, 4t+2, 4t+3          (t = tig, relative to 16*kk)
+// The per-query constants are held for the lane's accumulator columns,
+// queries 2 tig (.x) and 2 tig + 1 (.y).
 template <int D>
 struct TDQuery {
     uint32_t qc0[D / 16], qc2[D / 16];  // bf16, for the 2-bit scan (scaled, see above)
     uint32_t qr0[D / 16], qr2[D / 16];  // fp16, for the residual
-    float qsum[D / 32];                 // sum of the query over each 32-channel group, times 2^(sq - 7)
-    float scan_scale;                   // softmax scale times 2^(7 - sq)
-    float qsumh[D / 32];                // the same over the fp16 values of the residual fragments
+    float2 qsum[D / 32];                // sum of the query over each 32-channel group, times 2^(sq - 7)
+    float2 off[D / 32];                 // 1152 times the same sum over the query's fp16 values
+    float2 scan_scale;                  // softmax scale times 2^(7 - sq)
 };
 
 // Scores s~ (natural-log units) of the warp's 16 rows of a tile whose codes
 // and (mn16, s16) rows sit in shared memory (plain row-major).  st[i] is the
-// score of row warp*16 + 2*tig + (i & 1) + 8*(i >> 1) for the lane's query.
+// score of row warp*16 + gid + 8*(i >> 1) for query 2*tig + (i & 1).
 //   s~ = scale * sum_g ( s_g * <q, code>_g + mn_g * sum_g(q) )
 // The per-group dots run on the tensor cores with the codes as exact bf16
-// (0x4300 | c is 128 + c; one subtraction leaves c); the group sums are
-// combined with explicitly rounded operations in a fixed order.
+// subnormals; the group sums are combined with explicitly rounded operations
+// in group order.
 template <int D>
 __device__ __forceinline__ void scan_tile(const unsigned char* codes, const unsigned char* ms, int warp, int lane,
                                           const TDQuery<D>& tq, float (&st)[4]) {
     using Gm = TGeo<D>;
     const int gid = lane >> 2, tig = lane & 3;
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        const int crow = warp * 16 + 8 * j + gid;  // the token row this lane's code words come from
-        const int row = warp * 16 + 8 * j + 2 * tig;  // the two rows of this lane's accumulator columns
-        // (mn16, s16) of every group for rows `row` and `row + 1`
-        uint32_t ma[Gm::NG], mb[Gm::NG];
-        if constexpr (Gm::NG == 4) {
-            const uint4 a = *reinterpret_cast<const uint4*>(ms + row * Gm::MS_ROW);
-            const uint4 bq = *reinterpret_cast<const uint4*>(ms + (row + 1) * Gm::MS_ROW);
-            ma[0] = a.x; ma[1] = a.y; ma[2] = a.z; ma[3] = a.w;
-            mb[0] = bq.x; mb[1] = bq.y; mb[2] = bq.z; mb[3] = bq.w;
-        } else {
-            const uint2 a = *reinterpret_cast<const uint2*>(ms + row * Gm::MS_ROW);
-            const uint2 bq = *reinterpret_cast<const uint2*>(ms + (row + 1) * Gm::MS_ROW);
-            ma[0] = a.x; ma[1] = a.y;
-            mb[0] = bq.x; mb[1] = bq.y;
-        }
-        const uint4* cw = reinterpret_cast<const uint4*>(codes + crow * Gm::CODES_ROW);
-        float2 v = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int kq = 0; kq < Gm::KS / 4; ++kq) {
-            const uint4 w4 = cw[kq];
-            const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-            for (int hg = 0; hg < 2; ++hg) {  // the two 32-channel groups of this 16-byte word
-                const int g = 2 * kq + hg;
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int e2 = 0; e2 < 2; ++e2) {
-                    const int kk = 2 * g + e2;
-                    const uint32_t w = wv[2 * hg + e2] >> (4 * tig);
-                    const uint32_t b0 = w & 0x00030003u;  // bf16 subnormals code * 2^-133
-                    // codes of the odd pair stay at bits 2-3: 4 * code * 2^-133; qc2 carries the 1/4
-                    const uint32_t b1 = w & 0x000C000Cu;
-                    mma_bf16(acc, tq.qc0[kk], 0u, tq.qc2[kk], 0u, b0, b1);
-                }
-                // group g of rows (row, row + 1): s_g * <q, code>_g + mn_g * sum_g(q), added in g order
-                const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&ma[g]));  // (mn, s) of row
-                const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&mb[g]));  // (mn, s) of row + 1
-                const float2 mn2 = make_float2(fa.x, fb.x), s2 = make_float2(fa.y, fb.y);
-                const float2 t = __ffma2_rn(s2, make_float2(acc[0], acc[1]),
-                                            __fmul2_rn(mn2, make_float2(tq.qsum[g], tq.qsum[g])));
-                v = __fadd2_rn(v, t);
-            }
-        }
-        // v is the group sum times 2^(sq - 7) exactly; scan_scale undoes the power of two
-        st[2 * j] = __fmul_rn(v.x, tq.scan_scale);
-        st[2 * j + 1] = __fmul_rn(v.y, tq.scan_scale);
+    const int r0 = warp * 16 + gid, r1 = r0 + 8;
+    // (mn16, s16) of every group for rows r0 and r1
+    uint32_t ma[Gm::NG], mb[Gm::NG];
+    if constexpr (Gm::NG == 4) {
+        const uint4 a = *reinterpret_cast<const uint4*>(ms + r0 * Gm::MS_ROW);
+        const uint4 bq = *reinterpret_cast<const uint4*>(ms + r1 * Gm::MS_ROW);
+        ma[0] = a.x; ma[1] = a.y; ma[2] = a.z; ma[3] = a.w;
+        mb[0] = bq.x; mb[1] = bq.y; mb[2] = bq.z; mb[3] = bq.w;
+    } else {
+        const uint2 a = *reinterpret_cast<const uint2*>(ms + r0 * Gm::MS_ROW);
+        const uint2 bq = *reinterpret_cast<const uint2*>(ms + r1 * Gm::MS_ROW);
+        ma[0] = a.x; ma[1] = a.y;
+        mb[0] = bq.x; mb[1] = bq.y;
     }
+    const uint4* ca = reinterpret_cast<const uint4*>(codes + r0 * Gm::CODES_ROW);
+    const uint4* cb = reinterpret_cast<const uint4*>(codes + r1 * Gm::CODES_ROW);
+    float2 v0 = make_float2(0.f, 0.f), v1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int kq = 0; kq < Gm::KS / 4; ++kq) {
+        const uint4 wa4 = ca[kq], wb4 = cb[kq];
+        const uint32_t wa[4] = {wa4.x, wa4.y, wa4.z, wa4.w};
+        const uint32_t wb[4] = {wb4.x, wb4.y, wb4.z, wb4.w};
+#pragma unroll
+        for (int hg = 0; hg < 2; ++hg) {  // the two 32-channel groups of this 16-byte word
+            const int g = 2 * kq + hg;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int e2 = 0; e2 < 2; ++e2) {
+                const int kk = 2 * g + e2;
+                const uint32_t ua = wa[2 * hg + e2] >> (4 * tig), ub = wb[2 * hg + e2] >> (4 * tig);
+                // bits 0-1 / 16-17: codes of the even pair as bf16 subnormals code * 2^-133; bits 2-3 /
+                // 18-19: the odd pair as 4 * code * 2^-133 (qc2 carries the 1/4)
+                mma_bf16(acc, ua & 0x00030003u, ub & 0x00030003u, ua & 0x000C000Cu, ub & 0x000C000Cu, tq.qc0[kk],
+                         tq.qc2[kk]);
+            }
+            // group g of rows r0 / r1, queries 2 tig and 2 tig + 1: s_g * <q, code>_g + mn_g * sum_g(q),
+            // added in g order
+            const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&ma[g]));  // (mn, s) of row r0
+            const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&mb[g]));  // (mn, s) of row r1
+            v0 = __fadd2_rn(v0, __ffma2_rn(make_float2(fa.y, fa.y), make_float2(acc[0], acc[1]),
+                                           __fmul2_rn(make_float2(fa.x, fa.x), tq.qsum[g])));
+            v1 = __fadd2_rn(v1, __ffma2_rn(make_float2(fb.y, fb.y), make_float2(acc[2], acc[3]),
+                                           __fmul2_rn(make_float2(fb.x, fb.x), tq.qsum[g])));
+        }
+    }
+    // v is the group sum times 2^(sq - 7) exactly; scan_scale undoes the power of two
+    st[0] = __fmul_rn(v0.x, tq.scan_scale.x);
+    st[1] = __fmul_rn(v0.y, tq.scan_scale.y);
+    st[2] = __fmul_rn(v1.x, tq.scan_scale.x);
+    st[3] = __fmul_rn(v1.y, tq.scan_scale.y);
 }
 
-// Residual term sum_g rs_g * <q, rq>_g of the warp's 16 rows (same row
-// order as scan_tile).  The int8 residual tile is one swizzled box; each
-// lane's ldmatrix word holds 4 consecutive bytes, which prmt with 0x64 high
-// bytes turns into the exact fp16 values 1152 + x.  The offset is removed
-// from the fp32 sums afterwards; its rounding error (~1e-3 in units of rq)
-// is scaled down by rs (~1e-2) and the softmax scale before it reaches a
-// score.  Each group is folded into the running sum right after its two
-// k-steps, in group order.
+// Residual term sum_g rs_g * <q, rq>_g of the warp's 16 rows (same layout as
+// scan_tile).  The int8 residual tile is one swizzled box; each lane's
+// ldmatrix word holds 4 consecutive bytes of one row, which prmt with 0x64
+// high bytes turns into the exact fp16 values 1152 + x.  The offset is
+// removed from the fp32 sums afterwards; its rounding error (~1e-3 in units
+// of rq) is scaled down by rs (~1e-2) and the softmax scale before it
+// reaches a score.  Each group is folded into the running sum right after
+// its two k-steps, in group order.
 template <int D>
 __device__ __forceinline__ void residual_tile(uint32_t res_s, const unsigned char* rs, int warp, int lane,
                                               const TDQuery<D>& tq, float (&rt)[4]) {
     using Gm = TGeo<D>;
-    const int tig = lane & 3;
+    const int gid = lane >> 2;
     const int mi = lane >> 3;
     const int ld_row = warp * 16 + 8 * (mi >> 1) + (lane & 7);
-    // rs16 of every group for the lane's rows (row, row + 1) of both n-tiles
-    __half2 ra[2][Gm::NG / 2], rb[2][Gm::NG / 2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        const int row = warp * 16 + 8 * j + 2 * tig;
-        if constexpr (Gm::NG == 4) {
-            const uint2 a = *reinterpret_cast<const uint2*>(rs + row * Gm::RS_ROW);
-            const uint2 bq = *reinterpret_cast<const uint2*>(rs + (row + 1) * Gm::RS_ROW);
-            ra[j][0] = *reinterpret_cast<const __half2*>(&a.x);
-            ra[j][1] = *reinterpret_cast<const __half2*>(&a.y);
-            rb[j][0] = *reinterpret_cast<const __half2*>(&bq.x);
-            rb[j][1] = *reinterpret_cast<const __half2*>(&bq.y);
-        } else {
-            const uint32_t a = *reinterpret_cast<const uint32_t*>(rs + row * Gm::RS_ROW);
-            const uint32_t bq = *reinterpret_cast<const uint32_t*>(rs + (row + 1) * Gm::RS_ROW);
-            ra[j][0] = *reinterpret_cast<const __half2*>(&a);
-            rb[j][0] = *reinterpret_cast<const __half2*>(&bq);
-        }
+    const int r0 = warp * 16 + gid, r1 = r0 + 8;
+    // rs16 of every group for rows r0 and r1
+    __half2 ra[Gm::NG / 2], rb[Gm::NG / 2];
+    if constexpr (Gm::NG == 4) {
+        const uint2 a = *reinterpret_cast<const uint2*>(rs + r0 * Gm::RS_ROW);
+        const uint2 bq = *reinterpret_cast<const uint2*>(rs + r1 * Gm::RS_ROW);
+        ra[0] = *reinterpret_cast<const __half2*>(&a.x);
+        ra[1] = *reinterpret_cast<const __half2*>(&a.y);
+        rb[0] = *reinterpret_cast<const __half2*>(&bq.x);
+        rb[1] = *reinterpret_cast<const __half2*>(&bq.y);
+    } else {
+        const uint32_t a = *reinterpret_cast<const uint32_t*>(rs + r0 * Gm::RS_ROW);
+        const uint32_t bq = *reinterpret_cast<const uint32_t*>(rs + r1 * Gm::RS_ROW);
+        ra[0] = *reinterpret_cast<const __half2*>(&a);
+        rb[0] = *reinterpret_cast<const __half2*>(&bq);
     }
-    float2 v[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    float2 v0 = make_float2(0.f, 0.f), v1 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int g = 0; g < Gm::NG; ++g) {
         const int chunk = 2 * g + (mi & 1);
         const uint32_t addr = res_s + (D == 128 ? swz(ld_row, chunk) : swz64(ld_row, chunk));
         uint32_t r[4];
-        ldsm_x4(addr, r[0], r[1], r[2], r[3]);  // (n-tile 0, kk 2g), (0, 2g+1), (1, 2g), (1, 2g+1)
-        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        ldsm_x4(addr, r[0], r[1], r[2], r[3]);  // (row r0, kk 2g), (r0, 2g+1), (r1, 2g), (r1, 2g+1)
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
+        for (int e = 0; e < 2; ++e) {
             // fp16 0x64uu is 1024 + uu exactly; with uu = x + 128 the operand is 1152 + x and
             // the offset leaves the sum as 1152 * (sum of q over the group), removed below
-            const uint32_t u = r[m] ^ 0x80808080u;
-            const uint32_t b0 = __byte_perm(u, 0x64646464u, 0x4140);
-            const uint32_t b1 = __byte_perm(u, 0x64646464u, 0x4342);
-            const int kk = 2 * g + (m & 1);
-            mma_f16(acc[m >> 1], tq.qr0[kk], 0u, tq.qr2[kk], 0u, b0, b1);
+            const uint32_t ua = r[e] ^ 0x80808080u, ub = r[e + 2] ^ 0x80808080u;
+            mma_f16(acc, __byte_perm(ua, 0x64646464u, 0x4140), __byte_perm(ub, 0x64646464u, 0x4140),
+                    __byte_perm(ua, 0x64646464u, 0x4342), __byte_perm(ub, 0x64646464u, 0x4342), tq.qr0[2 * g + e],
+                    tq.qr2[2 * g + e]);
         }
-        const float off = 1152.f * tq.qsumh[g];
+        const float2 fa = __half22float2(ra[g >> 1]), fb = __half22float2(rb[g >> 1]);
+        const float rsa = (g & 1) ? fa.y : fa.x, rsb = (g & 1) ? fb.y : fb.x;
+        v0 = __ffma2_rn(make_float2(rsa, rsa), make_float2(acc[0] - tq.off[g].x, acc[1] - tq.off[g].y), v0);
+        v1 = __ffma2_rn(make_float2(rsb, rsb), make_float2(acc[2] - tq.off[g].x, acc[3] - tq.off[g].y), v1);
+    }
+    rt[0] = v0.x;
+    rt[1] = v0.y;
+    rt[2] = v1.x;
+    rt[3] = v1.y;
+}
+
+// Transpose of an 8x8 matrix of 16-bit values held one row pair per lane
+// (lane gid*4 + t holds row gid, columns 2t and 2t + 1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+// Attend state of one warp: O^T (D rows x 8 query columns, the lane holds
+// columns 2 tig and 2 tig + 1), and per column the running max (log2 units)
+// and the lane's share of the exp-sum.
+template <int D>
+struct TDAcc {
+    float o[D / 16][4];
+    float2 m, l;
+};
+
+// Online softmax over one tile and O^T += V^T P^T for scores in the
+// transposed layout (sc[i]: row warp*16 + gid + 8*(i >> 1), query
+// 2*tig + (i & 1); -inf = not attended).  V rows at or past `rows` are
+// cleared first (P is 0 there, but 0 * NaN is NaN).  P goes to the tensor
+// cores as bf16 hi + lo; movmatrix turns each 8x8 block of the lane's P
+// values into the B fragment of P^T.
+template <int D>
+__device__ __forceinline__ void softmax_pv_t(TDAcc<D>& ac, const float (&sc)[4], uint32_t vs, unsigned char* vgen,
+                                             int warp, int lane, int rows) {
+    const int mi = lane >> 3;
+    const int ld_row = warp * 16 + 8 * (mi >> 1) + (lane & 7);
+    if (warp * 16 + 16 > rows) {
+        for (int i = lane; i < 16 * (D / 8); i += 32) {
+            const int r = warp * 16 + i / (D / 8);
+            if (r >= rows) *reinterpret_cast<uint4*>(vgen + swz(r, i % (D / 8))) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        // order these generic stores before the tile copy that later refills the stage
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+    }
+    // per query: max over the 16 rows (the lanes of equal tig)
+    float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const float2 fa = __half22float2(ra[j][g >> 1]), fb = __half22float2(rb[j][g >> 1]);
-            const float2 rsg = (g & 1) ? make_float2(fa.y, fb.y) : make_float2(fa.x, fb.x);
-            v[j] = __ffma2_rn(rsg, make_float2(acc[j][0] - off, acc[j][1] - off), v[j]);
+    for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    const float m0 = fmaxf(ac.m.x, mx0), m1 = fmaxf(ac.m.y, mx1);
+    const bool none0 = m0 == -INFINITY, none1 = m1 == -INFINITY;
+    const float a0 = none0 ? 1.f : exp2_approx(ac.m.x - m0);
+    const float a1 = none1 ? 1.f : exp2_approx(ac.m.y - m1);
+    float pr[4];
+    pr[0] = none0 ? 0.f : exp2_approx(sc[0] - m0);
+    pr[1] = none1 ? 0.f : exp2_approx(sc[1] - m1);
+    pr[2] = none0 ? 0.f : exp2_approx(sc[2] - m0);
+    pr[3] = none1 ? 0.f : exp2_approx(sc[3] - m1);
+    ac.m = make_float2(m0, m1);
+    ac.l.x = ac.l.x * a0 + (pr[0] + pr[2]);
+    ac.l.y = ac.l.y * a1 + (pr[1] + pr[3]);
+    uint32_t h0, l0, h1, l1;
+    split_bf16(pr[0], pr[1], h0, l0);  // row gid
+    split_bf16(pr[2], pr[3], h1, l1);  // row gid + 8
+    h0 = movmatrix_trans(h0);
+    l0 = movmatrix_trans(l0);
+    h1 = movmatrix_trans(h1);
+    l1 = movmatrix_trans(l1);
+    // rescale only when some query's max moved
+    if (!__all_sync(0xffffffffu, a0 == 1.f && a1 == 1.f)) {
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+            ac.o[mt][0] *= a0;
+            ac.o[mt][1] *= a1;
+            ac.o[mt][2] *= a0;
+            ac.o[mt][3] *= a1;
         }
     }
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        rt[2 * j] = v[j].x;
-        rt[2 * j + 1] = v[j].y;
+    for (int mt = 0; mt < D / 16; ++mt) {
+        uint32_t v0, v1, v2, v3;
+        ldsm_x4_t(vs + swz(ld_row, 2 * mt + (mi & 1)), v0, v1, v2, v3);
+        mma_bf16(ac.o[mt], v0, v1, v2, v3, h0, h1);
+        mma_bf16(ac.o[mt], v0, v1, v2, v3, l0, l1);
     }
 }
 
@@ -450,9 +532,10 @@ topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constan
 
     // ------------------------------- consumers -----------------------------------
     const int gid = lane >> 2, tig = lane & 3;
-    const bool q_real = gid < p.G;
+    const bool q_real = gid < p.G;                                // the lane's B-fragment query
+    const bool c_real[2] = {2 * tig < p.G, 2 * tig + 1 < p.G};    // its accumulator columns' queries
     TDQuery<D> tq;
-    MmaWarpState<D> ws;
+    TDAcc<D> ac;
     {
         const uint16_t* qrow = p.q + (size_t)(b * p.Hq + hq0 + gid) * D;
         auto qf = [&](int c) { return q_real ? __uint_as_float((uint32_t)qrow[c] << 16) : 0.f; };
@@ -472,9 +555,9 @@ topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constan
             tq.qc2[kk] = pack_bf16(0.25f * qs(c0 + 2 * tig + 1), 0.25f * qs(c0 + 2 * tig + 9));  // exact
             tq.qr0[kk] = pack_f16(qf(c0 + 4 * tig), qf(c0 + 4 * tig + 1));
             tq.qr2[kk] = pack_f16(qf(c0 + 4 * tig + 2), qf(c0 + 4 * tig + 3));
-            ws.qa0[kk] = 0u;
-            ws.qa2[kk] = 0u;
         }
+        // per-query constants of query gid, then moved to the lanes whose
+        // accumulator columns hold that query (lane 4q holds query q)
 #pragma unroll
         for (int g = 0; g < D / 32; ++g) {
             float sum = 0.f, sumh = 0.f;
@@ -482,23 +565,26 @@ topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constan
                 sum = __fadd_rn(sum, qf(32 * g + c));
                 sumh += __half2float(__float2half_rn(qf(32 * g + c)));
             }
-            tq.qsum[g] = ldexpf(sum, sq - 7);  // exact
-            tq.qsumh[g] = sumh;
+            const float qsum = ldexpf(sum, sq - 7);  // exact
+            const float off = 1152.f * sumh;
+            tq.qsum[g] = make_float2(__shfl_sync(0xffffffffu, qsum, 8 * tig), __shfl_sync(0xffffffffu, qsum, 8 * tig + 4));
+            tq.off[g] = make_float2(__shfl_sync(0xffffffffu, off, 8 * tig), __shfl_sync(0xffffffffu, off, 8 * tig + 4));
         }
-        tq.scan_scale = ldexpf(p.scale, 7 - sq);
+        const float ssc = ldexpf(p.scale, 7 - sq);
+        tq.scan_scale = make_float2(__shfl_sync(0xffffffffu, ssc, 8 * tig), __shfl_sync(0xffffffffu, ssc, 8 * tig + 4));
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) ws.o[mt][i] = 0.f;
-        ws.m_run = -INFINITY;
-        ws.l_run = 0.f;
+            for (int i = 0; i < 4; ++i) ac.o[mt][i] = 0.f;
+        ac.m = make_float2(-INFINITY, -INFINITY);
+        ac.l = make_float2(0.f, 0.f);
     }
 
     // ---------------- anchor pass: pseudo-max per query head --------------------
     // Anchor tiles are staged in the first detail stage (untouched until the
     // first tile is flagged) in the scan ring's layout and scored by the same
     // code, so m^ equals the scan's s~ of the best anchor bit for bit.
-    float mh = -INFINITY;
+    float mh[2] = {-INFINITY, -INFINITY};  // queries 2 tig, 2 tig + 1
     {
         unsigned char* stage = smem + Ly::DET_OFF;
         const int sink_end = min(p.n_sink, L);
@@ -532,22 +618,32 @@ topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constan
             scan_tile<D>(stage, stage + kTile * Gm::CODES_ROW, warp, lane, tq, st);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int r = warp * 16 + 2 * tig + (i & 1) + 8 * (i >> 1);
+                const int r = warp * 16 + gid + 8 * (i >> 1);
                 const int j = tb + r;
-                if (r < rows && (j < sink_end || j >= win_beg)) mh = fmaxf(mh, st[i]);
+                if (r < rows && (j < sink_end || j >= win_beg)) mh[i & 1] = fmaxf(mh[i & 1], st[i]);
             }
         }
-        mh = fmaxf(mh, __shfl_xor_sync(0xffffffffu, mh, 1));
-        mh = fmaxf(mh, __shfl_xor_sync(0xffffffffu, mh, 2));
-        if (tig == 0) mh_red[warp * 8 + gid] = mh;
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            mh[0] = fmaxf(mh[0], __shfl_xor_sync(0xffffffffu, mh[0], o));
+            mh[1] = fmaxf(mh[1], __shfl_xor_sync(0xffffffffu, mh[1], o));
+        }
+        if (gid == 0) {
+            mh_red[warp * 8 + 2 * tig] = mh[0];
+            mh_red[warp * 8 + 2 * tig + 1] = mh[1];
+        }
         // staging stores must be ordered before the tile copies that reuse the area
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         named_barrier(1, CW * 32);
 #pragma unroll
-        for (int w = 0; w < CW; ++w) mh = fmaxf(mh, mh_red[w * 8 + gid]);
+        for (int w = 0; w < CW; ++w) {
+            mh[0] = fmaxf(mh[0], mh_red[w * 8 + 2 * tig]);
+            mh[1] = fmaxf(mh[1], mh_red[w * 8 + 2 * tig + 1]);
+        }
     }
-    const float thr = __fsub_rn(mh, p.delta);  // delta = inf keeps every key
-    int cnt = 0;
+    // delta = inf keeps every key
+    const float thr[2] = {__fsub_rn(mh[0], p.delta), __fsub_rn(mh[1], p.delta)};
+    int cnt[2] = {0, 0};
     bool failed = false;
 
     auto scan_step = [&](int k) {
@@ -565,8 +661,8 @@ topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constan
         bool any = false;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const int r = warp * 16 + 2 * tig + (i & 1) + 8 * (i >> 1);
-            any |= q_real && r < rows && st[i] >= thr;
+            const int r = warp * 16 + gid + 8 * (i >> 1);
+            any |= c_real[i & 1] && r < rows && st[i] >= thr[i & 1];
         }
         any = __any_sync(0xffffffffu, any);
         __syncwarp();
@@ -600,20 +696,20 @@ topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constan
             float sc[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int r = warp * 16 + 2 * tig + (i & 1) + 8 * (i >> 1);
-                const bool sel = q_real && r < rows && stv[i] >= thr;
+                const int r = warp * 16 + gid + 8 * (i >> 1);
+                const bool sel = c_real[i & 1] && r < rows && stv[i] >= thr[i & 1];
                 sc[i] = sel ? fmaf(p.scale, rt[i], stv[i]) * kLog2e : -INFINITY;
                 if (sel) {
-                    ++cnt;
+                    ++cnt[i & 1];
                     if (p.sel_mask) {
                         const int j = tok0 + r;
                         const int words = (p.L_max + 31) / 32;
-                        atomicOr(&p.sel_mask[(size_t)(b * p.Hq + hq0 + gid) * words + j / 32], 1u << (j % 32));
+                        const int qh = hq0 + 2 * tig + (i & 1);
+                        atomicOr(&p.sel_mask[(size_t)(b * p.Hq + qh) * words + j / 32], 1u << (j % 32));
                     }
                 }
             }
-            mma_softmax_pv<D>(ws, sc, smem_u32(st_base + Gm::RES_BYTES), st_base + Gm::RES_BYTES, warp, lane,
-                              rows);
+            softmax_pv_t<D>(ac, sc, smem_u32(st_base + Gm::RES_BYTES), st_base + Gm::RES_BYTES, warp, lane, rows);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&det_empty[ds]);
@@ -621,13 +717,25 @@ topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constan
     if (failed) atomicOr(&g_status_topdelta, kStatusTimeout);
     pdl_launch_dependents();
 
-    if (p.sel_count) {
-        cnt += __shfl_xor_sync(0xffffffffu, cnt, 1);
-        cnt += __shfl_xor_sync(0xffffffffu, cnt, 2);
-        if (tig == 0 && q_real && cnt) atomicAdd(&p.sel_count[b * p.Hq + hq0 + gid], cnt);
+    // per column: counts and exp-sums over the 16 rows (lanes of equal tig)
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+        cnt[0] += __shfl_xor_sync(0xffffffffu, cnt[0], o);
+        cnt[1] += __shfl_xor_sync(0xffffffffu, cnt[1], o);
+        ac.l.x += __shfl_xor_sync(0xffffffffu, ac.l.x, o);
+        ac.l.y += __shfl_xor_sync(0xffffffffu, ac.l.y, o);
     }
-    combine_mma_warps_and_store<D, 8, CW>(smem, warp, lane, p.G, b * p.Hq + hq0, split, ws.m_run, ws.l_run, ws.o,
-                                          failed, p.st);
+    if (p.sel_count && gid == 0) {
+        if (c_real[0] && cnt[0]) atomicAdd(&p.sel_count[b * p.Hq + hq0 + 2 * tig], cnt[0]);
+        if (c_real[1] && cnt[1]) atomicAdd(&p.sel_count[b * p.Hq + hq0 + 2 * tig + 1], cnt[1]);
+    }
+    // (m, l) of query gid from lane gid / 2, column gid & 1; the combine sums l over the quad
+    const float me = __shfl_sync(0xffffffffu, ac.m.x, gid >> 1), mo = __shfl_sync(0xffffffffu, ac.m.y, gid >> 1);
+    const float le = __shfl_sync(0xffffffffu, ac.l.x, gid >> 1), lo = __shfl_sync(0xffffffffu, ac.l.y, gid >> 1);
+    const float m_q = (gid & 1) ? mo : me;
+    const float l_q = tig == 0 ? ((gid & 1) ? lo : le) : 0.f;
+    combine_mma_warps_and_store<D, 8, CW>(smem, warp, lane, p.G, b * p.Hq + hq0, split, m_q, l_q, ac.o, failed,
+                                          p.st);
 }
 
 template <int D>
