@@ -21,8 +21,11 @@
 //     LA tiles before the consumers attend to it, so the residual and V of
 //     tiles without candidates are never read from HBM.
 //   * attend: exact scores s = s~ + scale * sum_g rs_g <q_g, rq_g> for the
-//     candidates, online softmax and P.V as in the dense pass, then the same
-//     warp combine and chunk merge.
+//     candidates, online softmax and O^T += V^T P^T, then the same warp
+//     combine and chunk merge as the dense pass.
+// Both dot stages put the warp's 16 tokens in the MMA's M dimension and the
+// group's query heads in N (S = K Q^T), so no accumulator is spent on
+// padding query rows; movmatrix turns the P values into P^T fragments.
 #include <cmath>
 #include <cuda_fp16.h>
 
