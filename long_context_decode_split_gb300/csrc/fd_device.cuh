@@ -204,6 +204,17 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Transpose of an 8x8 matrix of 16-bit values held as in an MMA fragment
+// (lane 4*gid + t holds row gid, columns 2t and 2t + 1; the lower column in
+// the lower half): the result holds the transpose in the same layout.  This
+// turns the P values of an S = K Q^T accumulator (rows = tokens) into the B
+// fragment of P^T (k = tokens, n = query heads).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
 // Two fp32 -> packed bf16x2 (round to nearest even); `lo` in the low half.
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     uint32_t r;

@@ -16,21 +16,23 @@
 // ring), warps 0..3 each own 16 tokens of every tile, take NT tiles per step
 // (one online-softmax update per step) and run both products on the tensor
 // cores with fp16 operands (every e4m3 value is exact in fp16):
-//   S = Q K^T   A = the query group (padded to 16 rows) in fp16, scaled per
-//               query by a power of two so that |q| < 1 (exact); B = K codes
-//               fetched by ldmatrix (4 bytes = 4 channels per lane) and
-//               widened with cvt.rn.f16x2.e4m3x2.  The channel order inside
-//               each 16-channel k-step is permuted identically on Q, so the
-//               dot products are unchanged.  The row scale of K and the
-//               power of two of Q are applied to the fp32 scores.
+//   S = K Q^T   A = the warp's 16 K rows: codes fetched by ldmatrix (4 bytes
+//               = 4 channels per lane) and widened with cvt.rn.f16x2.e4m3x2;
+//               B = the query group (up to 8 columns) in fp16, scaled per
+//               query by a power of two so that |q| < 1 (exact).  The channel
+//               order inside each 16-channel k-step is permuted identically
+//               on Q, so the dot products are unchanged.  The row scale of K
+//               and the power of two of Q are applied to the fp32 scores.
 //   O^T += V^T P^T
 //               A = V codes: lane group gid reads channels D/8 * gid ..
 //               + D/8 - 1 of its four tokens in one shared load each, and
 //               byte permutes pair the tokens up before widening (row gid +
-//               8r of output tile j is channel D/8 * gid + 2j + r); B = P * s_V / s_ref in
-//               fp16, where s_ref, the largest V scale the warp has seen,
-//               keeps the operand in [0, 1]; a growing s_ref rescales O like
-//               a growing running max.  O is multiplied by s_ref at the end.
+//               8r of output tile j is channel D/8 * gid + 2j + r);
+//               B = P * s_V / s_ref in fp16, transposed from the S layout by
+//               movmatrix, where s_ref, the largest V scale the warp has
+//               seen, keeps the operand in [0, 1]; a growing s_ref rescales O
+//               like a growing running max.  O is multiplied by s_ref at the
+//               end.
 // The chunk's (m_i, l_i, O_i) then go through the same combine and merge as
 // the bf16 pass.
 #include <cmath>
@@ -243,10 +245,12 @@ fp8_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
 
     // ------------------------------ consumers ------------------------------
     const int gid = lane >> 2, tig = lane & 3, mi = lane >> 3;
-    // Q fragments: channels 16c + 4*tig + {0,1} (qa0) and {2,3} (qa2) of query
-    // gid, times 2^-e with e the exponent of the query's largest |q|.
+    // Q as the B fragment of S = K Q^T: channels 16c + 4*tig + {0,1} (qa0) and
+    // {2,3} (qa2) of query gid, times 2^-e with e the exponent of the query's
+    // largest |q|.  The accumulators hold rows (tokens) gid, gid + 8 and
+    // columns (queries) 2 tig, 2 tig + 1.
     uint32_t qa0[D / 16], qa2[D / 16];
-    float qmul;
+    float2 qmul;  // columns 2 tig, 2 tig + 1
     {
         float qv[D / 16][4];
         float amax = 0.f;
@@ -272,7 +276,8 @@ fp8_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
             qa0[c] = pack_f16(ldexpf(qv[c][0], -ex), ldexpf(qv[c][1], -ex));
             qa2[c] = pack_f16(ldexpf(qv[c][2], -ex), ldexpf(qv[c][3], -ex));
         }
-        qmul = ldexpf(p.scale_log2, ex);
+        const float qm = ldexpf(p.scale_log2, ex);  // query gid's; lane 4q holds query q
+        qmul = make_float2(__shfl_sync(0xffffffffu, qm, 8 * tig), __shfl_sync(0xffffffffu, qm, 8 * tig + 4));
     }
 
     float o[D / 16][4];
@@ -280,10 +285,12 @@ fp8_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
     for (int mt = 0; mt < D / 16; ++mt)
 #pragma unroll
         for (int i = 0; i < 4; ++i) o[mt][i] = 0.f;
-    float m_run = -INFINITY, l_run = 0.f, vref = 0.f;
+    float2 m_run = make_float2(-INFINITY, -INFINITY), l_run = make_float2(0.f, 0.f);  // columns 2 tig, 2 tig + 1
+    float vref = 0.f;
     bool failed = false;
     const int ld_row = warp * 16 + 8 * (mi >> 1) + (lane & 7);  // row this lane addresses for ldmatrix
-    const int r0 = warp * 16 + 2 * tig;                         // tokens r0, r0+1, r0+8, r0+9 are this lane's
+    const int r0 = warp * 16 + 2 * tig;                         // V^T P^T: tokens r0, r0+1, r0+8, r0+9
+    const int srow[2] = {warp * 16 + gid, warp * 16 + gid + 8};  // S = K Q^T: the lane's accumulator rows
     constexpr int VW = D / 32;                                  // V words per token and lane (D/8 channels)
     // byte offset of this lane's V channels D/8 * gid .. within a code row
     const uint32_t vofs_lo = D == 128 ? 0u : 8u * (uint32_t)(gid & 1);
@@ -310,76 +317,85 @@ fp8_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
             break;
         }
 
-        // ---- S = Q K^T over this warp's 16 tokens of each stage ---------------
-        float sacc[NT][2][4];
+        // ---- S = K Q^T over this warp's 16 tokens of each stage ---------------
+        float sacc[NT][4];
 #pragma unroll
         for (int k = 0; k < NT; ++k) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) sacc[k][0][i] = sacc[k][1][i] = 0.f;
+            for (int i = 0; i < 4; ++i) sacc[k][i] = 0.f;
             const uint32_t kt = smem_u32(smem + st[k] * STAGE);
 #pragma unroll
             for (int kk = 0; kk < D / 32; ++kk) {
-                uint32_t w0, w1, w2, w3, blo, bhi;
+                // w0 / w2: rows gid / gid + 8, channels 32 kk + 4 tig ..; w1 / w3: the next 16 channels
+                uint32_t w0, w1, w2, w3, a0, a1, a2, a3;
                 ldsm_x4(kt + code_off<D>(ld_row, 2 * kk + (mi & 1)), w0, w1, w2, w3);
-                e4m3x4_to_f16x4(w0, blo, bhi);
-                mma_f16(sacc[k][0], qa0[2 * kk], 0u, qa2[2 * kk], 0u, blo, bhi);
-                e4m3x4_to_f16x4(w1, blo, bhi);
-                mma_f16(sacc[k][0], qa0[2 * kk + 1], 0u, qa2[2 * kk + 1], 0u, blo, bhi);
-                e4m3x4_to_f16x4(w2, blo, bhi);
-                mma_f16(sacc[k][1], qa0[2 * kk], 0u, qa2[2 * kk], 0u, blo, bhi);
-                e4m3x4_to_f16x4(w3, blo, bhi);
-                mma_f16(sacc[k][1], qa0[2 * kk + 1], 0u, qa2[2 * kk + 1], 0u, blo, bhi);
+                e4m3x4_to_f16x4(w0, a0, a2);
+                e4m3x4_to_f16x4(w2, a1, a3);
+                mma_f16(sacc[k], a0, a1, a2, a3, qa0[2 * kk], qa2[2 * kk]);
+                e4m3x4_to_f16x4(w1, a0, a2);
+                e4m3x4_to_f16x4(w3, a1, a3);
+                mma_f16(sacc[k], a0, a1, a2, a3, qa0[2 * kk + 1], qa2[2 * kk + 1]);
             }
         }
-        float sc[NT][4], vs[NT][4];
+        float sc[NT][4], vs[NT][2];  // scores (rows gid, gid + 8 x columns); V scales of rows gid, gid + 8
 #pragma unroll
         for (int k = 0; k < NT; ++k) {
             const float* ksc = reinterpret_cast<const float*>(scl + st[k] * SSTAGE) + stage_off[st[k]];
             const float* vsc = reinterpret_cast<const float*>(scl + st[k] * SSTAGE + kScaleSlot) + stage_off[st[k]];
-            const float raw[4] = {sacc[k][0][0], sacc[k][0][1], sacc[k][1][0], sacc[k][1][1]};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const bool ok = tok[i] < rows[k];
-                sc[k][i] = ok ? raw[i] * ksc[tok[i]] * qmul : -INFINITY;
-                vs[k][i] = ok ? vsc[tok[i]] : 0.f;
+            for (int r = 0; r < 2; ++r) {
+                const bool ok = srow[r] < rows[k];
+                const float ks = ok ? ksc[srow[r]] : 0.f;
+                sc[k][2 * r] = ok ? sacc[k][2 * r] * ks * qmul.x : -INFINITY;
+                sc[k][2 * r + 1] = ok ? sacc[k][2 * r + 1] * ks * qmul.y : -INFINITY;
+                vs[k][r] = ok ? vsc[srow[r]] : 0.f;
             }
         }
 
-        // ---- online softmax and the V reference scale ------------------------
-        float mx = -INFINITY, vmax = 0.f;
+        // ---- online softmax per column and the V reference scale ---------------
+        float mx0 = -INFINITY, mx1 = -INFINITY, vmax = 0.f;
 #pragma unroll
         for (int k = 0; k < NT; ++k) {
-            mx = fmaxf(mx, fmaxf(fmaxf(sc[k][0], sc[k][1]), fmaxf(sc[k][2], sc[k][3])));
-            vmax = fmaxf(vmax, fmaxf(fmaxf(vs[k][0], vs[k][1]), fmaxf(vs[k][2], vs[k][3])));
+            mx0 = fmaxf(mx0, fmaxf(sc[k][0], sc[k][2]));
+            mx1 = fmaxf(mx1, fmaxf(sc[k][1], sc[k][3]));
+            vmax = fmaxf(vmax, fmaxf(vs[k][0], vs[k][1]));
         }
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 1));
-        vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {  // over the 16 rows: the lanes of equal tig
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, off));
+        }
         const float vref_new = fmaxf(vref, vmax);
         const float vinv = vref_new > 0.f ? __fdividef(1.f, vref_new) : 0.f;
         const float vf = vref_new > 0.f ? vref * vinv : 1.f;
         vref = vref_new;
-        const float m_new = fmaxf(m_run, mx);
-        const bool none = m_new == -INFINITY;
-        const float alpha = none ? 1.f : exp2_approx(m_run - m_new);
-        m_run = m_new;
-        float lsum = 0.f;
+        const float m0 = fmaxf(m_run.x, mx0), m1 = fmaxf(m_run.y, mx1);
+        const bool none0 = m0 == -INFINITY, none1 = m1 == -INFINITY;
+        const float alpha0 = none0 ? 1.f : exp2_approx(m_run.x - m0);
+        const float alpha1 = none1 ? 1.f : exp2_approx(m_run.y - m1);
+        m_run = make_float2(m0, m1);
+        float lsum0 = 0.f, lsum1 = 0.f;
         uint32_t pb[NT][2];
 #pragma unroll
         for (int k = 0; k < NT; ++k) {
             float pr[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) pr[i] = none ? 0.f : exp2_approx(sc[k][i] - m_new);
-            lsum += (pr[0] + pr[1]) + (pr[2] + pr[3]);
-            pb[k][0] = pack_f16(pr[0] * (vs[k][0] * vinv), pr[1] * (vs[k][1] * vinv));
-            pb[k][1] = pack_f16(pr[2] * (vs[k][2] * vinv), pr[3] * (vs[k][3] * vinv));
+            pr[0] = none0 ? 0.f : exp2_approx(sc[k][0] - m0);
+            pr[1] = none1 ? 0.f : exp2_approx(sc[k][1] - m1);
+            pr[2] = none0 ? 0.f : exp2_approx(sc[k][2] - m0);
+            pr[3] = none1 ? 0.f : exp2_approx(sc[k][3] - m1);
+            lsum0 += pr[0] + pr[2];
+            lsum1 += pr[1] + pr[3];
+            // P * s_V / s_ref of rows gid and gid + 8, then each 8x8 block transposed into P^T
+            const float v0 = vs[k][0] * vinv, v1 = vs[k][1] * vinv;
+            pb[k][0] = movmatrix_trans(pack_f16(pr[0] * v0, pr[1] * v0));
+            pb[k][1] = movmatrix_trans(pack_f16(pr[2] * v1, pr[3] * v1));
         }
-        l_run = l_run * alpha + lsum;
-        if (!__all_sync(0xffffffffu, alpha == 1.f && vf == 1.f)) {
-            // accumulator columns are queries 2*tig and 2*tig+1
-            const float a_even = __shfl_sync(0xffffffffu, alpha, 8 * tig) * vf;
-            const float a_odd = __shfl_sync(0xffffffffu, alpha, 8 * tig + 4) * vf;
+        l_run.x = l_run.x * alpha0 + lsum0;
+        l_run.y = l_run.y * alpha1 + lsum1;
+        if (!__all_sync(0xffffffffu, alpha0 == 1.f && alpha1 == 1.f && vf == 1.f)) {
+            // accumulator columns are the lane's own queries 2*tig and 2*tig+1
+            const float a_even = alpha0 * vf, a_odd = alpha1 * vf;
 #pragma unroll
             for (int mt = 0; mt < D / 16; ++mt) {
                 o[mt][0] *= a_even;
@@ -431,8 +447,11 @@ fp8_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
     pdl_launch_dependents();
 
     // ---- combine the consumer warps and store --------------------------------
-    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {  // exp-sums over the 16 rows (the lanes of equal tig)
+        l_run.x += __shfl_xor_sync(0xffffffffu, l_run.x, off);
+        l_run.y += __shfl_xor_sync(0xffffffffu, l_run.y, off);
+    }
     named_barrier(1, CW * 32);  // every consumer is done with the stage ring
     float* red_o = reinterpret_cast<float*>(smem);  // [CW][8][D]
     float* red_m = red_o + CW * 8 * D;              // [CW][8]
@@ -448,9 +467,11 @@ fp8_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
             *reinterpret_cast<float4*>(red_o + (warp * 8 + qi) * D + (D / 8) * gid + 4 * jj) = val;
         }
     }
-    if (tig == 0) {
-        red_m[warp * 8 + gid] = failed ? -INFINITY : m_run;
-        red_l[warp * 8 + gid] = failed ? 0.f : l_run;
+    if (gid == 0) {
+        red_m[warp * 8 + 2 * tig] = failed ? -INFINITY : m_run.x;
+        red_m[warp * 8 + 2 * tig + 1] = failed ? -INFINITY : m_run.y;
+        red_l[warp * 8 + 2 * tig] = failed ? 0.f : l_run.x;
+        red_l[warp * 8 + 2 * tig + 1] = failed ? 0.f : l_run.y;
     }
     named_barrier(1, CW * 32);
     store_combined<D, 8, CW>(smem, threadIdx.x, p.G, b * p.Hq + hq0, split, p.st);

@@ -332,14 +332,6 @@ __device__ __forceinline__ void residual_tile(uint32_t res_s, const unsigned cha
     rt[3] = v1.y;
 }
 
-// Transpose of an 8x8 matrix of 16-bit values held one row pair per lane
-// (lane gid*4 + t holds row gid, columns 2t and 2t + 1).
-__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
-    uint32_t y;
-    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
-    return y;
-}
-
 // Attend state of one warp: O^T (D rows x 8 query columns, the lane holds
 // columns 2 tig and 2 tig + 1), and per column the running max (log2 units)
 // and the lane's share of the exp-sum.
