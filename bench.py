@@ -176,9 +176,13 @@ class Workload:
         self.paged = p.paged
         self.out_dtype = p.out_dtype
         B, Hq, Hkv, d = p.B, p.Hq, p.Hkv, p.d
-        self.out = torch.empty((B, Hq, d), device=device,
-                               dtype=torch.float32 if p.out_dtype == "f32" else torch.bfloat16)
-        self.lse = torch.empty((B, Hq), device=device, dtype=torch.float32)
+        # out and lse share one device buffer, so a step's result leaves the GPU in one copy
+        out_t = torch.float32 if p.out_dtype == "f32" else torch.bfloat16
+        n_out = B * Hq * d * (4 if p.out_dtype == "f32" else 2)
+        lse_at = (n_out + 15) // 16 * 16
+        self.io = torch.empty(lse_at + B * Hq * 4, dtype=torch.uint8, device=device)
+        self.out = self.io[:n_out].view(out_t).view(B, Hq, d)
+        self.lse = self.io[lse_at:].view(torch.float32).view(B, Hq)
         self.sel_stats = None
         if self.fp8 or self.fp4:
             # encode the cache once (outside the timed region); keep the bf16 copy for e2e rows
@@ -237,29 +241,30 @@ class Workload:
                 "union_tokens": int(ubits.sum()), "tiles_loaded": int(tiles.sum()),
                 "tiles_total": int(tiles.size)}
 
-    def call(self, stream=None):
+    def call(self, stream=None, q=None):
         p, fd = self.p, self.fd
+        q = p.q if q is None else q
         if self.fp8 or self.fp4:
             kc, ks, vc, vs = self.kv8
             if self.paged:
                 paged = fd.fd_decode_paged_fp8 if self.fp8 else fd.fd_decode_paged_fp4
-                paged(p.q, kc, ks, vc, vs, p.page_table, p.num_pages, p.seq_lens, p.scale, p.num_splits,
+                paged(q, kc, ks, vc, vs, p.page_table, p.num_pages, p.seq_lens, p.scale, p.num_splits,
                       out=self.out, lse=self.lse, out_dtype=self.out_dtype, workspace=self.ws, stream=stream)
             else:
                 dense = fd.fd_decode_dense_fp8 if self.fp8 else fd.fd_decode_dense_fp4
-                dense(p.q, kc, ks, vc, vs, None, p.scale, p.num_splits, out=self.out, lse=self.lse,
+                dense(q, kc, ks, vc, vs, None, p.scale, p.num_splits, out=self.out, lse=self.lse,
                       out_dtype=self.out_dtype, workspace=self.ws, stream=stream)
         elif self.topdelta is not None:
             c, ms, r, rs = self.qk
-            fd.fd_decode_topdelta(p.q, c, ms, r, rs, p.v, p.seq_lens, p.scale, self.topdelta, self.n_sink,
+            fd.fd_decode_topdelta(q, c, ms, r, rs, p.v, p.seq_lens, p.scale, self.topdelta, self.n_sink,
                                   self.window, p.num_splits, out=self.out, lse=self.lse, out_dtype=self.out_dtype,
                                   workspace=self.ws, stream=stream)
         elif self.paged:
-            fd.fd_decode_paged(p.q, p.k_pages, p.v_pages, p.page_table, p.num_pages, p.seq_lens, p.scale,
+            fd.fd_decode_paged(q, p.k_pages, p.v_pages, p.page_table, p.num_pages, p.seq_lens, p.scale,
                                p.num_splits, out=self.out, lse=self.lse, out_dtype=self.out_dtype,
                                workspace=self.ws, stream=stream)
         else:
-            fd.fd_decode_dense(p.q, p.k, p.v, None, p.scale, p.num_splits, out=self.out, lse=self.lse,
+            fd.fd_decode_dense(q, p.k, p.v, None, p.scale, p.num_splits, out=self.out, lse=self.lse,
                                out_dtype=self.out_dtype, workspace=self.ws, stream=stream)
 
     def launches_per_call(self):
@@ -346,82 +351,84 @@ def time_device(wl, steps, warmup, dist_ctx, graph=0):
 
 def time_e2e(wl, steps, warmup, dist_ctx):
     """Same call through the public API, with this step's new inputs copied
-    from pinned host memory (the query and the newest token's K/V rows) and
-    the result (out, lse) read back, inside the timed region."""
+    from pinned host memory and the result read back, inside the timed
+    region.  Per step: one host->device copy of the query and the newest
+    token's K/V rows (packed in one pinned buffer), the rows written into the
+    cache in the form the decode reads (bf16 rows; fp8/fp4 codes and scales
+    from the cache encoder; for top-delta the key encoding from
+    fd_quantize_keys plus the bf16 V row), the decode call on the copied
+    query, and one device->host copy of out and lse."""
     import torch
 
     p = wl.p
     fd = wl.fd
     dev = wl.device
-    q_h = p.q.detach().cpu().pin_memory()
+    # newest token of every sequence: (page, row) in the paged pool, else position L_max - 1
     if wl.paged:
-        # newest token of every sequence: its row inside its last page
         lens = p.seq_lens.cpu().tolist()
         tgt = [(int(p.page_table[b, (L - 1) // 64]), (L - 1) % 64) for b, L in enumerate(lens) if L > 0]
-        k_rows = torch.stack([p.k_pages[pg, :, r] for pg, r in tgt]).cpu().pin_memory()
-        v_rows = torch.stack([p.v_pages[pg, :, r] for pg, r in tgt]).cpu().pin_memory()
+        pg = torch.tensor([t[0] for t in tgt], dtype=torch.long, device=dev)
+        rr = torch.tensor([t[1] for t in tgt], dtype=torch.long, device=dev)
+        k_rows, v_rows = p.k_pages[pg, :, rr], p.v_pages[pg, :, rr]  # [n, Hkv, d]
     else:
-        L = p.L_max
-        k_rows = p.k[:, :, L - 1].contiguous().cpu().pin_memory()
-        v_rows = p.v[:, :, L - 1].contiguous().cpu().pin_memory()
-        tgt = None
-    k_dev = torch.empty(k_rows.shape, dtype=k_rows.dtype, device=dev)
-    v_dev = torch.empty(v_rows.shape, dtype=v_rows.dtype, device=dev)
+        k_rows, v_rows = p.k[:, :, p.L_max - 1], p.v[:, :, p.L_max - 1]  # [B, Hkv, d]
+    n, H, dd = k_rows.shape
+    nq, nr = p.q.numel() * 2, k_rows.numel() * 2
+    host = torch.empty(nq + 2 * nr, dtype=torch.uint8).pin_memory()
+    host[:nq].view(torch.bfloat16).copy_(p.q.reshape(-1).cpu())
+    host[nq:nq + nr].view(torch.bfloat16).copy_(k_rows.reshape(-1).cpu())
+    host[nq + nr:].view(torch.bfloat16).copy_(v_rows.reshape(-1).cpu())
+    staged = torch.empty_like(host, device=dev)
+    q_d = staged[:nq].view(torch.bfloat16).view(p.q.shape)
+    k_d = staged[nq:nq + nr].view(torch.bfloat16).view(n, H, dd)
+    v_d = staged[nq + nr:].view(torch.bfloat16).view(n, H, dd)
+    kv_d = staged[nq:].view(torch.bfloat16).view(2 * n, H, 1, dd)  # K rows, then V rows, as one-token caches
+    result = torch.empty(wl.io.shape, dtype=torch.uint8).pin_memory()
+
     if wl.fp8 or wl.fp4:
-        # the new rows are encoded on the device (fd_quantize_kv_fp8/fp4) and written into the cache
-        if wl.paged:  # rows [n, Hkv, d] -> n * Hkv cache rows of one token
-            k_new = k_dev.view(-1, 1, 1, k_dev.shape[-1])
-            v_new = v_dev.view(-1, 1, 1, v_dev.shape[-1])
-        else:         # rows [B, Hkv, d] -> token L_max - 1 of every head
-            k_new = k_dev.view(k_dev.shape[0], k_dev.shape[1], 1, -1)
-            v_new = v_dev.view(v_dev.shape[0], v_dev.shape[1], 1, -1)
-        dd = k_new.shape[-1]
         if wl.fp8:
-            kc_new = torch.empty(k_new.shape, dtype=torch.uint8, device=dev)
-            vc_new = torch.empty(v_new.shape, dtype=torch.uint8, device=dev)
-            ks_new = torch.empty(k_new.shape[:3], dtype=torch.float32, device=dev)
-            vs_new = torch.empty(v_new.shape[:3], dtype=torch.float32, device=dev)
+            c_new = torch.empty((2 * n, H, 1, dd), dtype=torch.uint8, device=dev)
+            s_new = torch.empty((2 * n, H, 1), dtype=torch.float32, device=dev)
         else:
-            kc_new = torch.empty(k_new.shape[:3] + (dd // 2,), dtype=torch.uint8, device=dev)
-            vc_new = torch.empty(v_new.shape[:3] + (dd // 2,), dtype=torch.uint8, device=dev)
-            ks_new = torch.empty(k_new.shape[:3] + (dd // 32,), dtype=torch.uint8, device=dev)
-            vs_new = torch.empty(v_new.shape[:3] + (dd // 32,), dtype=torch.uint8, device=dev)
+            c_new = torch.empty((2 * n, H, 1, dd // 2), dtype=torch.uint8, device=dev)
+            s_new = torch.empty((2 * n, H, 1, dd // 32), dtype=torch.uint8, device=dev)
         encode = fd.fd_quantize_kv_fp8 if wl.fp8 else fd.fd_quantize_kv_fp4
-    out_h = torch.empty(wl.out.shape, dtype=wl.out.dtype).pin_memory()
-    lse_h = torch.empty(wl.lse.shape, dtype=wl.lse.dtype).pin_memory()
-    h2d = q_h.numel() * 2 + k_rows.numel() * 2 + v_rows.numel() * 2
-    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
+    elif wl.topdelta is not None:
+        k_one = staged[nq:nq + nr].view(torch.bfloat16).view(n, H, 1, dd)
+        enc_new = (torch.empty((n, H, 1, dd // 4), dtype=torch.uint8, device=dev),
+                   torch.empty((n, H, 1, dd // 32, 2), dtype=torch.float16, device=dev),
+                   torch.empty((n, H, 1, dd), dtype=torch.int8, device=dev),
+                   torch.empty((n, H, 1, dd // 32), dtype=torch.float16, device=dev))
+
+    def put(cache, rows):
+        """Write one row per (sequence, head) at the newest token's position."""
+        if wl.paged:
+            cache[pg, :, rr] = rows
+        else:
+            cache[:, :, p.L_max - 1] = rows
 
     def step():
-        p.q.copy_(q_h, non_blocking=True)
-        k_dev.copy_(k_rows, non_blocking=True)
-        v_dev.copy_(v_rows, non_blocking=True)
+        staged.copy_(host, non_blocking=True)
         if wl.fp8 or wl.fp4:
-            encode(k_new, codes=kc_new, scales=ks_new)
-            encode(v_new, codes=vc_new, scales=vs_new)
+            encode(kv_d, codes=c_new, scales=s_new)
             kc, ks, vc, vs = wl.kv8
-            if wl.paged:
-                H = k_dev.shape[1]
-                for i, (pg, r) in enumerate(tgt):
-                    kc[pg, :, r] = kc_new[i * H:(i + 1) * H, 0, 0]
-                    ks[pg, :, r] = ks_new[i * H:(i + 1) * H, 0, 0]
-                    vc[pg, :, r] = vc_new[i * H:(i + 1) * H, 0, 0]
-                    vs[pg, :, r] = vs_new[i * H:(i + 1) * H, 0, 0]
-            else:
-                kc[:, :, p.L_max - 1] = kc_new[:, :, 0]
-                ks[:, :, p.L_max - 1] = ks_new[:, :, 0]
-                vc[:, :, p.L_max - 1] = vc_new[:, :, 0]
-                vs[:, :, p.L_max - 1] = vs_new[:, :, 0]
+            put(kc, c_new[:n, :, 0])
+            put(ks, s_new[:n, :, 0])
+            put(vc, c_new[n:, :, 0])
+            put(vs, s_new[n:, :, 0])
+        elif wl.topdelta is not None:
+            fd.fd_quantize_keys(k_one, None, *enc_new)
+            for cache, row in zip(wl.qk, enc_new):
+                put(cache, row[:, :, 0])
+            put(p.v, v_d)
         elif wl.paged:
-            for i, (pg, r) in enumerate(tgt):
-                p.k_pages[pg, :, r] = k_dev[i]
-                p.v_pages[pg, :, r] = v_dev[i]
+            put(p.k_pages, k_d)
+            put(p.v_pages, v_d)
         else:
-            p.k[:, :, p.L_max - 1] = k_dev
-            p.v[:, :, p.L_max - 1] = v_dev
-        wl.call()
-        out_h.copy_(wl.out, non_blocking=True)
-        lse_h.copy_(wl.lse, non_blocking=True)
+            put(p.k, k_d)
+            put(p.v, v_d)
+        wl.call(q=q_d)
+        result.copy_(wl.io, non_blocking=True)
 
     for _ in range(warmup):
         step()
@@ -434,7 +441,7 @@ def time_e2e(wl, steps, warmup, dist_ctx):
     torch.cuda.synchronize()
     t1 = time.perf_counter()
     dist_ctx.barrier()
-    return dist_ctx.max((t1 - t0) * 1e3), h2d, d2h
+    return dist_ctx.max((t1 - t0) * 1e3), host.numel(), result.numel()
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -669,7 +676,9 @@ def main():
     if not args.no_e2e:
         e2e = {"value": n * B * e2e_steps / (ms_e2e / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-               "note": "per step: query + newest token's K/V rows host->device, out + lse device->host"}
+               "note": "per step: one host->device copy (query + newest token's K/V rows), the rows written "
+                       "into the cache in the form the decode reads (encoded for fp8/fp4/top-delta), the "
+                       "decode, one device->host copy (out + lse)"}
     cpu = None
     if ctx.rank == 0 and n == 1 and not args.no_cpu_baseline:
         sample = OracleSample(args.workload, args.seed, 1.0)
