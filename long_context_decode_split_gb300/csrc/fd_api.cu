@@ -142,6 +142,125 @@ Plan topdelta_plan(int B, int Hq, int Hkv, int L_max, int d, int requested) {
 
 int to_status(cudaError_t e) { return e == cudaSuccess ? FD_OK : FD_ERR_CUDA; }
 
+enum class Cache { BF16, FP8, FP4 };
+
+Plan cache_plan(Cache cache, int B, int Hq, int Hkv, int L_max, int d, int requested, bool ragged) {
+    switch (cache) {
+        case Cache::FP8: return fp8_plan(B, Hq, Hkv, L_max, d, requested, ragged);
+        case Cache::FP4: return fp4_plan(B, Hq, Hkv, L_max, d, requested, ragged);
+        default: return decode_plan(B, Hq, Hkv, L_max, d, requested, ragged);
+    }
+}
+
+// Chunks per sequence (negative status on bad arguments) and workspace bytes
+// (0 on bad arguments) of a dense or paged call over the given cache.
+int num_splits_for(Cache cache, int B, int Hq, int Hkv, int L_max, int d, int num_splits, int ragged) {
+    const int st = check_shape(B, Hq, Hkv, L_max, d);
+    if (st != FD_OK) return -st;
+    if (num_splits < 0) return -FD_ERR_INVALID_ARG;
+    return cache_plan(cache, B, Hq, Hkv, L_max, d, num_splits, ragged != 0).splits;
+}
+
+size_t workspace_for(Cache cache, int B, int Hq, int Hkv, int L_max, int d, int num_splits, int ragged) {
+    if (check_shape(B, Hq, Hkv, L_max, d) != FD_OK || num_splits < 0) return 0;
+    const Plan pl = cache_plan(cache, B, Hq, Hkv, L_max, d, num_splits, ragged != 0);
+    return fd::decode_workspace_bytes(B, Hq, d, pl.splits);
+}
+
+// Validates the arguments every decode entry point shares, plans the chunks
+// and enqueues the partial pass (+ merge) for the given cache.
+int decode_common(fd::DecodeArgs& a, int num_splits, bool ragged, int out_dtype, void* workspace,
+                  size_t workspace_bytes, void* stream, Cache cache) {
+    const bool quantized = cache != Cache::BF16;  // scale arrays required
+    if (out_dtype != FD_OUT_F32 && out_dtype != FD_OUT_BF16) return FD_ERR_INVALID_ARG;
+    if (num_splits < 0 || !std::isfinite(a.scale)) return FD_ERR_INVALID_ARG;
+    if (a.B > 0 && (!a.q || !a.k || !a.v || !a.out)) return FD_ERR_INVALID_ARG;
+    if (!aligned16(a.q) || !aligned16(a.k) || !aligned16(a.v) || !aligned16(a.out)) return FD_ERR_INVALID_ARG;
+    if (quantized && ((a.B > 0 && (!a.k_scales || !a.v_scales)) || !aligned16(a.k_scales) || !aligned16(a.v_scales)))
+        return FD_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(a.lse) & 3u) || (reinterpret_cast<uintptr_t>(a.seq_lens) & 3u))
+        return FD_ERR_INVALID_ARG;
+    // tile copies address cache rows with 32-bit coordinates
+    const long long cache_rows = a.page_table ? (long long)a.num_pages * a.Hkv * kTile
+                                              : (long long)a.B * a.Hkv * a.L_max;
+    if (cache_rows > 0x7fffffffLL) return FD_ERR_UNSUPPORTED;
+    const Plan pl = cache_plan(cache, a.B, a.Hq, a.Hkv, a.L_max, a.D, num_splits, ragged);
+    const size_t need = fd::decode_workspace_bytes(a.B, a.Hq, a.D, pl.splits);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return FD_ERR_WORKSPACE_TOO_SMALL;
+        if (!aligned16(workspace)) return FD_ERR_INVALID_ARG;
+    }
+    a.splits = pl.splits;
+    a.chunk_fixed = pl.chunk_fixed;
+    a.out_bf16 = out_dtype == FD_OUT_BF16;
+    float* ws = static_cast<float*>(workspace);
+    a.part_o = ws;
+    a.part_ml = ws ? ws + (size_t)a.B * a.Hq * pl.splits * a.D : nullptr;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return to_status(cache == Cache::FP8   ? fd::launch_decode_fp8(a, st)
+                     : cache == Cache::FP4 ? fd::launch_decode_fp4(a, st)
+                                           : fd::launch_decode(a, st));
+}
+
+// Contiguous cache [B, Hkv, L_max, ...]: K and V (codes for fp8/fp4) and, for
+// the quantized caches, their scale arrays.
+int dense_entry(Cache cache, const void* q, const void* k, const void* v, const void* k_scales,
+                const void* v_scales, const int32_t* seq_lens, int B, int Hq, int Hkv, int L_max, int d,
+                float scale, int num_splits, void* out, int out_dtype, float* lse, void* workspace,
+                size_t workspace_bytes, void* stream) {
+    const int st = check_shape(B, Hq, Hkv, L_max, d);
+    if (st != FD_OK) return st;
+    fd::DecodeArgs a = {};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.k_scales = k_scales;
+    a.v_scales = v_scales;
+    a.seq_lens = seq_lens;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.L_max = L_max;
+    a.D = d;
+    a.scale = scale;
+    a.out = out;
+    a.lse = lse;
+    return decode_common(a, num_splits, seq_lens != nullptr, out_dtype, workspace, workspace_bytes, stream, cache);
+}
+
+// Paged cache: pools [num_pages, Hkv, 64, ...] and a page table [B, max_pages].
+int paged_entry(Cache cache, const void* q, const void* k_pages, const void* v_pages, const void* k_scales,
+                const void* v_scales, const int32_t* page_table, int max_pages, int num_pages,
+                const int32_t* seq_lens, int page_size, int B, int Hq, int Hkv, int d, float scale, int num_splits,
+                void* out, int out_dtype, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+    if (page_size != kTile) return page_size > 0 ? FD_ERR_UNSUPPORTED : FD_ERR_INVALID_ARG;
+    if (max_pages <= 0 || num_pages < 0 || max_pages > (1 << 24)) return FD_ERR_INVALID_ARG;
+    const int L_max = max_pages * page_size;
+    const int st = check_shape(B, Hq, Hkv, L_max, d);
+    if (st != FD_OK) return st;
+    if (B > 0 && (!page_table || !seq_lens)) return FD_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(page_table) & 3u) return FD_ERR_INVALID_ARG;
+    fd::DecodeArgs a = {};
+    a.q = q;
+    a.k = k_pages;
+    a.v = v_pages;
+    a.k_scales = k_scales;
+    a.v_scales = v_scales;
+    a.seq_lens = seq_lens;
+    a.page_table = page_table;
+    a.max_pages = max_pages;
+    a.num_pages = num_pages;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.L_max = L_max;
+    a.D = d;
+    a.scale = scale;
+    a.out = out;
+    a.lse = lse;
+    return decode_common(a, num_splits, true, out_dtype, workspace, workspace_bytes, stream, cache);
+}
+
 }  // namespace
 
 extern "C" {
@@ -162,76 +281,19 @@ const char* fd_status_string(int status) {
 }
 
 int fd_num_splits(int B, int Hq, int Hkv, int L_max, int d, int num_splits, int ragged) {
-    const int st = check_shape(B, Hq, Hkv, L_max, d);
-    if (st != FD_OK) return -st;
-    if (num_splits < 0) return -FD_ERR_INVALID_ARG;
-    return decode_plan(B, Hq, Hkv, L_max, d, num_splits, ragged != 0).splits;
+    return num_splits_for(Cache::BF16, B, Hq, Hkv, L_max, d, num_splits, ragged);
 }
 
 size_t fd_decode_workspace_size(int B, int Hq, int Hkv, int L_max, int d, int num_splits, int ragged) {
-    if (check_shape(B, Hq, Hkv, L_max, d) != FD_OK || num_splits < 0) return 0;
-    const Plan pl = decode_plan(B, Hq, Hkv, L_max, d, num_splits, ragged != 0);
-    return fd::decode_workspace_bytes(B, Hq, d, pl.splits);
-}
-
-enum class Cache { BF16, FP8, FP4 };
-
-static int decode_common(fd::DecodeArgs& a, int num_splits, bool ragged, int out_dtype, void* workspace,
-                         size_t workspace_bytes, void* stream, Cache cache = Cache::BF16) {
-    const bool quantized = cache != Cache::BF16;  // scale arrays required
-    if (out_dtype != FD_OUT_F32 && out_dtype != FD_OUT_BF16) return FD_ERR_INVALID_ARG;
-    if (num_splits < 0 || !std::isfinite(a.scale)) return FD_ERR_INVALID_ARG;
-    if (a.B > 0 && (!a.q || !a.k || !a.v || !a.out)) return FD_ERR_INVALID_ARG;
-    if (!aligned16(a.q) || !aligned16(a.k) || !aligned16(a.v) || !aligned16(a.out)) return FD_ERR_INVALID_ARG;
-    if (quantized && ((a.B > 0 && (!a.k_scales || !a.v_scales)) || !aligned16(a.k_scales) || !aligned16(a.v_scales)))
-        return FD_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(a.lse) & 3u) || (reinterpret_cast<uintptr_t>(a.seq_lens) & 3u))
-        return FD_ERR_INVALID_ARG;
-    // tile copies address cache rows with 32-bit coordinates
-    const long long cache_rows = a.page_table ? (long long)a.num_pages * a.Hkv * kTile
-                                              : (long long)a.B * a.Hkv * a.L_max;
-    if (cache_rows > 0x7fffffffLL) return FD_ERR_UNSUPPORTED;
-    const Plan pl = cache == Cache::FP8 ? fp8_plan(a.B, a.Hq, a.Hkv, a.L_max, a.D, num_splits, ragged)
-                    : cache == Cache::FP4 ? fp4_plan(a.B, a.Hq, a.Hkv, a.L_max, a.D, num_splits, ragged)
-                                          : decode_plan(a.B, a.Hq, a.Hkv, a.L_max, a.D, num_splits, ragged);
-    const size_t need = fd::decode_workspace_bytes(a.B, a.Hq, a.D, pl.splits);
-    if (need > 0) {
-        if (!workspace || workspace_bytes < need) return FD_ERR_WORKSPACE_TOO_SMALL;
-        if (!aligned16(workspace)) return FD_ERR_INVALID_ARG;
-    }
-    a.splits = pl.splits;
-    a.chunk_fixed = pl.chunk_fixed;
-    a.out_bf16 = out_dtype == FD_OUT_BF16;
-    float* ws = static_cast<float*>(workspace);
-    a.part_o = ws;
-    a.part_ml = ws ? ws + (size_t)a.B * a.Hq * pl.splits * a.D : nullptr;
-    const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    return to_status(cache == Cache::FP8   ? fd::launch_decode_fp8(a, st)
-                     : cache == Cache::FP4 ? fd::launch_decode_fp4(a, st)
-                                           : fd::launch_decode(a, st));
+    return workspace_for(Cache::BF16, B, Hq, Hkv, L_max, d, num_splits, ragged);
 }
 
 int fd_decode_dense(const void* q, const void* k, const void* v, const int32_t* seq_lens,
                     int B, int Hq, int Hkv, int L_max, int d, float scale, int num_splits,
                     void* out, int out_dtype, float* lse,
                     void* workspace, size_t workspace_bytes, void* stream) {
-    const int st = check_shape(B, Hq, Hkv, L_max, d);
-    if (st != FD_OK) return st;
-    fd::DecodeArgs a = {};
-    a.q = q;
-    a.k = k;
-    a.v = v;
-    a.seq_lens = seq_lens;
-    a.page_table = nullptr;
-    a.B = B;
-    a.Hq = Hq;
-    a.Hkv = Hkv;
-    a.L_max = L_max;
-    a.D = d;
-    a.scale = scale;
-    a.out = out;
-    a.lse = lse;
-    return decode_common(a, num_splits, seq_lens != nullptr, out_dtype, workspace, workspace_bytes, stream);
+    return dense_entry(Cache::BF16, q, k, v, nullptr, nullptr, seq_lens, B, Hq, Hkv, L_max, d, scale, num_splits,
+                       out, out_dtype, lse, workspace, workspace_bytes, stream);
 }
 
 int fd_decode_paged(const void* q, const void* k_pages, const void* v_pages,
@@ -240,30 +302,9 @@ int fd_decode_paged(const void* q, const void* k_pages, const void* v_pages,
                     int B, int Hq, int Hkv, int d, float scale, int num_splits,
                     void* out, int out_dtype, float* lse,
                     void* workspace, size_t workspace_bytes, void* stream) {
-    if (page_size != kTile) return page_size > 0 ? FD_ERR_UNSUPPORTED : FD_ERR_INVALID_ARG;
-    if (max_pages <= 0 || num_pages < 0 || max_pages > (1 << 24)) return FD_ERR_INVALID_ARG;
-    const int L_max = max_pages * page_size;
-    const int st = check_shape(B, Hq, Hkv, L_max, d);
-    if (st != FD_OK) return st;
-    if (B > 0 && (!page_table || !seq_lens)) return FD_ERR_INVALID_ARG;
-    if (reinterpret_cast<uintptr_t>(page_table) & 3u) return FD_ERR_INVALID_ARG;
-    fd::DecodeArgs a = {};
-    a.q = q;
-    a.k = k_pages;
-    a.v = v_pages;
-    a.seq_lens = seq_lens;
-    a.page_table = page_table;
-    a.max_pages = max_pages;
-    a.num_pages = num_pages;
-    a.B = B;
-    a.Hq = Hq;
-    a.Hkv = Hkv;
-    a.L_max = L_max;
-    a.D = d;
-    a.scale = scale;
-    a.out = out;
-    a.lse = lse;
-    return decode_common(a, num_splits, true, out_dtype, workspace, workspace_bytes, stream);
+    return paged_entry(Cache::BF16, q, k_pages, v_pages, nullptr, nullptr, page_table, max_pages, num_pages,
+                       seq_lens, page_size, B, Hq, Hkv, d, scale, num_splits, out, out_dtype, lse, workspace,
+                       workspace_bytes, stream);
 }
 
 int fd_quantize_kv_fp8(const void* x, const int32_t* seq_lens, int B, int H, int L_max, int d,
@@ -278,42 +319,19 @@ int fd_quantize_kv_fp8(const void* x, const int32_t* seq_lens, int B, int H, int
 }
 
 int fd_num_splits_fp8(int B, int Hq, int Hkv, int L_max, int d, int num_splits, int ragged) {
-    const int st = check_shape(B, Hq, Hkv, L_max, d);
-    if (st != FD_OK) return -st;
-    if (num_splits < 0) return -FD_ERR_INVALID_ARG;
-    return fp8_plan(B, Hq, Hkv, L_max, d, num_splits, ragged != 0).splits;
+    return num_splits_for(Cache::FP8, B, Hq, Hkv, L_max, d, num_splits, ragged);
 }
 
 size_t fd_decode_fp8_workspace_size(int B, int Hq, int Hkv, int L_max, int d, int num_splits, int ragged) {
-    if (check_shape(B, Hq, Hkv, L_max, d) != FD_OK || num_splits < 0) return 0;
-    const Plan pl = fp8_plan(B, Hq, Hkv, L_max, d, num_splits, ragged != 0);
-    return fd::decode_workspace_bytes(B, Hq, d, pl.splits);
+    return workspace_for(Cache::FP8, B, Hq, Hkv, L_max, d, num_splits, ragged);
 }
 
 int fd_decode_dense_fp8(const void* q, const uint8_t* k_codes, const float* k_scales, const uint8_t* v_codes,
                         const float* v_scales, const int32_t* seq_lens, int B, int Hq, int Hkv, int L_max, int d,
                         float scale, int num_splits, void* out, int out_dtype, float* lse,
                         void* workspace, size_t workspace_bytes, void* stream) {
-    const int st = check_shape(B, Hq, Hkv, L_max, d);
-    if (st != FD_OK) return st;
-    fd::DecodeArgs a = {};
-    a.q = q;
-    a.k = k_codes;
-    a.v = v_codes;
-    a.k_scales = k_scales;
-    a.v_scales = v_scales;
-    a.seq_lens = seq_lens;
-    a.page_table = nullptr;
-    a.B = B;
-    a.Hq = Hq;
-    a.Hkv = Hkv;
-    a.L_max = L_max;
-    a.D = d;
-    a.scale = scale;
-    a.out = out;
-    a.lse = lse;
-    return decode_common(a, num_splits, seq_lens != nullptr, out_dtype, workspace, workspace_bytes, stream,
-                         Cache::FP8);
+    return dense_entry(Cache::FP8, q, k_codes, v_codes, k_scales, v_scales, seq_lens, B, Hq, Hkv, L_max, d, scale,
+                       num_splits, out, out_dtype, lse, workspace, workspace_bytes, stream);
 }
 
 int fd_decode_paged_fp8(const void* q, const uint8_t* k_pages, const float* k_page_scales, const uint8_t* v_pages,
@@ -321,32 +339,9 @@ int fd_decode_paged_fp8(const void* q, const uint8_t* k_pages, const float* k_pa
                         const int32_t* seq_lens, int page_size, int B, int Hq, int Hkv, int d, float scale,
                         int num_splits, void* out, int out_dtype, float* lse,
                         void* workspace, size_t workspace_bytes, void* stream) {
-    if (page_size != kTile) return page_size > 0 ? FD_ERR_UNSUPPORTED : FD_ERR_INVALID_ARG;
-    if (max_pages <= 0 || num_pages < 0 || max_pages > (1 << 24)) return FD_ERR_INVALID_ARG;
-    const int L_max = max_pages * page_size;
-    const int st = check_shape(B, Hq, Hkv, L_max, d);
-    if (st != FD_OK) return st;
-    if (B > 0 && (!page_table || !seq_lens)) return FD_ERR_INVALID_ARG;
-    if (reinterpret_cast<uintptr_t>(page_table) & 3u) return FD_ERR_INVALID_ARG;
-    fd::DecodeArgs a = {};
-    a.q = q;
-    a.k = k_pages;
-    a.v = v_pages;
-    a.k_scales = k_page_scales;
-    a.v_scales = v_page_scales;
-    a.seq_lens = seq_lens;
-    a.page_table = page_table;
-    a.max_pages = max_pages;
-    a.num_pages = num_pages;
-    a.B = B;
-    a.Hq = Hq;
-    a.Hkv = Hkv;
-    a.L_max = L_max;
-    a.D = d;
-    a.scale = scale;
-    a.out = out;
-    a.lse = lse;
-    return decode_common(a, num_splits, true, out_dtype, workspace, workspace_bytes, stream, Cache::FP8);
+    return paged_entry(Cache::FP8, q, k_pages, v_pages, k_page_scales, v_page_scales, page_table, max_pages,
+                       num_pages, seq_lens, page_size, B, Hq, Hkv, d, scale, num_splits, out, out_dtype, lse,
+                       workspace, workspace_bytes, stream);
 }
 
 int fd_quantize_kv_fp4(const void* x, const int32_t* seq_lens, int B, int H, int L_max, int d,
@@ -361,42 +356,19 @@ int fd_quantize_kv_fp4(const void* x, const int32_t* seq_lens, int B, int H, int
 }
 
 int fd_num_splits_fp4(int B, int Hq, int Hkv, int L_max, int d, int num_splits, int ragged) {
-    const int st = check_shape(B, Hq, Hkv, L_max, d);
-    if (st != FD_OK) return -st;
-    if (num_splits < 0) return -FD_ERR_INVALID_ARG;
-    return fp4_plan(B, Hq, Hkv, L_max, d, num_splits, ragged != 0).splits;
+    return num_splits_for(Cache::FP4, B, Hq, Hkv, L_max, d, num_splits, ragged);
 }
 
 size_t fd_decode_fp4_workspace_size(int B, int Hq, int Hkv, int L_max, int d, int num_splits, int ragged) {
-    if (check_shape(B, Hq, Hkv, L_max, d) != FD_OK || num_splits < 0) return 0;
-    const Plan pl = fp4_plan(B, Hq, Hkv, L_max, d, num_splits, ragged != 0);
-    return fd::decode_workspace_bytes(B, Hq, d, pl.splits);
+    return workspace_for(Cache::FP4, B, Hq, Hkv, L_max, d, num_splits, ragged);
 }
 
 int fd_decode_dense_fp4(const void* q, const uint8_t* k_codes, const uint8_t* k_scales, const uint8_t* v_codes,
                         const uint8_t* v_scales, const int32_t* seq_lens, int B, int Hq, int Hkv, int L_max, int d,
                         float scale, int num_splits, void* out, int out_dtype, float* lse,
                         void* workspace, size_t workspace_bytes, void* stream) {
-    const int st = check_shape(B, Hq, Hkv, L_max, d);
-    if (st != FD_OK) return st;
-    fd::DecodeArgs a = {};
-    a.q = q;
-    a.k = k_codes;
-    a.v = v_codes;
-    a.k_scales = k_scales;
-    a.v_scales = v_scales;
-    a.seq_lens = seq_lens;
-    a.page_table = nullptr;
-    a.B = B;
-    a.Hq = Hq;
-    a.Hkv = Hkv;
-    a.L_max = L_max;
-    a.D = d;
-    a.scale = scale;
-    a.out = out;
-    a.lse = lse;
-    return decode_common(a, num_splits, seq_lens != nullptr, out_dtype, workspace, workspace_bytes, stream,
-                         Cache::FP4);
+    return dense_entry(Cache::FP4, q, k_codes, v_codes, k_scales, v_scales, seq_lens, B, Hq, Hkv, L_max, d, scale,
+                       num_splits, out, out_dtype, lse, workspace, workspace_bytes, stream);
 }
 
 int fd_decode_paged_fp4(const void* q, const uint8_t* k_pages, const uint8_t* k_page_scales, const uint8_t* v_pages,
@@ -404,32 +376,9 @@ int fd_decode_paged_fp4(const void* q, const uint8_t* k_pages, const uint8_t* k_
                         const int32_t* seq_lens, int page_size, int B, int Hq, int Hkv, int d, float scale,
                         int num_splits, void* out, int out_dtype, float* lse,
                         void* workspace, size_t workspace_bytes, void* stream) {
-    if (page_size != kTile) return page_size > 0 ? FD_ERR_UNSUPPORTED : FD_ERR_INVALID_ARG;
-    if (max_pages <= 0 || num_pages < 0 || max_pages > (1 << 24)) return FD_ERR_INVALID_ARG;
-    const int L_max = max_pages * page_size;
-    const int st = check_shape(B, Hq, Hkv, L_max, d);
-    if (st != FD_OK) return st;
-    if (B > 0 && (!page_table || !seq_lens)) return FD_ERR_INVALID_ARG;
-    if (reinterpret_cast<uintptr_t>(page_table) & 3u) return FD_ERR_INVALID_ARG;
-    fd::DecodeArgs a = {};
-    a.q = q;
-    a.k = k_pages;
-    a.v = v_pages;
-    a.k_scales = k_page_scales;
-    a.v_scales = v_page_scales;
-    a.seq_lens = seq_lens;
-    a.page_table = page_table;
-    a.max_pages = max_pages;
-    a.num_pages = num_pages;
-    a.B = B;
-    a.Hq = Hq;
-    a.Hkv = Hkv;
-    a.L_max = L_max;
-    a.D = d;
-    a.scale = scale;
-    a.out = out;
-    a.lse = lse;
-    return decode_common(a, num_splits, true, out_dtype, workspace, workspace_bytes, stream, Cache::FP4);
+    return paged_entry(Cache::FP4, q, k_pages, v_pages, k_page_scales, v_page_scales, page_table, max_pages,
+                       num_pages, seq_lens, page_size, B, Hq, Hkv, d, scale, num_splits, out, out_dtype, lse,
+                       workspace, workspace_bytes, stream);
 }
 
 int fd_quantize_keys(const void* k, const int32_t* seq_lens, int B, int Hkv, int L_max, int d,
