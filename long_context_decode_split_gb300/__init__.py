@@ -328,63 +328,127 @@ def fd_decode_dense_noalloc(q, k, v, out, seq_lens=None, scale=None, num_splits=
     return out, lse
 
 
-def fd_quantize_kv_fp8(x, seq_lens=None, codes=None, scales=None, stream=None):
-    """fp8 cache encoder.  x [B,H,L_max,d] bf16 -> (codes uint8 [B,H,L_max,d],
-    scales float32 [B,H,L_max]).  Rows past seq_lens[b] are left as passed
-    (zero when this wrapper allocates them)."""
+# Quantized KV caches: code bytes per row and the scale entries per row, with their dtype.
+#   fp8: d codes (e4m3), one float32 scale per row
+#   fp4: d/2 codes (two e2m1 per byte), d/32 uint8 block exponents per row
+_QCACHE = {
+    "fp8": (lambda d: d, lambda d: (), torch.float32),
+    "fp4": (lambda d: d // 2, lambda d: (d // 32,), torch.uint8),
+}
+
+
+def _quantize_kv(kind, x, seq_lens, codes, scales, stream):
+    code_bytes, scale_shape, scale_dtype = _QCACHE[kind]
+    name = "fd_quantize_kv_" + kind
     lib = load()
     _check_cuda(x, "x", torch.bfloat16)
     _need(x.dim() == 4, "x must be [B, H, L_max, d]")
     B, H, L_max, d = x.shape
+    cshape, sshape = (B, H, L_max, code_bytes(d)), (B, H, L_max) + scale_shape(d)
     if codes is None:
-        codes = torch.zeros((B, H, L_max, d), dtype=torch.uint8, device=x.device)
+        codes = torch.zeros(cshape, dtype=torch.uint8, device=x.device)
     if scales is None:
-        scales = torch.zeros((B, H, L_max), dtype=torch.float32, device=x.device)
-    _check_cuda(codes, "codes", torch.uint8, (B, H, L_max, d))
-    _check_cuda(scales, "scales", torch.float32, (B, H, L_max))
+        scales = torch.zeros(sshape, dtype=scale_dtype, device=x.device)
+    _check_cuda(codes, "codes", torch.uint8, cshape)
+    _check_cuda(scales, "scales", scale_dtype, sshape)
     if seq_lens is not None:
         _check_cuda(seq_lens, "seq_lens", torch.int32, (B,))
-    st = lib.fd_quantize_kv_fp8(_p(x), _p(seq_lens), B, H, L_max, d, _p(codes), _p(scales), _stream(stream))
-    _raise(st, "fd_quantize_kv_fp8")
+    st = getattr(lib, name)(_p(x), _p(seq_lens), B, H, L_max, d, _p(codes), _p(scales), _stream(stream))
+    _raise(st, name)
     return codes, scales
 
 
-def fd_num_splits_fp8(B, Hq, Hkv, L_max, d, num_splits=0, ragged=False) -> int:
-    r = int(load().fd_num_splits_fp8(B, Hq, Hkv, L_max, d, num_splits, int(bool(ragged))))
+def _num_splits_q(kind, B, Hq, Hkv, L_max, d, num_splits, ragged):
+    name = "fd_num_splits_" + kind
+    r = int(getattr(load(), name)(B, Hq, Hkv, L_max, d, num_splits, int(bool(ragged))))
     if r < 0:
-        raise FdError(-r, "fd_num_splits_fp8")
+        raise FdError(-r, name)
     return r
 
 
+def _workspace_size_q(kind, B, Hq, Hkv, L_max, d, num_splits, ragged):
+    fn = getattr(load(), "fd_decode_%s_workspace_size" % kind)
+    return int(fn(B, Hq, Hkv, L_max, d, num_splits, int(bool(ragged))))
+
+
+def _decode_dense_q(kind, q, k_codes, k_scales, v_codes, v_scales, seq_lens, scale, num_splits, out, lse,
+                    out_dtype, want_lse, workspace, stream):
+    code_bytes, scale_shape, scale_dtype = _QCACHE[kind]
+    name = "fd_decode_dense_" + kind
+    lib = load()
+    _check_cuda(q, "q", torch.bfloat16)
+    B, Hq, d = q.shape
+    _check_cuda(k_codes, "k_codes", torch.uint8)
+    _need(k_codes.dim() == 4 and k_codes.shape[0] == B and k_codes.shape[3] == code_bytes(d),
+          "k_codes must be [B, Hkv, L_max, %s]" % ("d" if kind == "fp8" else "d/2"))
+    _, Hkv, L_max, _ = k_codes.shape
+    _check_cuda(v_codes, "v_codes", torch.uint8, k_codes.shape)
+    _check_cuda(k_scales, "k_scales", scale_dtype, (B, Hkv, L_max) + scale_shape(d))
+    _check_cuda(v_scales, "v_scales", scale_dtype, (B, Hkv, L_max) + scale_shape(d))
+    if seq_lens is not None:
+        _check_cuda(seq_lens, "seq_lens", torch.int32, (B,))
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    code, out, lse = _outputs(B, Hq, d, q.device, out, lse, out_dtype, want_lse)
+    need = _workspace_size_q(kind, B, Hq, Hkv, L_max, d, num_splits, seq_lens is not None)
+    ws = _workspace(need, q.device, workspace)
+    st = getattr(lib, name)(_p(q), _p(k_codes), _p(k_scales), _p(v_codes), _p(v_scales), _p(seq_lens),
+                            B, Hq, Hkv, L_max, d, scale, int(num_splits), _p(out), code, _p(lse), _p(ws),
+                            0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
+    _raise(st, name)
+    return out, lse
+
+
+def _decode_paged_q(kind, q, k_pages, k_page_scales, v_pages, v_page_scales, page_table, num_pages, seq_lens,
+                    scale, num_splits, out, lse, out_dtype, want_lse, workspace, stream):
+    code_bytes, scale_shape, scale_dtype = _QCACHE[kind]
+    name = "fd_decode_paged_" + kind
+    lib = load()
+    _check_cuda(q, "q", torch.bfloat16)
+    B, Hq, d = q.shape
+    _check_cuda(k_pages, "k_pages", torch.uint8)
+    _need(k_pages.dim() == 4 and k_pages.shape[3] == code_bytes(d),
+          "k_pages must be [P, Hkv, page, %s]" % ("d" if kind == "fp8" else "d/2"))
+    P, Hkv, page_size, _ = k_pages.shape
+    _check_cuda(v_pages, "v_pages", torch.uint8, k_pages.shape)
+    _check_cuda(k_page_scales, "k_page_scales", scale_dtype, (P, Hkv, page_size) + scale_shape(d))
+    _check_cuda(v_page_scales, "v_page_scales", scale_dtype, (P, Hkv, page_size) + scale_shape(d))
+    _check_cuda(page_table, "page_table", torch.int32)
+    _need(page_table.dim() == 2 and page_table.shape[0] == B, "page_table must be [B, max_pages]")
+    max_pages = page_table.shape[1]
+    _check_cuda(seq_lens, "seq_lens", torch.int32, (B,))
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    code, out, lse = _outputs(B, Hq, d, q.device, out, lse, out_dtype, want_lse)
+    need = _workspace_size_q(kind, B, Hq, Hkv, max_pages * page_size, d, num_splits, True)
+    ws = _workspace(need, q.device, workspace)
+    st = getattr(lib, name)(_p(q), _p(k_pages), _p(k_page_scales), _p(v_pages), _p(v_page_scales),
+                            _p(page_table), max_pages, int(num_pages), _p(seq_lens), page_size, B, Hq, Hkv,
+                            d, scale, int(num_splits), _p(out), code, _p(lse), _p(ws),
+                            0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
+    _raise(st, name)
+    return out, lse
+
+
+def fd_quantize_kv_fp8(x, seq_lens=None, codes=None, scales=None, stream=None):
+    """fp8 cache encoder.  x [B,H,L_max,d] bf16 -> (codes uint8 [B,H,L_max,d],
+    scales float32 [B,H,L_max]).  Rows past seq_lens[b] are left as passed
+    (zero when this wrapper allocates them)."""
+    return _quantize_kv("fp8", x, seq_lens, codes, scales, stream)
+
+
+def fd_num_splits_fp8(B, Hq, Hkv, L_max, d, num_splits=0, ragged=False) -> int:
+    return _num_splits_q("fp8", B, Hq, Hkv, L_max, d, num_splits, ragged)
+
+
 def fd_decode_fp8_workspace_size(B, Hq, Hkv, L_max, d, num_splits=0, ragged=False) -> int:
-    return int(load().fd_decode_fp8_workspace_size(B, Hq, Hkv, L_max, d, num_splits, int(bool(ragged))))
+    return _workspace_size_q("fp8", B, Hq, Hkv, L_max, d, num_splits, ragged)
 
 
 def fd_decode_dense_fp8(q, k_codes, k_scales, v_codes, v_scales, seq_lens=None, scale=None, num_splits=0,
                         out=None, lse=None, out_dtype="bf16", want_lse=True, workspace=None, stream=None):
     """Split-KV decode over an fp8 cache.  q [B,Hq,d] bf16; k_codes, v_codes
     [B,Hkv,L_max,d] uint8; k_scales, v_scales [B,Hkv,L_max] float32."""
-    lib = load()
-    _check_cuda(q, "q", torch.bfloat16)
-    B, Hq, d = q.shape
-    _check_cuda(k_codes, "k_codes", torch.uint8)
-    _need(k_codes.dim() == 4 and k_codes.shape[0] == B and k_codes.shape[3] == d,
-          "k_codes must be [B, Hkv, L_max, d]")
-    _, Hkv, L_max, _ = k_codes.shape
-    _check_cuda(v_codes, "v_codes", torch.uint8, k_codes.shape)
-    _check_cuda(k_scales, "k_scales", torch.float32, (B, Hkv, L_max))
-    _check_cuda(v_scales, "v_scales", torch.float32, (B, Hkv, L_max))
-    if seq_lens is not None:
-        _check_cuda(seq_lens, "seq_lens", torch.int32, (B,))
-    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    code, out, lse = _outputs(B, Hq, d, q.device, out, lse, out_dtype, want_lse)
-    need = fd_decode_fp8_workspace_size(B, Hq, Hkv, L_max, d, num_splits, seq_lens is not None)
-    ws = _workspace(need, q.device, workspace)
-    st = lib.fd_decode_dense_fp8(_p(q), _p(k_codes), _p(k_scales), _p(v_codes), _p(v_scales), _p(seq_lens),
-                                 B, Hq, Hkv, L_max, d, scale, int(num_splits), _p(out), code, _p(lse), _p(ws),
-                                 0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
-    _raise(st, "fd_decode_dense_fp8")
-    return out, lse
+    return _decode_dense_q("fp8", q, k_codes, k_scales, v_codes, v_scales, seq_lens, scale, num_splits, out, lse,
+                           out_dtype, want_lse, workspace, stream)
 
 
 def fd_decode_paged_fp8(q, k_pages, k_page_scales, v_pages, v_page_scales, page_table, num_pages, seq_lens,
@@ -392,88 +456,31 @@ def fd_decode_paged_fp8(q, k_pages, k_page_scales, v_pages, v_page_scales, page_
                         workspace=None, stream=None):
     """Paged split-KV decode over an fp8 cache.  k_pages/v_pages [P,Hkv,64,d]
     uint8, k_page_scales/v_page_scales [P,Hkv,64] float32."""
-    lib = load()
-    _check_cuda(q, "q", torch.bfloat16)
-    B, Hq, d = q.shape
-    _check_cuda(k_pages, "k_pages", torch.uint8)
-    _need(k_pages.dim() == 4 and k_pages.shape[3] == d, "k_pages must be [P, Hkv, page, d]")
-    P, Hkv, page_size, _ = k_pages.shape
-    _check_cuda(v_pages, "v_pages", torch.uint8, k_pages.shape)
-    _check_cuda(k_page_scales, "k_page_scales", torch.float32, (P, Hkv, page_size))
-    _check_cuda(v_page_scales, "v_page_scales", torch.float32, (P, Hkv, page_size))
-    _check_cuda(page_table, "page_table", torch.int32)
-    _need(page_table.dim() == 2 and page_table.shape[0] == B, "page_table must be [B, max_pages]")
-    max_pages = page_table.shape[1]
-    _check_cuda(seq_lens, "seq_lens", torch.int32, (B,))
-    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    code, out, lse = _outputs(B, Hq, d, q.device, out, lse, out_dtype, want_lse)
-    need = fd_decode_fp8_workspace_size(B, Hq, Hkv, max_pages * page_size, d, num_splits, True)
-    ws = _workspace(need, q.device, workspace)
-    st = lib.fd_decode_paged_fp8(_p(q), _p(k_pages), _p(k_page_scales), _p(v_pages), _p(v_page_scales),
-                                 _p(page_table), max_pages, int(num_pages), _p(seq_lens), page_size, B, Hq, Hkv,
-                                 d, scale, int(num_splits), _p(out), code, _p(lse), _p(ws),
-                                 0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
-    _raise(st, "fd_decode_paged_fp8")
-    return out, lse
+    return _decode_paged_q("fp8", q, k_pages, k_page_scales, v_pages, v_page_scales, page_table, num_pages,
+                           seq_lens, scale, num_splits, out, lse, out_dtype, want_lse, workspace, stream)
 
 
 def fd_quantize_kv_fp4(x, seq_lens=None, codes=None, scales=None, stream=None):
     """fp4 cache encoder.  x [B,H,L_max,d] bf16 -> (codes uint8 [B,H,L_max,d/2],
     scales uint8 [B,H,L_max,d/32]).  Rows past seq_lens[b] are left as passed
     (zero when this wrapper allocates them)."""
-    lib = load()
-    _check_cuda(x, "x", torch.bfloat16)
-    _need(x.dim() == 4, "x must be [B, H, L_max, d]")
-    B, H, L_max, d = x.shape
-    if codes is None:
-        codes = torch.zeros((B, H, L_max, d // 2), dtype=torch.uint8, device=x.device)
-    if scales is None:
-        scales = torch.zeros((B, H, L_max, d // 32), dtype=torch.uint8, device=x.device)
-    _check_cuda(codes, "codes", torch.uint8, (B, H, L_max, d // 2))
-    _check_cuda(scales, "scales", torch.uint8, (B, H, L_max, d // 32))
-    if seq_lens is not None:
-        _check_cuda(seq_lens, "seq_lens", torch.int32, (B,))
-    st = lib.fd_quantize_kv_fp4(_p(x), _p(seq_lens), B, H, L_max, d, _p(codes), _p(scales), _stream(stream))
-    _raise(st, "fd_quantize_kv_fp4")
-    return codes, scales
+    return _quantize_kv("fp4", x, seq_lens, codes, scales, stream)
 
 
 def fd_num_splits_fp4(B, Hq, Hkv, L_max, d, num_splits=0, ragged=False) -> int:
-    r = int(load().fd_num_splits_fp4(B, Hq, Hkv, L_max, d, num_splits, int(bool(ragged))))
-    if r < 0:
-        raise FdError(-r, "fd_num_splits_fp4")
-    return r
+    return _num_splits_q("fp4", B, Hq, Hkv, L_max, d, num_splits, ragged)
 
 
 def fd_decode_fp4_workspace_size(B, Hq, Hkv, L_max, d, num_splits=0, ragged=False) -> int:
-    return int(load().fd_decode_fp4_workspace_size(B, Hq, Hkv, L_max, d, num_splits, int(bool(ragged))))
+    return _workspace_size_q("fp4", B, Hq, Hkv, L_max, d, num_splits, ragged)
 
 
 def fd_decode_dense_fp4(q, k_codes, k_scales, v_codes, v_scales, seq_lens=None, scale=None, num_splits=0,
                         out=None, lse=None, out_dtype="bf16", want_lse=True, workspace=None, stream=None):
     """Split-KV decode over an fp4 cache.  q [B,Hq,d] bf16; k_codes, v_codes
     [B,Hkv,L_max,d/2] uint8; k_scales, v_scales [B,Hkv,L_max,d/32] uint8."""
-    lib = load()
-    _check_cuda(q, "q", torch.bfloat16)
-    B, Hq, d = q.shape
-    _check_cuda(k_codes, "k_codes", torch.uint8)
-    _need(k_codes.dim() == 4 and k_codes.shape[0] == B and k_codes.shape[3] * 2 == d,
-          "k_codes must be [B, Hkv, L_max, d/2]")
-    _, Hkv, L_max, _ = k_codes.shape
-    _check_cuda(v_codes, "v_codes", torch.uint8, k_codes.shape)
-    _check_cuda(k_scales, "k_scales", torch.uint8, (B, Hkv, L_max, d // 32))
-    _check_cuda(v_scales, "v_scales", torch.uint8, (B, Hkv, L_max, d // 32))
-    if seq_lens is not None:
-        _check_cuda(seq_lens, "seq_lens", torch.int32, (B,))
-    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    code, out, lse = _outputs(B, Hq, d, q.device, out, lse, out_dtype, want_lse)
-    need = fd_decode_fp4_workspace_size(B, Hq, Hkv, L_max, d, num_splits, seq_lens is not None)
-    ws = _workspace(need, q.device, workspace)
-    st = lib.fd_decode_dense_fp4(_p(q), _p(k_codes), _p(k_scales), _p(v_codes), _p(v_scales), _p(seq_lens),
-                                 B, Hq, Hkv, L_max, d, scale, int(num_splits), _p(out), code, _p(lse), _p(ws),
-                                 0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
-    _raise(st, "fd_decode_dense_fp4")
-    return out, lse
+    return _decode_dense_q("fp4", q, k_codes, k_scales, v_codes, v_scales, seq_lens, scale, num_splits, out, lse,
+                           out_dtype, want_lse, workspace, stream)
 
 
 def fd_decode_paged_fp4(q, k_pages, k_page_scales, v_pages, v_page_scales, page_table, num_pages, seq_lens,
@@ -481,29 +488,8 @@ def fd_decode_paged_fp4(q, k_pages, k_page_scales, v_pages, v_page_scales, page_
                         workspace=None, stream=None):
     """Paged split-KV decode over an fp4 cache.  k_pages/v_pages [P,Hkv,64,d/2]
     uint8, k_page_scales/v_page_scales [P,Hkv,64,d/32] uint8."""
-    lib = load()
-    _check_cuda(q, "q", torch.bfloat16)
-    B, Hq, d = q.shape
-    _check_cuda(k_pages, "k_pages", torch.uint8)
-    _need(k_pages.dim() == 4 and k_pages.shape[3] * 2 == d, "k_pages must be [P, Hkv, page, d/2]")
-    P, Hkv, page_size, _ = k_pages.shape
-    _check_cuda(v_pages, "v_pages", torch.uint8, k_pages.shape)
-    _check_cuda(k_page_scales, "k_page_scales", torch.uint8, (P, Hkv, page_size, d // 32))
-    _check_cuda(v_page_scales, "v_page_scales", torch.uint8, (P, Hkv, page_size, d // 32))
-    _check_cuda(page_table, "page_table", torch.int32)
-    _need(page_table.dim() == 2 and page_table.shape[0] == B, "page_table must be [B, max_pages]")
-    max_pages = page_table.shape[1]
-    _check_cuda(seq_lens, "seq_lens", torch.int32, (B,))
-    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    code, out, lse = _outputs(B, Hq, d, q.device, out, lse, out_dtype, want_lse)
-    need = fd_decode_fp4_workspace_size(B, Hq, Hkv, max_pages * page_size, d, num_splits, True)
-    ws = _workspace(need, q.device, workspace)
-    st = lib.fd_decode_paged_fp4(_p(q), _p(k_pages), _p(k_page_scales), _p(v_pages), _p(v_page_scales),
-                                 _p(page_table), max_pages, int(num_pages), _p(seq_lens), page_size, B, Hq, Hkv,
-                                 d, scale, int(num_splits), _p(out), code, _p(lse), _p(ws),
-                                 0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
-    _raise(st, "fd_decode_paged_fp4")
-    return out, lse
+    return _decode_paged_q("fp4", q, k_pages, k_page_scales, v_pages, v_page_scales, page_table, num_pages,
+                           seq_lens, scale, num_splits, out, lse, out_dtype, want_lse, workspace, stream)
 
 
 def fd_device_status(clear=True, stream=None) -> int:
