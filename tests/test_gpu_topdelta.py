@@ -170,6 +170,29 @@ def test_topdelta_infinite_delta_is_dense_over_dequantized_keys(fd, oracle):
     assert torch.all(cnt == 3000)
 
 
+def test_topdelta_deterministic_and_split_invariant(fd, oracle):
+    # the same inputs and chunk count give the same bits (selection bits and counts are
+    # order-free atomics, the arithmetic order is fixed); other chunk counts change the
+    # output only by fp32 rounding and leave the selection untouched
+    p = W.ffd(seed=9, B=2, L=6000, Hq=8, Hkv=2, d=128)
+    p = W.Problem(p.name, p.q.to(DEV), p.k.to(DEV), p.v.to(DEV), p.seq_lens.to(DEV), p.scale, p.L_max)
+    c, ms, r, rs = to_dev(oracle.quantize_keys(bits(p.k)))
+    runs = {}
+    for ns in (1, 3, 7, 0, 3):
+        runs.setdefault(ns, []).append(
+            fd.fd_decode_topdelta(p.q, c, ms, r, rs, p.v, None, p.scale, 5.0, num_splits=ns, out_dtype="f32",
+                                  want_selection=True))
+    a, b = runs[3]
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    out0, lse0, mask0, cnt0 = runs[1][0]
+    for ns in (3, 7, 0):
+        out, lse, mask, cnt = runs[ns][0]
+        assert torch.equal(mask, mask0) and torch.equal(cnt, cnt0)
+        assert (out - out0).abs().max().item() < 1e-5
+        assert (lse - lse0).abs().max().item() < 1e-5
+
+
 def crafted_dev(mn_values, d=64):
     """2-bit body constant mn_t on every channel (s16 = 0): with q = 1/d and
     scale 1 the 2-bit score is exactly mn_t."""
