@@ -14,18 +14,21 @@
 // warp 4 copies per 64-token tile one K and one V code box and two scale
 // boxes into a STAGES-deep ring; warps 0..3 each own 16 tokens of every tile.
 // Both products run on fp16 tensor cores (every e2m1 value is exact in fp16):
-//   S = Q K^T   one ldmatrix word per lane holds 8 channels of one block;
-//               each of its bytes widens (cvt.rn.f16x2.e2m1x2) to the B
-//               fragment of half a k-step, Q's channel order inside each
-//               block permuted alike; every block accumulates on its own and
-//               is scaled by 2^e_b of its token before the blocks are summed.
+//   S = K Q^T   the warp's 16 K rows are the A operand, the query group
+//               (up to 8 columns) the B operand; one ldmatrix word per lane
+//               holds 8 channels of one block of one row, each of its bytes
+//               widens (cvt.rn.f16x2.e2m1x2) to one A register, Q's channel
+//               order inside each block permuted alike; every block
+//               accumulates on its own and is scaled by 2^e_b of its token
+//               before the blocks are summed.
 //   O^T += V^T P^T
 //               the 16 output rows of tile j are 4 channels of 4 lane groups
 //               inside block j/2 (row gid + 8r of tile 2c + h is channel
 //               32c + 4*gid + 2h + r); the two token nibbles of a channel are
 //               interleaved into one byte and widened; P carries
 //               2^e_b(token) / s_ref, s_ref the largest V block scale the
-//               warp has seen, so each block has its own P operand.
+//               warp has seen, so each block has its own P operand, turned
+//               from the score layout into P^T fragments by movmatrix.
 #include <cmath>
 #include <cstdio>
 
@@ -166,7 +169,7 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
                    const Fp4Params p) {
     using Gm = F4Geo<D>;
     constexpr int CW = 4;
-    constexpr int NT = 1;                 // stages a consumer warp takes per step (two spill registers)
+    constexpr int NT = 2;                 // stages a consumer warp takes per step
     constexpr int CB = Gm::CB;
     constexpr int STAGE = 2 * CB;         // K tile + V tile
     constexpr int SSTAGE = 2 * kScaleSlot;
@@ -263,11 +266,13 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
 
     // ------------------------------ consumers ------------------------------
     const int gid = lane >> 2, tig = lane & 3, mi = lane >> 3;
-    // Q fragments of query gid, per block c: qa[c][0] = channels 32c + 8*tig
-    // + {0,1}, [1] = {2,3}, [2] = {4,5}, [3] = {6,7}, as fp16 times 2^-e (e the
-    // exponent of the query's largest |q|; exact).
+    // Q as the B fragment of S = K Q^T, query gid, per block c: qa[c][0] =
+    // channels 32c + 8*tig + {0,1}, [1] = {2,3}, [2] = {4,5}, [3] = {6,7}, as
+    // fp16 times 2^-e (e the exponent of the query's largest |q|; exact).  The
+    // accumulators hold rows (tokens) gid, gid + 8 and columns (queries)
+    // 2 tig, 2 tig + 1.
     uint32_t qa[NB][4];
-    float qmul;
+    float2 qmul;  // columns 2 tig, 2 tig + 1
     {
         const uint16_t* qrow = p.q + (size_t)(b * p.Hq + hq0 + gid) * D;
         float amax = 0.f;
@@ -295,7 +300,8 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
                 qa[c][i] = pack_f16(ldexpf(f.x, -ex), ldexpf(f.y, -ex));
             }
         }
-        qmul = ldexpf(p.scale_log2, ex);
+        const float qm = ldexpf(p.scale_log2, ex);  // query gid's; lane 4q holds query q
+        qmul = make_float2(__shfl_sync(0xffffffffu, qm, 8 * tig), __shfl_sync(0xffffffffu, qm, 8 * tig + 4));
     }
 
     float o[D / 16][4];
@@ -303,11 +309,13 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
     for (int mt = 0; mt < D / 16; ++mt)
 #pragma unroll
         for (int i = 0; i < 4; ++i) o[mt][i] = 0.f;
-    float m_run = -INFINITY, l_run = 0.f, vref = 0.f;
+    float2 m_run = make_float2(-INFINITY, -INFINITY), l_run = make_float2(0.f, 0.f);  // columns 2 tig, 2 tig + 1
+    float vref = 0.f;
     bool failed = false;
     const int ld_row = warp * 16 + 8 * (mi >> 1) + (lane & 7);  // row this lane addresses for ldmatrix
-    const int r0 = warp * 16 + 2 * tig;                         // tokens r0, r0+1, r0+8, r0+9 are this lane's
+    const int r0 = warp * 16 + 2 * tig;                         // V^T P^T: tokens r0, r0+1, r0+8, r0+9
     const int tok[4] = {r0, r0 + 1, r0 + 8, r0 + 9};
+    const int srow[2] = {warp * 16 + gid, warp * 16 + gid + 8};  // S = K Q^T: the lane's accumulator rows
 
     for (int t = 0; t < ntiles; t += NT) {
         int st[NT], rows[NT];
@@ -328,91 +336,97 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
         }
 
         // ---- scores, block by block, and the block scales of V ---------------
-        float sc[NT][4];
-        uint32_t ve[NT][4];  // V scale bytes of the lane's four tokens (0 for rows past the tile)
+        float sc[NT][4];     // rows gid, gid + 8 x columns 2 tig, 2 tig + 1
+        uint32_t ve[NT][2];  // V scale bytes of rows gid, gid + 8 (0 for rows past the tile)
 #pragma unroll
         for (int k = 0; k < NT; ++k) {
             const uint32_t kt = smem_u32(smem + st[k] * STAGE);
             const unsigned char* ksc = scl + st[k] * SSTAGE + stage_off[st[k]] * Gm::SB;
             const unsigned char* vsc = ksc + kScaleSlot;
-            uint32_t ke[4];  // the K scale bytes of the lane's four tokens
+            uint32_t ke[2];  // the K scale bytes of rows gid, gid + 8
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int r = 0; r < 2; ++r) {
                 if constexpr (NB == 4) {
-                    ke[i] = *reinterpret_cast<const uint32_t*>(ksc + 4 * tok[i]);
-                    ve[k][i] = *reinterpret_cast<const uint32_t*>(vsc + 4 * tok[i]);
+                    ke[r] = *reinterpret_cast<const uint32_t*>(ksc + 4 * srow[r]);
+                    ve[k][r] = *reinterpret_cast<const uint32_t*>(vsc + 4 * srow[r]);
                 } else {
-                    ke[i] = *reinterpret_cast<const uint16_t*>(ksc + 2 * tok[i]);
-                    ve[k][i] = *reinterpret_cast<const uint16_t*>(vsc + 2 * tok[i]);
+                    ke[r] = *reinterpret_cast<const uint16_t*>(ksc + 2 * srow[r]);
+                    ve[k][r] = *reinterpret_cast<const uint16_t*>(vsc + 2 * srow[r]);
                 }
             }
-            float s4[4] = {0.f, 0.f, 0.f, 0.f};
+            float2 s0 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);  // rows gid, gid + 8
 #pragma unroll
             for (int cp = 0; cp < NB / 2; ++cp) {
-                // (token block 0, block 2cp), (0, 2cp+1), (1, 2cp), (1, 2cp+1)
+                // (rows gid, block 2cp), (gid, 2cp+1), (gid + 8, 2cp), (gid + 8, 2cp+1)
                 uint32_t w[4];
                 ldsm_x4(kt + code4_off<D>(ld_row, 2 * cp + (mi & 1)), w[0], w[1], w[2], w[3]);
 #pragma unroll
                 for (int hb = 0; hb < 2; ++hb) {
                     const int c = 2 * cp + hb;
-                    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        uint32_t hf[4];
-                        e2m1x8_to_f16x8(w[2 * j + hb], hf);
-                        mma_f16(acc[j], qa[c][0], 0u, qa[c][1], 0u, hf[0], hf[1]);
-                        mma_f16(acc[j], qa[c][2], 0u, qa[c][3], 0u, hf[2], hf[3]);
-                    }
-                    const float a4[4] = {acc[0][0], acc[0][1], acc[1][0], acc[1][1]};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) s4[i] = fmaf(a4[i], scale_value((ke[i] >> (8 * c)) & 0xffu), s4[i]);
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                    uint32_t ha[4], hb8[4];
+                    e2m1x8_to_f16x8(w[hb], ha);       // row gid: channels 32c + 8 tig ..
+                    e2m1x8_to_f16x8(w[2 + hb], hb8);  // row gid + 8
+                    mma_f16(acc, ha[0], hb8[0], ha[1], hb8[1], qa[c][0], qa[c][1]);
+                    mma_f16(acc, ha[2], hb8[2], ha[3], hb8[3], qa[c][2], qa[c][3]);
+                    const float k0 = scale_value((ke[0] >> (8 * c)) & 0xffu);
+                    const float k1 = scale_value((ke[1] >> (8 * c)) & 0xffu);
+                    s0 = __ffma2_rn(make_float2(acc[0], acc[1]), make_float2(k0, k0), s0);
+                    s1 = __ffma2_rn(make_float2(acc[2], acc[3]), make_float2(k1, k1), s1);
                 }
             }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const bool ok = tok[i] < rows[k];
-                sc[k][i] = ok ? s4[i] * qmul : -INFINITY;
-                ve[k][i] = ok ? ve[k][i] : 0u;  // scale byte 0 decodes to 0
-            }
+            const bool ok0 = srow[0] < rows[k], ok1 = srow[1] < rows[k];
+            sc[k][0] = ok0 ? s0.x * qmul.x : -INFINITY;
+            sc[k][1] = ok0 ? s0.y * qmul.y : -INFINITY;
+            sc[k][2] = ok1 ? s1.x * qmul.x : -INFINITY;
+            sc[k][3] = ok1 ? s1.y * qmul.y : -INFINITY;
+            ve[k][0] = ok0 ? ve[k][0] : 0u;  // scale byte 0 decodes to 0
+            ve[k][1] = ok1 ? ve[k][1] : 0u;
         }
 
-        // ---- online softmax and the V reference scale ------------------------
-        float mx = -INFINITY;
+        // ---- online softmax per column and the V reference scale ---------------
+        float mx0 = -INFINITY, mx1 = -INFINITY;
         uint32_t emax = 0u;  // per-byte maximum of the V scale bytes (a larger byte is a larger scale)
 #pragma unroll
         for (int k = 0; k < NT; ++k) {
-            mx = fmaxf(mx, fmaxf(fmaxf(sc[k][0], sc[k][1]), fmaxf(sc[k][2], sc[k][3])));
-            emax = __vmaxu4(emax, __vmaxu4(__vmaxu4(ve[k][0], ve[k][1]), __vmaxu4(ve[k][2], ve[k][3])));
+            mx0 = fmaxf(mx0, fmaxf(sc[k][0], sc[k][2]));
+            mx1 = fmaxf(mx1, fmaxf(sc[k][1], sc[k][3]));
+            emax = __vmaxu4(emax, __vmaxu4(ve[k][0], ve[k][1]));
         }
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        emax = __vmaxu4(emax, __shfl_xor_sync(0xffffffffu, emax, 1));
-        emax = __vmaxu4(emax, __shfl_xor_sync(0xffffffffu, emax, 2));
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {  // over the 16 rows: the lanes of equal tig
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            emax = __vmaxu4(emax, __shfl_xor_sync(0xffffffffu, emax, off));
+        }
         emax = max(max(emax & 0xffu, (emax >> 8) & 0xffu), max((emax >> 16) & 0xffu, emax >> 24));
         const float vref_new = fmaxf(vref, scale_value(emax));
         const float vinv = vref_new > 0.f ? __fdividef(1.f, vref_new) : 0.f;
         const float vf = vref_new > 0.f ? vref * vinv : 1.f;
         vref = vref_new;
-        const float m_new = fmaxf(m_run, mx);
-        const bool none = m_new == -INFINITY;
-        const float alpha = none ? 1.f : exp2_approx(m_run - m_new);
-        m_run = m_new;
-        float lsum = 0.f;
-        float pr[NT][4];  // p / s_ref of the lane's tokens
+        const float m0 = fmaxf(m_run.x, mx0), m1 = fmaxf(m_run.y, mx1);
+        const bool none0 = m0 == -INFINITY, none1 = m1 == -INFINITY;
+        const float alpha0 = none0 ? 1.f : exp2_approx(m_run.x - m0);
+        const float alpha1 = none1 ? 1.f : exp2_approx(m_run.y - m1);
+        m_run = make_float2(m0, m1);
+        float lsum0 = 0.f, lsum1 = 0.f;
+        float pr[NT][4];  // p / s_ref, same layout as sc
 #pragma unroll
         for (int k = 0; k < NT; ++k) {
+            pr[k][0] = none0 ? 0.f : exp2_approx(sc[k][0] - m0);
+            pr[k][1] = none1 ? 0.f : exp2_approx(sc[k][1] - m1);
+            pr[k][2] = none0 ? 0.f : exp2_approx(sc[k][2] - m0);
+            pr[k][3] = none1 ? 0.f : exp2_approx(sc[k][3] - m1);
+            lsum0 += pr[k][0] + pr[k][2];
+            lsum1 += pr[k][1] + pr[k][3];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                pr[k][i] = none ? 0.f : exp2_approx(sc[k][i] - m_new);
-                lsum += pr[k][i];
-                pr[k][i] *= vinv;
-            }
+            for (int i = 0; i < 4; ++i) pr[k][i] *= vinv;
         }
-        l_run = l_run * alpha + lsum;
-        if (!__all_sync(0xffffffffu, alpha == 1.f && vf == 1.f)) {
-            // accumulator columns are queries 2*tig and 2*tig+1
-            const float a_even = __shfl_sync(0xffffffffu, alpha, 8 * tig) * vf;
-            const float a_odd = __shfl_sync(0xffffffffu, alpha, 8 * tig + 4) * vf;
+        l_run.x = l_run.x * alpha0 + lsum0;
+        l_run.y = l_run.y * alpha1 + lsum1;
+        if (!__all_sync(0xffffffffu, alpha0 == 1.f && alpha1 == 1.f && vf == 1.f)) {
+            // accumulator columns are the lane's own queries 2*tig and 2*tig+1
+            const float a_even = alpha0 * vf, a_odd = alpha1 * vf;
 #pragma unroll
             for (int mt = 0; mt < D / 16; ++mt) {
                 o[mt][0] *= a_even;
@@ -436,11 +450,12 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
                     w[i] = *reinterpret_cast<const uint16_t*>(vt + code4_off<D>(tok[i], c) + 2 * gid);
                     if (tail) w[i] = tok[i] < rows[k] ? w[i] : 0u;  // rows past the end may hold anything
                 }
-                // P^T of this stage for V block c: p * 2^e_c(token) / s_ref
-                float sv[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) sv[i] = pr[k][i] * scale_value((ve[k][i] >> (8 * c)) & 0xffu);
-                const uint32_t pb0 = pack_f16(sv[0], sv[1]), pb1 = pack_f16(sv[2], sv[3]);
+                // P^T of this stage for V block c: p * 2^e_c(token) / s_ref of rows gid and
+                // gid + 8, each 8x8 block transposed from the score layout
+                const float e0 = scale_value((ve[k][0] >> (8 * c)) & 0xffu);
+                const float e1 = scale_value((ve[k][1] >> (8 * c)) & 0xffu);
+                const uint32_t pb0 = movmatrix_trans(pack_f16(pr[k][0] * e0, pr[k][1] * e0));
+                const uint32_t pb1 = movmatrix_trans(pack_f16(pr[k][2] * e1, pr[k][3] * e1));
                 uint32_t x01[4], x89[4];
                 e2m1x8_to_f16x8(interleave_nibbles(w[0], w[1]), x01);
                 e2m1x8_to_f16x8(interleave_nibbles(w[2], w[3]), x89);
@@ -458,8 +473,11 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
     pdl_launch_dependents();
 
     // ---- combine the consumer warps and store --------------------------------
-    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {  // exp-sums over the 16 rows (the lanes of equal tig)
+        l_run.x += __shfl_xor_sync(0xffffffffu, l_run.x, off);
+        l_run.y += __shfl_xor_sync(0xffffffffu, l_run.y, off);
+    }
     named_barrier(1, CW * 32);  // every consumer is done with the stage ring
     float* red_o = reinterpret_cast<float*>(smem);  // [CW][8][D]
     float* red_m = red_o + CW * 8 * D;              // [CW][8]
@@ -475,9 +493,11 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
             *reinterpret_cast<float4*>(red_o + (warp * 8 + qi) * D + 32 * c + 4 * gid) = val;
         }
     }
-    if (tig == 0) {
-        red_m[warp * 8 + gid] = failed ? -INFINITY : m_run;
-        red_l[warp * 8 + gid] = failed ? 0.f : l_run;
+    if (gid == 0) {
+        red_m[warp * 8 + 2 * tig] = failed ? -INFINITY : m_run.x;
+        red_m[warp * 8 + 2 * tig + 1] = failed ? -INFINITY : m_run.y;
+        red_l[warp * 8 + 2 * tig] = failed ? 0.f : l_run.x;
+        red_l[warp * 8 + 2 * tig + 1] = failed ? 0.f : l_run.y;
     }
     named_barrier(1, CW * 32);
     store_combined<D, 8, CW>(smem, threadIdx.x, p.G, b * p.Hq + hq0, split, p.st);
