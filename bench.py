@@ -37,7 +37,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "decode-attention tokens/s and µs/call at 1 GB300; achieved HBM GB/s vs 8 TB/s"
-NORTH_STAR_HBM_GBS = 8000.0
+NOMINAL_HBM_GBS = 8000.0  # nominal GB300 HBM3e bandwidth, the denominator of frac_of_8tbs
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
 
@@ -703,7 +703,7 @@ def main():
             "us_per_call": per_call_s * 1e6,
             "kv_tokens_per_s": wl.kv_tokens * n / per_call_s,
             "achieved_hbm_gbs": achieved_gbs,
-            "frac_of_8tbs": achieved_gbs / NORTH_STAR_HBM_GBS,
+            "frac_of_8tbs": achieved_gbs / NOMINAL_HBM_GBS,
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak_gbs, "unit": "GB/s",
                          "frac": achieved_gbs / peak_gbs, "traffic": traffic, "peak_source": peak_src,
                          "kernel": "split partial pass + merge (whole call)",
