@@ -169,7 +169,8 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
                    const Fp4Params p) {
     using Gm = F4Geo<D>;
     constexpr int CW = 4;
-    constexpr int NT = 2;                 // stages a consumer warp takes per step
+    constexpr int NT = 3;                 // stages a consumer warp takes per step
+    static_assert(STAGES >= 2 * NT, "the producer needs stages to fill while NT are consumed");
     constexpr int CB = Gm::CB;
     constexpr int STAGE = 2 * CB;         // K tile + V tile
     constexpr int SSTAGE = 2 * kScaleSlot;
