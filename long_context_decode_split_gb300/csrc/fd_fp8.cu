@@ -139,8 +139,13 @@ __device__ __forceinline__ uint32_t code_off(int row, int ch) {
     else return swz64(row, ch);
 }
 
+// Resident CTAs per SM the partial pass is compiled for: 3 for the paged pool
+// (4 stages, 128 registers), 2 for the contiguous cache (6 stages).
+template <bool PAGED>
+constexpr int fp8_min_ctas() { return PAGED ? 3 : 2; }
+
 template <int D, int STAGES, int NT, bool PAGED>
-__global__ void __launch_bounds__(5 * 32, 2)
+__global__ void __launch_bounds__(5 * 32, fp8_min_ctas<PAGED>())
 fp8_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                    const __grid_constant__ CUtensorMap tmks, const __grid_constant__ CUtensorMap tmvs,
                    const Fp8Params p) {
@@ -480,8 +485,10 @@ fp8_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
 template <int D, bool PAGED>
 struct Fp8Launcher {
     // two stages per consumer step share the softmax bookkeeping and give each
-    // warp two independent MMA chains; six stages keep ~100 KiB per CTA in flight
-    static constexpr int STAGES = 6;
+    // warp two independent MMA chains.  Contiguous cache: six stages keep ~100
+    // KiB per CTA in flight at 2 CTAs/SM.  Paged pool (ragged batches, where
+    // more resident CTAs shorten the tail): four stages at 3 CTAs/SM.
+    static constexpr int STAGES = PAGED ? 4 : 6;
     static constexpr int NT = 2;  // stages a consumer warp takes per step
     static_assert(STAGES >= 2 * NT, "the producer needs stages to fill while NT are consumed");
     static constexpr int STAGE = 2 * 64 * D;
