@@ -11,8 +11,11 @@
 //     keep, for every query head of the GQA group, a running max m, exp-sum l
 //     and output accumulator o in registers (online softmax in base 2).  So
 //     every K/V byte is read from HBM once per KV head, whatever the group
-//     size.  Dot products run on packed fp32x2 FMAs; per-row partial sums are
-//     combined by a transposing butterfly (one shuffle per token per query).
+//     size.  For one query head (MHA) the dot products run on packed fp32x2
+//     FMAs and per-row partial sums are combined by a transposing butterfly
+//     (one shuffle per token); for a group of 2..8 they run on mma.sync as
+//     S = K Q^T (the warp's 16 tokens as M, the group as N) and O^T += V^T P^T
+//     with P^T formed by movmatrix.
 //   * at the end the consumer warps combine their states through shared
 //     memory and write either the final output (one chunk) or the chunk's
 //     (m_i, l_i, O_i / l_i) to the workspace.
@@ -63,30 +66,31 @@ struct PartialParams {
     StoreTarget st;
 };
 
-// Tensor-core consumer, one warp, 16 rows of a 64-token tile: S = Q K^T on
-// mma.sync (A = Q fragments in registers, B = K rows by ldmatrix from the
-// swizzled tile), then the shared online-softmax / P.V step.
+// Tensor-core consumer, one warp, 16 rows of a 64-token tile: S = K Q^T on
+// mma.sync (A = the warp's K rows by ldmatrix from the swizzled tile, B = Q
+// fragments in registers; accumulator rows gid, gid + 8 are tokens, columns
+// 2 tig, 2 tig + 1 query heads), then the shared online-softmax / P.V step.
 template <int D>
-__device__ __forceinline__ void mma_consume_tile(MmaWarpState<D>& ws, uint32_t ks, uint32_t vs, unsigned char* vgen,
-                                                 int warp, int lane, int rows, float scale_log2) {
-    const int tig = lane & 3;
+__device__ __forceinline__ void mma_consume_tile(TokAcc<D>& ac, const uint32_t (&qa0)[D / 16],
+                                                 const uint32_t (&qa2)[D / 16], uint32_t ks, uint32_t vs,
+                                                 unsigned char* vgen, int warp, int lane, int rows, float scale_log2) {
+    const int gid = lane >> 2;
     const int mi = lane >> 3;
-    const int ld_row = warp * 16 + 8 * (mi >> 1) + (lane & 7);  // row this lane addresses for ldmatrix
-    float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    const int a_row = warp * 16 + 8 * (mi & 1) + (lane & 7);  // K row this lane addresses (A fragment)
+    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-        uint32_t b00, b01, b10, b11;
-        ldsm_x4(ks + swz(ld_row, 2 * kk + (mi & 1)), b00, b01, b10, b11);
-        mma_bf16(sacc[0], ws.qa0[kk], 0u, ws.qa2[kk], 0u, b00, b01);
-        mma_bf16(sacc[1], ws.qa0[kk], 0u, ws.qa2[kk], 0u, b10, b11);
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(ks + swz(a_row, 2 * kk + (mi >> 1)), a0, a1, a2, a3);
+        mma_bf16(sacc, a0, a1, a2, a3, qa0[kk], qa2[kk]);
     }
-    const int r0 = warp * 16 + 2 * tig;
+    const int r0 = warp * 16 + gid;
     float sc[4];
-    sc[0] = r0 < rows ? sacc[0][0] * scale_log2 : -INFINITY;
-    sc[1] = r0 + 1 < rows ? sacc[0][1] * scale_log2 : -INFINITY;
-    sc[2] = r0 + 8 < rows ? sacc[1][0] * scale_log2 : -INFINITY;
-    sc[3] = r0 + 9 < rows ? sacc[1][1] * scale_log2 : -INFINITY;
-    mma_softmax_pv<D>(ws, sc, vs, vgen, warp, lane, rows);
+    sc[0] = r0 < rows ? sacc[0] * scale_log2 : -INFINITY;
+    sc[1] = r0 < rows ? sacc[1] * scale_log2 : -INFINITY;
+    sc[2] = r0 + 8 < rows ? sacc[2] * scale_log2 : -INFINITY;
+    sc[3] = r0 + 8 < rows ? sacc[3] * scale_log2 : -INFINITY;
+    mma_softmax_pv<D>(ac, sc, vs, vgen, warp, lane, rows);
 }
 
 template <int D, int GP, int CW, int STAGES, bool PAGED, bool MMA>
@@ -185,19 +189,15 @@ partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
     if constexpr (MMA) {
         // ------------------- tensor-core consumers (groups of 2..8) --------
         const int gid = lane >> 2, tig = lane & 3;
-        MmaWarpState<D> ws;
+        uint32_t qa0[D / 16], qa2[D / 16];  // B fragments of query gid
+        TokAcc<D> ac;
         const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + (size_t)(b * p.Hq + hq0 + gid) * D);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-            ws.qa0[kk] = gid < p.G ? qrow[8 * kk + tig] : 0u;
-            ws.qa2[kk] = gid < p.G ? qrow[8 * kk + 4 + tig] : 0u;
+            qa0[kk] = gid < p.G ? qrow[8 * kk + tig] : 0u;
+            qa2[kk] = gid < p.G ? qrow[8 * kk + 4 + tig] : 0u;
         }
-#pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) ws.o[mt][i] = 0.f;
-        ws.m_run = -INFINITY;
-        ws.l_run = 0.f;
+        tok_acc_init(ac);
         for (int t = 0; t < ntiles; ++t) {
             const int s = t % STAGES;
             if (!warp_wait(&full[s], (uint32_t)(t / STAGES) & 1u)) {
@@ -207,14 +207,13 @@ partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
             }
             const int rows = stage_rows[s];
             unsigned char* sk = smem + s * STAGE;
-            mma_consume_tile<D>(ws, smem_u32(sk), smem_u32(sk + BOXES * kBoxBytes), sk + BOXES * kBoxBytes, warp,
-                                lane, rows, p.scale_log2);
+            mma_consume_tile<D>(ac, qa0, qa2, smem_u32(sk), smem_u32(sk + BOXES * kBoxBytes), sk + BOXES * kBoxBytes,
+                                warp, lane, rows, p.scale_log2);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
         }
         pdl_launch_dependents();
-        combine_mma_warps_and_store<D, 8, CW>(smem, warp, lane, p.G, b * p.Hq + hq0, split, ws.m_run, ws.l_run,
-                                              ws.o, failed, p.st);
+        combine_tok_warps_and_store<D, CW>(smem, warp, lane, p.G, b * p.Hq + hq0, split, ac, failed, p.st);
         return;
     } else {
     // ------------------------ CUDA-core consumers --------------------------

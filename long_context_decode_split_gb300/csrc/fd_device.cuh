@@ -297,26 +297,38 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[N], int lane) {
 }
 
 
-// State of one tensor-core consumer warp (queries padded to 8; the warp
-// owns 16 rows of every 64-token tile).  gid = lane / 4 is the lane's query,
-// tig = lane % 4.
+// Attend state of one tensor-core consumer warp in the S = K Q^T layout: the
+// warp owns 16 token rows of every 64-token tile; lane (gid, tig) holds
+// accumulator rows gid, gid + 8 (tokens) and columns 2 tig, 2 tig + 1 (query
+// heads of the group, padded to 8).  O^T is D rows x 8 columns; m and l are
+// the running max (log2 units) and the lane's share of the exp-sum of its two
+// columns.
 template <int D>
-struct MmaWarpState {
-    uint32_t qa0[D / 16], qa2[D / 16];  // bf16 A fragments of Q (row gid), one pair per 16 dims
-    float o[D / 16][4];                 // O^T accumulators: [query 2*tig + (i&1)][dim 16*mt + gid + 8*(i>>1)]
-    float m_run, l_run;                 // query gid: running max (log2 units), per-lane exp-sum share
+struct TokAcc {
+    float o[D / 16][4];  // O^T: [column 2*tig + (i&1)][dim 16*mt + gid + 8*(i>>1)]
+    float2 m, l;
 };
 
-// Online softmax over one tile for the lane's query and O^T += V^T P^T.
-// sc[i] are the scores (log2 units; -inf = not attended) of the lane's rows
-// warp*16 + 2*tig + (i & 1) + 8*(i >> 1).  V rows at or past `rows` are
-// cleared first (they may hold anything; P is 0 there, but 0 * NaN is NaN).
-// P goes to the tensor cores as bf16 hi + lo, so the product keeps ~2^-16
-// relative accuracy; B = P^T comes straight from the lane's own scores.
 template <int D>
-__device__ __forceinline__ void mma_softmax_pv(MmaWarpState<D>& ws, const float (&sc)[4], uint32_t vs,
-                                               unsigned char* vgen, int warp, int lane, int rows) {
-    const int tig = lane & 3;
+__device__ __forceinline__ void tok_acc_init(TokAcc<D>& ac) {
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ac.o[mt][i] = 0.f;
+    ac.m = make_float2(-INFINITY, -INFINITY);
+    ac.l = make_float2(0.f, 0.f);
+}
+
+// Online softmax over one tile and O^T += V^T P^T for scores in the S = K Q^T
+// layout (sc[i]: row warp*16 + gid + 8*(i >> 1), column 2*tig + (i & 1), log2
+// units; -inf = not attended).  V rows at or past `rows` are cleared first
+// (they may hold anything; P is 0 there, but 0 * NaN is NaN).  P goes to the
+// tensor cores as bf16 hi + lo (~2^-16 relative accuracy); movmatrix turns
+// each 8x8 block of the lane's P values into the B fragment of P^T.  The V
+// tile is stored as 64-row x 128-byte swizzled boxes.
+template <int D>
+__device__ __forceinline__ void mma_softmax_pv(TokAcc<D>& ac, const float (&sc)[4], uint32_t vs, unsigned char* vgen,
+                                               int warp, int lane, int rows) {
     const int mi = lane >> 3;
     const int ld_row = warp * 16 + 8 * (mi >> 1) + (lane & 7);
     if (warp * 16 + 16 > rows) {
@@ -328,39 +340,48 @@ __device__ __forceinline__ void mma_softmax_pv(MmaWarpState<D>& ws, const float 
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
     }
-    float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const float m_new = fmaxf(ws.m_run, mx);
-    const bool none = m_new == -INFINITY;
-    const float alpha = none ? 1.f : exp2_approx(ws.m_run - m_new);
-    float pr[4];
+    // per column: max over the 16 rows (the lanes of equal tig)
+    float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) pr[i] = none ? 0.f : exp2_approx(sc[i] - m_new);
-    ws.m_run = m_new;
-    ws.l_run = ws.l_run * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
+    for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float m0 = fmaxf(ac.m.x, mx0), m1 = fmaxf(ac.m.y, mx1);
+    const bool none0 = m0 == -INFINITY, none1 = m1 == -INFINITY;
+    const float a0 = none0 ? 1.f : exp2_approx(ac.m.x - m0);
+    const float a1 = none1 ? 1.f : exp2_approx(ac.m.y - m1);
+    float pr[4];
+    pr[0] = none0 ? 0.f : exp2_approx(sc[0] - m0);
+    pr[1] = none1 ? 0.f : exp2_approx(sc[1] - m1);
+    pr[2] = none0 ? 0.f : exp2_approx(sc[2] - m0);
+    pr[3] = none1 ? 0.f : exp2_approx(sc[3] - m1);
+    ac.m = make_float2(m0, m1);
+    ac.l.x = ac.l.x * a0 + (pr[0] + pr[2]);
+    ac.l.y = ac.l.y * a1 + (pr[1] + pr[3]);
     uint32_t h0, l0, h1, l1;
-    split_bf16(pr[0], pr[1], h0, l0);
-    split_bf16(pr[2], pr[3], h1, l1);
-    // rescale only when some query's max moved (accumulator columns are
-    // queries 2*tig and 2*tig+1)
-    if (!__all_sync(0xffffffffu, alpha == 1.f)) {
-        const float a_even = __shfl_sync(0xffffffffu, alpha, 8 * tig);
-        const float a_odd = __shfl_sync(0xffffffffu, alpha, 8 * tig + 4);
+    split_bf16(pr[0], pr[1], h0, l0);  // row gid
+    split_bf16(pr[2], pr[3], h1, l1);  // row gid + 8
+    h0 = movmatrix_trans(h0);
+    l0 = movmatrix_trans(l0);
+    h1 = movmatrix_trans(h1);
+    l1 = movmatrix_trans(l1);
+    // rescale only when some column's max moved (the lane holds its own columns' factors)
+    if (!__all_sync(0xffffffffu, a0 == 1.f && a1 == 1.f)) {
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt) {
-            ws.o[mt][0] *= a_even;
-            ws.o[mt][1] *= a_odd;
-            ws.o[mt][2] *= a_even;
-            ws.o[mt][3] *= a_odd;
+            ac.o[mt][0] *= a0;
+            ac.o[mt][1] *= a1;
+            ac.o[mt][2] *= a0;
+            ac.o[mt][3] *= a1;
         }
     }
 #pragma unroll
     for (int mt = 0; mt < D / 16; ++mt) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4_t(vs + swz(ld_row, 2 * mt + (mi & 1)), a0, a1, a2, a3);
-        mma_bf16(ws.o[mt], a0, a1, a2, a3, h0, h1);
-        mma_bf16(ws.o[mt], a0, a1, a2, a3, l0, l1);
+        uint32_t v0, v1, v2, v3;
+        ldsm_x4_t(vs + swz(ld_row, 2 * mt + (mi & 1)), v0, v1, v2, v3);
+        mma_bf16(ac.o[mt], v0, v1, v2, v3, h0, h1);
+        mma_bf16(ac.o[mt], v0, v1, v2, v3, l0, l1);
     }
 }
 
@@ -499,6 +520,27 @@ __device__ __forceinline__ void combine_mma_warps_and_store(unsigned char* smem,
     }
     named_barrier(1, CW * 32);
     store_combined<D, GP, CW>(smem, warp * 32 + lane, G, row0, split, st);
+}
+
+// The end of a TokAcc consumer: exp-sums over the warp's 16 rows, (m, l) of
+// query gid moved to the lane layout combine_mma_warps_and_store expects
+// (query gid's values from lane gid / 2, column gid & 1; l only in the
+// quad's first lane, the combine sums l over the quad), then the combine.
+template <int D, int CW>
+__device__ __forceinline__ void combine_tok_warps_and_store(unsigned char* smem, int warp, int lane, int G, int row0,
+                                                            int split, TokAcc<D>& ac, bool failed,
+                                                            const StoreTarget& st) {
+    const int gid = lane >> 2, tig = lane & 3;
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        ac.l.x += __shfl_xor_sync(0xffffffffu, ac.l.x, off);
+        ac.l.y += __shfl_xor_sync(0xffffffffu, ac.l.y, off);
+    }
+    const float me = __shfl_sync(0xffffffffu, ac.m.x, gid >> 1), mo = __shfl_sync(0xffffffffu, ac.m.y, gid >> 1);
+    const float le = __shfl_sync(0xffffffffu, ac.l.x, gid >> 1), lo = __shfl_sync(0xffffffffu, ac.l.y, gid >> 1);
+    const float m_q = (gid & 1) ? mo : me;
+    const float l_q = tig == 0 ? ((gid & 1) ? lo : le) : 0.f;
+    combine_mma_warps_and_store<D, 8, CW>(smem, warp, lane, G, row0, split, m_q, l_q, ac.o, failed, st);
 }
 
 }  // namespace fd

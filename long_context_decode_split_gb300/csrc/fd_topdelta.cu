@@ -332,80 +332,6 @@ __device__ __forceinline__ void residual_tile(uint32_t res_s, const unsigned cha
     rt[3] = v1.y;
 }
 
-// Attend state of one warp: O^T (D rows x 8 query columns, the lane holds
-// columns 2 tig and 2 tig + 1), and per column the running max (log2 units)
-// and the lane's share of the exp-sum.
-template <int D>
-struct TDAcc {
-    float o[D / 16][4];
-    float2 m, l;
-};
-
-// Online softmax over one tile and O^T += V^T P^T for scores in the
-// transposed layout (sc[i]: row warp*16 + gid + 8*(i >> 1), query
-// 2*tig + (i & 1); -inf = not attended).  V rows at or past `rows` are
-// cleared first (P is 0 there, but 0 * NaN is NaN).  P goes to the tensor
-// cores as bf16 hi + lo; movmatrix turns each 8x8 block of the lane's P
-// values into the B fragment of P^T.
-template <int D>
-__device__ __forceinline__ void softmax_pv_t(TDAcc<D>& ac, const float (&sc)[4], uint32_t vs, unsigned char* vgen,
-                                             int warp, int lane, int rows) {
-    const int mi = lane >> 3;
-    const int ld_row = warp * 16 + 8 * (mi >> 1) + (lane & 7);
-    if (warp * 16 + 16 > rows) {
-        for (int i = lane; i < 16 * (D / 8); i += 32) {
-            const int r = warp * 16 + i / (D / 8);
-            if (r >= rows) *reinterpret_cast<uint4*>(vgen + swz(r, i % (D / 8))) = make_uint4(0u, 0u, 0u, 0u);
-        }
-        // order these generic stores before the tile copy that later refills the stage
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-    }
-    // per query: max over the 16 rows (the lanes of equal tig)
-    float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-    }
-    const float m0 = fmaxf(ac.m.x, mx0), m1 = fmaxf(ac.m.y, mx1);
-    const bool none0 = m0 == -INFINITY, none1 = m1 == -INFINITY;
-    const float a0 = none0 ? 1.f : exp2_approx(ac.m.x - m0);
-    const float a1 = none1 ? 1.f : exp2_approx(ac.m.y - m1);
-    float pr[4];
-    pr[0] = none0 ? 0.f : exp2_approx(sc[0] - m0);
-    pr[1] = none1 ? 0.f : exp2_approx(sc[1] - m1);
-    pr[2] = none0 ? 0.f : exp2_approx(sc[2] - m0);
-    pr[3] = none1 ? 0.f : exp2_approx(sc[3] - m1);
-    ac.m = make_float2(m0, m1);
-    ac.l.x = ac.l.x * a0 + (pr[0] + pr[2]);
-    ac.l.y = ac.l.y * a1 + (pr[1] + pr[3]);
-    uint32_t h0, l0, h1, l1;
-    split_bf16(pr[0], pr[1], h0, l0);  // row gid
-    split_bf16(pr[2], pr[3], h1, l1);  // row gid + 8
-    h0 = movmatrix_trans(h0);
-    l0 = movmatrix_trans(l0);
-    h1 = movmatrix_trans(h1);
-    l1 = movmatrix_trans(l1);
-    // rescale only when some query's max moved
-    if (!__all_sync(0xffffffffu, a0 == 1.f && a1 == 1.f)) {
-#pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt) {
-            ac.o[mt][0] *= a0;
-            ac.o[mt][1] *= a1;
-            ac.o[mt][2] *= a0;
-            ac.o[mt][3] *= a1;
-        }
-    }
-#pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt) {
-        uint32_t v0, v1, v2, v3;
-        ldsm_x4_t(vs + swz(ld_row, 2 * mt + (mi & 1)), v0, v1, v2, v3);
-        mma_bf16(ac.o[mt], v0, v1, v2, v3, h0, h1);
-        mma_bf16(ac.o[mt], v0, v1, v2, v3, l0, l1);
-    }
-}
-
 template <int D>
 __global__ void __launch_bounds__((CW + 1) * 32, 2)
 topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant__ CUtensorMap tm_v,
@@ -530,7 +456,7 @@ topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constan
     const bool q_real = gid < p.G;                                // the lane's B-fragment query
     const bool c_real[2] = {2 * tig < p.G, 2 * tig + 1 < p.G};    // its accumulator columns' queries
     TDQuery<D> tq;
-    TDAcc<D> ac;
+    TokAcc<D> ac;
     {
         const uint16_t* qrow = p.q + (size_t)(b * p.Hq + hq0 + gid) * D;
         auto qf = [&](int c) { return q_real ? __uint_as_float((uint32_t)qrow[c] << 16) : 0.f; };
@@ -567,12 +493,7 @@ topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constan
         }
         const float ssc = ldexpf(p.scale, 7 - sq);
         tq.scan_scale = make_float2(__shfl_sync(0xffffffffu, ssc, 8 * tig), __shfl_sync(0xffffffffu, ssc, 8 * tig + 4));
-#pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) ac.o[mt][i] = 0.f;
-        ac.m = make_float2(-INFINITY, -INFINITY);
-        ac.l = make_float2(0.f, 0.f);
+        tok_acc_init(ac);
     }
 
     // ---------------- anchor pass: pseudo-max per query head --------------------
@@ -704,7 +625,7 @@ topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constan
                     }
                 }
             }
-            softmax_pv_t<D>(ac, sc, smem_u32(st_base + Gm::RES_BYTES), st_base + Gm::RES_BYTES, warp, lane, rows);
+            mma_softmax_pv<D>(ac, sc, smem_u32(st_base + Gm::RES_BYTES), st_base + Gm::RES_BYTES, warp, lane, rows);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&det_empty[ds]);
@@ -712,25 +633,17 @@ topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constan
     if (failed) atomicOr(&g_status_topdelta, kStatusTimeout);
     pdl_launch_dependents();
 
-    // per column: counts and exp-sums over the 16 rows (lanes of equal tig)
+    // per column: selected counts over the 16 rows (lanes of equal tig)
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
         cnt[0] += __shfl_xor_sync(0xffffffffu, cnt[0], o);
         cnt[1] += __shfl_xor_sync(0xffffffffu, cnt[1], o);
-        ac.l.x += __shfl_xor_sync(0xffffffffu, ac.l.x, o);
-        ac.l.y += __shfl_xor_sync(0xffffffffu, ac.l.y, o);
     }
     if (p.sel_count && gid == 0) {
         if (c_real[0] && cnt[0]) atomicAdd(&p.sel_count[b * p.Hq + hq0 + 2 * tig], cnt[0]);
         if (c_real[1] && cnt[1]) atomicAdd(&p.sel_count[b * p.Hq + hq0 + 2 * tig + 1], cnt[1]);
     }
-    // (m, l) of query gid from lane gid / 2, column gid & 1; the combine sums l over the quad
-    const float me = __shfl_sync(0xffffffffu, ac.m.x, gid >> 1), mo = __shfl_sync(0xffffffffu, ac.m.y, gid >> 1);
-    const float le = __shfl_sync(0xffffffffu, ac.l.x, gid >> 1), lo = __shfl_sync(0xffffffffu, ac.l.y, gid >> 1);
-    const float m_q = (gid & 1) ? mo : me;
-    const float l_q = tig == 0 ? ((gid & 1) ? lo : le) : 0.f;
-    combine_mma_warps_and_store<D, 8, CW>(smem, warp, lane, p.G, b * p.Hq + hq0, split, m_q, l_q, ac.o, failed,
-                                          p.st);
+    combine_tok_warps_and_store<D, CW>(smem, warp, lane, p.G, b * p.Hq + hq0, split, ac, failed, p.st);
 }
 
 template <int D>
