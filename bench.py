@@ -5,12 +5,17 @@ workload uses: split planning, the per-chunk partial pass, the merge; for the
 sparse workloads the fused 2-bit scan / top-delta / residual / attention pass)
 over one batch of synthetic inputs already resident in HBM.
 
-Default workload: MHA decode, B=1, Hq=Hkv=32, d=128, L=32768, bf16 KV cache
-(512 MiB of K+V per call, larger than the 129 MB L2, so no flush is needed
-between calls).  Other workloads: --workload tiny|mha32k|gqa_paged|million|
-ffd_dense|ffd_topdelta5|ffd_topdelta7, and mha32k_fp8|million_fp8|ffd_dense_fp8|
-gqa_paged_fp8 (the same caches in the fp8 e4m3 encoding, per-row f32 scales) and
-the *_fp4 variants (e2m1 codes with power-of-two scales per 32 channels).
+Default workload: million-token decode, B=1, Hq=32, Hkv=8, d=128,
+L=1048576, bf16 KV cache with attention sinks (4 GiB of K+V per call, larger
+than the 129 MB L2, so no flush is needed between calls), the largest of the
+workloads that fits one GPU.  Its JSON line also carries `ffd_compare`: the
+dense pass and the top-delta pass at delta 5 and 7 timed in the same process
+on the same FFD cache (B=4, Hq=32, Hkv=8, d=128, L=131072), interleaved, each
+arm --steps calls after --warmup calls per round.  Other workloads:
+--workload tiny|mha32k|gqa_paged|million|ffd_dense|ffd_topdelta5|
+ffd_topdelta7, and mha32k_fp8|million_fp8|ffd_dense_fp8|gqa_paged_fp8 (the same
+caches in the fp8 e4m3 encoding, per-row f32 scales) and the *_fp4 variants
+(e2m1 codes with power-of-two scales per 32 channels).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fd|reference]
 
@@ -39,7 +44,6 @@ if ROOT not in sys.path:
 METRIC = "decode-attention tokens/s and µs/call at 1 GB300; achieved HBM GB/s vs 8 TB/s"
 NOMINAL_HBM_GBS = 8000.0  # nominal GB300 HBM3e bandwidth, the denominator of frac_of_8tbs
 FALLBACK_HBM_GBS = 6800.0
-L2_BYTES = 129 * 1024 * 1024
 
 DEFAULT_STEPS = {"tiny": 20000, "mha32k": 20000, "gqa_paged": 3000, "million": 3000,
                  "ffd_dense": 4000, "ffd_topdelta5": 4000, "ffd_topdelta7": 4000,
@@ -133,7 +137,10 @@ class ClockSampler:
 class Workload:
     """Resident inputs plus a `call()` that runs one decode through the C ABI."""
 
-    def __init__(self, name, seed, device, batch=None, seq_len=None, num_splits=None, n_sink=4, window=64):
+    def __init__(self, name, seed, device, batch=None, seq_len=None, num_splits=None, n_sink=4, window=64,
+                 problem=None, encoded_keys=None):
+        """`problem` (and, for top-delta, `encoded_keys`) reuse another
+        workload's resident inputs instead of generating them again."""
         import torch
 
         import long_context_decode_split_gb300 as fd
@@ -151,7 +158,11 @@ class Workload:
         over = {}
         if seq_len is not None:
             over["L"] = seq_len
-        if name == "tiny":
+        if problem is not None:
+            p = problem
+            if name.startswith("ffd_top"):
+                self.topdelta = 5.0 if name.endswith("5") else 7.0
+        elif name == "tiny":
             p = W.tiny(seed=seed, device=device)
         elif name == "mha32k":
             p = W.mha32k(seed=seed, device=device, **over)
@@ -170,7 +181,7 @@ class Workload:
                 self.topdelta = 5.0 if name.endswith("5") else 7.0
         else:
             raise ValueError(name)
-        if num_splits is not None:
+        if num_splits is not None and problem is None:
             p.num_splits = num_splits
         self.p = p
         self.paged = p.paged
@@ -199,7 +210,7 @@ class Workload:
                 need = fd.fd_decode_fp4_workspace_size(B, Hq, Hkv, p.L_max, d, p.num_splits, self.paged)
                 self.splits = fd.fd_num_splits_fp4(B, Hq, Hkv, p.L_max, d, p.num_splits, self.paged)
         elif self.topdelta is not None:
-            self.qk = fd.fd_quantize_keys(p.k, p.seq_lens)
+            self.qk = encoded_keys if encoded_keys is not None else fd.fd_quantize_keys(p.k, p.seq_lens)
             need = fd.fd_topdelta_workspace_size(B, Hq, Hkv, p.L_max, d, p.num_splits)
             self.splits = None
             self.sel_stats = self._selection_stats()
@@ -289,18 +300,48 @@ class Workload:
         detail = union * (d + (d // 32) * 2 + d * 2)
         return scan + detail + io
 
-    def config(self):
+    def plan(self):
+        """What this run's inputs and the library's planner made of the workload
+        (known only once the inputs exist and the device is queried)."""
         p = self.p
-        c = {"workload": self.name, "B": p.B, "Hq": p.Hq, "Hkv": p.Hkv, "d": p.d,
-             "L": p.L_max if not self.paged else "ragged", "kv_tokens": self.kv_tokens,
-             "num_splits": self.splits if self.splits is not None else p.num_splits,
-             "cache": "paged-64" if self.paged else "contiguous", "out_dtype": p.out_dtype,
-             "kv_dtype": ("e4m3 codes + f32 row scales" if self.fp8 else
-                          "e2m1 codes + power-of-two scales per 32 channels" if self.fp4 else "bf16")}
+        c = {"kv_tokens": self.kv_tokens,
+             "chunks_per_sequence": self.splits if self.splits is not None else
+             ("planner (top-delta)" if not p.num_splits else p.num_splits),
+             "launches_per_call": self.launches_per_call()}
         if self.topdelta is not None:
-            c.update(delta=self.topdelta, n_sink=self.n_sink, window=self.window, selection=self.sel_stats,
-                     dense_equivalent_bytes=self.kv_tokens * p.Hkv * p.d * 4)
+            c.update(selection=self.sel_stats, dense_equivalent_bytes=self.kv_tokens * p.Hkv * p.d * 4)
         return c
+
+
+def workload_config(args):
+    """The workload as the command line names it: the same dict in the GPU
+    arm and in the reference arm (nothing here depends on the device)."""
+    name = args.workload
+    base = name[:-4] if name.endswith(("_fp8", "_fp4")) else name
+    B, Hq, Hkv, L, d = FULL_SHAPES[name]
+    if args.batch is not None and (base == "gqa_paged" or base.startswith("ffd")):
+        B = args.batch
+    if base == "gqa_paged":
+        hi = args.seq_len if args.seq_len is not None else 131072
+        lo = max(64, hi // 8) if args.seq_len is not None else 16384
+        L = f"U{{{lo}..{hi}}} per sequence"
+    elif args.seq_len is not None and base in ("mha32k", "million"):
+        L = args.seq_len
+    kv = ("e4m3 codes + f32 row scales" if name.endswith("_fp8") else
+          "e2m1 codes + power-of-two scales per 32 channels" if name.endswith("_fp4") else "bf16")
+    c = {"workload": name, "B": B, "Hq": Hq, "Hkv": Hkv, "d": d, "L": L,
+         "cache": "paged-64" if base == "gqa_paged" else "contiguous",
+         "out_dtype": "f32" if base == "tiny" else "bf16", "kv_dtype": kv,
+         "num_splits": "planner" if not args.num_splits else args.num_splits,
+         "l2": "inputs smaller than L2 (no flush)" if base == "tiny" else "inputs larger than L2",
+         "parallelism": f"replicas x{args.gpus}"}
+    if base == "tiny":
+        c["num_splits"] = args.num_splits or 4
+    if base.startswith("ffd_top"):
+        c.update(delta=5.0 if base.endswith("5") else 7.0, n_sink=args.n_sink, window=args.window)
+    if args.graph:
+        c["timing"] = f"CUDA graph of {args.graph} calls, replayed"
+    return c
 
 
 # ------------------------------------------------------------------ timing
@@ -442,6 +483,38 @@ def time_e2e(wl, steps, warmup, dist_ctx):
     t1 = time.perf_counter()
     dist_ctx.barrier()
     return dist_ctx.max((t1 - t0) * 1e3), host.numel(), result.numel()
+
+
+def ffd_compare(args, ctx, sampler, dev):
+    """Dense pass vs top-delta at delta 5 and 7 on one FFD cache (B=4, Hq=32,
+    Hkv=8, d=128, L=131072; the same K/V, the keys encoded once): `rounds`
+    interleaved rounds, in each every arm times --steps calls after --warmup
+    calls with CUDA events; medians over the rounds."""
+    seed = args.seed + ctx.rank
+    dense = Workload("ffd_dense", seed, dev)
+    td5 = Workload("ffd_topdelta5", seed, dev, problem=dense.p)
+    td7 = Workload("ffd_topdelta7", seed, dev, problem=dense.p, encoded_keys=td5.qk)
+    arms = (("dense", dense), ("topdelta5", td5), ("topdelta7", td7))
+    rounds = 3
+    us = {n: [] for n, _ in arms}
+    t0 = time.time()
+    for _ in range(rounds):
+        for n, wl in arms:
+            ms, _, steps = time_device(wl, args.steps, args.warmup, ctx)
+            us[n].append(ms * 1e3 / steps)
+    t1 = time.time()
+    med = {n: statistics.median(v) for n, v in us.items()}
+    res = {"workload": "ffd: B=4, Hq=32, Hkv=8, d=128, L=131072, sinks and last 64 tokens +2.5 q_hat, "
+                       "1% of tokens +N(2,0.5) q_hat; n_sink=4, window=64",
+           "rounds": rounds, "steps_per_round": args.steps, "warmup_per_round": args.warmup,
+           "us_per_call": med, "us_per_call_rounds": us,
+           "achieved_gbs": {n: wl.algorithmic_bytes() / (med[n] * 1e-6) / 1e9 for n, wl in arms},
+           "algorithmic_bytes": {n: wl.algorithmic_bytes() for n, wl in arms},
+           "topdelta5_speedup_vs_dense": med["dense"] / med["topdelta5"],
+           "topdelta7_speedup_vs_dense": med["dense"] / med["topdelta7"],
+           "selection": {"topdelta5": td5.sel_stats, "topdelta7": td7.sel_stats},
+           "clocks": sampler.summary(t0, t1)}
+    return res
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -592,7 +665,7 @@ def run_reference(args, ctx):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": s_per_step * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": args.workload},
+            "data": "synthetic", "config": workload_config(args),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": sample.threads, "kind": "oracle",
                              "sample": sample.desc + " per step"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -605,7 +678,7 @@ def main():
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["fd", "reference"], default="fd")
-    ap.add_argument("--workload", default="mha32k", choices=WORKLOADS)
+    ap.add_argument("--workload", default="million", choices=WORKLOADS)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--batch", type=int, default=None, help="override B (gqa_paged, ffd_*)")
     ap.add_argument("--seq-len", type=int, default=None, help="override L (L_max for gqa_paged)")
@@ -614,6 +687,8 @@ def main():
     ap.add_argument("--n-sink", type=int, default=4, help="top-delta: attention-sink anchors")
     ap.add_argument("--window", type=int, default=64, help="top-delta: local-window anchors")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ffd-compare", choices=["auto", "on", "off"], default="auto",
+                    help="time dense vs top-delta 5/7 on the FFD cache in the same run (auto: with million)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     args = ap.parse_args()
@@ -648,6 +723,9 @@ def main():
     if not args.no_e2e:
         e2e_steps = max(3, min(args.steps, 2000))
         ms_e2e, h2d, d2h = time_e2e(wl, e2e_steps, args.warmup, ctx)
+    compare = None
+    if args.ffd_compare == "on" or (args.ffd_compare == "auto" and args.workload == "million"):
+        compare = ffd_compare(args, ctx, sampler, dev)
     sampler.stop()
 
     status = fd.fd_device_status(clear=True)
@@ -689,17 +767,13 @@ def main():
         cpu = {"value": v, "unit": "tokens/s", "cores": sample.threads, "kind": "oracle",
                "sample": f"{sample.desc}; {reps} timed runs of {s_rep * 1e3:.1f} ms"}
     if ctx.rank == 0:
-        cfg = wl.config()
-        cfg["l2"] = ("inputs larger than L2" if algo > L2_BYTES else "inputs smaller than L2 (no flush)")
-        cfg["parallelism"] = f"replicas x{n}"
-        if args.graph:
-            cfg["timing"] = f"CUDA graph of {args.graph} calls, replayed"
+        cfg = workload_config(args)
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": n, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "kv_dtype": "e4m3" if wl.fp8 else "e2m1" if wl.fp4 else "bf16",
-            "data": "synthetic", "config": cfg,
+            "data": "synthetic", "config": cfg, "plan": wl.plan(),
             "us_per_call": per_call_s * 1e6,
             "kv_tokens_per_s": wl.kv_tokens * n / per_call_s,
             "achieved_hbm_gbs": achieved_gbs,
@@ -714,6 +788,8 @@ def main():
             "clocks": sampler_summary,
             "device_status": fd.fd_status_string(status),
         }
+        if compare is not None:
+            line["ffd_compare"] = compare
         print(json.dumps(line), flush=True)
     ctx.close()
 

@@ -20,8 +20,25 @@ def run_bench(args, env=None):
     return r
 
 
+def gpu_arm_config(workload, gpus=1):
+    """The config dict bench.py's GPU arm builds for `--workload <workload>`
+    (it needs no device: the planner's choices go to a separate key)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    args = bench.argparse.Namespace(workload=workload, batch=None, seq_len=None, num_splits=None,
+                                    n_sink=4, window=64, gpus=gpus, graph=0)
+    return bench.workload_config(args)
+
+
+def test_default_workload_is_the_largest_single_gpu_config():
+    c = gpu_arm_config("million")
+    assert (c["B"], c["Hq"], c["Hkv"], c["d"], c["L"]) == (1, 32, 8, 128, 1 << 20)
+    with open(os.path.join(ROOT, "bench.py")) as f:
+        assert 'ap.add_argument("--workload", default="million"' in f.read()
+
+
 @pytest.mark.timeout(600)
-@pytest.mark.parametrize("workload", ["tiny", "mha32k_fp8"])
+@pytest.mark.parametrize("workload", ["tiny", "mha32k_fp8", "ffd_topdelta5"])
 def test_reference_arm_json_line(workload):
     r = run_bench(["--impl", "reference", "--workload", workload, "--steps", "3", "--warmup", "3"])
     assert r.returncode == 0, r.stderr[-2000:]
@@ -34,6 +51,8 @@ def test_reference_arm_json_line(workload):
         assert key in d, key
     assert d["steps"] == 3 and d["warmup"] == 3 and d["higher_is_better"] is True
     assert d["value"] > 0 and d["unit"] == "tokens/s" and d["config"]["workload"] == workload
+    # the GPU arm prints the same config dict for the same command line
+    assert d["config"] == gpu_arm_config(workload)
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
