@@ -10,6 +10,7 @@ unloadable libfd.so raises an error.
 from __future__ import annotations
 
 import ctypes
+import functools
 import math
 import os
 import re
@@ -108,8 +109,25 @@ def _p(t):
 
 
 def _stream(stream):
-    s = torch.cuda.current_stream() if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+    """The stream handle for a call on the current device: `stream`, which must
+    belong to that device, or the device's current torch stream."""
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    _need(stream.device.index == torch.cuda.current_device(),
+          f"stream is on {stream.device}, the tensors on cuda:{torch.cuda.current_device()}")
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _on_device_of_first_tensor(fn):
+    """Run a wrapper with its leading tensor's device current, so the
+    library's planner, its scratch lookup and the default stream all refer to
+    the device that holds the data (every other tensor is checked against it)."""
+    @functools.wraps(fn)
+    def wrapper(t, *args, **kwargs):
+        _need(isinstance(t, torch.Tensor) and t.is_cuda, f"{fn.__name__}: the first argument must be a CUDA tensor")
+        with torch.cuda.device(t.device):
+            return fn(t, *args, **kwargs)
+    return wrapper
 
 
 def _need(cond, what):
@@ -119,6 +137,8 @@ def _need(cond, what):
 
 def _check_cuda(t, name, dtype=None, shape=None):
     _need(t.is_cuda, f"{name} must be a CUDA tensor")
+    _need(t.device.index == torch.cuda.current_device(),
+          f"{name} is on {t.device}, expected cuda:{torch.cuda.current_device()} (the first tensor's device)")
     _need(t.is_contiguous(), f"{name} must be contiguous")
     if dtype is not None:
         _need(t.dtype == dtype, f"{name} must be {dtype}, got {t.dtype}")
@@ -184,6 +204,7 @@ def _outputs(B, Hq, d, device, out, lse, out_dtype, want_lse):
     return code, out, lse
 
 
+@_on_device_of_first_tensor
 def fd_decode_dense(q, k, v, seq_lens=None, scale=None, num_splits=0, out=None, lse=None,
                     out_dtype="bf16", want_lse=True, workspace=None, stream=None):
     """Dense split-KV decode.  q [B,Hq,d] bf16; k, v [B,Hkv,L_max,d] bf16;
@@ -208,6 +229,7 @@ def fd_decode_dense(q, k, v, seq_lens=None, scale=None, num_splits=0, out=None, 
     return out, lse
 
 
+@_on_device_of_first_tensor
 def fd_decode_paged(q, k_pages, v_pages, page_table, num_pages, seq_lens, scale=None, num_splits=0,
                     out=None, lse=None, out_dtype="bf16", want_lse=True, workspace=None, stream=None):
     """Paged split-KV decode.  k_pages/v_pages [P,Hkv,64,d] bf16,
@@ -235,6 +257,7 @@ def fd_decode_paged(q, k_pages, v_pages, page_table, num_pages, seq_lens, scale=
     return out, lse
 
 
+@_on_device_of_first_tensor
 def fd_quantize_keys(k, seq_lens=None, codes=None, mn_scale=None, res=None, res_scale=None, stream=None):
     """Key encoder.  Returns (codes u8 [B,Hkv,L,d/4], mn_scale fp16 [B,Hkv,L,d/32,2],
     res int8 [B,Hkv,L,d], res_scale fp16 [B,Hkv,L,d/32])."""
@@ -262,6 +285,7 @@ def fd_quantize_keys(k, seq_lens=None, codes=None, mn_scale=None, res=None, res_
     return codes, mn_scale, res, res_scale
 
 
+@_on_device_of_first_tensor
 def fd_decode_topdelta(q, codes, mn_scale, res, res_scale, v, seq_lens=None, scale=None, delta=5.0,
                        n_sink=4, window=64, num_splits=0, out=None, lse=None, out_dtype="bf16",
                        want_lse=True, sel_mask=None, sel_count=None, want_selection=False,
@@ -302,6 +326,7 @@ def fd_decode_topdelta(q, codes, mn_scale, res, res_scale, v, seq_lens=None, sca
     return out, lse, sel_mask, sel_count
 
 
+@_on_device_of_first_tensor
 def fd_decode_dense_noalloc(q, k, v, out, seq_lens=None, scale=None, num_splits=0, lse=None, stream=None):
     """fd_decode_dense for callers that cannot allocate: the library's fixed
     device scratch array stands in for the workspace, and this wrapper
@@ -428,6 +453,7 @@ def _decode_paged_q(kind, q, k_pages, k_page_scales, v_pages, v_page_scales, pag
     return out, lse
 
 
+@_on_device_of_first_tensor
 def fd_quantize_kv_fp8(x, seq_lens=None, codes=None, scales=None, stream=None):
     """fp8 cache encoder.  x [B,H,L_max,d] bf16 -> (codes uint8 [B,H,L_max,d],
     scales float32 [B,H,L_max]).  Rows past seq_lens[b] are left as passed
@@ -443,6 +469,7 @@ def fd_decode_fp8_workspace_size(B, Hq, Hkv, L_max, d, num_splits=0, ragged=Fals
     return _workspace_size_q("fp8", B, Hq, Hkv, L_max, d, num_splits, ragged)
 
 
+@_on_device_of_first_tensor
 def fd_decode_dense_fp8(q, k_codes, k_scales, v_codes, v_scales, seq_lens=None, scale=None, num_splits=0,
                         out=None, lse=None, out_dtype="bf16", want_lse=True, workspace=None, stream=None):
     """Split-KV decode over an fp8 cache.  q [B,Hq,d] bf16; k_codes, v_codes
@@ -451,6 +478,7 @@ def fd_decode_dense_fp8(q, k_codes, k_scales, v_codes, v_scales, seq_lens=None, 
                            out_dtype, want_lse, workspace, stream)
 
 
+@_on_device_of_first_tensor
 def fd_decode_paged_fp8(q, k_pages, k_page_scales, v_pages, v_page_scales, page_table, num_pages, seq_lens,
                         scale=None, num_splits=0, out=None, lse=None, out_dtype="bf16", want_lse=True,
                         workspace=None, stream=None):
@@ -460,6 +488,7 @@ def fd_decode_paged_fp8(q, k_pages, k_page_scales, v_pages, v_page_scales, page_
                            seq_lens, scale, num_splits, out, lse, out_dtype, want_lse, workspace, stream)
 
 
+@_on_device_of_first_tensor
 def fd_quantize_kv_fp4(x, seq_lens=None, codes=None, scales=None, stream=None):
     """fp4 cache encoder.  x [B,H,L_max,d] bf16 -> (codes uint8 [B,H,L_max,d/2],
     scales uint8 [B,H,L_max,d/32]).  Rows past seq_lens[b] are left as passed
@@ -475,6 +504,7 @@ def fd_decode_fp4_workspace_size(B, Hq, Hkv, L_max, d, num_splits=0, ragged=Fals
     return _workspace_size_q("fp4", B, Hq, Hkv, L_max, d, num_splits, ragged)
 
 
+@_on_device_of_first_tensor
 def fd_decode_dense_fp4(q, k_codes, k_scales, v_codes, v_scales, seq_lens=None, scale=None, num_splits=0,
                         out=None, lse=None, out_dtype="bf16", want_lse=True, workspace=None, stream=None):
     """Split-KV decode over an fp4 cache.  q [B,Hq,d] bf16; k_codes, v_codes
@@ -483,6 +513,7 @@ def fd_decode_dense_fp4(q, k_codes, k_scales, v_codes, v_scales, seq_lens=None, 
                            out_dtype, want_lse, workspace, stream)
 
 
+@_on_device_of_first_tensor
 def fd_decode_paged_fp4(q, k_pages, k_page_scales, v_pages, v_page_scales, page_table, num_pages, seq_lens,
                         scale=None, num_splits=0, out=None, lse=None, out_dtype="bf16", want_lse=True,
                         workspace=None, stream=None):

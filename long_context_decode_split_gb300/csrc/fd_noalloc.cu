@@ -14,6 +14,8 @@
 // code cannot use the array's name as a device address, so the address is
 // looked up with cudaGetSymbolAddress once per device, on the first call made
 // with that device current, and then passed to the kernels.
+#include <atomic>
+
 #include <cuda_runtime.h>
 
 #include "fd.h"
@@ -26,15 +28,19 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 // Device address of g_noalloc_scratch on the current device (nullptr on
-// failure).  Looked up once per device and cached.
+// failure).  Looked up once per device and cached; host threads making their
+// first calls at the same time may each look it up, and store the same value.
 void* scratch_address() {
-    static void* cache[kMaxDevices] = {};
+    static std::atomic<void*> cache[kMaxDevices] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
-    if (dev >= 0 && dev < kMaxDevices && cache[dev]) return cache[dev];
+    if (dev >= 0 && dev < kMaxDevices) {
+        void* hit = cache[dev].load(std::memory_order_relaxed);
+        if (hit) return hit;
+    }
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
-    if (dev >= 0 && dev < kMaxDevices) cache[dev] = p;
+    if (dev >= 0 && dev < kMaxDevices) cache[dev].store(p, std::memory_order_relaxed);
     return p;
 }
 
