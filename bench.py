@@ -14,8 +14,12 @@ on the same FFD cache (B=4, Hq=32, Hkv=8, d=128, L=131072), interleaved, each
 arm --steps calls after --warmup calls per round.  Other workloads:
 --workload tiny|mha32k|gqa_paged|million|ffd_dense|ffd_topdelta5|
 ffd_topdelta7, and mha32k_fp8|million_fp8|ffd_dense_fp8|gqa_paged_fp8 (the same
-caches in the fp8 e4m3 encoding, per-row f32 scales) and the *_fp4 variants
-(e2m1 codes with power-of-two scales per 32 channels).
+caches in the fp8 e4m3 encoding, per-row f32 scales), the *_fp4 variants
+(e2m1 codes with power-of-two scales per 32 channels), the *_unified variants
+(one fixed max value --phi for every chunk), ffd_topdelta{5,7}_union (one
+candidate set per KV group) and ffd_sparse_{dense,topdelta5[_union]} (a
+sparser FFD cache: --plant-frac of the tokens and the anchors far above the
+rest).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fd|reference]
 
@@ -48,7 +52,13 @@ FALLBACK_HBM_GBS = 6800.0
 DEFAULT_STEPS = {"tiny": 20000, "mha32k": 20000, "gqa_paged": 3000, "million": 3000,
                  "ffd_dense": 4000, "ffd_topdelta5": 4000, "ffd_topdelta7": 4000,
                  "mha32k_fp8": 20000, "million_fp8": 4000, "ffd_dense_fp8": 6000, "gqa_paged_fp8": 4000,
-                 "mha32k_fp4": 20000, "million_fp4": 4000, "ffd_dense_fp4": 6000, "gqa_paged_fp4": 4000}
+                 "mha32k_fp4": 20000, "million_fp4": 4000, "ffd_dense_fp4": 6000, "gqa_paged_fp4": 4000,
+                 "mha32k_unified": 20000, "million_unified": 3000, "gqa_paged_unified": 3000,
+                 "ffd_topdelta5_union": 4000, "ffd_topdelta7_union": 4000,
+                 "ffd_sparse_dense": 4000, "ffd_sparse_topdelta5": 4000, "ffd_sparse_topdelta5_union": 4000}
+# The sparse FFD cache: anchors and planted tokens boosted by 20 along q_hat
+# (a ~13-unit score lead at G=4), --plant-frac of the tokens planted.
+SPARSE_BOOST = 20.0
 WORKLOADS = list(DEFAULT_STEPS)
 
 
@@ -138,7 +148,7 @@ class Workload:
     """Resident inputs plus a `call()` that runs one decode through the C ABI."""
 
     def __init__(self, name, seed, device, batch=None, seq_len=None, num_splits=None, n_sink=4, window=64,
-                 problem=None, encoded_keys=None):
+                 problem=None, encoded_keys=None, phi=6.5, plant_frac=0.001):
         """`problem` (and, for top-delta, `encoded_keys`) reuse another
         workload's resident inputs instead of generating them again."""
         import torch
@@ -152,8 +162,16 @@ class Workload:
         self.topdelta = None
         self.fp8 = name.endswith("_fp8")
         self.fp4 = name.endswith("_fp4")
+        self.unified = name.endswith("_unified")
+        self.group_union = name.endswith("_union")
         if self.fp8 or self.fp4:
             name = name[:-4]
+        if self.unified:
+            name = name[:-len("_unified")]
+        if self.group_union:
+            name = name[:-len("_union")]
+        self.sparse = name.startswith("ffd_sparse")
+        self.phi = phi
         self.n_sink, self.window = n_sink, window
         over = {}
         if seq_len is not None:
@@ -176,8 +194,10 @@ class Workload:
         elif name.startswith("ffd"):
             if batch is not None:
                 over["B"] = batch
+            if self.sparse:
+                over.update(anchor_boost=SPARSE_BOOST, plant_mean=SPARSE_BOOST, plant_frac=plant_frac)
             p = W.ffd(seed=seed, device=device, **over)
-            if name != "ffd_dense":
+            if not name.endswith("_dense"):
                 self.topdelta = 5.0 if name.endswith("5") else 7.0
         else:
             raise ValueError(name)
@@ -231,7 +251,8 @@ class Workload:
         c, ms, r, rs = self.qk
         out_s, lse_s, mask, cnt = fd.fd_decode_topdelta(p.q, c, ms, r, rs, p.v, p.seq_lens, p.scale, self.topdelta,
                                                         self.n_sink, self.window, p.num_splits,
-                                                        out_dtype=self.out_dtype, want_selection=True)
+                                                        out_dtype=self.out_dtype, want_selection=True,
+                                                        group_union=self.group_union)
         # quality proxy: the dense softmax mass the candidate set captures, exp(lse_sel - lse_dense),
         # and the largest output deviation from dense attention over the bf16 keys
         out_d, lse_d = fd.fd_decode_dense(p.q, p.k, p.v, p.seq_lens, p.scale, out_dtype=self.out_dtype)
@@ -246,6 +267,7 @@ class Workload:
         tiles = np.pad(ubits, ((0, 0), (0, 0), (0, pad))).reshape(B, p.Hkv, -1, 64).any(axis=-1)
         L = p.kv_tokens() / B
         return {"selected_per_query": float(cnt.float().mean().item()) / L,
+                "attended": "group union" if self.group_union else "per query head",
                 "captured_mass_min": float(mass.min().item()), "captured_mass_mean": float(mass.mean().item()),
                 "max_abs_dev_vs_dense": dev,
                 "union_per_kv_head": float(ubits.sum()) / (B * p.Hkv * L),
@@ -269,7 +291,14 @@ class Workload:
             c, ms, r, rs = self.qk
             fd.fd_decode_topdelta(q, c, ms, r, rs, p.v, p.seq_lens, p.scale, self.topdelta, self.n_sink,
                                   self.window, p.num_splits, out=self.out, lse=self.lse, out_dtype=self.out_dtype,
-                                  workspace=self.ws, stream=stream)
+                                  workspace=self.ws, stream=stream, group_union=self.group_union)
+        elif self.unified and self.paged:
+            fd.fd_decode_paged_unified(q, p.k_pages, p.v_pages, p.page_table, p.num_pages, p.seq_lens, p.scale,
+                                       self.phi, p.num_splits, out=self.out, lse=self.lse, out_dtype=self.out_dtype,
+                                       workspace=self.ws, stream=stream)
+        elif self.unified:
+            fd.fd_decode_dense_unified(q, p.k, p.v, None, p.scale, self.phi, p.num_splits, out=self.out, lse=self.lse,
+                                       out_dtype=self.out_dtype, workspace=self.ws, stream=stream)
         elif self.paged:
             fd.fd_decode_paged(q, p.k_pages, p.v_pages, p.page_table, p.num_pages, p.seq_lens, p.scale,
                                p.num_splits, out=self.out, lse=self.lse, out_dtype=self.out_dtype,
@@ -318,6 +347,7 @@ def workload_config(args):
     arm and in the reference arm (nothing here depends on the device)."""
     name = args.workload
     base = name[:-4] if name.endswith(("_fp8", "_fp4")) else name
+    base = base[:-len("_unified")] if base.endswith("_unified") else base
     B, Hq, Hkv, L, d = FULL_SHAPES[name]
     if args.batch is not None and (base == "gqa_paged" or base.startswith("ffd")):
         B = args.batch
@@ -337,8 +367,15 @@ def workload_config(args):
          "parallelism": f"replicas x{args.gpus}"}
     if base == "tiny":
         c["num_splits"] = args.num_splits or 4
-    if base.startswith("ffd_top"):
-        c.update(delta=5.0 if base.endswith("5") else 7.0, n_sink=args.n_sink, window=args.window)
+    top = base[:-len("_union")] if base.endswith("_union") else base
+    if top.startswith("ffd") and not top.endswith("_dense"):
+        c.update(delta=5.0 if top.endswith("5") else 7.0, n_sink=args.n_sink, window=args.window,
+                 selection="group union" if base.endswith("_union") else "per query head")
+    if base.startswith("ffd_sparse"):
+        c["keys"] = (f"sparse FFD cache: sinks, last 64 tokens and {args.plant_frac:g} of the tokens "
+                     f"+{SPARSE_BOOST:g} q_hat")
+    if name.endswith("_unified"):
+        c["softmax"] = f"unified max value phi={args.phi} (FlashDecoding++), running-max fallback"
     if args.graph:
         c["timing"] = f"CUDA graph of {args.graph} calls, replayed"
     return c
@@ -525,6 +562,8 @@ FULL_SHAPES = {"tiny": (1, 1, 1, 1024, 64), "mha32k": (1, 32, 32, 32768, 128),
                "ffd_topdelta7": (4, 32, 8, 131072, 128)}
 FULL_SHAPES.update({k + "_fp8": FULL_SHAPES[k] for k in ("mha32k", "million", "gqa_paged", "ffd_dense")})
 FULL_SHAPES.update({k + "_fp4": FULL_SHAPES[k] for k in ("mha32k", "million", "gqa_paged", "ffd_dense")})
+FULL_SHAPES.update({k + "_unified": FULL_SHAPES[k] for k in ("mha32k", "million", "gqa_paged")})
+FULL_SHAPES.update({k: FULL_SHAPES["ffd_dense"] for k in WORKLOADS if k.startswith("ffd")})
 
 
 class OracleSample:
@@ -533,7 +572,7 @@ class OracleSample:
     sequence.  `frac` is the slice's share of one full call's work.  For the
     ragged paged batch the full call is taken at the mean length."""
 
-    def __init__(self, name, seed, target_s):
+    def __init__(self, name, seed, target_s, plant_frac=0.001):
         import numpy as np
         import torch
 
@@ -548,15 +587,20 @@ class OracleSample:
         G = Hq // Hkv
         self.B = B
         self.delta = None
-        if name.startswith("ffd_top"):
-            self.delta = 5.0 if name.endswith("5") else 7.0
+        self.union = name.endswith("_union")
+        top = name[:-len("_union")] if self.union else name
+        if top.startswith("ffd") and not top.endswith("_dense"):
+            self.delta = 5.0 if top.endswith("5") else 7.0
 
         def bits(t):
             return t.contiguous().view(torch.int16).numpy().view(np.uint16)
 
         heads, Ls = 1, min(L, 2048)
         while True:
-            if name.startswith("ffd"):
+            if name.startswith("ffd_sparse"):
+                p = W.ffd(seed=seed, B=B, L=Ls, Hq=heads * G, Hkv=heads, d=d, anchor_boost=SPARSE_BOOST,
+                          plant_mean=SPARSE_BOOST, plant_frac=plant_frac)
+            elif name.startswith("ffd"):
                 p = W.ffd(seed=seed, B=B, L=Ls, Hq=heads * G, Hkv=heads, d=d)
             else:
                 p = W.random_problem(B, heads * G, heads, Ls, d, seed=seed)
@@ -592,7 +636,8 @@ class OracleSample:
             self.oracle.decode_dense_fp4(q, kc, ks, vc, vs, None, scale)
         elif self.delta is not None:
             c, ms, r, rs = self.enc
-            self.oracle.decode_topdelta(q, c, ms, r, rs, v, None, scale, self.delta)
+            fn = self.oracle.decode_topdelta_group_union if self.union else self.oracle.decode_topdelta
+            fn(q, c, ms, r, rs, v, None, scale, self.delta)
         else:
             self.oracle.decode_dense(q, k, v, None, scale)
 
@@ -660,7 +705,7 @@ def run_reference(args, ctx):
     if ctx.rank != 0:
         return
     per_step = max(0.002, min(2.0, 90.0 / max(1, args.steps + args.warmup)))
-    sample = OracleSample(args.workload, args.seed, per_step)
+    sample = OracleSample(args.workload, args.seed, per_step, args.plant_frac)
     value, s_per_step = time_oracle(sample, args.steps, args.warmup)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": s_per_step * 1e3,
@@ -686,6 +731,8 @@ def main():
     ap.add_argument("--graph", type=int, default=0, help="replay calls from a CUDA graph of this many calls")
     ap.add_argument("--n-sink", type=int, default=4, help="top-delta: attention-sink anchors")
     ap.add_argument("--window", type=int, default=64, help="top-delta: local-window anchors")
+    ap.add_argument("--phi", type=float, default=6.5, help="*_unified: the fixed max value (natural-log units)")
+    ap.add_argument("--plant-frac", type=float, default=0.001, help="ffd_sparse_*: fraction of planted tokens")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--ffd-compare", choices=["auto", "on", "off"], default="auto",
                     help="time dense vs top-delta 5/7 on the FFD cache in the same run (auto: with million)")
@@ -712,7 +759,8 @@ def main():
     fd.load()
     dev = f"cuda:{ctx.local_rank}"
     wl = Workload(args.workload, args.seed + ctx.rank, dev, batch=args.batch, seq_len=args.seq_len,
-                  num_splits=args.num_splits, n_sink=args.n_sink, window=args.window)
+                  num_splits=args.num_splits, n_sink=args.n_sink, window=args.window, phi=args.phi,
+                  plant_frac=args.plant_frac)
 
     sampler = ClockSampler(ctx.local_rank)
     sampler.start()
@@ -759,7 +807,7 @@ def main():
                        "decode, one device->host copy (out + lse)"}
     cpu = None
     if ctx.rank == 0 and n == 1 and not args.no_cpu_baseline:
-        sample = OracleSample(args.workload, args.seed, 1.0)
+        sample = OracleSample(args.workload, args.seed, 1.0, args.plant_frac)
         t0 = time.perf_counter()
         sample.run()
         reps = max(1, int(args.cpu_budget / max(time.perf_counter() - t0, 1e-3)))
@@ -802,7 +850,7 @@ def kernel_family(workload):
         return "fp8"
     if workload.endswith("_fp4"):
         return "fp4"
-    if workload.startswith("ffd_top"):
+    if workload.startswith("ffd") and not workload.endswith("_dense"):
         return "topdelta"
     return "bf16"
 

@@ -15,6 +15,9 @@
  *         sinks and the local window), section 5 (2-bit body for the full
  *         scan, 8-bit residual loaded for candidates only), section 6 and
  *         Fig. 2 (one fused kernel: scan, select, correct, attend, aggregate).
+ *   [FD++] FlashDecoding++ summary (nxbn.cn blog): asynchronous partial
+ *         softmax with a unified (fixed) max value, and the fallback to the
+ *         safe computation when the inputs leave its range.
  *   [KV8] Benchmarking blog on a hosted 1M-context model (xxmr.cn/news/240041),
  *         section 1: a narrow floating-point KV cache as the lever on the
  *         bytes a decode step reads.  The page gives no format; the fp8
@@ -135,6 +138,39 @@ FD_API int fd_decode_paged(const void* q, const void* k_pages, const void* v_pag
                     void* out, int out_dtype, float* lse,
                     void* workspace, size_t workspace_bytes, void* stream);
 
+/* Unified-max variants of fd_decode_dense and fd_decode_paged ([FD++]
+ * sections 1 and 3, asynchronous
+ * partial softmax with one fixed max value instead of a per-chunk maximum,
+ * and section 5, the fallback to the safe computation when the softmax inputs
+ * leave the range that value was chosen for).
+ *   phi  the fixed max value, in natural-log units of the scaled score
+ *        s = scale * <q, k>; finite (|phi| <= 1e30, else FD_ERR_INVALID_ARG).
+ *        A good choice is the upper end of the scores the model produces
+ *        (that summary quotes [-16.8, 6.5] for Llama2-7B).
+ * Every chunk weights its keys by e^(s - phi) directly, with no maximum
+ * reduction and no rescaling, while all of its scores lie in
+ * [phi - 60, phi]; then every weight is a normal binary32 number in
+ * [e^-60, 1] and no sum can overflow.  A chunk that meets a score outside
+ * that range (above phi, or more than 60 below it) rebases what it has
+ * accumulated to the largest score it attended and continues with the
+ * running maximum of fd_decode_dense.  The result is the attention that
+ * fd_decode_dense computes, up to fp32 rounding, for any phi.  All other
+ * arguments, layouts, the workspace (fd_decode_workspace_size with the same
+ * sizes) and errors are those of fd_decode_dense / fd_decode_paged. */
+FD_API int fd_decode_dense_unified(const void* q, const void* k, const void* v,
+                                   const int32_t* seq_lens,
+                                   int B, int Hq, int Hkv, int L_max, int d,
+                                   float scale, float phi, int num_splits,
+                                   void* out, int out_dtype, float* lse,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+FD_API int fd_decode_paged_unified(const void* q, const void* k_pages, const void* v_pages,
+                                   const int32_t* page_table, int max_pages, int num_pages,
+                                   const int32_t* seq_lens, int page_size,
+                                   int B, int Hq, int Hkv, int d,
+                                   float scale, float phi, int num_splits,
+                                   void* out, int out_dtype, float* lse,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
 /* Key encoder for the sparse path ([FFD] section 5): per token and per
  * group of 32 channels, a 2-bit asymmetric body and an int8 symmetric
  * residual.  With x the group's bf16 values, in IEEE binary32 arithmetic:
@@ -188,6 +224,26 @@ FD_API int fd_decode_topdelta(const void* q, const uint8_t* codes, const void* m
                        void* out, int out_dtype, float* lse,
                        uint32_t* sel_mask, int32_t* sel_count,
                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* fd_decode_topdelta with one candidate set per KV group: steps 1-3 are
+ * taken per query head as above, then every query head of a group (the
+ * Hq / Hkv heads that read one KV head) attends, in steps 4-5, to the union
+ * of the group's sets, Sel_group = U_g Sel_g, each with its own exact scores.
+ * The pages define the rule per query ([FFD] section 3) and give no group
+ * variant; this one reads no more bytes than the per-head rule (the tiles
+ * whose residual and V are loaded are the same) and every head keeps at
+ * least its own candidates.  sel_mask / sel_count report the attended set
+ * (the same for every head of a group).  Arguments, layouts, workspace
+ * (fd_topdelta_workspace_size) and errors are those of fd_decode_topdelta. */
+FD_API int fd_decode_topdelta_group_union(const void* q, const uint8_t* codes, const void* mn_scale,
+                                          const int8_t* res, const void* res_scale, const void* v,
+                                          const int32_t* seq_lens,
+                                          int B, int Hq, int Hkv, int L_max, int d,
+                                          float scale, float delta, int n_sink, int window,
+                                          int num_splits,
+                                          void* out, int out_dtype, float* lse,
+                                          uint32_t* sel_mask, int32_t* sel_count,
+                                          void* workspace, size_t workspace_bytes, void* stream);
 
 /* fp8 KV cache encoder ([KV8]).  For each cache row x (one token of one
  * head, d bf16 values), in IEEE binary32 arithmetic:
@@ -324,6 +380,21 @@ FD_API int fd_decode_dense_noalloc(const void* q, const void* k, const void* v,
                                    int B, int Hq, int Hkv, int L_max, int d,
                                    float scale, int num_splits,
                                    void* out, int out_dtype, float* lse, void* stream);
+
+/* Fault injection for tests of the time-out path; not for production use.
+ * Applies to the bf16 dense and paged decode (fd_decode_dense,
+ * fd_decode_paged, their unified-max variants and fd_decode_dense_noalloc)
+ * launched afterwards from this process:
+ *   wait_limit_ns  > 0: the time limit of every pipeline wait (default 2 s;
+ *                  0 restores it)
+ *   withhold_tile  >= 0: the producer of every chunk issues no copy and no
+ *                  arrival for that tile index of the chunk (-1: off), so the
+ *                  consumers' wait for it runs out.
+ * A kernel whose wait runs out records FD_ERR_DEVICE_TIMEOUT in the device
+ * status word, stops using its pipeline, lets every copy it started land
+ * and exits; the call's out and lse are then undefined.  The GPU stays
+ * usable.  Always returns FD_OK. */
+FD_API int fd_debug_inject_wait_timeout(unsigned long long wait_limit_ns, int withhold_tile);
 
 /* Synchronises `stream`, then reports the device status word of the current
  * device: FD_ERR_DEVICE_TIMEOUT, FD_ERR_BAD_PAGE_TABLE, FD_ERR_INVALID_ARG (a

@@ -23,7 +23,8 @@ __all__ = [
     "fd_topdelta_workspace_size", "fd_decode_topdelta", "fd_device_status", "fd_decode_dense_noalloc",
     "fd_quantize_kv_fp8", "fd_num_splits_fp8", "fd_decode_fp8_workspace_size", "fd_decode_dense_fp8",
     "fd_decode_paged_fp8", "fd_quantize_kv_fp4", "fd_num_splits_fp4", "fd_decode_fp4_workspace_size",
-    "fd_decode_dense_fp4", "fd_decode_paged_fp4",
+    "fd_decode_dense_fp4", "fd_decode_paged_fp4", "fd_decode_dense_unified", "fd_decode_paged_unified",
+    "fd_decode_topdelta_group_union", "fd_debug_inject_wait_timeout",
     "FD_OK", "FD_ERR_INVALID_ARG", "FD_ERR_UNSUPPORTED", "FD_ERR_WORKSPACE_TOO_SMALL",
     "FD_ERR_BAD_PAGE_TABLE", "FD_ERR_CUDA", "FD_ERR_DEVICE_TIMEOUT", "FD_OUT_F32", "FD_OUT_BF16",
 ]
@@ -74,10 +75,15 @@ def open_library(path: str):
         "fd_decode_workspace_size": (S, [I, I, I, I, I, I, I]),
         "fd_decode_dense": (I, [P, P, P, P, I, I, I, I, I, F, I, P, I, P, P, S, P]),
         "fd_decode_paged": (I, [P, P, P, P, I, I, P, I, I, I, I, I, F, I, P, I, P, P, S, P]),
+        "fd_decode_dense_unified": (I, [P, P, P, P, I, I, I, I, I, F, F, I, P, I, P, P, S, P]),
+        "fd_decode_paged_unified": (I, [P, P, P, P, I, I, P, I, I, I, I, I, F, F, I, P, I, P, P, S, P]),
         "fd_quantize_keys": (I, [P, P, I, I, I, I, P, P, P, P, P]),
         "fd_topdelta_workspace_size": (S, [I, I, I, I, I, I]),
         "fd_decode_topdelta": (I, [P, P, P, P, P, P, P, I, I, I, I, I, F, F, I, I, I, P, I, P, P, P, P, S, P]),
+        "fd_decode_topdelta_group_union": (I, [P, P, P, P, P, P, P, I, I, I, I, I, F, F, I, I, I, P, I, P, P, P, P,
+                                               S, P]),
         "fd_device_status": (I, [I, P]),
+        "fd_debug_inject_wait_timeout": (I, [ctypes.c_ulonglong, I]),
         "fd_decode_dense_noalloc": (I, [P, P, P, P, I, I, I, I, I, F, I, P, I, P, P]),
         "fd_quantize_kv_fp8": (I, [P, P, I, I, I, I, P, P, P]),
         "fd_num_splits_fp8": (I, [I, I, I, I, I, I, I]),
@@ -206,7 +212,7 @@ def _outputs(B, Hq, d, device, out, lse, out_dtype, want_lse):
 
 @_on_device_of_first_tensor
 def fd_decode_dense(q, k, v, seq_lens=None, scale=None, num_splits=0, out=None, lse=None,
-                    out_dtype="bf16", want_lse=True, workspace=None, stream=None):
+                    out_dtype="bf16", want_lse=True, workspace=None, stream=None, _unified_phi=None):
     """Dense split-KV decode.  q [B,Hq,d] bf16; k, v [B,Hkv,L_max,d] bf16;
     seq_lens [B] int32 or None.  Returns (out [B,Hq,d], lse [B,Hq] or None)."""
     lib = load()
@@ -222,16 +228,42 @@ def fd_decode_dense(q, k, v, seq_lens=None, scale=None, num_splits=0, out=None, 
     code, out, lse = _outputs(B, Hq, d, q.device, out, lse, out_dtype, want_lse)
     need = fd_decode_workspace_size(B, Hq, Hkv, L_max, d, num_splits, seq_lens is not None)
     ws = _workspace(need, q.device, workspace)
-    st = lib.fd_decode_dense(_p(q), _p(k), _p(v), _p(seq_lens), B, Hq, Hkv, L_max, d, scale,
-                             int(num_splits), _p(out), code, _p(lse), _p(ws),
-                             0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
-    _raise(st, "fd_decode_dense")
+    head = (_p(q), _p(k), _p(v), _p(seq_lens), B, Hq, Hkv, L_max, d, scale)
+    tail = (int(num_splits), _p(out), code, _p(lse), _p(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+            _stream(stream))
+    if _unified_phi is None:
+        st = lib.fd_decode_dense(*head, *tail)
+        _raise(st, "fd_decode_dense")
+    else:
+        st = lib.fd_decode_dense_unified(*head, _unified_phi, *tail)
+        _raise(st, "fd_decode_dense_unified")
     return out, lse
 
 
 @_on_device_of_first_tensor
+def fd_decode_dense_unified(q, k, v, seq_lens=None, scale=None, phi=6.5, num_splits=0, out=None, lse=None,
+                            out_dtype="bf16", want_lse=True, workspace=None, stream=None):
+    """fd_decode_dense with one fixed max value `phi` (natural-log units of
+    the scaled score) for every chunk, falling back to the running maximum
+    where scores leave [phi - 60, phi].  Same result up to fp32 rounding."""
+    return fd_decode_dense(q, k, v, seq_lens, scale, num_splits, out, lse, out_dtype, want_lse, workspace,
+                           stream, _unified_phi=float(phi))
+
+
+@_on_device_of_first_tensor
+def fd_decode_paged_unified(q, k_pages, v_pages, page_table, num_pages, seq_lens, scale=None, phi=6.5,
+                            num_splits=0, out=None, lse=None, out_dtype="bf16", want_lse=True, workspace=None,
+                            stream=None):
+    """fd_decode_paged with the unified max value `phi` (see
+    fd_decode_dense_unified)."""
+    return fd_decode_paged(q, k_pages, v_pages, page_table, num_pages, seq_lens, scale, num_splits, out, lse,
+                           out_dtype, want_lse, workspace, stream, _unified_phi=float(phi))
+
+
+@_on_device_of_first_tensor
 def fd_decode_paged(q, k_pages, v_pages, page_table, num_pages, seq_lens, scale=None, num_splits=0,
-                    out=None, lse=None, out_dtype="bf16", want_lse=True, workspace=None, stream=None):
+                    out=None, lse=None, out_dtype="bf16", want_lse=True, workspace=None, stream=None,
+                    _unified_phi=None):
     """Paged split-KV decode.  k_pages/v_pages [P,Hkv,64,d] bf16,
     page_table [B,max_pages] int32, seq_lens [B] int32."""
     lib = load()
@@ -249,11 +281,16 @@ def fd_decode_paged(q, k_pages, v_pages, page_table, num_pages, seq_lens, scale=
     code, out, lse = _outputs(B, Hq, d, q.device, out, lse, out_dtype, want_lse)
     need = fd_decode_workspace_size(B, Hq, Hkv, max_pages * page_size, d, num_splits, True)
     ws = _workspace(need, q.device, workspace)
-    st = lib.fd_decode_paged(_p(q), _p(k_pages), _p(v_pages), _p(page_table), max_pages, int(num_pages),
-                             _p(seq_lens), page_size, B, Hq, Hkv, d, scale, int(num_splits), _p(out), code,
-                             _p(lse), _p(ws), 0 if ws is None else ws.numel() * ws.element_size(),
-                             _stream(stream))
-    _raise(st, "fd_decode_paged")
+    head = (_p(q), _p(k_pages), _p(v_pages), _p(page_table), max_pages, int(num_pages), _p(seq_lens), page_size,
+            B, Hq, Hkv, d, scale)
+    tail = (int(num_splits), _p(out), code, _p(lse), _p(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+            _stream(stream))
+    if _unified_phi is None:
+        st = lib.fd_decode_paged(*head, *tail)
+        _raise(st, "fd_decode_paged")
+    else:
+        st = lib.fd_decode_paged_unified(*head, _unified_phi, *tail)
+        _raise(st, "fd_decode_paged_unified")
     return out, lse
 
 
@@ -289,9 +326,11 @@ def fd_quantize_keys(k, seq_lens=None, codes=None, mn_scale=None, res=None, res_
 def fd_decode_topdelta(q, codes, mn_scale, res, res_scale, v, seq_lens=None, scale=None, delta=5.0,
                        n_sink=4, window=64, num_splits=0, out=None, lse=None, out_dtype="bf16",
                        want_lse=True, sel_mask=None, sel_count=None, want_selection=False,
-                       workspace=None, stream=None):
+                       workspace=None, stream=None, group_union=False):
     """Top-delta sparse decode over fd_quantize_keys' outputs.  Returns
-    (out, lse, sel_mask or None, sel_count or None)."""
+    (out, lse, sel_mask or None, sel_count or None).  group_union=True calls
+    fd_decode_topdelta_group_union: every head of a KV group attends to the
+    union of the group's candidate sets."""
     lib = load()
     _check_cuda(q, "q", torch.bfloat16)
     B, Hq, d = q.shape
@@ -318,11 +357,12 @@ def fd_decode_topdelta(q, codes, mn_scale, res, res_scale, v, seq_lens=None, sca
         _check_cuda(sel_count, "sel_count", torch.int32, (B, Hq))
     need = fd_topdelta_workspace_size(B, Hq, Hkv, L_max, d, num_splits)
     ws = _workspace(need, q.device, workspace)
-    st = lib.fd_decode_topdelta(_p(q), _p(codes), _p(mn_scale), _p(res), _p(res_scale), _p(v), _p(seq_lens),
-                                B, Hq, Hkv, L_max, d, scale, delta, int(n_sink), int(window), int(num_splits),
-                                _p(out), code, _p(lse), _p(sel_mask), _p(sel_count), _p(ws),
-                                0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
-    _raise(st, "fd_decode_topdelta")
+    name = "fd_decode_topdelta_group_union" if group_union else "fd_decode_topdelta"
+    st = getattr(lib, name)(_p(q), _p(codes), _p(mn_scale), _p(res), _p(res_scale), _p(v), _p(seq_lens),
+                            B, Hq, Hkv, L_max, d, scale, delta, int(n_sink), int(window), int(num_splits),
+                            _p(out), code, _p(lse), _p(sel_mask), _p(sel_count), _p(ws),
+                            0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
+    _raise(st, name)
     return out, lse, sel_mask, sel_count
 
 
@@ -521,6 +561,13 @@ def fd_decode_paged_fp4(q, k_pages, k_page_scales, v_pages, v_page_scales, page_
     uint8, k_page_scales/v_page_scales [P,Hkv,64,d/32] uint8."""
     return _decode_paged_q("fp4", q, k_pages, k_page_scales, v_pages, v_page_scales, page_table, num_pages,
                            seq_lens, scale, num_splits, out, lse, out_dtype, want_lse, workspace, stream)
+
+
+def fd_debug_inject_wait_timeout(wait_limit_ns=0, withhold_tile=-1) -> int:
+    """Test-only fault injection for the bf16 dense/paged decode: a pipeline
+    wait limit in ns (0 = the default 2 s) and a tile index whose copies the
+    producer withholds (-1 = none).  See include/fd.h."""
+    return int(load().fd_debug_inject_wait_timeout(int(wait_limit_ns), int(withhold_tile)))
 
 
 def fd_device_status(clear=True, stream=None) -> int:

@@ -204,13 +204,19 @@ int decode_common(fd::DecodeArgs& a, int num_splits, bool ragged, int out_dtype,
 
 // Contiguous cache [B, Hkv, L_max, ...]: K and V (codes for fp8/fp4) and, for
 // the quantized caches, their scale arrays.
+// The unified-max variant takes a finite fixed max value phi.
+constexpr float kMaxAbsPhi = 1e30f;
+
 int dense_entry(Cache cache, const void* q, const void* k, const void* v, const void* k_scales,
                 const void* v_scales, const int32_t* seq_lens, int B, int Hq, int Hkv, int L_max, int d,
                 float scale, int num_splits, void* out, int out_dtype, float* lse, void* workspace,
-                size_t workspace_bytes, void* stream) {
+                size_t workspace_bytes, void* stream, bool unified = false, float phi = 0.f) {
     const int st = check_shape(B, Hq, Hkv, L_max, d);
     if (st != FD_OK) return st;
+    if (unified && !(std::fabs(phi) <= kMaxAbsPhi)) return FD_ERR_INVALID_ARG;
     fd::DecodeArgs a = {};
+    a.unified = unified ? 1 : 0;
+    a.phi = phi;
     a.q = q;
     a.k = k;
     a.v = v;
@@ -232,8 +238,10 @@ int dense_entry(Cache cache, const void* q, const void* k, const void* v, const 
 int paged_entry(Cache cache, const void* q, const void* k_pages, const void* v_pages, const void* k_scales,
                 const void* v_scales, const int32_t* page_table, int max_pages, int num_pages,
                 const int32_t* seq_lens, int page_size, int B, int Hq, int Hkv, int d, float scale, int num_splits,
-                void* out, int out_dtype, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+                void* out, int out_dtype, float* lse, void* workspace, size_t workspace_bytes, void* stream,
+                bool unified = false, float phi = 0.f) {
     if (page_size != kTile) return page_size > 0 ? FD_ERR_UNSUPPORTED : FD_ERR_INVALID_ARG;
+    if (unified && !(std::fabs(phi) <= kMaxAbsPhi)) return FD_ERR_INVALID_ARG;
     if (max_pages <= 0 || num_pages < 0 || max_pages > (1 << 24)) return FD_ERR_INVALID_ARG;
     const int L_max = max_pages * page_size;
     const int st = check_shape(B, Hq, Hkv, L_max, d);
@@ -241,6 +249,8 @@ int paged_entry(Cache cache, const void* q, const void* k_pages, const void* v_p
     if (B > 0 && (!page_table || !seq_lens)) return FD_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(page_table) & 3u) return FD_ERR_INVALID_ARG;
     fd::DecodeArgs a = {};
+    a.unified = unified ? 1 : 0;
+    a.phi = phi;
     a.q = q;
     a.k = k_pages;
     a.v = v_pages;
@@ -305,6 +315,25 @@ int fd_decode_paged(const void* q, const void* k_pages, const void* v_pages,
     return paged_entry(Cache::BF16, q, k_pages, v_pages, nullptr, nullptr, page_table, max_pages, num_pages,
                        seq_lens, page_size, B, Hq, Hkv, d, scale, num_splits, out, out_dtype, lse, workspace,
                        workspace_bytes, stream);
+}
+
+int fd_decode_dense_unified(const void* q, const void* k, const void* v, const int32_t* seq_lens,
+                            int B, int Hq, int Hkv, int L_max, int d, float scale, float phi, int num_splits,
+                            void* out, int out_dtype, float* lse,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+    return dense_entry(Cache::BF16, q, k, v, nullptr, nullptr, seq_lens, B, Hq, Hkv, L_max, d, scale, num_splits,
+                       out, out_dtype, lse, workspace, workspace_bytes, stream, true, phi);
+}
+
+int fd_decode_paged_unified(const void* q, const void* k_pages, const void* v_pages,
+                            const int32_t* page_table, int max_pages, int num_pages,
+                            const int32_t* seq_lens, int page_size,
+                            int B, int Hq, int Hkv, int d, float scale, float phi, int num_splits,
+                            void* out, int out_dtype, float* lse,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+    return paged_entry(Cache::BF16, q, k_pages, v_pages, nullptr, nullptr, page_table, max_pages, num_pages,
+                       seq_lens, page_size, B, Hq, Hkv, d, scale, num_splits, out, out_dtype, lse, workspace,
+                       workspace_bytes, stream, true, phi);
 }
 
 int fd_quantize_kv_fp8(const void* x, const int32_t* seq_lens, int B, int H, int L_max, int d,
@@ -399,12 +428,16 @@ size_t fd_topdelta_workspace_size(int B, int Hq, int Hkv, int L_max, int d, int 
     return fd::decode_workspace_bytes(B, Hq, d, pl.splits);
 }
 
-int fd_decode_topdelta(const void* q, const uint8_t* codes, const void* mn_scale, const int8_t* res,
-                       const void* res_scale, const void* v, const int32_t* seq_lens,
-                       int B, int Hq, int Hkv, int L_max, int d, float scale, float delta,
-                       int n_sink, int window, int num_splits,
-                       void* out, int out_dtype, float* lse, uint32_t* sel_mask, int32_t* sel_count,
-                       void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+int topdelta_entry(const void* q, const uint8_t* codes, const void* mn_scale, const int8_t* res,
+                   const void* res_scale, const void* v, const int32_t* seq_lens,
+                   int B, int Hq, int Hkv, int L_max, int d, float scale, float delta,
+                   int n_sink, int window, int num_splits,
+                   void* out, int out_dtype, float* lse, uint32_t* sel_mask, int32_t* sel_count,
+                   void* workspace, size_t workspace_bytes, void* stream, bool group_union) {
     const int st = check_shape(B, Hq, Hkv, L_max, d);
     if (st != FD_OK) return st;
     if (out_dtype != FD_OUT_F32 && out_dtype != FD_OUT_BF16) return FD_ERR_INVALID_ARG;
@@ -444,6 +477,7 @@ int fd_decode_topdelta(const void* q, const uint8_t* codes, const void* mn_scale
     a.window = window;
     a.splits = pl.splits;
     a.chunk_fixed = pl.chunk_fixed;
+    a.group_union = group_union ? 1 : 0;
     a.out = out;
     a.out_bf16 = out_dtype == FD_OUT_BF16;
     a.lse = lse;
@@ -453,6 +487,37 @@ int fd_decode_topdelta(const void* q, const uint8_t* codes, const void* mn_scale
     a.part_o = ws;
     a.part_ml = ws ? ws + (size_t)B * Hq * pl.splits * d : nullptr;
     return to_status(fd::launch_topdelta(a, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+int fd_decode_topdelta(const void* q, const uint8_t* codes, const void* mn_scale, const int8_t* res,
+                       const void* res_scale, const void* v, const int32_t* seq_lens,
+                       int B, int Hq, int Hkv, int L_max, int d, float scale, float delta,
+                       int n_sink, int window, int num_splits,
+                       void* out, int out_dtype, float* lse, uint32_t* sel_mask, int32_t* sel_count,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+    return topdelta_entry(q, codes, mn_scale, res, res_scale, v, seq_lens, B, Hq, Hkv, L_max, d, scale, delta,
+                          n_sink, window, num_splits, out, out_dtype, lse, sel_mask, sel_count, workspace,
+                          workspace_bytes, stream, false);
+}
+
+int fd_decode_topdelta_group_union(const void* q, const uint8_t* codes, const void* mn_scale, const int8_t* res,
+                                   const void* res_scale, const void* v, const int32_t* seq_lens,
+                                   int B, int Hq, int Hkv, int L_max, int d, float scale, float delta,
+                                   int n_sink, int window, int num_splits,
+                                   void* out, int out_dtype, float* lse, uint32_t* sel_mask, int32_t* sel_count,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+    return topdelta_entry(q, codes, mn_scale, res, res_scale, v, seq_lens, B, Hq, Hkv, L_max, d, scale, delta,
+                          n_sink, window, num_splits, out, out_dtype, lse, sel_mask, sel_count, workspace,
+                          workspace_bytes, stream, true);
+}
+
+int fd_debug_inject_wait_timeout(unsigned long long wait_limit_ns, int withhold_tile) {
+    fd::inject_wait_timeout(wait_limit_ns, withhold_tile);
+    return FD_OK;
 }
 
 int fd_device_status(int clear, void* stream) {

@@ -25,6 +25,7 @@
 // launch overlaps the tail of the partial pass, and the next call's partial
 // pass is scheduled while this call's merge runs (each waits on the grid
 // dependency before its first global memory access).
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 
@@ -63,8 +64,104 @@ struct PartialParams {
     int Hq, Hkv, L_max, G;
     float scale_log2;
     int splits, chunk_fixed;
+    float phi2, lo2;  // unified-max variant: phi and phi - kUnifiedRange, log2 units
+    unsigned long long wait_limit_ns;  // time limit of every pipeline wait
+    int withhold_tile;                 // >= 0: fault injection, that tile of each chunk is never copied
     StoreTarget st;
 };
+
+// Fault injection for the tests of the time-out path (fd_debug_inject_wait_timeout).
+std::atomic<unsigned long long> g_inject_wait_limit_ns{0};
+std::atomic<int> g_inject_withhold_tile{-1};
+
+// Unified-max variant (FlashDecoding++ summary, sections 1, 3 and 5: one
+// fixed max value phi for every chunk, so no chunk reduces its scores to a
+// max; a fallback to the running-max computation when the scores leave the
+// range in which that is exact).  A warp stays on the fixed reference while
+// every score it attends lies in [phi - R, phi] (R = kUnifiedRange nats):
+// then each weight 2^(s - phi) is a normal binary32 number in [e^-R, 1] and
+// no sum can overflow.  At the first tile with a score outside that range it
+// rebases its O and l from phi to the largest score it has attended so far
+// (the exact state the running-max computation would hold) and continues on
+// the running-max path.  Every result is the one the plain path computes, up
+// to fp32 rounding.
+constexpr float kUnifiedRange = 60.f;
+
+// Column-wise (per query) maximum over the 8 lanes of equal tig of a value
+// held per lane for its two accumulator columns.
+__device__ __forceinline__ float2 column_max(float2 v) {
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        v.x = fmaxf(v.x, __shfl_xor_sync(0xffffffffu, v.x, off));
+        v.y = fmaxf(v.y, __shfl_xor_sync(0xffffffffu, v.y, off));
+    }
+    return v;
+}
+
+// One tile of the tensor-core consumer on the fixed reference phi2 (log2
+// units), or the switch to the running-max path (see kUnifiedRange).
+// `seen` is the lane's max of the scores attended on the reference.
+template <int D>
+__device__ __forceinline__ void unified_softmax_pv(TokAcc<D>& ac, bool& unified, float2& seen, const float (&sc)[4],
+                                                   uint32_t vs, unsigned char* vgen, int warp, int lane, int rows,
+                                                   float phi2, float lo2) {
+    if (unified) {
+        bool ok = true;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ok &= sc[i] == -INFINITY || (sc[i] >= lo2 && sc[i] <= phi2);
+        if (__all_sync(0xffffffffu, ok)) {
+            const int mi = lane >> 3;
+            const int ld_row = warp * 16 + 8 * (mi >> 1) + (lane & 7);
+            if (warp * 16 + 16 > rows) {
+                for (int i = lane; i < 16 * (D / 8); i += 32) {
+                    const int r = warp * 16 + i / (D / 8);
+                    if (r >= rows) *reinterpret_cast<uint4*>(vgen + swz(r, i % (D / 8))) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+            }
+            float pr[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) pr[i] = exp2_approx(sc[i] - phi2);  // 2^-inf = +0
+            seen.x = fmaxf(seen.x, fmaxf(sc[0], sc[2]));
+            seen.y = fmaxf(seen.y, fmaxf(sc[1], sc[3]));
+            ac.l.x += pr[0] + pr[2];
+            ac.l.y += pr[1] + pr[3];
+            uint32_t h0, l0, h1, l1;
+            split_bf16(pr[0], pr[1], h0, l0);
+            split_bf16(pr[2], pr[3], h1, l1);
+            h0 = movmatrix_trans(h0);
+            l0 = movmatrix_trans(l0);
+            h1 = movmatrix_trans(h1);
+            l1 = movmatrix_trans(l1);
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                uint32_t v0, v1, v2, v3;
+                ldsm_x4_t(vs + swz(ld_row, 2 * mt + (mi & 1)), v0, v1, v2, v3);
+                mma_bf16(ac.o[mt], v0, v1, v2, v3, h0, h1);
+                mma_bf16(ac.o[mt], v0, v1, v2, v3, l0, l1);
+            }
+            return;
+        }
+        // fallback: O and l are relative to phi2; rebase them to the largest
+        // attended score (every one of them lies in [lo2, phi2])
+        unified = false;
+        const float2 m = column_max(seen);
+        const float a0 = m.x == -INFINITY ? 1.f : exp2_approx(phi2 - m.x);
+        const float a1 = m.y == -INFINITY ? 1.f : exp2_approx(phi2 - m.y);
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+            ac.o[mt][0] *= a0;
+            ac.o[mt][1] *= a1;
+            ac.o[mt][2] *= a0;
+            ac.o[mt][3] *= a1;
+        }
+        ac.l.x *= a0;
+        ac.l.y *= a1;
+        ac.m = m;
+    }
+    mma_softmax_pv<D>(ac, sc, vs, vgen, warp, lane, rows);
+}
 
 // Tensor-core consumer, one warp, 16 rows of a 64-token tile: S = K Q^T on
 // mma.sync (A = the warp's K rows by ldmatrix from the swizzled tile, B = Q
@@ -93,7 +190,32 @@ __device__ __forceinline__ void mma_consume_tile(TokAcc<D>& ac, const uint32_t (
     mma_softmax_pv<D>(ac, sc, vs, vgen, warp, lane, rows);
 }
 
-template <int D, int GP, int CW, int STAGES, bool PAGED, bool MMA>
+// The same tile step through the unified-max variant.
+template <int D>
+__device__ __forceinline__ void mma_consume_tile_unified(TokAcc<D>& ac, bool& unified, float2& seen,
+                                                         const uint32_t (&qa0)[D / 16], const uint32_t (&qa2)[D / 16],
+                                                         uint32_t ks, uint32_t vs, unsigned char* vgen, int warp,
+                                                         int lane, int rows, float scale_log2, float phi2, float lo2) {
+    const int gid = lane >> 2;
+    const int mi = lane >> 3;
+    const int a_row = warp * 16 + 8 * (mi & 1) + (lane & 7);
+    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(ks + swz(a_row, 2 * kk + (mi >> 1)), a0, a1, a2, a3);
+        mma_bf16(sacc, a0, a1, a2, a3, qa0[kk], qa2[kk]);
+    }
+    const int r0 = warp * 16 + gid;
+    float sc[4];
+    sc[0] = r0 < rows ? sacc[0] * scale_log2 : -INFINITY;
+    sc[1] = r0 < rows ? sacc[1] * scale_log2 : -INFINITY;
+    sc[2] = r0 + 8 < rows ? sacc[2] * scale_log2 : -INFINITY;
+    sc[3] = r0 + 8 < rows ? sacc[3] * scale_log2 : -INFINITY;
+    unified_softmax_pv<D>(ac, unified, seen, sc, vs, vgen, warp, lane, rows, phi2, lo2);
+}
+
+template <int D, int GP, int CW, int STAGES, bool PAGED, bool MMA, bool UMAX>
 __global__ void __launch_bounds__((CW + 1) * 32, (MMA || GP < 8) ? 2 : 1)
 partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                const PartialParams p) {
@@ -147,13 +269,15 @@ partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
             prefetch_tmap(&tmv);
             const uint64_t pol = l2_evict_first_policy();
             const int head_row0 = PAGED ? 0 : (b * p.Hkv + h) * p.L_max;
-            for (int t = 0; t < ntiles; ++t) {
+            int t = 0;
+            for (; t < ntiles; ++t) {
                 const int s = t % STAGES;
                 const uint32_t ph = (uint32_t)(t / STAGES) & 1u;
-                if (!mbar_wait(&empty[s], ph ^ 1u)) {
+                if (!mbar_wait(&empty[s], ph ^ 1u, p.wait_limit_ns)) {
                     atomicOr(&g_status_decode, kStatusTimeout);
                     break;
                 }
+                if (t == p.withhold_tile) continue;  // fault injection: no copy, no arrival
                 const int tok = t0 + t * kTile;
                 const int rows = min(kTile, t1 - tok);
                 int y;
@@ -180,6 +304,14 @@ partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
                     mbar_arrive(&full[s]);
                 }
             }
+            if (t < ntiles || p.withhold_tile >= 0) {
+                // the consumers may have stopped early: before the CTA exits, let
+                // every copy this loop started land (the last tile of each stage)
+                for (int u = t - 1; u >= 0 && u >= t - STAGES; --u) {
+                    if (u == p.withhold_tile) continue;
+                    mbar_wait(&full[u % STAGES], (uint32_t)(u / STAGES) & 1u, p.wait_limit_ns);
+                }
+            }
         }
         pdl_launch_dependents();
         return;
@@ -198,19 +330,31 @@ partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
             qa2[kk] = gid < p.G ? qrow[8 * kk + 4 + tig] : 0u;
         }
         tok_acc_init(ac);
+        bool unified = UMAX;
+        float2 seen = make_float2(-INFINITY, -INFINITY);
         for (int t = 0; t < ntiles; ++t) {
             const int s = t % STAGES;
-            if (!warp_wait(&full[s], (uint32_t)(t / STAGES) & 1u)) {
+            if (!warp_wait(&full[s], (uint32_t)(t / STAGES) & 1u, p.wait_limit_ns)) {
                 atomicOr(&g_status_decode, kStatusTimeout);
                 failed = true;
                 break;
             }
             const int rows = stage_rows[s];
             unsigned char* sk = smem + s * STAGE;
-            mma_consume_tile<D>(ac, qa0, qa2, smem_u32(sk), smem_u32(sk + BOXES * kBoxBytes), sk + BOXES * kBoxBytes,
-                                warp, lane, rows, p.scale_log2);
+            if constexpr (UMAX)
+                mma_consume_tile_unified<D>(ac, unified, seen, qa0, qa2, smem_u32(sk), smem_u32(sk + BOXES * kBoxBytes),
+                                            sk + BOXES * kBoxBytes, warp, lane, rows, p.scale_log2, p.phi2, p.lo2);
+            else
+                mma_consume_tile<D>(ac, qa0, qa2, smem_u32(sk), smem_u32(sk + BOXES * kBoxBytes),
+                                    sk + BOXES * kBoxBytes, warp, lane, rows, p.scale_log2);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
+        }
+        if (UMAX && unified) {
+            // still on the reference: a column's partial is relative to phi2
+            // (none when it attended nothing)
+            const float2 m = column_max(seen);
+            ac.m = make_float2(m.x == -INFINITY ? -INFINITY : p.phi2, m.y == -INFINITY ? -INFINITY : p.phi2);
         }
         pdl_launch_dependents();
         combine_tok_warps_and_store<D, CW>(smem, warp, lane, p.G, b * p.Hq + hq0, split, ac, failed, p.st);
@@ -239,20 +383,22 @@ partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         }
     }
 
-    float m_run[GP], l_lane[GP];
+    float m_run[GP], l_lane[GP], seen[GP];
     float2 o[GP][4];
 #pragma unroll
     for (int g = 0; g < GP; ++g) {
         m_run[g] = -INFINITY;
         l_lane[g] = 0.f;
+        seen[g] = -INFINITY;
 #pragma unroll
         for (int e = 0; e < 4; ++e) o[g][e] = make_float2(0.f, 0.f);
     }
+    bool unified = UMAX;  // on the fixed reference phi (see kUnifiedRange)
 
     for (int t = 0; t < ntiles; ++t) {
         const int s = t % STAGES;
         const uint32_t ph = (uint32_t)(t / STAGES) & 1u;
-        if (!warp_wait(&full[s], ph)) {
+        if (!warp_wait(&full[s], ph, p.wait_limit_ns)) {
             atomicOr(&g_status_decode, kStatusTimeout);
             failed = true;
             break;
@@ -288,6 +434,39 @@ partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
 
         // ---- online softmax update -----------------------------------------
         float pr[GP];
+        bool on_reference = false;
+        if constexpr (UMAX) {
+            if (unified) {
+                bool ok = true;
+#pragma unroll
+                for (int g = 0; g < GP; ++g) ok &= sc[g] == -INFINITY || (sc[g] >= p.lo2 && sc[g] <= p.phi2);
+                if (__all_sync(0xffffffffu, ok)) {
+                    on_reference = true;  // weights 2^(s - phi), no max, no rescale
+#pragma unroll
+                    for (int g = 0; g < GP; ++g) {
+                        pr[g] = exp2_approx(sc[g] - p.phi2);
+                        seen[g] = fmaxf(seen[g], sc[g]);
+                        l_lane[g] += my_dup ? 0.f : pr[g];
+                    }
+                } else {
+                    // fallback: rebase O and l from phi to the largest attended score
+                    unified = false;
+#pragma unroll
+                    for (int g = 0; g < GP; ++g) {
+                        float m = seen[g];
+#pragma unroll
+                        for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+                        const float a = m == -INFINITY ? 1.f : exp2_approx(p.phi2 - m);
+                        m_run[g] = m;
+                        l_lane[g] *= a;
+                        const float2 a2 = make_float2(a, a);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) o[g][e] = f2mul(o[g][e], a2);
+                    }
+                }
+            }
+        }
+        if (!on_reference) {
 #pragma unroll
         for (int g = 0; g < GP; ++g) {
             float mx = sc[g];
@@ -306,6 +485,7 @@ partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
             const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
             for (int e = 0; e < 4; ++e) o[g][e] = f2mul(o[g][e], a2);
+        }
         }
 
         // ---- o += p * v over my rows --------------------------------------
@@ -332,6 +512,17 @@ partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    if (UMAX && unified) {
+        // still on the reference: the partial is relative to phi (none when
+        // nothing was attended)
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+            float m = seen[g];
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+            m_run[g] = m == -INFINITY ? -INFINITY : p.phi2;
+        }
     }
     pdl_launch_dependents();
     combine_warps_and_store<D, GP, CW>(smem, warp, lane, p.G, b * p.Hq + hq0, split, m_run, l_lane, o, failed,
@@ -375,7 +566,7 @@ merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml
     if (dim == 0 && lse) lse[row] = wsum > 0.f ? (M + __log2f(wsum)) * kLn2 : -INFINITY;
 }
 
-template <int D, int GP, bool PAGED>
+template <int D, int GP, bool PAGED, bool UMAX = false>
 struct PartialLauncher {
     // groups of 2..8 run on the tensor cores; single queries on CUDA cores
     static constexpr bool MMA = GP >= 2;
@@ -385,7 +576,7 @@ struct PartialLauncher {
     static constexpr int SMEM = 1024 + STAGES * STAGE + STAGES * 16 + STAGES * 4 + 64;
     static constexpr int RED = CW * 8 * D * 4 + 2 * CW * 8 * 4;
     static_assert(STAGES * STAGE >= RED, "reduction scratch must fit in the ring");
-    static constexpr auto kernel = partial_kernel<D, MMA ? 8 : GP, CW, STAGES, PAGED, MMA>;
+    static constexpr auto kernel = partial_kernel<D, MMA ? 8 : GP, CW, STAGES, PAGED, MMA, UMAX>;
 
     // Per device: raise the dynamic shared-memory limit once, and remember
     // the occupancy the planner sizes its grids with.
@@ -425,11 +616,18 @@ int ctas_per_sm_dispatch(int G) {
     return PartialLauncher<D, 8, PAGED>::ctas_per_sm();
 }
 
+template <int D, bool PAGED, bool UMAX>
+cudaError_t launch_dispatch_v(int G, const CUtensorMap& tk, const CUtensorMap& tv, const PartialParams& pp,
+                              dim3 grid, cudaStream_t st) {
+    if (G <= 1) return PartialLauncher<D, 1, PAGED, UMAX>::launch(tk, tv, pp, grid, st);
+    return PartialLauncher<D, 8, PAGED, UMAX>::launch(tk, tv, pp, grid, st);
+}
+
 template <int D, bool PAGED>
-cudaError_t launch_dispatch(int G, const CUtensorMap& tk, const CUtensorMap& tv, const PartialParams& pp, dim3 grid,
-                            cudaStream_t st) {
-    if (G <= 1) return PartialLauncher<D, 1, PAGED>::launch(tk, tv, pp, grid, st);
-    return PartialLauncher<D, 8, PAGED>::launch(tk, tv, pp, grid, st);
+cudaError_t launch_dispatch(int G, bool unified, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const PartialParams& pp, dim3 grid, cudaStream_t st) {
+    return unified ? launch_dispatch_v<D, PAGED, true>(G, tk, tv, pp, grid, st)
+                   : launch_dispatch_v<D, PAGED, false>(G, tk, tv, pp, grid, st);
 }
 
 }  // namespace
@@ -481,6 +679,11 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     pp.scale_log2 = a.scale * kLog2e;
     pp.splits = a.splits;
     pp.chunk_fixed = a.chunk_fixed;
+    pp.phi2 = a.phi * kLog2e;
+    pp.lo2 = (a.phi - kUnifiedRange) * kLog2e;
+    const unsigned long long lim = g_inject_wait_limit_ns.load(std::memory_order_relaxed);
+    pp.wait_limit_ns = lim ? lim : kWaitLimitNs;
+    pp.withhold_tile = g_inject_withhold_tile.load(std::memory_order_relaxed);
     pp.st.part_o = a.part_o;
     pp.st.part_ml = a.part_ml;
     pp.st.out = a.out;
@@ -490,13 +693,19 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     pp.st.splits = a.splits;
     const dim3 grid((unsigned)a.splits, (unsigned)a.Hkv, (unsigned)a.B);
     cudaError_t e;
-    if (a.D == 128) e = paged ? launch_dispatch<128, true>(pp.G, tk, tv, pp, grid, stream)
-                              : launch_dispatch<128, false>(pp.G, tk, tv, pp, grid, stream);
-    else e = paged ? launch_dispatch<64, true>(pp.G, tk, tv, pp, grid, stream)
-                   : launch_dispatch<64, false>(pp.G, tk, tv, pp, grid, stream);
+    const bool u = a.unified != 0;
+    if (a.D == 128) e = paged ? launch_dispatch<128, true>(pp.G, u, tk, tv, pp, grid, stream)
+                              : launch_dispatch<128, false>(pp.G, u, tk, tv, pp, grid, stream);
+    else e = paged ? launch_dispatch<64, true>(pp.G, u, tk, tv, pp, grid, stream)
+                   : launch_dispatch<64, false>(pp.G, u, tk, tv, pp, grid, stream);
     if (e != cudaSuccess || a.splits == 1) return e;
     return launch_merge(a.part_o, a.part_ml, a.seq_lens, a.B, a.Hq, a.L_max, a.D, a.splits, a.chunk_fixed,
                         a.out, a.out_bf16, a.lse, stream);
+}
+
+void inject_wait_timeout(unsigned long long wait_limit_ns, int withhold_tile) {
+    g_inject_wait_limit_ns.store(wait_limit_ns, std::memory_order_relaxed);
+    g_inject_withhold_tile.store(withhold_tile < 0 ? -1 : withhold_tile, std::memory_order_relaxed);
 }
 
 cudaError_t decode_status_read(unsigned* bits, bool clear) {

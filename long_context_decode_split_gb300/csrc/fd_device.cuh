@@ -83,22 +83,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Returns false if
-// the wait hit its limit (the caller records kStatusTimeout and stops).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// the wait hit its limit (the caller records kStatusTimeout and stops):
+// limit_ns of %globaltimer (checked every 16 polls) or kWaitLimitPolls polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
     const unsigned long long t0 = global_timer_ns();
     for (unsigned it = 1; it < kWaitLimitPolls; ++it) {
         if (mbar_try_wait(a, parity)) return true;
-        if ((it & 1023u) == 0u && global_timer_ns() - t0 > kWaitLimitNs) return false;
+        if ((it & 15u) == 0u && global_timer_ns() - t0 > limit_ns) return false;
     }
     return false;
 }
 
 // mbar_wait for all 32 lanes of a warp, with one verdict for the whole warp
 // (so a time-out can never split the warp before its shuffles).
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
-    const bool ok = mbar_wait(bar, parity);
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
+    const bool ok = mbar_wait(bar, parity, limit_ns);
     return __all_sync(0xffffffffu, ok);
 }
 

@@ -45,6 +45,8 @@ struct DecodeArgs {
     float* lse;               // [B, Hq] or null
     float* part_o;            // workspace: [B, Hq, splits, D]
     float* part_ml;           // workspace: [B, Hq, splits, 2]
+    int unified;              // bf16 cache only: unified-max variant with fixed max value `phi`
+    float phi;                // (natural-log units of the scaled score)
 };
 
 // Workspace bytes for `splits` chunks (0 when splits == 1).
@@ -58,6 +60,9 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
 // Device status words, one per translation unit that owns kernels.
 cudaError_t decode_status_read(unsigned* bits, bool clear);
+
+// Fault injection for the bf16 dense/paged pass (fd_debug_inject_wait_timeout).
+void inject_wait_timeout(unsigned long long wait_limit_ns, int withhold_tile);
 
 struct QuantArgs {
     const void* k;            // [B, Hkv, L_max, D] bf16
@@ -82,6 +87,7 @@ struct TopDeltaArgs {
     float scale, delta;
     int n_sink, window;
     int splits, chunk_fixed;
+    int group_union;
     void* out;
     int out_bf16;
     float* lse;

@@ -22,7 +22,10 @@
 //     tiles without candidates are never read from HBM.
 //   * attend: exact scores s = s~ + scale * sum_g rs_g <q_g, rq_g> for the
 //     candidates, online softmax and O^T += V^T P^T, then the same warp
-//     combine and chunk merge as the dense pass.
+//     combine and chunk merge as the dense pass.  With `group_union` every
+//     query head of a KV group attends to the union of the group's candidate
+//     sets (the tiles loaded are the same: a tile is loaded when any head of
+//     the group selected one of its tokens).
 // Both dot stages put the warp's 16 tokens in the MMA's M dimension and the
 // group's query heads in N (S = K Q^T), so no accumulator is spent on
 // padding query rows; movmatrix turns the P values into P^T fragments.
@@ -173,6 +176,7 @@ struct TDParams {
     float scale, delta;
     int n_sink, window;
     int splits, chunk_fixed;
+    int group_union;  // every head of a KV group attends to the union of the group's candidates
     uint32_t* sel_mask;
     int32_t* sel_count;
     StoreTarget st;
@@ -609,11 +613,26 @@ topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constan
             residual_tile<D>(smem_u32(st_base), st_base + Gm::RES_BYTES + Gm::V_BYTES, warp, lane, tq, rt);
             const float4 sv = reinterpret_cast<const float4*>(dec_s)[(ds * CW + warp) * 32 + lane];
             const float stv[4] = {sv.x, sv.y, sv.z, sv.w};
+            bool selv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = warp * 16 + gid + 8 * (i >> 1);
+                selv[i] = c_real[i & 1] && r < rows && stv[i] >= thr[i & 1];
+            }
+            if (p.group_union) {
+                // a token some head of the group selected is attended by every head
+                // (the lanes of a quad hold the 8 query columns of the same two rows)
+                uint32_t any = (selv[0] || selv[1] ? 1u : 0u) | (selv[2] || selv[3] ? 2u : 0u);
+                any |= __shfl_xor_sync(0xffffffffu, any, 1);
+                any |= __shfl_xor_sync(0xffffffffu, any, 2);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) selv[i] = c_real[i & 1] && ((any >> (i >> 1)) & 1u);
+            }
             float sc[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int r = warp * 16 + gid + 8 * (i >> 1);
-                const bool sel = c_real[i & 1] && r < rows && stv[i] >= thr[i & 1];
+                const bool sel = selv[i];
                 sc[i] = sel ? fmaf(p.scale, rt[i], stv[i]) * kLog2e : -INFINITY;
                 if (sel) {
                     ++cnt[i & 1];
@@ -735,6 +754,7 @@ cudaError_t launch_topdelta(const TopDeltaArgs& a, cudaStream_t stream) {
     pp.window = a.window;
     pp.splits = a.splits;
     pp.chunk_fixed = a.chunk_fixed;
+    pp.group_union = a.group_union;
     pp.sel_mask = a.sel_mask;
     pp.sel_count = a.sel_count;
     pp.st.out = a.out;

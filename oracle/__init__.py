@@ -14,6 +14,10 @@ Functions (each follows the passage cited in ``fd_oracle.c``):
   quantize_keys       2-bit body + int8 residual encoding (FFD summary section 5)
   dequantize_keys     k~ = deq2 (+ deq8) as binary64
   decode_topdelta     FFD pipeline, Fig. 2 order (sections 3-5)
+  decode_topdelta_group_union
+                      the same selection rule per query head, the union of
+                      the sets over the heads that share a KV head, attention
+                      of every head of the group over that union
   float_to_half       IEEE binary32 -> binary16, round to nearest even
   quantize_kv_fp8     per-row scaled e4m3 KV cache encoding
   dequantize_kv_fp8   its exact binary64 values
@@ -363,3 +367,55 @@ def decode_dense_fp4(q, k_codes, k_scales, v_codes, v_scales, seq_lens, scale, n
     kt = dequantize_kv_fp4(k_codes, k_scales, seq_lens)
     vt = dequantize_kv_fp4(v_codes, v_scales, seq_lens)
     return decode_dense_f64(qf, kt, vt, seq_lens, scale, n_threads)
+
+
+def _bf16_to_f64(a):
+    """bf16 bit patterns (uint16) -> their exact binary64 values."""
+    return (np.asarray(a, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def decode_topdelta_group_union(q, codes, mn_scale, res, res_scale, v, seq_lens, scale, delta,
+                                n_sink=4, window=64, want_scores=False, n_threads=0):
+    """Top-delta with one candidate set per KV group (FFD summary: the rule
+    of section 3 and the pseudo-max of section 4 per query head, Fig. 2's
+    exact attention over the candidates; the set shared by a group is this
+    library's option, not the page's).  Steps:
+      1-3. Sel_g per query head g, exactly as decode_topdelta;
+      4.   Sel_group = union of Sel_g over the G heads that read one KV head;
+      5.   every head of the group: softmax over Sel_group of the residual-
+           corrected scores s_j = scale * <q, k~_j> (k~ from dequantize_keys),
+           times the bf16 V rows -- the binary64 dense definition
+           (decode_dense_f64) restricted to the tokens of Sel_group.
+    Returns decode_topdelta's dict with sel_mask / sel_count describing the
+    attended set (Sel_group, the same for every head of a group), plus
+    head_sel_mask / head_sel_count (each head's own Sel_g) and m_hat."""
+    per_head = decode_topdelta(q, codes, mn_scale, res, res_scale, v, seq_lens, scale, delta, n_sink, window,
+                               want_scores=want_scores, n_threads=n_threads)
+    q, v = _u16(q), _u16(v)
+    B, Hq, d = q.shape
+    _, Hkv, L_max, _ = v.shape
+    G = Hq // Hkv
+    words = per_head["sel_mask"].shape[-1]
+    group = np.bitwise_or.reduce(per_head["sel_mask"].reshape(B, Hkv, G, words), axis=2)     # [B, Hkv, words]
+    sel = np.unpackbits(group.view(np.uint8), axis=-1, bitorder="little")[..., :L_max].astype(bool)
+    kt = dequantize_keys(codes, mn_scale, res, res_scale, seq_lens)
+    qf, vf = _bf16_to_f64(q), _bf16_to_f64(v)
+    lens = [L_max] * B if seq_lens is None else [int(x) for x in _i32(seq_lens)]
+    out = np.zeros((B, Hq, d), np.float64)
+    lse = np.full((B, Hq), -np.inf, np.float64)
+    cnt = np.zeros((B, Hq), np.int32)
+    for b in range(B):
+        for h in range(Hkv):
+            idx = np.nonzero(sel[b, h, :lens[b]])[0]
+            cnt[b, h * G:(h + 1) * G] = idx.size
+            if idx.size == 0:
+                continue
+            o, l = decode_dense_f64(qf[b:b + 1, h * G:(h + 1) * G], kt[b:b + 1, h:h + 1, idx],
+                                    vf[b:b + 1, h:h + 1, idx], None, scale, n_threads)
+            out[b, h * G:(h + 1) * G] = o[0]
+            lse[b, h * G:(h + 1) * G] = l[0]
+    r = dict(out=out, lse=lse, sel_mask=np.repeat(group, G, axis=1), sel_count=cnt, m_hat=per_head["m_hat"],
+             head_sel_mask=per_head["sel_mask"], head_sel_count=per_head["sel_count"])
+    if want_scores:
+        r["s_tilde"] = per_head["s_tilde"]
+    return r

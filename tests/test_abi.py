@@ -116,3 +116,17 @@ def test_fp4_host_validation(lib):
     assert lib.fd_quantize_kv_fp4(a, None, 1, 2, 100, 128, a, P(0x10008), None) == fd.FD_ERR_INVALID_ARG
     assert fd.fd_num_splits_fp4(1, 32, 32, 32768, 128, 6) == 6
     assert fd.fd_decode_fp4_workspace_size(2, 8, 2, 1000, 64, 3) == 2 * 8 * 3 * (64 + 2) * 4 + 256
+
+
+def test_unified_max_host_validation(lib):
+    a = P(0x10000)
+    for phi in (float("inf"), float("nan"), 1e31):
+        assert lib.fd_decode_dense_unified(a, a, a, None, 1, 8, 2, 256, 128, 0.1, phi, 1, a, 1, None, None, 0,
+                                           None) == fd.FD_ERR_INVALID_ARG
+        assert lib.fd_decode_paged_unified(a, a, a, a, 4, 4, a, 64, 1, 8, 2, 128, 0.1, phi, 1, a, 1, None,
+                                           None, 0, None) == fd.FD_ERR_INVALID_ARG
+    # the other checks are fd_decode_dense's
+    assert lib.fd_decode_dense_unified(a, a, a, None, 1, 8, 2, 256, 96, 0.1, 6.5, 1, a, 1, None, None, 0,
+                                       None) == fd.FD_ERR_UNSUPPORTED
+    assert lib.fd_decode_dense_unified(a, a, a, None, 1, 8, 2, 256, 128, 0.1, 6.5, 2, a, 1, None, None, 0,
+                                       None) == fd.FD_ERR_WORKSPACE_TOO_SMALL

@@ -26,7 +26,8 @@ def gpu_arm_config(workload, gpus=1):
     sys.path.insert(0, ROOT)
     import bench
     args = bench.argparse.Namespace(workload=workload, batch=None, seq_len=None, num_splits=None,
-                                    n_sink=4, window=64, gpus=gpus, graph=0)
+                                    n_sink=4, window=64, gpus=gpus, graph=0, phi=6.5,
+                                    plant_frac=0.001)
     return bench.workload_config(args)
 
 
@@ -38,7 +39,7 @@ def test_default_workload_is_the_largest_single_gpu_config():
 
 
 @pytest.mark.timeout(600)
-@pytest.mark.parametrize("workload", ["tiny", "mha32k_fp8", "ffd_topdelta5"])
+@pytest.mark.parametrize("workload", ["tiny", "mha32k_fp8", "ffd_topdelta5", "ffd_sparse_topdelta5_union"])
 def test_reference_arm_json_line(workload):
     r = run_bench(["--impl", "reference", "--workload", workload, "--steps", "3", "--warmup", "3"])
     assert r.returncode == 0, r.stderr[-2000:]

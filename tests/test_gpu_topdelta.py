@@ -80,19 +80,20 @@ def test_encoder_full_ffd_sample(fd, oracle):
 
 # -------------------------------------------------------------- top-delta
 
-def run_both(fd, oracle, p, delta, n_sink=4, window=64, num_splits=0, out_dtype="bf16"):
+def run_both(fd, oracle, p, delta, n_sink=4, window=64, num_splits=0, out_dtype="bf16", group_union=False):
     sl = p.seq_lens
     enc = oracle.quantize_keys(bits(p.k), sl.cpu())
-    ref = oracle.decode_topdelta(bits(p.q), *enc, bits(p.v), sl.cpu(), p.scale, delta, n_sink, window,
-                                 want_scores=True)
+    ref_fn = oracle.decode_topdelta_group_union if group_union else oracle.decode_topdelta
+    ref = ref_fn(bits(p.q), *enc, bits(p.v), sl.cpu(), p.scale, delta, n_sink, window, want_scores=True)
     c, ms, r, rs = to_dev(enc)
     out, lse, mask, cnt = fd.fd_decode_topdelta(p.q, c, ms, r, rs, p.v, sl, p.scale, delta, n_sink, window,
-                                                num_splits=num_splits, out_dtype=out_dtype, want_selection=True)
+                                                num_splits=num_splits, out_dtype=out_dtype, want_selection=True,
+                                                group_union=group_union)
     torch.cuda.synchronize()
     return enc, ref, out, lse, mask.cpu().numpy().view(np.uint32), cnt.cpu().numpy()
 
 
-def check_topdelta(oracle, p, enc, ref, out, lse, mask, cnt, delta, tol):
+def check_topdelta(oracle, p, enc, ref, out, lse, mask, cnt, delta, tol, group_union=False):
     L_max = p.L_max
     lens = p.seq_lens.cpu().numpy()
     got_sel = mask_bits(mask, L_max)
@@ -109,7 +110,11 @@ def check_topdelta(oracle, p, enc, ref, out, lse, mask, cnt, delta, tol):
         for hq in range(p.Hq):
             diff = np.nonzero(got_sel[b, hq, :L] != ref_sel[b, hq, :L])[0]
             if diff.size:
-                near = np.abs(st[b, hq, diff] - thr[b, hq, 0]) <= TIE
+                # a token may differ only at a tie: of this head, or (shared sets) of any head of its group
+                heads = range((hq // G) * G, (hq // G + 1) * G) if group_union else (hq,)
+                near = np.zeros(diff.size, bool)
+                for g in heads:
+                    near |= np.abs(st[b, g, diff] - thr[b, g, 0]) <= TIE
                 assert near.all(), f"selection differs away from the threshold at b={b} hq={hq} j={diff[~near]}"
                 ties += diff.size
             assert cnt[b, hq] == int(got_sel[b, hq, :L].sum())
@@ -251,3 +256,51 @@ def test_topdelta_full_ffd_sampled(fd, oracle):
             ties += check_topdelta(oracle, sub, enc, ref, out[:, h * G:(h + 1) * G], lse[:, h * G:(h + 1) * G],
                                    mask[:, h * G:(h + 1) * G], cnt[:, h * G:(h + 1) * G], delta, BF16_TOL)
         print(f"delta={delta}: tie tokens with differing membership: {ties}")
+
+
+# ------------------------------------------------- anchor settings, shared sets
+
+@pytest.mark.parametrize("n_sink", [0, 1, 16, 64])
+@pytest.mark.parametrize("window", [0, 16, 256, 1024])
+def test_topdelta_anchor_settings(fd, oracle, n_sink, window):
+    """The sink counts and window lengths the anchor sweep times, against the
+    oracle: they move the anchor pass's tile walk (sink tiles, the jump to the
+    window, windows longer than the sequence, no anchors at all: m^ = -inf,
+    everything selected)."""
+    p = W.ffd(seed=17, B=4, L=2500, Hq=8, Hkv=2, d=128)
+    lens = torch.tensor([2500, 700, 5, 0], dtype=torch.int32)
+    p = W.Problem(p.name, p.q.to(DEV), p.k.to(DEV), p.v.to(DEV), lens.to(DEV), p.scale, p.L_max)
+    enc, ref, out, lse, mask, cnt = run_both(fd, oracle, p, 5.0, n_sink, window)
+    check_topdelta(oracle, p, enc, ref, out, lse, mask, cnt, 5.0, BF16_TOL)
+    if n_sink == 0 and window == 0:
+        assert np.array_equal(cnt, np.repeat(lens.numpy()[:, None], p.Hq, axis=1))
+
+
+@pytest.mark.parametrize("G", [1, 4, 8])
+@pytest.mark.parametrize("delta", [2.0, 5.0])
+def test_topdelta_group_union_parity(fd, oracle, G, delta):
+    Hkv = 2
+    p = W.ffd(seed=23 + G, B=2, L=3000, Hq=Hkv * G, Hkv=Hkv, d=128)
+    lens = torch.tensor([3000, 1234], dtype=torch.int32)
+    p = W.Problem(p.name, p.q.to(DEV), p.k.to(DEV), p.v.to(DEV), lens.to(DEV), p.scale, p.L_max)
+    for ns, dt, tol in ((0, "bf16", BF16_TOL), (3, "f32", F32_TOL)):
+        enc, ref, out, lse, mask, cnt = run_both(fd, oracle, p, delta, num_splits=ns, out_dtype=dt,
+                                                 group_union=True)
+        check_topdelta(oracle, p, enc, ref, out, lse, mask, cnt, delta, tol, group_union=True)
+        # one set per group
+        m = mask.reshape(p.B, Hkv, G, -1)
+        assert np.all(m == m[:, :, :1])
+
+
+def test_topdelta_sparse_cache_skips_tiles(fd, oracle):
+    """A sparse cache (anchors and 0.2% planted tokens far above
+    the rest): few 64-token tiles hold a candidate, so the residual and V of
+    most tiles are never read; sets and outputs still match the oracle."""
+    p = W.ffd(seed=29, B=2, L=8192, Hq=8, Hkv=2, d=128, anchor_boost=20.0, plant_mean=20.0, plant_frac=0.002)
+    p = W.Problem(p.name, p.q.to(DEV), p.k.to(DEV), p.v.to(DEV), p.seq_lens.to(DEV), p.scale, p.L_max)
+    for group_union in (False, True):
+        enc, ref, out, lse, mask, cnt = run_both(fd, oracle, p, 5.0, group_union=group_union)
+        check_topdelta(oracle, p, enc, ref, out, lse, mask, cnt, 5.0, BF16_TOL, group_union=group_union)
+        sel = mask_bits(mask, p.L_max).reshape(p.B, p.Hkv, p.Hq // p.Hkv, -1).any(axis=2)
+        tiles = sel.reshape(p.B, p.Hkv, -1, 64).any(axis=-1)
+        assert tiles.mean() < 0.25, tiles.mean()

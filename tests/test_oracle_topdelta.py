@@ -299,3 +299,92 @@ def test_rule_laws(oracle):
             np.testing.assert_array_equal(mask, st >= st[anchors].max() - 5.0)
             # the anchor that sets the pseudo-max is always a candidate
             assert mask[anchors[np.argmax(st[anchors])]]
+
+
+# ------------------------------------------- candidate set shared by a KV group
+
+def two_head_profiles(mn0, mn1):
+    """Two query heads on one KV head, d = 64: head 0 reads only channels
+    0..31 (q = 1/32 there), head 1 only channels 32..63, and the 2-bit body of
+    token t is the constant mn0[t] on the first group and mn1[t] on the
+    second (s16 = 0), so with scale 1 head g's 2-bit score is mn_g[t]."""
+    L = len(mn0)
+    d = 64
+    codes = np.zeros((1, 1, L, d // 4), np.uint8)
+    ms = np.zeros((1, 1, L, 2, 2), np.uint16)
+    ms[0, 0, :, 0, 0] = np.asarray(mn0, np.float16).view(np.uint16)
+    ms[0, 0, :, 1, 0] = np.asarray(mn1, np.float16).view(np.uint16)
+    res = np.zeros((1, 1, L, d), np.int8)
+    rs = np.zeros((1, 1, L, 2), np.uint16)
+    q = torch.zeros((1, 2, d))
+    q[0, 0, :32] = 1.0 / 32
+    q[0, 1, 32:] = 1.0 / 32
+    q = q.to(torch.bfloat16)
+    v = torch.randn((1, 1, L, d), generator=torch.Generator().manual_seed(3)).to(torch.bfloat16)
+    return q, codes, ms, res, rs, v
+
+
+def test_group_union_hand_profile(oracle):
+    scipy_special = pytest.importorskip("scipy.special")
+    # L = 100, 4 sinks, window 64 -> anchors {0..3} U {36..99}, all at 0 for both heads: m^ = 0.
+    # Token 10: head 0 scores -2 (kept at delta 5), head 1 scores -9 (dropped).
+    # Token 20: head 0 scores -8 (dropped), head 1 scores -1 (kept).  Other tokens -20.
+    L = 100
+    mn0 = np.full(L, -20.0)
+    mn1 = np.full(L, -20.0)
+    for mn in (mn0, mn1):
+        mn[:4] = 0.0
+        mn[36:] = 0.0
+    mn0[10], mn1[10] = -2.0, -9.0
+    mn0[20], mn1[20] = -8.0, -1.0
+    q, codes, ms, res, rs, v = two_head_profiles(mn0, mn1)
+    r = oracle.decode_topdelta_group_union(q, codes, ms, res, rs, v, None, 1.0, 5.0, 4, 64)
+    anchors = list(range(4)) + list(range(36, L))
+    own = {0: sorted(anchors + [10]), 1: sorted(anchors + [20])}
+    union = sorted(anchors + [10, 20])
+    for g, mn in ((0, mn0), (1, mn1)):
+        got_own = [j for j in range(L) if (r["head_sel_mask"][0, g, j // 32] >> (j % 32)) & 1]
+        got = [j for j in range(L) if (r["sel_mask"][0, g, j // 32] >> (j % 32)) & 1]
+        assert got_own == own[g] and got == union
+        assert r["sel_count"][0, g] == len(union) and r["head_sel_count"][0, g] == len(own[g])
+        # every head weighs the whole union with its own scores
+        s = mn[union]
+        w = scipy_special.softmax(s)
+        np.testing.assert_allclose(r["out"][0, g], w @ v[0, 0, union].double().numpy(), atol=1e-13)
+        assert r["lse"][0, g] == pytest.approx(scipy_special.logsumexp(s), abs=1e-13)
+
+
+def test_group_union_laws(oracle):
+    p = ffd_small(seed=11, L=900)
+    codes, ms, res, rs = oracle.quantize_keys(bits(p.k))
+    args = (bits(p.q), codes, ms, res, rs, bits(p.v), None, p.scale)
+    G = p.Hq // p.Hkv
+    for delta in (2.0, 5.0):
+        per = oracle.decode_topdelta(*args, delta)
+        uni = oracle.decode_topdelta_group_union(*args, delta)
+        np.testing.assert_array_equal(uni["head_sel_mask"], per["sel_mask"])
+        grp = uni["sel_mask"].reshape(p.B, p.Hkv, G, -1)
+        # the union contains every head's set and is the same for the whole group
+        assert np.all((per["sel_mask"] & ~uni["sel_mask"]) == 0)
+        assert np.all(grp == grp[:, :, :1])
+        # attending to more keys can only raise log sum exp
+        assert np.all(uni["lse"] >= per["lse"] - 1e-12)
+    # delta = inf: everything is selected and the result is dense attention on k~
+    uni = oracle.decode_topdelta_group_union(*args, math.inf)
+    kt = oracle.dequantize_keys(codes, ms, res, rs)
+    ref, lref = oracle.decode_dense_f64(p.q.double().numpy(), kt, p.v.double().numpy(), None, p.scale)
+    np.testing.assert_allclose(uni["out"], ref, atol=1e-12)
+    np.testing.assert_allclose(uni["lse"], lref, atol=1e-12)
+
+
+def test_group_union_of_one_head_is_the_per_head_rule(oracle):
+    p = W.ffd(seed=12, B=2, L=700, Hq=4, Hkv=4, d=64)
+    lens = torch.tensor([700, 333], dtype=torch.int32)
+    codes, ms, res, rs = oracle.quantize_keys(bits(p.k), lens)
+    args = (bits(p.q), codes, ms, res, rs, bits(p.v), lens, p.scale, 5.0)
+    per = oracle.decode_topdelta(*args)
+    uni = oracle.decode_topdelta_group_union(*args)
+    np.testing.assert_array_equal(uni["sel_mask"], per["sel_mask"])
+    np.testing.assert_array_equal(uni["sel_count"], per["sel_count"])
+    np.testing.assert_allclose(uni["out"], per["out"], atol=1e-12)
+    np.testing.assert_allclose(uni["lse"], per["lse"], atol=1e-12)

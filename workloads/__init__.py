@@ -155,19 +155,25 @@ def million(seed=0, device="cpu", L=1 << 20) -> Problem:
     return Problem("million", q, k, v, sl, 1.0 / math.sqrt(d), L)
 
 
-def ffd(seed=0, device="cpu", B=4, L=131072, Hq=32, Hkv=8, d=128) -> Problem:
+def ffd(seed=0, device="cpu", B=4, L=131072, Hq=32, Hkv=8, d=128, anchor_boost=2.5, plant_mean=2.0,
+        plant_std=0.5, plant_frac=0.01) -> Problem:
+    """The FFD recipe; the keyword arguments after d change it into a sparser
+    cache (e.g. anchor_boost=20, plant_mean=20, plant_frac=0.001: the anchors
+    and the planted tokens score ~13 units above the rest at G=4, so at
+    delta 5 the candidates are those tokens alone, and the 64-token tiles
+    holding one are ~1 - (1 - plant_frac)^64 of the cache)."""
     g = _gen(seed, device)
     q = _randn((B, Hq, d), g, device).to(torch.bfloat16)
-    n_planted = int(round(0.01 * L))
+    n_planted = int(round(plant_frac * L))
     anchors = torch.cat([torch.arange(0, min(4, L), device=device),
                          torch.arange(max(0, L - 64), L, device=device)]).unique()
-    anchor_coef = torch.full((anchors.numel(),), 2.5, device=device)
+    anchor_coef = torch.full((anchors.numel(),), float(anchor_boost), device=device)
     lo, hi = 4, L - 64
 
     def boosts(b, h):
         if hi > lo and n_planted > 0:
             pl = torch.randperm(hi - lo, generator=g, device=device)[:n_planted] + lo
-            c = 2.0 + 0.5 * _randn((pl.numel(),), g, device)
+            c = plant_mean + plant_std * _randn((pl.numel(),), g, device)
             return torch.cat([anchors, pl]), torch.cat([anchor_coef, c])
         return anchors, anchor_coef
 
