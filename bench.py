@@ -32,6 +32,7 @@ Prints ONE JSON line on rank 0.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -55,7 +56,8 @@ DEFAULT_STEPS = {"tiny": 20000, "mha32k": 20000, "gqa_paged": 3000, "million": 3
                  "mha32k_fp4": 20000, "million_fp4": 4000, "ffd_dense_fp4": 6000, "gqa_paged_fp4": 4000,
                  "mha32k_unified": 20000, "million_unified": 3000, "gqa_paged_unified": 3000,
                  "ffd_topdelta5_union": 4000, "ffd_topdelta7_union": 4000,
-                 "ffd_sparse_dense": 4000, "ffd_sparse_topdelta5": 4000, "ffd_sparse_topdelta5_union": 4000}
+                 "ffd_sparse_dense": 4000, "ffd_sparse_topdelta5": 4000, "ffd_sparse_topdelta5_union": 4000,
+                 "ladder": 50}
 # The sparse FFD cache: anchors and planted tokens boosted by 20 along q_hat
 # (a ~13-unit score lead at G=4), --plant-frac of the tokens planted.
 SPARSE_BOOST = 20.0
@@ -186,6 +188,8 @@ class Workload:
             p = W.mha32k(seed=seed, device=device, **over)
         elif name == "million":
             p = W.million(seed=seed, device=device, **over)
+        elif name == "ladder":
+            p = W.ladder(B=batch or 1, seed=seed, device=device, **over)
         elif name == "gqa_paged":
             kw = {"B": batch} if batch is not None else {}
             if seq_len is not None:
@@ -204,6 +208,13 @@ class Workload:
         if num_splits is not None and problem is None:
             p.num_splits = num_splits
         self.p = p
+        # a dense cache smaller than L2 is rotated through enough copies that
+        # consecutive calls read from HBM (the ladder's short rungs)
+        self.copies = [p]
+        if name == "ladder":
+            for _ in range(ladder_copies(p.B, p.kv_tokens() // max(1, p.B), p.Hkv, p.d) - 1):
+                self.copies.append(dataclasses.replace(p, k=p.k.clone(), v=p.v.clone()))
+        self._turn = 0
         self.paged = p.paged
         self.out_dtype = p.out_dtype
         B, Hq, Hkv, d = p.B, p.Hq, p.Hkv, p.d
@@ -275,7 +286,9 @@ class Workload:
                 "tiles_total": int(tiles.size)}
 
     def call(self, stream=None, q=None):
-        p, fd = self.p, self.fd
+        fd = self.fd
+        p = self.copies[self._turn % len(self.copies)]
+        self._turn += 1
         q = p.q if q is None else q
         if self.fp8 or self.fp4:
             kc, ks, vc, vs = self.kv8
@@ -342,6 +355,14 @@ class Workload:
         return c
 
 
+L2_BYTES = 129 * 1024 * 1024
+
+
+def ladder_copies(B, L, Hkv, d):
+    """Copies of a ladder cache that together exceed three times the L2."""
+    return max(1, -(-3 * L2_BYTES // (B * L * Hkv * d * 4)))
+
+
 def workload_config(args):
     """The workload as the command line names it: the same dict in the GPU
     arm and in the reference arm (nothing here depends on the device)."""
@@ -349,13 +370,13 @@ def workload_config(args):
     base = name[:-4] if name.endswith(("_fp8", "_fp4")) else name
     base = base[:-len("_unified")] if base.endswith("_unified") else base
     B, Hq, Hkv, L, d = FULL_SHAPES[name]
-    if args.batch is not None and (base == "gqa_paged" or base.startswith("ffd")):
+    if args.batch is not None and (base in ("gqa_paged", "ladder") or base.startswith("ffd")):
         B = args.batch
     if base == "gqa_paged":
         hi = args.seq_len if args.seq_len is not None else 131072
         lo = max(64, hi // 8) if args.seq_len is not None else 16384
         L = f"U{{{lo}..{hi}}} per sequence"
-    elif args.seq_len is not None and base in ("mha32k", "million"):
+    elif args.seq_len is not None and base in ("mha32k", "million", "ladder"):
         L = args.seq_len
     kv = ("e4m3 codes + f32 row scales" if name.endswith("_fp8") else
           "e2m1 codes + power-of-two scales per 32 channels" if name.endswith("_fp4") else "bf16")
@@ -363,7 +384,10 @@ def workload_config(args):
          "cache": "paged-64" if base == "gqa_paged" else "contiguous",
          "out_dtype": "f32" if base == "tiny" else "bf16", "kv_dtype": kv,
          "num_splits": "planner" if not args.num_splits else args.num_splits,
+         **({"split_sweep": True} if getattr(args, "split_sweep", False) else {}),
          "l2": "inputs smaller than L2 (no flush)" if base == "tiny" else "inputs larger than L2",
+         **({"l2": f"{ladder_copies(B, L, Hkv, d)} copies of the cache read in turn (together larger than L2)"}
+            if base == "ladder" and ladder_copies(B, L, Hkv, d) > 1 else {}),
          "parallelism": f"replicas x{args.gpus}"}
     if base == "tiny":
         c["num_splits"] = args.num_splits or 4
@@ -522,6 +546,25 @@ def time_e2e(wl, steps, warmup, dist_ctx):
     return dist_ctx.max((t1 - t0) * 1e3), host.numel(), result.numel()
 
 
+def split_sweep(args, wl, ctx):
+    """Chunk counts around the planner's choice for the same inputs: median
+    and spread of --rounds rounds of --steps calls each (dense bf16 only)."""
+    p = wl.p
+    planned = wl.splits
+    cands = sorted({max(1, int(round(planned * f))) for f in (0.5, 0.75, 1.0, 1.25, 1.5, 2.0)})
+    res = []
+    for S in cands:
+        w = Workload(wl.name, 0, wl.device, problem=dataclasses.replace(p, num_splits=S))
+        us = []
+        for _ in range(max(1, args.rounds)):
+            ms, _, steps = time_device(w, args.steps, args.warmup, ctx)
+            us.append(ms * 1e3 / steps)
+        res.append({"num_splits": S, "planner": S == planned, "median_us": statistics.median(us),
+                    "min_us": min(us), "max_us": max(us),
+                    "gbs": w.algorithmic_bytes() / (statistics.median(us) * 1e-6) / 1e9})
+    return res
+
+
 def ffd_compare(args, ctx, sampler, dev):
     """Dense pass vs top-delta at delta 5 and 7 on one FFD cache (B=4, Hq=32,
     Hkv=8, d=128, L=131072; the same K/V, the keys encoded once): `rounds`
@@ -564,6 +607,7 @@ FULL_SHAPES.update({k + "_fp8": FULL_SHAPES[k] for k in ("mha32k", "million", "g
 FULL_SHAPES.update({k + "_fp4": FULL_SHAPES[k] for k in ("mha32k", "million", "gqa_paged", "ffd_dense")})
 FULL_SHAPES.update({k + "_unified": FULL_SHAPES[k] for k in ("mha32k", "million", "gqa_paged")})
 FULL_SHAPES.update({k: FULL_SHAPES["ffd_dense"] for k in WORKLOADS if k.startswith("ffd")})
+FULL_SHAPES["ladder"] = (1, 32, 8, 32768, 128)
 
 
 class OracleSample:
@@ -572,7 +616,7 @@ class OracleSample:
     sequence.  `frac` is the slice's share of one full call's work.  For the
     ragged paged batch the full call is taken at the mean length."""
 
-    def __init__(self, name, seed, target_s, plant_frac=0.001):
+    def __init__(self, name, seed, target_s, plant_frac=0.001, batch=None, seq_len=None):
         import numpy as np
         import torch
 
@@ -582,6 +626,10 @@ class OracleSample:
         self.name = name
         self.oracle = oracle
         B, Hq, Hkv, L, d = FULL_SHAPES[name]
+        if batch is not None and (name == "ladder" or name.startswith("ffd")):
+            B = batch
+        if seq_len is not None and name.split("_")[0] in ("mha32k", "million", "ladder"):
+            L = seq_len
         self.fp8 = name.endswith("_fp8")
         self.fp4 = name.endswith("_fp4")
         G = Hq // Hkv
@@ -705,7 +753,7 @@ def run_reference(args, ctx):
     if ctx.rank != 0:
         return
     per_step = max(0.002, min(2.0, 90.0 / max(1, args.steps + args.warmup)))
-    sample = OracleSample(args.workload, args.seed, per_step, args.plant_frac)
+    sample = OracleSample(args.workload, args.seed, per_step, args.plant_frac, args.batch, args.seq_len)
     value, s_per_step = time_oracle(sample, args.steps, args.warmup)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": s_per_step * 1e3,
@@ -733,6 +781,9 @@ def main():
     ap.add_argument("--window", type=int, default=64, help="top-delta: local-window anchors")
     ap.add_argument("--phi", type=float, default=6.5, help="*_unified: the fixed max value (natural-log units)")
     ap.add_argument("--plant-frac", type=float, default=0.001, help="ffd_sparse_*: fraction of planted tokens")
+    ap.add_argument("--rounds", type=int, default=1, help="timed rounds of --steps calls (value = median)")
+    ap.add_argument("--split-sweep", action="store_true",
+                    help="also time chunk counts around the planner's (0.5x..2x), --rounds rounds each")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--ffd-compare", choices=["auto", "on", "off"], default="auto",
                     help="time dense vs top-delta 5/7 on the FFD cache in the same run (auto: with million)")
@@ -765,8 +816,17 @@ def main():
     sampler = ClockSampler(ctx.local_rank)
     sampler.start()
     time.sleep(0.3)
-    ms, (tw0, tw1), args.steps = time_device(wl, args.steps, args.warmup, ctx, graph=args.graph)
+    rounds_ms = []
+    for _ in range(max(1, args.rounds)):
+        ms_r, (tw0_r, tw1), steps_r = time_device(wl, args.steps, args.warmup, ctx, graph=args.graph)
+        rounds_ms.append(ms_r)
+        tw0 = tw0_r if len(rounds_ms) == 1 else tw0
+    args.steps = steps_r
+    ms = statistics.median(rounds_ms)
     sampler_summary = sampler.summary(tw0, tw1)
+    sweep = None
+    if args.split_sweep:
+        sweep = split_sweep(args, wl, ctx)
     e2e = None
     if not args.no_e2e:
         e2e_steps = max(3, min(args.steps, 2000))
@@ -807,7 +867,7 @@ def main():
                        "decode, one device->host copy (out + lse)"}
     cpu = None
     if ctx.rank == 0 and n == 1 and not args.no_cpu_baseline:
-        sample = OracleSample(args.workload, args.seed, 1.0, args.plant_frac)
+        sample = OracleSample(args.workload, args.seed, 1.0, args.plant_frac, args.batch, args.seq_len)
         t0 = time.perf_counter()
         sample.run()
         reps = max(1, int(args.cpu_budget / max(time.perf_counter() - t0, 1e-3)))
@@ -838,6 +898,12 @@ def main():
         }
         if compare is not None:
             line["ffd_compare"] = compare
+        if args.rounds > 1:
+            line["rounds"] = {"n": len(rounds_ms), "us_per_call": [r * 1e3 / args.steps for r in rounds_ms],
+                              "median_us": ms * 1e3 / args.steps,
+                              "spread_us": (max(rounds_ms) - min(rounds_ms)) * 1e3 / args.steps}
+        if sweep is not None:
+            line["split_sweep"] = sweep
         print(json.dumps(line), flush=True)
     ctx.close()
 

@@ -27,7 +27,7 @@ def gpu_arm_config(workload, gpus=1):
     import bench
     args = bench.argparse.Namespace(workload=workload, batch=None, seq_len=None, num_splits=None,
                                     n_sink=4, window=64, gpus=gpus, graph=0, phi=6.5,
-                                    plant_frac=0.001)
+                                    plant_frac=0.001, split_sweep=False)
     return bench.workload_config(args)
 
 

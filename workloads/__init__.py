@@ -16,6 +16,8 @@ Workload recipes (decode of one new token per sequence):
   ffd         B=4, Hq=32, Hkv=8, d=128, L=131072; keys of tokens 0-3 and of
               the last 64 tokens get +2.5*q_hat; round(1% of L) distinct
               tokens in [4, L-64) get +c*q_hat with c ~ N(2, 0.5) each
+  ladder      any B and L at Hq=32, Hkv=8, d=128, unstructured (the
+              context-length ladder of the split-count sweep)
 q, K, V ~ N(0, 1) in fp32, structure added in fp32, then rounded to bf16.
 q_hat for KV head h is u/|u| with u the sum of the group's query vectors
 (after their bf16 rounding), so one direction serves all heads of the group.
@@ -182,6 +184,18 @@ def ffd(seed=0, device="cpu", B=4, L=131072, Hq=32, Hkv=8, d=128, anchor_boost=2
     sl = torch.full((B,), L, dtype=torch.int32, device=device)
     return Problem("ffd", q, k, v, sl, 1.0 / math.sqrt(d), L,
                    meta=dict(n_sink=4, window=64, deltas=(5.0, 7.0), n_planted=n_planted))
+
+
+def ladder(B=1, L=32768, seed=0, device="cpu", Hq=32, Hkv=8, d=128) -> Problem:
+    """Context-length ladder shape (GQA group of 4, d=128) at any batch and
+    length: unstructured q, K, V ~ N(0,1) rounded to bf16, drawn one
+    (sequence, head) slab at a time so that large caches need no fp32 copy."""
+    g = _gen(seed, device)
+    q = _randn((B, Hq, d), g, device).to(torch.bfloat16)
+    k = _structured_keys(q, B, Hkv, L, d, g, device, lambda b, h: (None, None))
+    v = _values(B, Hkv, L, d, g, device)
+    sl = torch.full((B,), L, dtype=torch.int32, device=device)
+    return Problem("ladder", q, k, v, sl, 1.0 / math.sqrt(d), L)
 
 
 def page_layout(seq_lens, page_size, g, device, max_pages=None):
