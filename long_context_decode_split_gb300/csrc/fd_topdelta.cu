@@ -6,20 +6,22 @@
 // over them exactly (section 5, Fig. 2), with the stages fused as section 6
 // asks: nothing but the per-chunk (m_i, l_i, O_i) leaves the chip.
 //
-// Fused pass, one CTA per (chunk, KV head, sequence), 1 producer + 4
+// Fused pass, one CTA per (chunk, KV head, sequence), 2 producer + 4
 // consumer warps, 64-token tiles (the same tile grid as the dense path):
 //   * anchor pass: the consumer warps score the tiles that hold anchors and
 //     take m^ per query head.  Every CTA of a (sequence, head) computes the
 //     same m^ bit for bit: the anchor scores are produced by the same code,
 //     lanes and operation order as the main scan.
-//   * scan ring (2-bit codes + fp16 min/scale, 48 B per token at d=128) is
-//     filled LA+1 tiles ahead by bulk copies.  Consumers score tile k,
-//     store s~ in shared memory and flag whether any query head of the
-//     group selected a token of the tile.
+//   * scan ring (2-bit codes + fp16 min/scale, 48 B per token at d=128, SS
+//     stages): its own producer warp refills a stage with bulk copies as soon
+//     as the consumers have scored the tile in it, so on a sparse cache
+//     (few tiles with candidates, the pass reduced to the scan) the copies
+//     run SS tiles ahead.  Consumers score tile k, store s~ in shared memory
+//     and flag whether any query head of the group selected a token of it.
 //   * detail ring (int8 residual + fp16 scales + bf16 V, 392 B per token):
-//     the producer issues a tile's copies only once the consumers flagged it,
-//     LA tiles before the consumers attend to it, so the residual and V of
-//     tiles without candidates are never read from HBM.
+//     the detail producer warp issues a tile's copies only once the
+//     consumers flagged it, LA tiles before the consumers attend to it, so
+//     the residual and V of tiles without candidates are never read.
 //   * attend: exact scores s = s~ + scale * sum_g rs_g <q_g, rq_g> for the
 //     candidates, online softmax and O^T += V^T P^T, then the same warp
 //     combine and chunk merge as the dense pass.  With `group_union` every
@@ -44,9 +46,10 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int CW = 4;           // consumer warps
+constexpr int NW = CW + 2;      // + the detail producer warp (CW) and the scan producer warp (CW + 1)
 constexpr int LA = 2;           // tiles scanned ahead of the attend step
 constexpr int DS = LA + 1;      // detail ring depth (= decision slots)
-constexpr int SS = LA + 2;      // scan ring depth
+constexpr int SS = 8;           // scan ring depth: the scan producer keeps it full on its own
 
 // ============================================================== encoder
 
@@ -337,7 +340,7 @@ __device__ __forceinline__ void residual_tile(uint32_t res_s, const unsigned cha
 }
 
 template <int D>
-__global__ void __launch_bounds__((CW + 1) * 32, 2)
+__global__ void __launch_bounds__(NW * 32, 2)
 topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant__ CUtensorMap tm_v,
                 const TDParams p) {
     using Gm = TGeo<D>;
@@ -398,17 +401,19 @@ topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constan
     }
     __syncthreads();
 
-    if (warp == CW) {
-        // ----------------------------- producer --------------------------------
+    auto rows_of = [&](int t) { return min(kTile, t1 - (t0 + t * kTile)); };
+    auto copy_rows = [&](int t) { return (rows_of(t) + 3) & ~3; };  // L_max % 4 == 0 keeps this in bounds
+    if (warp == CW + 1) {
+        // --------------------------- scan producer ------------------------------
         if (lane == 0) {
-            prefetch_tmap(&tm_res);
-            prefetch_tmap(&tm_v);
             const uint64_t pol = l2_evict_first_policy();
-            auto rows_of = [&](int t) { return min(kTile, t1 - (t0 + t * kTile)); };
-            auto copy_rows = [&](int t) { return (rows_of(t) + 3) & ~3; };  // L_max % 4 == 0 keeps this in bounds
-            auto issue_scan = [&](int k) -> bool {
+            int k = 0;
+            for (; k < ntiles; ++k) {
                 const int s = k % SS;
-                if (!mbar_wait(&scan_empty[s], ((uint32_t)(k / SS) & 1u) ^ 1u)) return false;
+                if (!mbar_wait(&scan_empty[s], ((uint32_t)(k / SS) & 1u) ^ 1u)) {
+                    atomicOr(&g_status_topdelta, kStatusTimeout);
+                    break;
+                }
                 const size_t row0 = (size_t)head_row0 + t0 + (size_t)k * kTile;
                 const uint32_t rc = (uint32_t)copy_rows(k);
                 unsigned char* dst = smem + Ly::SCAN_OFF + s * Gm::SCAN_STAGE;
@@ -417,11 +422,23 @@ topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constan
                 bulk_g2s(dst, p.codes + row0 * Gm::CODES_ROW, rc * Gm::CODES_ROW, &scan_full[s], pol);
                 bulk_g2s(dst + kTile * Gm::CODES_ROW, p.mn_scale + row0 * Gm::MS_ROW, rc * Gm::MS_ROW, &scan_full[s],
                          pol);
-                return true;
-            };
+            }
+            // the consumers may stop early (a time-out): let every copy started
+            // land before the CTA can exit (the last tile of each stage)
+            for (int u = k - 1; u >= 0 && u >= k - SS; --u) mbar_wait(&scan_full[u % SS], (uint32_t)(u / SS) & 1u);
+        }
+        pdl_launch_dependents();
+        return;
+    }
+    if (warp == CW) {
+        // -------------------------- detail producer -----------------------------
+        if (lane == 0) {
+            prefetch_tmap(&tm_res);
+            prefetch_tmap(&tm_v);
+            const uint64_t pol = l2_evict_first_policy();
             bool ok = true;
-            for (int k = 0; k <= LA && k < ntiles && ok; ++k) ok = issue_scan(k);
-            for (int t = 0; t < ntiles && ok; ++t) {
+            int t = 0;
+            for (; t < ntiles; ++t) {
                 const int s = t % DS;
                 const uint32_t ph = (uint32_t)(t / DS) & 1u;
                 if (!mbar_wait(&decided[s], ph) || !mbar_wait(&det_empty[s], ph ^ 1u)) {
@@ -447,9 +464,9 @@ topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constan
                     loaded[s] = 0;
                     mbar_arrive(&det_full[s]);
                 }
-                if (t + LA + 1 < ntiles) ok = issue_scan(t + LA + 1);
             }
             if (!ok) atomicOr(&g_status_topdelta, kStatusTimeout);
+            for (int u = t - 1; u >= 0 && u >= t - DS; --u) mbar_wait(&det_full[u % DS], (uint32_t)(u / DS) & 1u);
         }
         pdl_launch_dependents();
         return;
@@ -685,7 +702,7 @@ struct TDLauncher {
         if (dev < kMaxDevices && cache[dev] > 0) return cache[dev];
         if (prepare() != cudaSuccess) return 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, topdelta_kernel<D>, (CW + 1) * 32, SMEM) !=
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, topdelta_kernel<D>, NW * 32, SMEM) !=
                 cudaSuccess ||
             n <= 0)
             return 1;
@@ -696,7 +713,7 @@ struct TDLauncher {
                               cudaStream_t st) {
         cudaError_t e = prepare();
         if (e != cudaSuccess) return e;
-        return launch_pdl(topdelta_kernel<D>, grid, dim3((CW + 1) * 32), SMEM, st, tr, tv, pp);
+        return launch_pdl(topdelta_kernel<D>, grid, dim3(NW * 32), SMEM, st, tr, tv, pp);
     }
 };
 
