@@ -22,10 +22,12 @@
 //               accumulates on its own and is scaled by 2^e_b of its token
 //               before the blocks are summed.
 //   O^T += V^T P^T
-//               the 16 output rows of tile j are 4 channels of 4 lane groups
-//               inside block j/2 (row gid + 8r of tile 2c + h is channel
-//               32c + 4*gid + 2h + r); the two token nibbles of a channel are
-//               interleaved into one byte and widened; P carries
+//               V is widened in its stored layout (the ldmatrix words of K:
+//               8 channels of one block of tokens gid and gid + 8 per lane)
+//               and every 8x8 block of it (8 tokens x 8 channels) is
+//               transposed by movmatrix into an A fragment of V^T; output
+//               tile 2c + j holds channels 32c + 8*(gid/2) + 4j + (gid%2)
+//               (row gid) and that + 2 (row gid + 8).  P carries
 //               2^e_b(token) / s_ref, s_ref the largest V block scale the
 //               warp has seen, so each block has its own P operand, turned
 //               from the score layout into P^T fragments by movmatrix.
@@ -94,13 +96,7 @@ __device__ __forceinline__ uint32_t e2m1x2_from_f32(float lo, float hi) {
 // 2^(E - 127) for a scale byte E in [1, 254] (a normal binary32, exact).
 __device__ __forceinline__ float scale_value(uint32_t E) { return __uint_as_float(E << 23); }
 
-// The two 16-bit nibble rows w0 (token a) and w1 (token b) of 4 channels
-// -> 4 bytes, byte c = (channel c of b) << 4 | (channel c of a).
-__device__ __forceinline__ uint32_t interleave_nibbles(uint32_t w0, uint32_t w1) {
-    uint32_t u = __byte_perm(w0, w1, 0x5140);  // halves: (b.byte0 : a.byte0), (b.byte1 : a.byte1)
-    const uint32_t t = (u ^ (u >> 4)) & 0x00F000F0u;  // swap nibble positions 1 and 2 of each half
-    return u ^ t ^ (t << 4);
-}
+
 
 // ---------------------------------------------------------------------------
 // Encoder: one warp per cache row; lane l holds channels D/32 * l ...
@@ -314,8 +310,6 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
     float vref = 0.f;
     bool failed = false;
     const int ld_row = warp * 16 + 8 * (mi >> 1) + (lane & 7);  // row this lane addresses for ldmatrix
-    const int r0 = warp * 16 + 2 * tig;                         // V^T P^T: tokens r0, r0+1, r0+8, r0+9
-    const int tok[4] = {r0, r0 + 1, r0 + 8, r0 + 9};
     const int srow[2] = {warp * 16 + gid, warp * 16 + gid + 8};  // S = K Q^T: the lane's accumulator rows
 
     for (int t = 0; t < ntiles; t += NT) {
@@ -411,7 +405,7 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
         const float alpha1 = none1 ? 1.f : exp2_approx(m_run.y - m1);
         m_run = make_float2(m0, m1);
         float lsum0 = 0.f, lsum1 = 0.f;
-        float pr[NT][4];  // p / s_ref, same layout as sc
+        float pr[NT][4];  // p, same layout as sc
 #pragma unroll
         for (int k = 0; k < NT; ++k) {
             pr[k][0] = none0 ? 0.f : exp2_approx(sc[k][0] - m0);
@@ -421,7 +415,6 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
             lsum0 += pr[k][0] + pr[k][2];
             lsum1 += pr[k][1] + pr[k][3];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) pr[k][i] *= vinv;
         }
         l_run.x = l_run.x * alpha0 + lsum0;
         l_run.y = l_run.y * alpha1 + lsum1;
@@ -440,28 +433,33 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
         // ---- O^T += V^T P^T -------------------------------------------------
 #pragma unroll
         for (int k = 0; k < NT; ++k) {
-            const unsigned char* vt = smem + st[k] * STAGE + CB;
-            const bool tail = warp * 16 + 16 > rows[k];  // warp-uniform
+            const uint32_t vt = smem_u32(smem + st[k] * STAGE + CB);
 #pragma unroll
-            for (int c = 0; c < NB; ++c) {
-                // channels 32c + 4*gid .. +3 of the lane's four tokens: two bytes each
+            for (int cp = 0; cp < NB / 2; ++cp) {
+                // (rows gid, block 2cp), (gid, 2cp+1), (gid + 8, 2cp), (gid + 8, 2cp+1)
                 uint32_t w[4];
+                ldsm_x4(vt + code4_off<D>(ld_row, 2 * cp + (mi & 1)), w[0], w[1], w[2], w[3]);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    w[i] = *reinterpret_cast<const uint16_t*>(vt + code4_off<D>(tok[i], c) + 2 * gid);
-                    if (tail) w[i] = tok[i] < rows[k] ? w[i] : 0u;  // rows past the end may hold anything
+                for (int hb = 0; hb < 2; ++hb) {
+                    const int c = 2 * cp + hb;
+                    // P^T for V block c: p * 2^e_c(token) / s_ref of rows gid and gid + 8 (the
+                    // scale is 0 past the tile, where the codes may be anything finite), each
+                    // 8x8 block transposed from the score layout
+                    const float e0 = scale_value((ve[k][0] >> (8 * c)) & 0xffu) * vinv;
+                    const float e1 = scale_value((ve[k][1] >> (8 * c)) & 0xffu) * vinv;
+                    const uint32_t pb0 = movmatrix_trans(pack_f16(pr[k][0] * e0, pr[k][1] * e0));
+                    const uint32_t pb1 = movmatrix_trans(pack_f16(pr[k][2] * e1, pr[k][3] * e1));
+                    uint32_t x0[4], x8[4];
+                    e2m1x8_to_f16x8(w[hb], x0);      // token gid: channels 32c + 8 tig + 2i, + 1
+                    e2m1x8_to_f16x8(w[2 + hb], x8);  // token gid + 8
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        x0[i] = movmatrix_trans(x0[i]);
+                        x8[i] = movmatrix_trans(x8[i]);
+                    }
+                    mma_f16(o[2 * c], x0[0], x0[1], x8[0], x8[1], pb0, pb1);
+                    mma_f16(o[2 * c + 1], x0[2], x0[3], x8[2], x8[3], pb0, pb1);
                 }
-                // P^T of this stage for V block c: p * 2^e_c(token) / s_ref of rows gid and
-                // gid + 8, each 8x8 block transposed from the score layout
-                const float e0 = scale_value((ve[k][0] >> (8 * c)) & 0xffu);
-                const float e1 = scale_value((ve[k][1] >> (8 * c)) & 0xffu);
-                const uint32_t pb0 = movmatrix_trans(pack_f16(pr[k][0] * e0, pr[k][1] * e0));
-                const uint32_t pb1 = movmatrix_trans(pack_f16(pr[k][2] * e1, pr[k][3] * e1));
-                uint32_t x01[4], x89[4];
-                e2m1x8_to_f16x8(interleave_nibbles(w[0], w[1]), x01);
-                e2m1x8_to_f16x8(interleave_nibbles(w[2], w[3]), x89);
-                mma_f16(o[2 * c], x01[0], x01[1], x89[0], x89[1], pb0, pb1);
-                mma_f16(o[2 * c + 1], x01[2], x01[3], x89[2], x89[3], pb0, pb1);
             }
         }
         __syncwarp();
@@ -487,11 +485,13 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
     for (int c = 0; c < NB; ++c) {
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
-            // query 2*tig + i, channels 32c + 4*gid .. + 3
-            const int qi = 2 * tig + i;
-            const float4 val = make_float4(o[2 * c][i] * vref, o[2 * c][i + 2] * vref, o[2 * c + 1][i] * vref,
-                                           o[2 * c + 1][i + 2] * vref);
-            *reinterpret_cast<float4*>(red_o + (warp * 8 + qi) * D + 32 * c + 4 * gid) = val;
+            // query 2*tig + i; output tile 2c + j, row gid + 8r: channel 32c + 8*(gid/2) + 4j + 2r + gid%2
+            float* dst = red_o + (warp * 8 + 2 * tig + i) * D + 32 * c + 8 * (gid >> 1) + (gid & 1);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                dst[4 * j] = o[2 * c + j][i] * vref;
+                dst[4 * j + 2] = o[2 * c + j][i + 2] * vref;
+            }
         }
     }
     if (gid == 0) {
