@@ -87,82 +87,6 @@ std::atomic<int> g_inject_withhold_tile{-1};
 // to fp32 rounding.
 constexpr float kUnifiedRange = 60.f;
 
-// Column-wise (per query) maximum over the 8 lanes of equal tig of a value
-// held per lane for its two accumulator columns.
-__device__ __forceinline__ float2 column_max(float2 v) {
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        v.x = fmaxf(v.x, __shfl_xor_sync(0xffffffffu, v.x, off));
-        v.y = fmaxf(v.y, __shfl_xor_sync(0xffffffffu, v.y, off));
-    }
-    return v;
-}
-
-// One tile of the tensor-core consumer on the fixed reference phi2 (log2
-// units), or the switch to the running-max path (see kUnifiedRange).
-// `seen` is the lane's max of the scores attended on the reference.
-template <int D>
-__device__ __forceinline__ void unified_softmax_pv(TokAcc<D>& ac, bool& unified, float2& seen, const float (&sc)[4],
-                                                   uint32_t vs, unsigned char* vgen, int warp, int lane, int rows,
-                                                   float phi2, float lo2) {
-    if (unified) {
-        bool ok = true;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) ok &= sc[i] == -INFINITY || (sc[i] >= lo2 && sc[i] <= phi2);
-        if (__all_sync(0xffffffffu, ok)) {
-            const int mi = lane >> 3;
-            const int ld_row = warp * 16 + 8 * (mi >> 1) + (lane & 7);
-            if (warp * 16 + 16 > rows) {
-                for (int i = lane; i < 16 * (D / 8); i += 32) {
-                    const int r = warp * 16 + i / (D / 8);
-                    if (r >= rows) *reinterpret_cast<uint4*>(vgen + swz(r, i % (D / 8))) = make_uint4(0u, 0u, 0u, 0u);
-                }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
-            }
-            float pr[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) pr[i] = exp2_approx(sc[i] - phi2);  // 2^-inf = +0
-            seen.x = fmaxf(seen.x, fmaxf(sc[0], sc[2]));
-            seen.y = fmaxf(seen.y, fmaxf(sc[1], sc[3]));
-            ac.l.x += pr[0] + pr[2];
-            ac.l.y += pr[1] + pr[3];
-            uint32_t h0, l0, h1, l1;
-            split_bf16(pr[0], pr[1], h0, l0);
-            split_bf16(pr[2], pr[3], h1, l1);
-            h0 = movmatrix_trans(h0);
-            l0 = movmatrix_trans(l0);
-            h1 = movmatrix_trans(h1);
-            l1 = movmatrix_trans(l1);
-#pragma unroll
-            for (int mt = 0; mt < D / 16; ++mt) {
-                uint32_t v0, v1, v2, v3;
-                ldsm_x4_t(vs + swz(ld_row, 2 * mt + (mi & 1)), v0, v1, v2, v3);
-                mma_bf16(ac.o[mt], v0, v1, v2, v3, h0, h1);
-                mma_bf16(ac.o[mt], v0, v1, v2, v3, l0, l1);
-            }
-            return;
-        }
-        // fallback: O and l are relative to phi2; rebase them to the largest
-        // attended score (every one of them lies in [lo2, phi2])
-        unified = false;
-        const float2 m = column_max(seen);
-        const float a0 = m.x == -INFINITY ? 1.f : exp2_approx(phi2 - m.x);
-        const float a1 = m.y == -INFINITY ? 1.f : exp2_approx(phi2 - m.y);
-#pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt) {
-            ac.o[mt][0] *= a0;
-            ac.o[mt][1] *= a1;
-            ac.o[mt][2] *= a0;
-            ac.o[mt][3] *= a1;
-        }
-        ac.l.x *= a0;
-        ac.l.y *= a1;
-        ac.m = m;
-    }
-    mma_softmax_pv<D>(ac, sc, vs, vgen, warp, lane, rows);
-}
-
 // Tensor-core consumer, one warp, 16 rows of a 64-token tile: S = K Q^T on
 // mma.sync (A = the warp's K rows by ldmatrix from the swizzled tile, B = Q
 // fragments in registers; accumulator rows gid, gid + 8 are tokens, columns
@@ -212,7 +136,8 @@ __device__ __forceinline__ void mma_consume_tile_unified(TokAcc<D>& ac, bool& un
     sc[1] = r0 < rows ? sacc[1] * scale_log2 : -INFINITY;
     sc[2] = r0 + 8 < rows ? sacc[2] * scale_log2 : -INFINITY;
     sc[3] = r0 + 8 < rows ? sacc[3] * scale_log2 : -INFINITY;
-    unified_softmax_pv<D>(ac, unified, seen, sc, vs, vgen, warp, lane, rows, phi2, lo2);
+    fixed_ref_softmax_pv<D>(ac, unified, seen, sc, vs, vgen, warp, lane, rows, make_float2(phi2, phi2),
+                            make_float2(lo2, lo2));
 }
 
 template <int D, int GP, int CW, int STAGES, bool PAGED, bool MMA, bool UMAX>
@@ -350,12 +275,7 @@ partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
         }
-        if (UMAX && unified) {
-            // still on the reference: a column's partial is relative to phi2
-            // (none when it attended nothing)
-            const float2 m = column_max(seen);
-            ac.m = make_float2(m.x == -INFINITY ? -INFINITY : p.phi2, m.y == -INFINITY ? -INFINITY : p.phi2);
-        }
+        if (UMAX && unified) fixed_ref_finish(ac, seen, make_float2(p.phi2, p.phi2));
         pdl_launch_dependents();
         combine_tok_warps_and_store<D, CW>(smem, warp, lane, p.G, b * p.Hq + hq0, split, ac, failed, p.st);
         return;

@@ -388,6 +388,103 @@ __device__ __forceinline__ void mma_softmax_pv(TokAcc<D>& ac, const float (&sc)[
     }
 }
 
+// Column-wise (per query) maximum over the 8 lanes of equal tig of a value
+// held per lane for its two accumulator columns.
+__device__ __forceinline__ float2 column_max(float2 v) {
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        v.x = fmaxf(v.x, __shfl_xor_sync(0xffffffffu, v.x, off));
+        v.y = fmaxf(v.y, __shfl_xor_sync(0xffffffffu, v.y, off));
+    }
+    return v;
+}
+
+// One tile of a TokAcc consumer on a fixed reference max (FlashDecoding++
+// summary, sections 1, 3, 5: one max value known before the scores, no
+// reduction to the tile's max, a fallback when the scores leave the range it
+// was chosen for).  phi2 / lo2 (log2 units) hold the reference and its lower
+// end for the lane's two columns (queries 2 tig, 2 tig + 1).  While every
+// valid score of the tile lies in [lo2, phi2] (one warp vote) the weights are
+// 2^(s - phi2), normal binary32 numbers in [2^(lo2 - phi2), 1]: no max
+// reduction, no rescale; `seen` keeps the lane's max of the attended scores.
+// At the first tile outside the range the warp rebases O and l from phi2 to
+// the largest score it attended (the state the running-max computation holds
+// there) and continues with mma_softmax_pv.
+template <int D>
+__device__ __forceinline__ void fixed_ref_softmax_pv(TokAcc<D>& ac, bool& on_ref, float2& seen, const float (&sc)[4],
+                                                     uint32_t vs, unsigned char* vgen, int warp, int lane, int rows,
+                                                     float2 phi2, float2 lo2) {
+    if (on_ref) {
+        bool ok = true;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float ph = (i & 1) ? phi2.y : phi2.x, lo = (i & 1) ? lo2.y : lo2.x;
+            ok &= sc[i] == -INFINITY || (sc[i] >= lo && sc[i] <= ph);
+        }
+        if (__all_sync(0xffffffffu, ok)) {
+            const int mi = lane >> 3;
+            const int ld_row = warp * 16 + 8 * (mi >> 1) + (lane & 7);
+            if (warp * 16 + 16 > rows) {
+                for (int i = lane; i < 16 * (D / 8); i += 32) {
+                    const int r = warp * 16 + i / (D / 8);
+                    if (r >= rows) *reinterpret_cast<uint4*>(vgen + swz(r, i % (D / 8))) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+            }
+            float pr[4];
+            pr[0] = exp2_approx(sc[0] - phi2.x);  // 2^-inf = +0
+            pr[1] = exp2_approx(sc[1] - phi2.y);
+            pr[2] = exp2_approx(sc[2] - phi2.x);
+            pr[3] = exp2_approx(sc[3] - phi2.y);
+            seen.x = fmaxf(seen.x, fmaxf(sc[0], sc[2]));
+            seen.y = fmaxf(seen.y, fmaxf(sc[1], sc[3]));
+            ac.l.x += pr[0] + pr[2];
+            ac.l.y += pr[1] + pr[3];
+            uint32_t h0, l0, h1, l1;
+            split_bf16(pr[0], pr[1], h0, l0);
+            split_bf16(pr[2], pr[3], h1, l1);
+            h0 = movmatrix_trans(h0);
+            l0 = movmatrix_trans(l0);
+            h1 = movmatrix_trans(h1);
+            l1 = movmatrix_trans(l1);
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                uint32_t v0, v1, v2, v3;
+                ldsm_x4_t(vs + swz(ld_row, 2 * mt + (mi & 1)), v0, v1, v2, v3);
+                mma_bf16(ac.o[mt], v0, v1, v2, v3, h0, h1);
+                mma_bf16(ac.o[mt], v0, v1, v2, v3, l0, l1);
+            }
+            return;
+        }
+        // fallback: O and l are relative to phi2; rebase them to the largest
+        // attended score (every one of them lies in [lo2, phi2])
+        on_ref = false;
+        const float2 m = column_max(seen);
+        const float a0 = m.x == -INFINITY ? 1.f : exp2_approx(phi2.x - m.x);
+        const float a1 = m.y == -INFINITY ? 1.f : exp2_approx(phi2.y - m.y);
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+            ac.o[mt][0] *= a0;
+            ac.o[mt][1] *= a1;
+            ac.o[mt][2] *= a0;
+            ac.o[mt][3] *= a1;
+        }
+        ac.l.x *= a0;
+        ac.l.y *= a1;
+        ac.m = m;
+    }
+    mma_softmax_pv<D>(ac, sc, vs, vgen, warp, lane, rows);
+}
+
+// End of a consumer that may still be on its fixed reference: a column's
+// partial is then relative to phi2 (none when it attended nothing).
+template <int D>
+__device__ __forceinline__ void fixed_ref_finish(TokAcc<D>& ac, float2 seen, float2 phi2) {
+    const float2 m = column_max(seen);
+    ac.m = make_float2(m.x == -INFINITY ? -INFINITY : phi2.x, m.y == -INFINITY ? -INFINITY : phi2.y);
+}
+
 // Where a CTA's combined result goes: the final output (one chunk per
 // sequence) or its chunk's slot of the merge workspace.
 struct StoreTarget {
