@@ -229,10 +229,11 @@ class Workload:
         if self.fp8 or self.fp4:
             # encode the cache once (outside the timed region); keep the bf16 copy for e2e rows
             enc = fd.fd_quantize_kv_fp8 if self.fp8 else fd.fd_quantize_kv_fp4
+            venc = fd.fd_quantize_kv_fp8 if self.fp8 else fd.fd_quantize_v_fp4  # fp4 values: token pairs
             if self.paged:
-                self.kv8 = enc(p.k_pages) + enc(p.v_pages)
+                self.kv8 = enc(p.k_pages) + venc(p.v_pages)
             else:
-                self.kv8 = enc(p.k) + enc(p.v)
+                self.kv8 = enc(p.k) + venc(p.v)
             torch.cuda.synchronize()
             if self.fp8:
                 need = fd.fd_decode_fp8_workspace_size(B, Hq, Hkv, p.L_max, d, p.num_splits, self.paged)
@@ -487,14 +488,30 @@ def time_e2e(wl, steps, warmup, dist_ctx):
     kv_d = staged[nq:].view(torch.bfloat16).view(2 * n, H, 1, dd)  # K rows, then V rows, as one-token caches
     result = torch.empty(wl.io.shape, dtype=torch.uint8).pin_memory()
 
-    if wl.fp8 or wl.fp4:
-        if wl.fp8:
-            c_new = torch.empty((2 * n, H, 1, dd), dtype=torch.uint8, device=dev)
-            s_new = torch.empty((2 * n, H, 1), dtype=torch.float32, device=dev)
+    if wl.fp8:
+        c_new = torch.empty((2 * n, H, 1, dd), dtype=torch.uint8, device=dev)
+        s_new = torch.empty((2 * n, H, 1), dtype=torch.float32, device=dev)
+        encode = fd.fd_quantize_kv_fp8
+    elif wl.fp4:
+        # keys: one row; values: the newest token's pair (tokens 2j, 2j + 1) encoded again, its
+        # partner read from the bf16 cache when the newest token is the second of the pair
+        kc_new = torch.empty((n, H, 1, dd // 2), dtype=torch.uint8, device=dev)
+        ks_new = torch.empty((n, H, 1, dd // 32), dtype=torch.uint8, device=dev)
+        vc_new = torch.empty((n, H, 1, dd), dtype=torch.uint8, device=dev)
+        vs_new = torch.empty((n, H, 2, dd // 32), dtype=torch.uint8, device=dev)
+        if wl.paged:
+            odd = (rr % 2) == 1
+            prev = p.v_pages[pg, :, torch.clamp(rr - 1, min=0)]
         else:
-            c_new = torch.empty((2 * n, H, 1, dd // 2), dtype=torch.uint8, device=dev)
-            s_new = torch.empty((2 * n, H, 1, dd // 32), dtype=torch.uint8, device=dev)
-        encode = fd.fd_quantize_kv_fp8 if wl.fp8 else fd.fd_quantize_kv_fp4
+            odd = torch.full((n,), (p.L_max - 1) % 2 == 1, device=dev)
+            prev = p.v[:, :, max(p.L_max - 2, 0)]
+        # the partner of an odd newest token is already in the cache: place it once; each step
+        # writes the newest row into its slot of the pair (1 when odd, 0 when even)
+        pair_x = torch.zeros((n, H, 2, dd), dtype=torch.bfloat16, device=dev)
+        pair_x[:, :, 0] = torch.where(odd.view(n, 1, 1), prev, torch.zeros_like(prev))
+        pair_len = torch.where(odd, 2, 1).to(torch.int32)
+        slot = odd.long()
+        ar = torch.arange(n, device=dev)
     elif wl.topdelta is not None:
         k_one = staged[nq:nq + nr].view(torch.bfloat16).view(n, H, 1, dd)
         enc_new = (torch.empty((n, H, 1, dd // 4), dtype=torch.uint8, device=dev),
@@ -502,22 +519,32 @@ def time_e2e(wl, steps, warmup, dist_ctx):
                    torch.empty((n, H, 1, dd), dtype=torch.int8, device=dev),
                    torch.empty((n, H, 1, dd // 32), dtype=torch.float16, device=dev))
 
-    def put(cache, rows):
-        """Write one row per (sequence, head) at the newest token's position."""
+    def put(cache, rows, pairs=False):
+        """Write one row per (sequence, head) at the newest token's position
+        (with pairs: at its pair row)."""
         if wl.paged:
-            cache[pg, :, rr] = rows
+            cache[pg, :, rr // 2 if pairs else rr] = rows
         else:
-            cache[:, :, p.L_max - 1] = rows
+            cache[:, :, (p.L_max - 1) // 2 if pairs else p.L_max - 1] = rows
 
     def step():
         staged.copy_(host, non_blocking=True)
-        if wl.fp8 or wl.fp4:
+        if wl.fp8:
             encode(kv_d, codes=c_new, scales=s_new)
             kc, ks, vc, vs = wl.kv8
             put(kc, c_new[:n, :, 0])
             put(ks, s_new[:n, :, 0])
             put(vc, c_new[n:, :, 0])
             put(vs, s_new[n:, :, 0])
+        elif wl.fp4:
+            kc, ks, vc, vs = wl.kv8
+            fd.fd_quantize_kv_fp4(k_d.view(n, H, 1, dd), codes=kc_new, scales=ks_new)
+            put(kc, kc_new[:, :, 0])
+            put(ks, ks_new[:, :, 0])
+            pair_x[ar, :, slot] = v_d
+            fd.fd_quantize_v_fp4(pair_x, pair_len, codes=vc_new, scales=vs_new)
+            put(vc, vc_new[:, :, 0], pairs=True)
+            put(vs, vs_new[ar, :, slot])
         elif wl.topdelta is not None:
             fd.fd_quantize_keys(k_one, None, *enc_new)
             for cache, row in zip(wl.qk, enc_new):

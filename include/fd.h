@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define FD_ABI_VERSION 1
+#define FD_ABI_VERSION 2  /* 2: the fp4 value cache is stored in token pairs (fd_quantize_v_fp4) */
 
 #if defined(__GNUC__)
 #define FD_API __attribute__((visibility("default")))
@@ -313,21 +313,38 @@ FD_API int fd_decode_paged_fp8(const void* q, const uint8_t* k_pages, const floa
  *   codes   [row, d/2]  uint8: channel c in byte c/2, the low nibble for even c
  *   scales  [row, d/32] uint8: e_b + 127
  * Rows with t >= seq_lens[b] (seq_lens may be NULL) are not written; the
- * sign of a code rounded to zero follows x.  d must be 64 or 128. */
+ * sign of a code rounded to zero follows x.  d must be 64 or 128.  This is
+ * the KEY cache layout; the value cache uses fd_quantize_v_fp4. */
 FD_API int fd_quantize_kv_fp4(const void* x, const int32_t* seq_lens,
                               int B, int H, int L_max, int d,
                               uint8_t* codes, uint8_t* scales, void* stream);
+
+/* The same fp4 encoding for the VALUE cache, stored in token pairs (the layout
+ * the P.V product of the decode reads without transposes).  Codes and scales
+ * of every row are those fd_quantize_kv_fp4 computes; only the code layout
+ * differs (pair p = tokens 2p, 2p + 1 of one head; Lp = (L_max + 1) / 2):
+ *   codes   [B, H, Lp, d] uint8: byte (p, c) = code(2p+1, c) << 4 | code(2p, c)
+ *   scales  [B, H, L_max, d/32] uint8: e_b + 127 (as fd_quantize_kv_fp4)
+ * A pair whose first token is at or past seq_lens[b] is not written; a second
+ * token past it writes code 0 and no scale byte.  To append a token to a
+ * cache, encode its pair again from the two bf16 rows (a token at an even
+ * position: with its partner still absent).  d must be 64 or 128. */
+FD_API int fd_quantize_v_fp4(const void* x, const int32_t* seq_lens,
+                             int B, int H, int L_max, int d,
+                             uint8_t* codes, uint8_t* scales, void* stream);
 
 /* fd_num_splits / fd_decode_workspace_size for the fp4 decode entry points. */
 FD_API int fd_num_splits_fp4(int B, int Hq, int Hkv, int L_max, int d, int num_splits, int ragged);
 FD_API size_t fd_decode_fp4_workspace_size(int B, int Hq, int Hkv, int L_max, int d,
                                            int num_splits, int ragged);
 
-/* Split-KV decode ([FD] sections 1-2) over an fp4 cache written by
- * fd_quantize_kv_fp4: the attention of q over the decoded rows (computed
- * with fp16 tensor-core products and fp32 accumulation).
- *   k_codes, v_codes    [B, Hkv, L_max, d/2]  uint8
- *   k_scales, v_scales  [B, Hkv, L_max, d/32] uint8
+/* Split-KV decode ([FD] sections 1-2) over an fp4 cache: keys written by
+ * fd_quantize_kv_fp4, values by fd_quantize_v_fp4; the attention of q over
+ * the decoded rows (computed with fp16 tensor-core products and fp32
+ * accumulation).
+ *   k_codes             [B, Hkv, L_max, d/2]         uint8
+ *   v_codes             [B, Hkv, (L_max + 1)/2, d]   uint8 (token pairs)
+ *   k_scales, v_scales  [B, Hkv, L_max, d/32]        uint8
  * All other arguments, outputs and the workspace contract are those of
  * fd_decode_dense, with fd_decode_fp4_workspace_size() for the workspace. */
 FD_API int fd_decode_dense_fp4(const void* q, const uint8_t* k_codes, const uint8_t* k_scales,
@@ -339,7 +356,8 @@ FD_API int fd_decode_dense_fp4(const void* q, const uint8_t* k_codes, const uint
                                void* workspace, size_t workspace_bytes, void* stream);
 
 /* The same over a paged fp4 cache ([FD] section 3): pages of 64 tokens,
- *   k_pages, v_pages              [num_pages, Hkv, 64, d/2]  uint8 codes
+ *   k_pages                       [num_pages, Hkv, 64, d/2]  uint8 codes
+ *   v_pages                       [num_pages, Hkv, 32, d]    uint8 codes (token pairs)
  *   k_page_scales, v_page_scales  [num_pages, Hkv, 64, d/32] uint8
  * page_table, seq_lens and the remaining arguments as fd_decode_paged
  * (workspace: fd_decode_fp4_workspace_size(..., L_max = max_pages * 64,

@@ -24,7 +24,7 @@ __all__ = [
     "fd_quantize_kv_fp8", "fd_num_splits_fp8", "fd_decode_fp8_workspace_size", "fd_decode_dense_fp8",
     "fd_decode_paged_fp8", "fd_quantize_kv_fp4", "fd_num_splits_fp4", "fd_decode_fp4_workspace_size",
     "fd_decode_dense_fp4", "fd_decode_paged_fp4", "fd_decode_dense_unified", "fd_decode_paged_unified",
-    "fd_decode_topdelta_group_union", "fd_debug_inject_wait_timeout",
+    "fd_decode_topdelta_group_union", "fd_debug_inject_wait_timeout", "fd_quantize_v_fp4",
     "FD_OK", "FD_ERR_INVALID_ARG", "FD_ERR_UNSUPPORTED", "FD_ERR_WORKSPACE_TOO_SMALL",
     "FD_ERR_BAD_PAGE_TABLE", "FD_ERR_CUDA", "FD_ERR_DEVICE_TIMEOUT", "FD_OUT_F32", "FD_OUT_BF16",
 ]
@@ -91,6 +91,7 @@ def open_library(path: str):
         "fd_decode_dense_fp8": (I, [P, P, P, P, P, P, I, I, I, I, I, F, I, P, I, P, P, S, P]),
         "fd_decode_paged_fp8": (I, [P, P, P, P, P, P, I, I, P, I, I, I, I, I, F, I, P, I, P, P, S, P]),
         "fd_quantize_kv_fp4": (I, [P, P, I, I, I, I, P, P, P]),
+        "fd_quantize_v_fp4": (I, [P, P, I, I, I, I, P, P, P]),
         "fd_num_splits_fp4": (I, [I, I, I, I, I, I, I]),
         "fd_decode_fp4_workspace_size": (S, [I, I, I, I, I, I, I]),
         "fd_decode_dense_fp4": (I, [P, P, P, P, P, P, I, I, I, I, I, F, I, P, I, P, P, S, P]),
@@ -395,21 +396,30 @@ def fd_decode_dense_noalloc(q, k, v, out, seq_lens=None, scale=None, num_splits=
 
 # Quantized KV caches: code bytes per row and the scale entries per row, with their dtype.
 #   fp8: d codes (e4m3), one float32 scale per row
-#   fp4: d/2 codes (two e2m1 per byte), d/32 uint8 block exponents per row
+#   fp4: d/2 codes (two e2m1 per byte), d/32 uint8 block exponents per row; the fp4 VALUE
+#        cache holds d codes per pair of rows (_v_code_shape)
 _QCACHE = {
     "fp8": (lambda d: d, lambda d: (), torch.float32),
     "fp4": (lambda d: d // 2, lambda d: (d // 32,), torch.uint8),
 }
 
 
-def _quantize_kv(kind, x, seq_lens, codes, scales, stream):
+def _v_code_shape(kind, lead, rows, d):
+    """Shape of the value codes: as the keys', except fp4 values in token pairs."""
+    if kind == "fp4":
+        return tuple(lead) + ((rows + 1) // 2, d)
+    return tuple(lead) + (rows, _QCACHE[kind][0](d))
+
+
+def _quantize_kv(kind, x, seq_lens, codes, scales, stream, values=False):
     code_bytes, scale_shape, scale_dtype = _QCACHE[kind]
-    name = "fd_quantize_kv_" + kind
+    name = "fd_quantize_v_fp4" if values else "fd_quantize_kv_" + kind
     lib = load()
     _check_cuda(x, "x", torch.bfloat16)
     _need(x.dim() == 4, "x must be [B, H, L_max, d]")
     B, H, L_max, d = x.shape
-    cshape, sshape = (B, H, L_max, code_bytes(d)), (B, H, L_max) + scale_shape(d)
+    cshape = _v_code_shape(kind, (B, H), L_max, d) if values else (B, H, L_max, code_bytes(d))
+    sshape = (B, H, L_max) + scale_shape(d)
     if codes is None:
         codes = torch.zeros(cshape, dtype=torch.uint8, device=x.device)
     if scales is None:
@@ -447,7 +457,7 @@ def _decode_dense_q(kind, q, k_codes, k_scales, v_codes, v_scales, seq_lens, sca
     _need(k_codes.dim() == 4 and k_codes.shape[0] == B and k_codes.shape[3] == code_bytes(d),
           "k_codes must be [B, Hkv, L_max, %s]" % ("d" if kind == "fp8" else "d/2"))
     _, Hkv, L_max, _ = k_codes.shape
-    _check_cuda(v_codes, "v_codes", torch.uint8, k_codes.shape)
+    _check_cuda(v_codes, "v_codes", torch.uint8, _v_code_shape(kind, (B, Hkv), L_max, d))
     _check_cuda(k_scales, "k_scales", scale_dtype, (B, Hkv, L_max) + scale_shape(d))
     _check_cuda(v_scales, "v_scales", scale_dtype, (B, Hkv, L_max) + scale_shape(d))
     if seq_lens is not None:
@@ -474,7 +484,7 @@ def _decode_paged_q(kind, q, k_pages, k_page_scales, v_pages, v_page_scales, pag
     _need(k_pages.dim() == 4 and k_pages.shape[3] == code_bytes(d),
           "k_pages must be [P, Hkv, page, %s]" % ("d" if kind == "fp8" else "d/2"))
     P, Hkv, page_size, _ = k_pages.shape
-    _check_cuda(v_pages, "v_pages", torch.uint8, k_pages.shape)
+    _check_cuda(v_pages, "v_pages", torch.uint8, _v_code_shape(kind, (P, Hkv), page_size, d))
     _check_cuda(k_page_scales, "k_page_scales", scale_dtype, (P, Hkv, page_size) + scale_shape(d))
     _check_cuda(v_page_scales, "v_page_scales", scale_dtype, (P, Hkv, page_size) + scale_shape(d))
     _check_cuda(page_table, "page_table", torch.int32)
@@ -530,10 +540,17 @@ def fd_decode_paged_fp8(q, k_pages, k_page_scales, v_pages, v_page_scales, page_
 
 @_on_device_of_first_tensor
 def fd_quantize_kv_fp4(x, seq_lens=None, codes=None, scales=None, stream=None):
-    """fp4 cache encoder.  x [B,H,L_max,d] bf16 -> (codes uint8 [B,H,L_max,d/2],
+    """fp4 KEY cache encoder.  x [B,H,L_max,d] bf16 -> (codes uint8 [B,H,L_max,d/2],
     scales uint8 [B,H,L_max,d/32]).  Rows past seq_lens[b] are left as passed
     (zero when this wrapper allocates them)."""
     return _quantize_kv("fp4", x, seq_lens, codes, scales, stream)
+
+
+@_on_device_of_first_tensor
+def fd_quantize_v_fp4(x, seq_lens=None, codes=None, scales=None, stream=None):
+    """fp4 VALUE cache encoder (token pairs).  x [B,H,L_max,d] bf16 -> (codes
+    uint8 [B,H,(L_max+1)//2,d], scales uint8 [B,H,L_max,d/32])."""
+    return _quantize_kv("fp4", x, seq_lens, codes, scales, stream, values=True)
 
 
 def fd_num_splits_fp4(B, Hq, Hkv, L_max, d, num_splits=0, ragged=False) -> int:
@@ -547,8 +564,9 @@ def fd_decode_fp4_workspace_size(B, Hq, Hkv, L_max, d, num_splits=0, ragged=Fals
 @_on_device_of_first_tensor
 def fd_decode_dense_fp4(q, k_codes, k_scales, v_codes, v_scales, seq_lens=None, scale=None, num_splits=0,
                         out=None, lse=None, out_dtype="bf16", want_lse=True, workspace=None, stream=None):
-    """Split-KV decode over an fp4 cache.  q [B,Hq,d] bf16; k_codes, v_codes
-    [B,Hkv,L_max,d/2] uint8; k_scales, v_scales [B,Hkv,L_max,d/32] uint8."""
+    """Split-KV decode over an fp4 cache.  q [B,Hq,d] bf16; k_codes [B,Hkv,L_max,d/2]
+    uint8 (fd_quantize_kv_fp4); v_codes [B,Hkv,(L_max+1)//2,d] uint8 (fd_quantize_v_fp4);
+    k_scales, v_scales [B,Hkv,L_max,d/32] uint8."""
     return _decode_dense_q("fp4", q, k_codes, k_scales, v_codes, v_scales, seq_lens, scale, num_splits, out, lse,
                            out_dtype, want_lse, workspace, stream)
 
@@ -557,8 +575,9 @@ def fd_decode_dense_fp4(q, k_codes, k_scales, v_codes, v_scales, seq_lens=None, 
 def fd_decode_paged_fp4(q, k_pages, k_page_scales, v_pages, v_page_scales, page_table, num_pages, seq_lens,
                         scale=None, num_splits=0, out=None, lse=None, out_dtype="bf16", want_lse=True,
                         workspace=None, stream=None):
-    """Paged split-KV decode over an fp4 cache.  k_pages/v_pages [P,Hkv,64,d/2]
-    uint8, k_page_scales/v_page_scales [P,Hkv,64,d/32] uint8."""
+    """Paged split-KV decode over an fp4 cache.  k_pages [P,Hkv,64,d/2] uint8,
+    v_pages [P,Hkv,32,d] uint8 (token pairs), k_page_scales/v_page_scales
+    [P,Hkv,64,d/32] uint8."""
     return _decode_paged_q("fp4", q, k_pages, k_page_scales, v_pages, v_page_scales, page_table, num_pages,
                            seq_lens, scale, num_splits, out, lse, out_dtype, want_lse, workspace, stream)
 

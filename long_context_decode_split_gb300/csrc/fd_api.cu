@@ -395,7 +395,18 @@ int fd_quantize_kv_fp4(const void* x, const int32_t* seq_lens, int B, int H, int
     if (B > 0 && L_max > 0 && (!x || !codes || !scales)) return FD_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(codes) || !aligned16(scales)) return FD_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(seq_lens) & 3u) return FD_ERR_INVALID_ARG;
-    fd::Fp4QuantArgs a = {x, seq_lens, B, H, L_max, d, codes, scales};
+    fd::Fp4QuantArgs a = {x, seq_lens, B, H, L_max, d, codes, scales, 0};
+    return to_status(fd::launch_quantize_fp4(a, static_cast<cudaStream_t>(stream)));
+}
+
+int fd_quantize_v_fp4(const void* x, const int32_t* seq_lens, int B, int H, int L_max, int d,
+                      uint8_t* codes, uint8_t* scales, void* stream) {
+    const int st = check_shape(B, H, H, L_max, d);
+    if (st != FD_OK) return st;
+    if (B > 0 && L_max > 0 && (!x || !codes || !scales)) return FD_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(codes) || !aligned16(scales)) return FD_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(seq_lens) & 3u) return FD_ERR_INVALID_ARG;
+    fd::Fp4QuantArgs a = {x, seq_lens, B, H, L_max, d, codes, scales, 1};
     return to_status(fd::launch_quantize_fp4(a, static_cast<cudaStream_t>(stream)));
 }
 

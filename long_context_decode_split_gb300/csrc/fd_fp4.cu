@@ -6,8 +6,9 @@
 //   per cache row (token, KV head) and 32-channel block b:
 //     e_b  = the smallest integer in [-126, 127] with 6 * 2^e_b >= max |x|
 //     code = e2m1(x * 2^-e_b)      (round to nearest even; |x * 2^-e_b| <= 6)
-//   codes two per byte (the low nibble holds the even channel), one byte
-//   e_b + 127 per block.
+//   one byte e_b + 127 per block; key codes two channels per byte (the low
+//   nibble holds the even channel), value codes two tokens per byte (the low
+//   nibble holds the even token, rows of pairs [(L_max + 1) / 2, D]).
 //
 // A row costs d/2 + d/32 bytes per operand (68 at d = 128), a quarter of the
 // bf16 cache.  The partial pass has the shape of the fp8 pass (fd_fp8.cu):
@@ -22,15 +23,17 @@
 //               accumulates on its own and is scaled by 2^e_b of its token
 //               before the blocks are summed.
 //   O^T += V^T P^T
-//               V is widened in its stored layout (the ldmatrix words of K:
-//               8 channels of one block of tokens gid and gid + 8 per lane)
-//               and every 8x8 block of it (8 tokens x 8 channels) is
-//               transposed by movmatrix into an A fragment of V^T; output
-//               tile 2c + j holds channels 32c + 8*(gid/2) + 4j + (gid%2)
-//               (row gid) and that + 2 (row gid + 8).  P carries
+//               the value cache is stored one channel of two consecutive
+//               tokens per byte (token pairs), so ldmatrix.trans of a tile's
+//               pair rows hands each lane bytes (pair, channel) that widen
+//               (one cvt each) straight into A fragments of V^T: output tile
+//               j holds channels 16j + 2*gid (row gid) and 16j + 2*gid + 1
+//               (row gid + 8), its k index 2*tig + i / 8 + 2*tig + i is token
+//               4*tig + i / 4*tig + 2 + i.  The score rows of S = K Q^T are
+//               ordered to match (accumulator row m is token sigma(m)), so
+//               movmatrix of P gives the B fragments directly.  P carries
 //               2^e_b(token) / s_ref, s_ref the largest V block scale the
-//               warp has seen, so each block has its own P operand, turned
-//               from the score layout into P^T fragments by movmatrix.
+//               warp has seen, so each block has its own P operand.
 #include <cmath>
 #include <cstdio>
 
@@ -145,6 +148,86 @@ fp4_quantize_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ 
     }
 }
 
+// The same encoding for the value cache, stored in token pairs: one warp per
+// pair of rows (tokens 2p, 2p + 1 of one head); lane l encodes channels
+// D/32 * l ... of both rows, and channel c of the pair is one byte (the even
+// token in the low nibble).  Pairs whose first token is past the sequence are
+// not written; a second token past it encodes as code 0 with its scale
+// byte not written.
+template <int D>
+__global__ void __launch_bounds__(256)
+fp4_quantize_pairs_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ seq_lens, int H, int L_max,
+                          long long pair_rows, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+    constexpr int E = D / 32;       // channels per lane: 4 or 2
+    constexpr int LPB = 32 / E;     // lanes per 32-channel block: 8 or 16
+    const int Lp = (L_max + 1) / 2;
+    const int lane = threadIdx.x & 31;
+    const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
+    for (long long pr = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); pr < pair_rows;
+         pr += nwarps) {
+        const long long bh = pr / Lp;
+        const int t0 = 2 * (int)(pr % Lp);
+        const int b = (int)(bh / H);
+        const int L = clamped_len(seq_lens, b, L_max, &g_status_fp4);
+        if (t0 >= L) continue;  // warp-uniform
+        const bool has1 = t0 + 1 < L;
+        float v[2][E];
+        int eb[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const long long row = bh * L_max + t0 + r;
+            if (r == 1 && !has1) {
+#pragma unroll
+                for (int e = 0; e < E; ++e) v[r][e] = 0.f;
+            } else if constexpr (E == 4) {
+                const uint2 w = *reinterpret_cast<const uint2*>(x + row * D + lane * 4);
+                const float2 a = bf16x2_to_float2(w.x), c = bf16x2_to_float2(w.y);
+                v[r][0] = a.x; v[r][1] = a.y; v[r][2] = c.x; v[r][3] = c.y;
+            } else {
+                const float2 a = bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(x + row * D + lane * 2));
+                v[r][0] = a.x; v[r][1] = a.y;
+            }
+            float amax = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(v[r][e]));
+#pragma unroll
+            for (int off = LPB / 2; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+            eb[r] = -126;
+            const uint32_t bits = __float_as_uint(amax);
+            if ((bits >> 23) != 0u) {
+                const int k = (int)(bits >> 23) - 127;
+                eb[r] = max(-126, k - 2 + ((bits & 0x7fffffu) > 0x400000u ? 1 : 0));
+            }
+        }
+        const float inv0 = __uint_as_float((uint32_t)(127 - eb[0]) << 23);  // 2^-eb, exact
+        const float inv1 = __uint_as_float((uint32_t)(127 - eb[1]) << 23);
+        uint32_t packed = 0;
+#pragma unroll
+        for (int e = 0; e < E; ++e) packed |= e2m1x2_from_f32(v[0][e] * inv0, v[1][e] * inv1) << (8 * e);
+        if constexpr (E == 4) *reinterpret_cast<uint32_t*>(codes + pr * D + lane * 4) = packed;
+        else *reinterpret_cast<uint16_t*>(codes + pr * D + lane * 2) = (uint16_t)packed;
+        if (lane % LPB == 0) {
+            scales[(bh * L_max + t0) * (D / 32) + lane / LPB] = (uint8_t)(eb[0] + 127);
+            if (has1) scales[(bh * L_max + t0 + 1) * (D / 32) + lane / LPB] = (uint8_t)(eb[1] + 127);
+        }
+    }
+}
+
+// Byte offset of 16-byte chunk `ch` of a value pair row (D bytes: the
+// 128-byte swizzle at D = 128, the 64-byte swizzle at D = 64).
+template <int D>
+__device__ __forceinline__ uint32_t vpair_off(int row, int ch) {
+    if constexpr (D == 128) return swz(row, ch);
+    else return swz64(row, ch);
+}
+
+// Token of the warp's 16-row slice that accumulator row m of S = K Q^T
+// holds: rows 0..7 are tokens 0,1,4,5,8,9,12,13 and rows 8..15 tokens
+// 2,3,6,7,10,11,14,15, so that the movmatrix transposes of P (k = 2*tig + i
+// and 8 + 2*tig + i) meet the token order of the value pairs (4*tig + i and
+// 4*tig + 2 + i).
+__device__ __forceinline__ int score_row_token(int m) { return 2 * (m & 7) - (m & 1) + ((m >> 3) << 1); }
+
 // ---------------------------------------------------------------------------
 // Partial pass.
 struct Fp4Params {
@@ -183,6 +266,7 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_wait_primary();  // the previous kernel in the stream may still be running
     const int L = clamped_len(p.seq_lens, b, p.L_max, &g_status_fp4);
+    const int Lp = (p.L_max + 1) / 2;  // value pair rows per head
     const int chunk = chunk_len(L, p.splits, p.chunk_fixed);
     const int t0 = split * chunk;
     const int t1 = min(L, t0 + chunk);
@@ -244,8 +328,10 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
                     stage_rows[s] = rows;
                     stage_off[s] = y & (Gm::ALIGN - 1);
                     mbar_arrive_expect_tx(&full[s], STAGE + 2 * Gm::SBOX * Gm::SB);
+                    // the value pair rows of the tile: 32 rows of D bytes
+                    const int yv = PAGED ? y / 2 : (b * p.Hkv + h) * Lp + tok / 2;
                     tma_load_box64(sk, &tmk, y, &full[s], pol);  // one box of 64 rows (x = 0)
-                    tma_load_box64(sk + CB, &tmv, y, &full[s], pol);
+                    tma_load_box64(sk + CB, &tmv, yv, &full[s], pol);
                     // the scale copies start on the 16-byte boundary at or below the tile
                     tma_load_1d(ss, &tmks, y & ~(Gm::ALIGN - 1), &full[s], pol);
                     tma_load_1d(ss + kScaleSlot, &tmvs, y & ~(Gm::ALIGN - 1), &full[s], pol);
@@ -309,8 +395,10 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
     float2 m_run = make_float2(-INFINITY, -INFINITY), l_run = make_float2(0.f, 0.f);  // columns 2 tig, 2 tig + 1
     float vref = 0.f;
     bool failed = false;
-    const int ld_row = warp * 16 + 8 * (mi >> 1) + (lane & 7);  // row this lane addresses for ldmatrix
-    const int srow[2] = {warp * 16 + gid, warp * 16 + gid + 8};  // S = K Q^T: the lane's accumulator rows
+    // S = K Q^T: the token each lane addresses for ldmatrix (accumulator row
+    // 8 * (mi / 2) + lane % 8) and the tokens of the lane's accumulator rows
+    const int ld_row = warp * 16 + score_row_token(8 * (mi >> 1) + (lane & 7));
+    const int srow[2] = {warp * 16 + score_row_token(gid), warp * 16 + score_row_token(gid + 8)};
 
     for (int t = 0; t < ntiles; t += NT) {
         int st[NT], rows[NT];
@@ -414,7 +502,6 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
             pr[k][3] = none1 ? 0.f : exp2_approx(sc[k][3] - m1);
             lsum0 += pr[k][0] + pr[k][2];
             lsum1 += pr[k][1] + pr[k][3];
-#pragma unroll
         }
         l_run.x = l_run.x * alpha0 + lsum0;
         l_run.y = l_run.y * alpha1 + lsum1;
@@ -434,31 +521,29 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
 #pragma unroll
         for (int k = 0; k < NT; ++k) {
             const uint32_t vt = smem_u32(smem + st[k] * STAGE + CB);
+            // P^T for each V block c: p * 2^e_c(token) / s_ref of accumulator rows gid and
+            // gid + 8 (the scale is 0 past the tile, where the codes may be anything
+            // finite), each 8x8 block transposed from the score layout
+            uint32_t pb[NB][2];
 #pragma unroll
-            for (int cp = 0; cp < NB / 2; ++cp) {
-                // (rows gid, block 2cp), (gid, 2cp+1), (gid + 8, 2cp), (gid + 8, 2cp+1)
+            for (int c = 0; c < NB; ++c) {
+                const float e0 = scale_value((ve[k][0] >> (8 * c)) & 0xffu) * vinv;
+                const float e1 = scale_value((ve[k][1] >> (8 * c)) & 0xffu) * vinv;
+                pb[c][0] = movmatrix_trans(pack_f16(pr[k][0] * e0, pr[k][1] * e0));
+                pb[c][1] = movmatrix_trans(pack_f16(pr[k][2] * e1, pr[k][3] * e1));
+            }
+#pragma unroll
+            for (int x = 0; x < D / 64; ++x) {
+                // matrix j: the warp's 8 pair rows x channels 16 (4x + j) .. + 15; lane (gid, tig)
+                // receives pairs 2 tig, 2 tig + 1 of channels 2 gid, 2 gid + 1 (one byte each)
                 uint32_t w[4];
-                ldsm_x4(vt + code4_off<D>(ld_row, 2 * cp + (mi & 1)), w[0], w[1], w[2], w[3]);
+                ldsm_x4_t(vt + vpair_off<D>(warp * 8 + (lane & 7), 4 * x + (lane >> 3)), w[0], w[1], w[2], w[3]);
 #pragma unroll
-                for (int hb = 0; hb < 2; ++hb) {
-                    const int c = 2 * cp + hb;
-                    // P^T for V block c: p * 2^e_c(token) / s_ref of rows gid and gid + 8 (the
-                    // scale is 0 past the tile, where the codes may be anything finite), each
-                    // 8x8 block transposed from the score layout
-                    const float e0 = scale_value((ve[k][0] >> (8 * c)) & 0xffu) * vinv;
-                    const float e1 = scale_value((ve[k][1] >> (8 * c)) & 0xffu) * vinv;
-                    const uint32_t pb0 = movmatrix_trans(pack_f16(pr[k][0] * e0, pr[k][1] * e0));
-                    const uint32_t pb1 = movmatrix_trans(pack_f16(pr[k][2] * e1, pr[k][3] * e1));
-                    uint32_t x0[4], x8[4];
-                    e2m1x8_to_f16x8(w[hb], x0);      // token gid: channels 32c + 8 tig + 2i, + 1
-                    e2m1x8_to_f16x8(w[2 + hb], x8);  // token gid + 8
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        x0[i] = movmatrix_trans(x0[i]);
-                        x8[i] = movmatrix_trans(x8[i]);
-                    }
-                    mma_f16(o[2 * c], x0[0], x0[1], x8[0], x8[1], pb0, pb1);
-                    mma_f16(o[2 * c + 1], x0[2], x0[3], x8[2], x8[3], pb0, pb1);
+                for (int j = 0; j < 4; ++j) {
+                    const int ch = 4 * x + j;
+                    uint32_t a[4];  // (ch 2gid: tokens 4tig, +1), (2gid+1: same), (2gid: 4tig+2, +3), (2gid+1: same)
+                    e2m1x8_to_f16x8(w[j], a);
+                    mma_f16(o[ch], a[0], a[1], a[2], a[3], pb[ch >> 1][0], pb[ch >> 1][1]);
                 }
             }
         }
@@ -482,16 +567,12 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
     float* red_m = red_o + CW * 8 * D;              // [CW][8]
     float* red_l = red_m + CW * 8;                  // [CW][8]
 #pragma unroll
-    for (int c = 0; c < NB; ++c) {
+    for (int ch = 0; ch < D / 16; ++ch) {
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
-            // query 2*tig + i; output tile 2c + j, row gid + 8r: channel 32c + 8*(gid/2) + 4j + 2r + gid%2
-            float* dst = red_o + (warp * 8 + 2 * tig + i) * D + 32 * c + 8 * (gid >> 1) + (gid & 1);
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                dst[4 * j] = o[2 * c + j][i] * vref;
-                dst[4 * j + 2] = o[2 * c + j][i + 2] * vref;
-            }
+            // query 2*tig + i; output tile ch: channels 16 ch + 2 gid (row gid) and + 1 (row gid + 8)
+            *reinterpret_cast<float2*>(red_o + (warp * 8 + 2 * tig + i) * D + 16 * ch + 2 * gid) =
+                make_float2(o[ch][i] * vref, o[ch][i + 2] * vref);
         }
     }
     if (gid == 0) {
@@ -557,27 +638,37 @@ cudaError_t launch_quantize_fp4(const Fp4QuantArgs& a, cudaStream_t stream) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    const long long want = (rows + 7) / 8;  // 8 rows (warps) per block
+    const long long units = a.token_pairs ? (long long)a.B * a.H * ((a.L_max + 1) / 2) : rows;
+    const long long want = (units + 7) / 8;  // 8 rows or pair rows (warps) per block
     const long long cap = (long long)sms * 8;
     const unsigned grid = (unsigned)(want < cap ? want : cap);
     const uint16_t* x = static_cast<const uint16_t*>(a.x);
-    if (a.D == 128)
+    if (a.token_pairs) {
+        if (a.D == 128)
+            fp4_quantize_pairs_kernel<128><<<grid, 256, 0, stream>>>(x, a.seq_lens, a.H, a.L_max, units, a.codes,
+                                                                     a.scales);
+        else
+            fp4_quantize_pairs_kernel<64><<<grid, 256, 0, stream>>>(x, a.seq_lens, a.H, a.L_max, units, a.codes,
+                                                                    a.scales);
+    } else if (a.D == 128) {
         fp4_quantize_kernel<128><<<grid, 256, 0, stream>>>(x, a.seq_lens, a.H, a.L_max, rows, a.codes, a.scales);
-    else
+    } else {
         fp4_quantize_kernel<64><<<grid, 256, 0, stream>>>(x, a.seq_lens, a.H, a.L_max, rows, a.codes, a.scales);
+    }
     return cudaGetLastError();
 }
 
 template <int D>
-static bool fp4_maps(const DecodeArgs& a, uint64_t rows, CUtensorMap& tk, CUtensorMap& tv, CUtensorMap& tks,
-                     CUtensorMap& tvs) {
+static bool fp4_maps(const DecodeArgs& a, uint64_t rows, uint64_t pair_rows, CUtensorMap& tk, CUtensorMap& tv,
+                     CUtensorMap& tks, CUtensorMap& tvs) {
     using Gm = F4Geo<D>;
     if (rows == 0) {
         // nothing can be read (an empty pool or cache): any well-formed map will do
-        return make_row_map(&tk, a.q, 1, Gm::RB) && make_row_map(&tv, a.q, 1, Gm::RB) &&
+        return make_row_map(&tk, a.q, 1, Gm::RB) && make_row_map(&tv, a.q, 1, D, 32) &&
                make_vec_map(&tks, a.q, 1, Gm::SBOX, Gm::SB) && make_vec_map(&tvs, a.q, 1, Gm::SBOX, Gm::SB);
     }
-    return make_row_map(&tk, a.k, rows, Gm::RB) && make_row_map(&tv, a.v, rows, Gm::RB) &&
+    // keys: rows of D/2 bytes in 64-row boxes; values: pair rows of D bytes in 32-row boxes
+    return make_row_map(&tk, a.k, rows, Gm::RB) && make_row_map(&tv, a.v, pair_rows, D, 32) &&
            make_vec_map(&tks, a.k_scales, rows, Gm::SBOX, Gm::SB) &&
            make_vec_map(&tvs, a.v_scales, rows, Gm::SBOX, Gm::SB);
 }
@@ -587,7 +678,10 @@ cudaError_t launch_decode_fp4(const DecodeArgs& a, cudaStream_t stream) {
     const bool paged = a.page_table != nullptr;
     const uint64_t rows = paged ? (uint64_t)a.num_pages * a.Hkv * kTile : (uint64_t)a.B * a.Hkv * a.L_max;
     CUtensorMap tk, tv, tks, tvs;
-    const bool ok = a.D == 128 ? fp4_maps<128>(a, rows, tk, tv, tks, tvs) : fp4_maps<64>(a, rows, tk, tv, tks, tvs);
+    const uint64_t pair_rows =
+        paged ? (uint64_t)a.num_pages * a.Hkv * (kTile / 2) : (uint64_t)a.B * a.Hkv * ((a.L_max + 1) / 2);
+    const bool ok = a.D == 128 ? fp4_maps<128>(a, rows, pair_rows, tk, tv, tks, tvs)
+                               : fp4_maps<64>(a, rows, pair_rows, tk, tv, tks, tvs);
     if (!ok) return cudaErrorInvalidValue;
     Fp4Params pp;
     pp.q = static_cast<const uint16_t*>(a.q);

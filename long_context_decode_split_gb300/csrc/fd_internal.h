@@ -119,8 +119,9 @@ struct Fp4QuantArgs {
     const void* x;            // [B, H, L_max, D] bf16
     const int32_t* seq_lens;
     int B, H, L_max, D;
-    uint8_t* codes;           // [B, H, L_max, D/2]
+    uint8_t* codes;           // [B, H, L_max, D/2] (channel pairs), or [B, H, (L_max+1)/2, D] (token pairs)
     uint8_t* scales;          // [B, H, L_max, D/32]
+    int token_pairs;          // the value-cache layout: one byte = one channel of tokens 2p, 2p + 1
 };
 cudaError_t launch_quantize_fp4(const Fp4QuantArgs& a, cudaStream_t stream);
 int fp4_ctas_per_sm(int D, bool paged);

@@ -31,21 +31,22 @@ inline EncodeTiledFn tensor_map_encoder() {
     return fn;
 }
 
-// Tensor map for `rows` rows of `row_bytes` bytes, read as boxes of 64 rows
-// x min(row_bytes, 128) bytes: row_bytes a multiple of 128 uses the 128-byte
+// Tensor map for `rows` rows of `row_bytes` bytes, read as boxes of box_rows
+// (64 unless given) rows x min(row_bytes, 128) bytes: row_bytes a multiple of 128 uses the 128-byte
 // swizzle, row_bytes == 64 the 64-byte swizzle (chunk c of row r at
 // position c ^ ((r / 2) % 4)), row_bytes == 32 no swizzle.  Elements are
 // taken as 16-bit values, so the first coordinate counts 2-byte units; byte
 // rows work the same way.  Returns false when the encoder is unavailable or
 // rejects the arguments.
-inline bool make_row_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t row_bytes) {
+inline bool make_row_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t row_bytes,
+                         uint32_t box_rows = 64) {
     EncodeTiledFn enc = tensor_map_encoder();
     if (!enc || rows == 0) return false;
     if (row_bytes % 128 != 0 && row_bytes != 64 && row_bytes != 32) return false;
     const uint32_t box_bytes = row_bytes >= 128 ? 128 : row_bytes;
     const cuuint64_t dims[2] = {row_bytes / 2, rows};
     const cuuint64_t strides[1] = {row_bytes};
-    const cuuint32_t box[2] = {box_bytes / 2, 64};
+    const cuuint32_t box[2] = {box_bytes / 2, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUtensorMapSwizzle sw = box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                   : box_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B

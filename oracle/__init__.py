@@ -24,6 +24,8 @@ Functions (each follows the passage cited in ``fd_oracle.c``):
   float_to_e4m3       binary32 -> e4m3 (RNE, saturating)
   quantize_kv_fp4     e2m1 codes with power-of-two scales per 32-channel block
   dequantize_kv_fp4   its exact binary64 values
+  quantize_v_fp4      the same encoding in the value layout (two tokens per byte)
+  dequantize_v_fp4    its exact binary64 values
   decode_dense_fp8/4  the dense definition over the decoded cache
 """
 from __future__ import annotations
@@ -359,13 +361,62 @@ def dequantize_kv_fp4(codes, scales, seq_lens=None):
     return out
 
 
+def fp4_rows_to_pairs(codes, seq_lens=None):
+    """Re-lay fp4 codes stored two channels per byte ([B,H,L,d/2], the key
+    layout) into the value layout, two tokens per byte ([B,H,(L+1)/2,d]):
+    byte (p, c) = code(2p+1, c) << 4 | code(2p, c).  A token at or past
+    seq_lens[b] contributes code 0; a pair whose first token is past it stays
+    zero.  Pure data movement (nibbles), no arithmetic."""
+    codes = np.ascontiguousarray(codes, np.uint8)
+    B, H, L, d2 = codes.shape
+    d = 2 * d2
+    nib = np.empty((B, H, L + (L % 2), d), np.uint8)
+    nib[:, :, :L, 0::2] = codes & 0x0F
+    nib[:, :, :L, 1::2] = codes >> 4
+    if L % 2:
+        nib[:, :, L] = 0
+    lens = [L] * B if seq_lens is None else [int(x) for x in _i32(seq_lens)]
+    for b, Lb in enumerate(lens):
+        nib[b, :, Lb:] = 0
+    pairs = (nib[:, :, 1::2] << 4) | nib[:, :, 0::2]
+    for b, Lb in enumerate(lens):
+        pairs[b, :, (Lb + 1) // 2:] = 0
+    return np.ascontiguousarray(pairs, np.uint8)
+
+
+def fp4_pairs_to_rows(pairs, L):
+    """Inverse of fp4_rows_to_pairs for the first L tokens: [B,H,(L+1)/2,d]
+    -> [B,H,L,d/2] (two channels per byte)."""
+    pairs = np.ascontiguousarray(pairs, np.uint8)
+    B, H, P, d = pairs.shape
+    nib = np.empty((B, H, 2 * P, d), np.uint8)
+    nib[:, :, 0::2] = pairs & 0x0F
+    nib[:, :, 1::2] = pairs >> 4
+    nib = nib[:, :, :L]
+    return np.ascontiguousarray((nib[..., 1::2] << 4) | nib[..., 0::2], np.uint8)
+
+
+def quantize_v_fp4(x, seq_lens=None, n_threads=0):
+    """The fp4 encoding of quantize_kv_fp4 in the value layout: (codes u8
+    [B,H,(L_max+1)/2,d] in token pairs, scales u8 [B,H,L_max,d/32])."""
+    codes, scales = quantize_kv_fp4(x, seq_lens, n_threads)
+    return fp4_rows_to_pairs(codes, seq_lens), scales
+
+
+def dequantize_v_fp4(pairs, scales, seq_lens=None):
+    """Decoded values of a token-pair fp4 value cache (binary64 [B,H,L_max,d])."""
+    scales = np.ascontiguousarray(scales, np.uint8)
+    return dequantize_kv_fp4(fp4_pairs_to_rows(pairs, scales.shape[2]), scales, seq_lens)
+
+
 def decode_dense_fp4(q, k_codes, k_scales, v_codes, v_scales, seq_lens, scale, n_threads=0):
     """Attention over an fp4 cache: the dense definition (tutorial section 1)
-    in binary64 on the decoded rows e2m1(code) * 2^e of K and V."""
+    in binary64 on the decoded rows e2m1(code) * 2^e of K (key layout) and V
+    (token-pair value layout)."""
     q = _u16(q)
     qf = (q.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     kt = dequantize_kv_fp4(k_codes, k_scales, seq_lens)
-    vt = dequantize_kv_fp4(v_codes, v_scales, seq_lens)
+    vt = dequantize_v_fp4(v_codes, v_scales, seq_lens)
     return decode_dense_f64(qf, kt, vt, seq_lens, scale, n_threads)
 
 

@@ -25,7 +25,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert fd.fd_abi_version() == 1
+    assert fd.fd_abi_version() == 2
     for code in range(7):
         assert fd.fd_status_string(code).startswith("FD_")
     assert "unknown" in fd.fd_status_string(99)
@@ -114,6 +114,8 @@ def test_fp4_host_validation(lib):
     assert lib.fd_decode_paged_fp4(a, a, a, a, a, a, 4, 4, a, 32, 1, 8, 2, 128, 0.1, 1, a, 1, None, None, 0,
                                    None) == fd.FD_ERR_UNSUPPORTED
     assert lib.fd_quantize_kv_fp4(a, None, 1, 2, 100, 128, a, P(0x10008), None) == fd.FD_ERR_INVALID_ARG
+    assert lib.fd_quantize_v_fp4(a, None, 1, 2, 100, 128, a, P(0x10008), None) == fd.FD_ERR_INVALID_ARG
+    assert lib.fd_quantize_v_fp4(a, None, 1, 2, 100, 96, a, a, None) == fd.FD_ERR_UNSUPPORTED
     assert fd.fd_num_splits_fp4(1, 32, 32, 32768, 128, 6) == 6
     assert fd.fd_decode_fp4_workspace_size(2, 8, 2, 1000, 64, 3) == 2 * 8 * 3 * (64 + 2) * 4 + 256
 

@@ -25,8 +25,20 @@ def oracle_codes(oracle, x, seq_lens=None):
     return torch.from_numpy(c).to(DEV), torch.from_numpy(s).to(DEV)
 
 
+def oracle_vcodes(oracle, x, seq_lens=None):
+    c, s = oracle.quantize_v_fp4(bits(x), None if seq_lens is None else seq_lens.cpu())
+    return torch.from_numpy(c).to(DEV), torch.from_numpy(s).to(DEV)
+
+
 def fp4_problem(oracle, p):
-    return oracle_codes(oracle, p.k) + oracle_codes(oracle, p.v)
+    return oracle_codes(oracle, p.k) + oracle_vcodes(oracle, p.v)
+
+
+def poison_value_tail(vc, b, L):
+    """Codes 0xF (-6) for every value token at or past L of sequence b."""
+    vc[b, :, (L + 1) // 2:] = 0xFF
+    if L % 2:
+        vc[b, :, L // 2] |= 0xF0
 
 
 def oracle_fp4(oracle, p, kc, ks, vc, vs, seq_lens=True):
@@ -35,7 +47,7 @@ def oracle_fp4(oracle, p, kc, ks, vc, vs, seq_lens=True):
 
 
 def f32_bound_check(out, ref, vc, vs, oracle):
-    vmax = np.abs(oracle.dequantize_kv_fp4(vc.cpu().numpy(), vs.cpu().numpy())).max()
+    vmax = np.abs(oracle.dequantize_v_fp4(vc.cpu().numpy(), vs.cpu().numpy())).max()
     g = out.float().cpu().numpy().astype(np.float64)
     err = np.abs(g - ref)
     assert np.all(err <= 2.0**-11 * vmax + 1e-4 * (1 + np.abs(ref))), err.max()
@@ -71,13 +83,41 @@ def test_encoder_bit_exact(fd, oracle, d):
     assert fd.fd_device_status(clear=True) == fd.FD_OK
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_value_encoder_bit_exact(fd, oracle, d):
+    g = torch.Generator().manual_seed(d + 7)
+    B, H, L = 3, 2, 301                                # odd L_max: the last pair of a head is half empty
+    mag = torch.exp2(torch.empty(B, H, L, 1).uniform_(-40, 40, generator=g))
+    x = (torch.randn(B, H, L, d, generator=g) * mag).to(torch.bfloat16)
+    x[0, 0, 4] = 0.0
+    x[0, 0, 5, ::2] = -0.0
+    x[1, 1, 6, :8] = torch.tensor([6.0, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+    x = x.to(DEV)
+    sl = torch.tensor([301, 124, 0], dtype=torch.int32, device=DEV)
+    codes = torch.full((B, H, (L + 1) // 2, d), 0xAB, dtype=torch.uint8, device=DEV)
+    scales = torch.full((B, H, L, d // 32), 0xCD, dtype=torch.uint8, device=DEV)
+    fd.fd_quantize_v_fp4(x, sl, codes=codes, scales=scales)
+    rc, rs = oracle.quantize_v_fp4(bits(x), sl.cpu())
+    c, s = codes.cpu().numpy(), scales.cpu().numpy()
+    for b, L_b in enumerate(sl.tolist()):
+        P_b = (L_b + 1) // 2
+        np.testing.assert_array_equal(c[b, :, :P_b], rc[b, :, :P_b])
+        np.testing.assert_array_equal(s[b, :, :L_b], rs[b, :, :L_b])
+        assert np.all(c[b, :, P_b:] == 0xAB) and np.all(s[b, :, L_b:] == 0xCD)  # untouched
+    assert fd.fd_device_status(clear=True) == fd.FD_OK
+
+
 def test_encoder_full_size_sampled(fd, oracle):
     p = W.mha32k(seed=0, device=DEV)
     codes, scales = fd.fd_quantize_kv_fp4(p.k)
+    vcodes, vscales = fd.fd_quantize_v_fp4(p.v)
     for h in (0, 19):
         rc, rs = oracle.quantize_kv_fp4(bits(p.k[:, h:h + 1]))
         np.testing.assert_array_equal(codes[:, h:h + 1].cpu().numpy(), rc)
         np.testing.assert_array_equal(scales[:, h:h + 1].cpu().numpy(), rs)
+        rc, rs = oracle.quantize_v_fp4(bits(p.v[:, h:h + 1]))
+        np.testing.assert_array_equal(vcodes[:, h:h + 1].cpu().numpy(), rc)
+        np.testing.assert_array_equal(vscales[:, h:h + 1].cpu().numpy(), rs)
 
 
 # ------------------------------------------------------------------ decode
@@ -119,7 +159,7 @@ def test_fp4_ragged_empty_and_poisoned_tails(fd, oracle, d):
     ref, lref = oracle_fp4(oracle, p, kc, ks, vc, vs)
     for b, L in enumerate(lens):  # -6 codes and infinite scales (byte 255) past each end
         kc[b, :, L:] = 0xFF
-        vc[b, :, L:] = 0xFF
+        poison_value_tail(vc, b, L)
         ks[b, :, L:] = 0xFF
         vs[b, :, L:] = 0xFF
     for ns in (0, 1, 5):
@@ -161,7 +201,7 @@ def test_fp4_extreme_scales(fd, oracle):
 def test_fp4_gpu_encoder_then_decode(fd, oracle):
     p = W.random_problem(2, 8, 2, 3000, 128, seed=42, device=DEV, seq_lens=[3000, 1234])
     kc, ks = fd.fd_quantize_kv_fp4(p.k, p.seq_lens)
-    vc, vs = fd.fd_quantize_kv_fp4(p.v, p.seq_lens)
+    vc, vs = fd.fd_quantize_v_fp4(p.v, p.seq_lens)
     ref, lref = oracle_fp4(oracle, p, *fp4_problem(oracle, p))
     out, lse = fd.fd_decode_dense_fp4(p.q, kc, ks, vc, vs, p.seq_lens, p.scale)
     assert_out_close(out, ref, BF16_TOL)
@@ -172,12 +212,13 @@ def test_fp4_gpu_encoder_then_decode(fd, oracle):
 
 def paged_codes(oracle, pp, lens):
     kc, ks = oracle_codes(oracle, pp.k_pages)
-    vc, vs = oracle_codes(oracle, pp.v_pages)
+    vc, vs = oracle_vcodes(oracle, pp.v_pages)  # pages [P, Hkv, 64, d] -> pair pages [P, Hkv, 32, d]
     for b, L in enumerate(lens):
         if L % 64:
             pid = int(pp.page_table[b, (L - 1) // 64])
-            for t in (kc, vc, ks, vs):
+            for t in (kc, ks, vs):
                 t[pid, :, L % 64:] = 0xFF
+            poison_value_tail(vc, pid, L % 64)
     return kc, ks, vc, vs
 
 
@@ -203,7 +244,7 @@ def test_fp4_paged_parity(fd, oracle, G, d):
 def test_fp4_full_mha32k_sampled(fd, oracle):
     p = W.mha32k(seed=0, device=DEV)
     kc, ks = fd.fd_quantize_kv_fp4(p.k)
-    vc, vs = fd.fd_quantize_kv_fp4(p.v)
+    vc, vs = fd.fd_quantize_v_fp4(p.v)
     out, lse = fd.fd_decode_dense_fp4(p.q, kc, ks, vc, vs, None, p.scale)
     for h in (0, 13, 31):
         sl = slice(h, h + 1)
@@ -216,7 +257,7 @@ def test_fp4_full_mha32k_sampled(fd, oracle):
 def test_fp4_full_gqa_sampled(fd, oracle):
     p = W.ffd(seed=0, device=DEV)
     kc, ks = fd.fd_quantize_kv_fp4(p.k)
-    vc, vs = fd.fd_quantize_kv_fp4(p.v)
+    vc, vs = fd.fd_quantize_v_fp4(p.v)
     out, lse = fd.fd_decode_dense_fp4(p.q, kc, ks, vc, vs, None, p.scale)
     G = p.Hq // p.Hkv
     for h in (0, 5):
@@ -234,7 +275,7 @@ def test_fp4_many_short_ragged_sequences(fd, oracle):
     lens = torch.randint(0, 201, (B,), generator=g).tolist()
     p = W.random_problem(B, 8, 2, 200, 128, seed=14, device=DEV, seq_lens=lens)
     kc, ks = fd.fd_quantize_kv_fp4(p.k, p.seq_lens)
-    vc, vs = fd.fd_quantize_kv_fp4(p.v, p.seq_lens)
+    vc, vs = fd.fd_quantize_v_fp4(p.v, p.seq_lens)
     ref, lref = oracle_fp4(oracle, p, kc, ks, vc, vs)
     out, lse = fd.fd_decode_dense_fp4(p.q, kc, ks, vc, vs, p.seq_lens, p.scale)
     assert_out_close(out, ref, BF16_TOL)

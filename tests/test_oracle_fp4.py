@@ -177,7 +177,44 @@ def test_fp4_attention_reduces_to_bf16_when_exact(oracle):
     v, vc, vs = grid_cache(rng, B, Hkv, L, d)
     q = bits(torch.randn(B, Hq, d).to(torch.bfloat16))
     sl = np.array([70, 33], np.int32)
-    out4, lse4 = oracle.decode_dense_fp4(q, kc, ks, vc, vs, sl, 0.02)
+    out4, lse4 = oracle.decode_dense_fp4(q, kc, ks, oracle.fp4_rows_to_pairs(vc, sl), vs, sl, 0.02)
     out, lse = oracle.decode_dense(q, k, v, sl, 0.02)
     np.testing.assert_allclose(out4, out, rtol=1e-13, atol=1e-13)
     np.testing.assert_allclose(lse4, lse, rtol=1e-13, atol=1e-13)
+
+
+# ------------------------------------------------- value cache in token pairs
+
+def test_value_pairs_by_hand(oracle):
+    # two rows of d = 64: channel c of row 0 has code c % 16, of row 1 code (c + 5) % 16
+    c0 = np.arange(64) % 16
+    c1 = (np.arange(64) + 5) % 16
+    rows = np.stack([c0, c1]).astype(np.uint8)                    # [2, 64] codes
+    keylayout = (rows[:, 0::2] | (rows[:, 1::2] << 4)).reshape(1, 1, 2, 32)
+    pairs = oracle.fp4_rows_to_pairs(keylayout)
+    assert pairs.shape == (1, 1, 1, 64)
+    np.testing.assert_array_equal(pairs[0, 0, 0], (c1 << 4) | c0)  # low nibble: the even token
+    np.testing.assert_array_equal(oracle.fp4_pairs_to_rows(pairs, 2), keylayout)
+
+
+def test_value_pairs_odd_length_and_seq_lens(oracle):
+    rng = np.random.default_rng(3)
+    codes = rng.integers(0, 256, size=(2, 3, 7, 32)).astype(np.uint8)   # L = 7 (odd)
+    sl = np.array([7, 4], np.int32)
+    pairs = oracle.fp4_rows_to_pairs(codes, sl)
+    assert pairs.shape == (2, 3, 4, 64)
+    # the last pair of a 7-token sequence holds token 6 and code 0 for the absent token 7
+    assert not (pairs[0, :, 3] >> 4).any()
+    np.testing.assert_array_equal(oracle.fp4_pairs_to_rows(pairs, 7)[0], codes[0])
+    # sequence 1 has 4 tokens: pairs 2, 3 stay zero, the first two round-trip
+    assert not pairs[1, :, 2:].any()
+    np.testing.assert_array_equal(oracle.fp4_pairs_to_rows(pairs, 7)[1, :, :4], codes[1, :, :4])
+
+
+def test_value_pair_encoding_decodes_like_the_key_layout(oracle):
+    x = bits(torch.randn(2, 2, 45, 128).to(torch.bfloat16))
+    sl = np.array([45, 20], np.int32)
+    kc, ks = oracle.quantize_kv_fp4(x, sl)
+    vc, vs = oracle.quantize_v_fp4(x, sl)
+    np.testing.assert_array_equal(vs, ks)
+    np.testing.assert_array_equal(oracle.dequantize_v_fp4(vc, vs, sl), oracle.dequantize_kv_fp4(kc, ks, sl))
