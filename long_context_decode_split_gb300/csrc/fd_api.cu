@@ -139,12 +139,15 @@ Plan fp8_plan(int B, int Hq, int Hkv, int L_max, int d, int requested, bool ragg
     return plan(B, Hkv, L_max, requested, ragged, occ, sms, saturating_ctas(d / 2, sms));
 }
 
-// The fp4 cache moves d/2 + d/32 bytes per row and operand: a tile carries
-// about the bytes of a bf16 tile of a quarter of the head size.
+// The fp4 cache moves d/2 + d/32 bytes per row and operand, but its pass is
+// bound by the widening of the codes on the CUDA cores, not by HBM: like the
+// top-delta pass it needs every resident CTA slot busy.  (Counting only the
+// CTAs that would saturate HBM left 48 of 304 slots empty on the 1M-token and
+// FFD caches: 293 -> 250 us and 149 -> 130 us when the chunks fill them.)
 Plan fp4_plan(int B, int Hq, int Hkv, int L_max, int d, int requested, bool ragged) {
     const int sms = current_sm_count();
     const int occ = requested > 0 ? 1 : fd::fp4_ctas_per_sm(d, ragged);
-    return plan(B, Hkv, L_max, requested, ragged, occ, sms, saturating_ctas(d / 4, sms));
+    return plan(B, Hkv, L_max, requested, ragged, occ, sms, (double)occ * (sms > 0 ? sms : 1));
 }
 
 Plan topdelta_plan(int B, int Hq, int Hkv, int L_max, int d, int requested) {
