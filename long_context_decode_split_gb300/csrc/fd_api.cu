@@ -58,7 +58,7 @@ struct Plan {
 // chunks such that sequences of length L_max span about four waves, so the
 // hardware block scheduler can even out the load.
 Plan plan(int B, int Hkv, int L_max, int requested, bool ragged, int ctas_per_sm, int sms, double r,
-          bool fill_slots = false) {
+          bool fill_slots = false, double wave_tiles = 0.0) {
     Plan pl{1, 0};
     if (requested > 0) {
         pl.splits = requested;
@@ -71,7 +71,7 @@ Plan plan(int B, int Hkv, int L_max, int requested, bool ragged, int ctas_per_sm
     const int min_chunk_tiles = 4;  // 256 tokens
     int best_chunk = tiles;
     if (!ragged) {
-        const double wave_cost = 400.0, split_cost = 20.0;
+        const double wave_cost = wave_tiles > 0.0 ? wave_tiles * (double)slots : 400.0, split_cost = 20.0;
         double best = 1e300;
         const int max_s = tiles / min_chunk_tiles;
         for (int S = 1; S <= max_s; ++S) {
@@ -144,10 +144,14 @@ Plan fp8_plan(int B, int Hq, int Hkv, int L_max, int d, int requested, bool ragg
 // top-delta pass it needs every resident CTA slot busy.  (Counting only the
 // CTAs that would saturate HBM left 48 of 304 slots empty on the 1M-token and
 // FFD caches: 293 -> 250 us and 149 -> 130 us when the chunks fill them.)
+// Each further wave costs about 4.5 tiles of a CTA's time (pipeline fill,
+// the last tile, the combine): a chunk-count sweep at 3 CTAs/SM measured one
+// full wave 7% faster than four on the FFD cache (124.3 vs 133.3 us) and 11%
+// faster than two on MHA-32K (40.0 vs 45.0 us).
 Plan fp4_plan(int B, int Hq, int Hkv, int L_max, int d, int requested, bool ragged) {
     const int sms = current_sm_count();
     const int occ = requested > 0 ? 1 : fd::fp4_ctas_per_sm(d, ragged);
-    return plan(B, Hkv, L_max, requested, ragged, occ, sms, (double)occ * (sms > 0 ? sms : 1));
+    return plan(B, Hkv, L_max, requested, ragged, occ, sms, (double)occ * (sms > 0 ? sms : 1), false, 4.5);
 }
 
 Plan topdelta_plan(int B, int Hq, int Hkv, int L_max, int d, int requested) {

@@ -242,7 +242,7 @@ struct Fp4Params {
 };
 
 template <int D, int STAGES, bool PAGED>
-__global__ void __launch_bounds__(5 * 32, 2)
+__global__ void __launch_bounds__(5 * 32, 3)
 fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                    const __grid_constant__ CUtensorMap tmks, const __grid_constant__ CUtensorMap tmvs,
                    const Fp4Params p) {
