@@ -158,8 +158,11 @@ Plan topdelta_plan(int B, int Hq, int Hkv, int L_max, int d, int requested) {
     const int sms = current_sm_count();
     const int occ = requested > 0 ? 1 : fd::topdelta_ctas_per_sm(d, Hq / Hkv);
     // the fused sparse pass is bound by its instruction issue, not by HBM: it
-    // needs every resident CTA slot busy to reach full speed
-    return plan(B, Hkv, L_max, requested, false, occ, sms, (double)occ * (sms > 0 ? sms : 1));
+    // needs every resident CTA slot busy to reach full speed.  A further wave
+    // costs it about 20 tiles of a CTA's time (the anchor pass, two pipelines
+    // to fill, the last tiles): on the FFD cache one wave of 9 chunks ran
+    // 272.7 us against 281.3 us for two waves of 19.
+    return plan(B, Hkv, L_max, requested, false, occ, sms, (double)occ * (sms > 0 ? sms : 1), false, 20.0);
 }
 
 int to_status(cudaError_t e) { return e == cudaSuccess ? FD_OK : FD_ERR_CUDA; }
