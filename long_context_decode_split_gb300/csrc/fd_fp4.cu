@@ -49,6 +49,10 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kScaleSlot = 384;  // bytes reserved per scale copy in shared memory (128-byte multiple)
+constexpr int kStepTiles = 3;    // tiles a consumer warp takes per step
+// per consumer warp and step: the decoded block scales of its 16 rows of each
+// tile, 8 floats per row (K blocks, then V blocks)
+constexpr int kScaleBufBytes = 4 * kStepTiles * 16 * 8 * 4;
 
 // Geometry per head size: code bytes per row, scale bytes per row, and the
 // scale copy (elements of SB bytes, a 64-token tile plus alignment slack).
@@ -248,7 +252,7 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
                    const Fp4Params p) {
     using Gm = F4Geo<D>;
     constexpr int CW = 4;
-    constexpr int NT = 3;                 // stages a consumer warp takes per step
+    constexpr int NT = kStepTiles;        // stages a consumer warp takes per step
     static_assert(STAGES >= 2 * NT, "the producer needs stages to fill while NT are consumed");
     constexpr int CB = Gm::CB;
     constexpr int STAGE = 2 * CB;         // K tile + V tile
@@ -257,7 +261,7 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     unsigned char* scl = smem + STAGES * STAGE;
-    uint64_t* full = reinterpret_cast<uint64_t*>(scl + STAGES * SSTAGE);
+    uint64_t* full = reinterpret_cast<uint64_t*>(scl + STAGES * SSTAGE + kScaleBufBytes);
     uint64_t* empty = full + STAGES;
     int* stage_rows = reinterpret_cast<int*>(empty + STAGES);
     int* stage_off = stage_rows + STAGES;
@@ -398,7 +402,9 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
     // S = K Q^T: the token each lane addresses for ldmatrix (accumulator row
     // 8 * (mi / 2) + lane % 8) and the tokens of the lane's accumulator rows
     const int ld_row = warp * 16 + score_row_token(8 * (mi >> 1) + (lane & 7));
-    const int srow[2] = {warp * 16 + score_row_token(gid), warp * 16 + score_row_token(gid + 8)};
+    const int srl[2] = {score_row_token(gid), score_row_token(gid + 8)};  // within the warp's 16 rows
+    const int srow[2] = {warp * 16 + srl[0], warp * 16 + srl[1]};
+    float* wsc = reinterpret_cast<float*>(scl + STAGES * SSTAGE) + warp * (NT * 16 * 8);
 
     for (int t = 0; t < ntiles; t += NT) {
         int st[NT], rows[NT];
@@ -418,23 +424,46 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
             break;
         }
 
-        // ---- scores, block by block, and the block scales of V ---------------
-        float sc[NT][4];     // rows gid, gid + 8 x columns 2 tig, 2 tig + 1
-        uint32_t ve[NT][2];  // V scale bytes of rows gid, gid + 8 (0 for rows past the tile)
+        // ---- block scales, decoded once per row --------------------------------
+        // Lane l decodes row l / 2 of the warp's 16 (natural token order): the K
+        // scale bytes for even l, the V scale bytes for odd l, as 2^(E - 127)
+        // into the warp's buffer [NT][16 rows][K blocks | V blocks]; rows past
+        // the tile decode to 0.
+        uint32_t vbytes = 0u;  // odd lanes: per-byte maximum of their rows' V scale bytes
+#pragma unroll
+        for (int k = 0; k < NT; ++k) {
+            const int lr = lane >> 1;
+            const unsigned char* src = scl + st[k] * SSTAGE + stage_off[st[k]] * Gm::SB + ((lane & 1) ? kScaleSlot : 0);
+            uint32_t w = 0u;
+            if (warp * 16 + lr < rows[k]) {
+                if constexpr (NB == 4) w = *reinterpret_cast<const uint32_t*>(src + 4 * (warp * 16 + lr));
+                else w = *reinterpret_cast<const uint16_t*>(src + 2 * (warp * 16 + lr));
+            }
+            if (lane & 1) vbytes = __vmaxu4(vbytes, w);
+            float* dst = wsc + (k * 16 + lr) * 8 + (lane & 1) * 4;
+            if constexpr (NB == 4)
+                *reinterpret_cast<float4*>(dst) = make_float4(scale_value(w & 0xffu), scale_value((w >> 8) & 0xffu),
+                                                              scale_value((w >> 16) & 0xffu), scale_value(w >> 24));
+            else
+                *reinterpret_cast<float2*>(dst) = make_float2(scale_value(w & 0xffu), scale_value(w >> 8));
+        }
+        __syncwarp();
+
+        // ---- scores, block by block -------------------------------------------
+        float sc[NT][4];  // rows gid, gid + 8 x columns 2 tig, 2 tig + 1
 #pragma unroll
         for (int k = 0; k < NT; ++k) {
             const uint32_t kt = smem_u32(smem + st[k] * STAGE);
-            const unsigned char* ksc = scl + st[k] * SSTAGE + stage_off[st[k]] * Gm::SB;
-            const unsigned char* vsc = ksc + kScaleSlot;
-            uint32_t ke[2];  // the K scale bytes of rows gid, gid + 8
+            float kf[2][NB];  // the K block scales of rows gid, gid + 8
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
+                const float* src = wsc + (k * 16 + srl[r]) * 8;
                 if constexpr (NB == 4) {
-                    ke[r] = *reinterpret_cast<const uint32_t*>(ksc + 4 * srow[r]);
-                    ve[k][r] = *reinterpret_cast<const uint32_t*>(vsc + 4 * srow[r]);
+                    const float4 f = *reinterpret_cast<const float4*>(src);
+                    kf[r][0] = f.x; kf[r][1] = f.y; kf[r][2] = f.z; kf[r][3] = f.w;
                 } else {
-                    ke[r] = *reinterpret_cast<const uint16_t*>(ksc + 2 * srow[r]);
-                    ve[k][r] = *reinterpret_cast<const uint16_t*>(vsc + 2 * srow[r]);
+                    const float2 f = *reinterpret_cast<const float2*>(src);
+                    kf[r][0] = f.x; kf[r][1] = f.y;
                 }
             }
             float2 s0 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);  // rows gid, gid + 8
@@ -452,10 +481,8 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
                     e2m1x8_to_f16x8(w[2 + hb], hb8);  // row gid + 8
                     mma_f16(acc, ha[0], hb8[0], ha[1], hb8[1], qa[c][0], qa[c][1]);
                     mma_f16(acc, ha[2], hb8[2], ha[3], hb8[3], qa[c][2], qa[c][3]);
-                    const float k0 = scale_value((ke[0] >> (8 * c)) & 0xffu);
-                    const float k1 = scale_value((ke[1] >> (8 * c)) & 0xffu);
-                    s0 = __ffma2_rn(make_float2(acc[0], acc[1]), make_float2(k0, k0), s0);
-                    s1 = __ffma2_rn(make_float2(acc[2], acc[3]), make_float2(k1, k1), s1);
+                    s0 = __ffma2_rn(make_float2(acc[0], acc[1]), make_float2(kf[0][c], kf[0][c]), s0);
+                    s1 = __ffma2_rn(make_float2(acc[2], acc[3]), make_float2(kf[1][c], kf[1][c]), s1);
                 }
             }
             const bool ok0 = srow[0] < rows[k], ok1 = srow[1] < rows[k];
@@ -463,25 +490,24 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
             sc[k][1] = ok0 ? s0.y * qmul.y : -INFINITY;
             sc[k][2] = ok1 ? s1.x * qmul.x : -INFINITY;
             sc[k][3] = ok1 ? s1.y * qmul.y : -INFINITY;
-            ve[k][0] = ok0 ? ve[k][0] : 0u;  // scale byte 0 decodes to 0
-            ve[k][1] = ok1 ? ve[k][1] : 0u;
         }
 
         // ---- online softmax per column and the V reference scale ---------------
         float mx0 = -INFINITY, mx1 = -INFINITY;
-        uint32_t emax = 0u;  // per-byte maximum of the V scale bytes (a larger byte is a larger scale)
+        uint32_t emax = vbytes;  // per-byte maximum of the V scale bytes (a larger byte is a larger scale)
 #pragma unroll
         for (int k = 0; k < NT; ++k) {
             mx0 = fmaxf(mx0, fmaxf(sc[k][0], sc[k][2]));
             mx1 = fmaxf(mx1, fmaxf(sc[k][1], sc[k][3]));
-            emax = __vmaxu4(emax, __vmaxu4(ve[k][0], ve[k][1]));
         }
+        emax = __vmaxu4(emax, __shfl_xor_sync(0xffffffffu, emax, 2));
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {  // over the 16 rows: the lanes of equal tig
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
             emax = __vmaxu4(emax, __shfl_xor_sync(0xffffffffu, emax, off));
         }
+        emax = __vmaxu4(emax, __shfl_xor_sync(0xffffffffu, emax, 1));  // the odd lanes hold the V bytes
         emax = max(max(emax & 0xffu, (emax >> 8) & 0xffu), max((emax >> 16) & 0xffu, emax >> 24));
         const float vref_new = fmaxf(vref, scale_value(emax));
         const float vinv = vref_new > 0.f ? __fdividef(1.f, vref_new) : 0.f;
@@ -524,11 +550,23 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
             // P^T for each V block c: p * 2^e_c(token) / s_ref of accumulator rows gid and
             // gid + 8 (the scale is 0 past the tile, where the codes may be anything
             // finite), each 8x8 block transposed from the score layout
+            float vf[2][NB];  // the V block scales of rows gid, gid + 8 (0 past the tile)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const float* src = wsc + (k * 16 + srl[r]) * 8 + 4;
+                if constexpr (NB == 4) {
+                    const float4 f = *reinterpret_cast<const float4*>(src);
+                    vf[r][0] = f.x; vf[r][1] = f.y; vf[r][2] = f.z; vf[r][3] = f.w;
+                } else {
+                    const float2 f = *reinterpret_cast<const float2*>(src);
+                    vf[r][0] = f.x; vf[r][1] = f.y;
+                }
+            }
             uint32_t pb[NB][2];
 #pragma unroll
             for (int c = 0; c < NB; ++c) {
-                const float e0 = scale_value((ve[k][0] >> (8 * c)) & 0xffu) * vinv;
-                const float e1 = scale_value((ve[k][1] >> (8 * c)) & 0xffu) * vinv;
+                const float e0 = vf[0][c] * vinv;
+                const float e1 = vf[1][c] * vinv;
                 pb[c][0] = movmatrix_trans(pack_f16(pr[k][0] * e0, pr[k][1] * e0));
                 pb[c][1] = movmatrix_trans(pack_f16(pr[k][2] * e1, pr[k][3] * e1));
             }
@@ -587,9 +625,10 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
 
 template <int D, bool PAGED>
 struct Fp4Launcher {
-    static constexpr int STAGES = 8;
+    static constexpr int STAGES = 7;
     static constexpr int STAGE = 2 * F4Geo<D>::CB;
-    static constexpr int SMEM = 1024 + STAGES * STAGE + STAGES * 2 * kScaleSlot + STAGES * 16 + STAGES * 8 + 64;
+    static constexpr int SMEM =
+        1024 + STAGES * STAGE + STAGES * 2 * kScaleSlot + kScaleBufBytes + STAGES * 16 + STAGES * 8 + 64;
     static constexpr int RED = 4 * 8 * D * 4 + 2 * 4 * 8 * 4;
     static_assert(STAGES * STAGE >= RED, "reduction scratch must fit in the ring");
     static constexpr auto kernel = fp4_partial_kernel<D, STAGES, PAGED>;
