@@ -31,9 +31,12 @@
 //               (row gid + 8), its k index 2*tig + i / 8 + 2*tig + i is token
 //               4*tig + i / 4*tig + 2 + i.  The score rows of S = K Q^T are
 //               ordered to match (accumulator row m is token sigma(m)), so
-//               movmatrix of P gives the B fragments directly.  P carries
-//               2^e_b(token) / s_ref, s_ref the largest V block scale the
-//               warp has seen, so each block has its own P operand.
+//               movmatrix of P gives the B fragments directly, once per
+//               tile; block b's operand multiplies them (mul.rn.f16x2) by
+//               the fp16 pairs 2^e_b(token) / s_ref of their tokens, s_ref
+//               the largest V block scale the warp has seen.  The block
+//               scales are decoded once per row and step into a per-warp
+//               buffer (K as floats, V as those fp16 pairs).
 #include <cmath>
 #include <cstdio>
 
@@ -50,9 +53,11 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int kScaleSlot = 384;  // bytes reserved per scale copy in shared memory (128-byte multiple)
 constexpr int kStepTiles = 3;    // tiles a consumer warp takes per step
-// per consumer warp and step: the decoded block scales of its 16 rows of each
-// tile, 8 floats per row (K blocks, then V blocks)
-constexpr int kScaleBufBytes = 4 * kStepTiles * 16 * 8 * 4;
+// per consumer warp and step, for each tile: the K block scales of its 16 rows
+// (4 floats per row) and the V block scales of its 8 token pairs relative to
+// the running reference (4 fp16x2 per pair)
+constexpr int kScaleTileBytes = 16 * 4 * 4 + 8 * 4 * 4;
+constexpr int kScaleBufBytes = 4 * kStepTiles * kScaleTileBytes;
 
 // Geometry per head size: code bytes per row, scale bytes per row, and the
 // scale copy (elements of SB bytes, a 64-token tile plus alignment slack).
@@ -98,6 +103,13 @@ __device__ __forceinline__ uint32_t e2m1x2_from_f32(float lo, float hi) {
         : "=r"(r)
         : "f"(hi), "f"(lo));
     return r;
+}
+
+// Element-wise fp16x2 product, round to nearest even.
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
 }
 
 // 2^(E - 127) for a scale byte E in [1, 254] (a normal binary32, exact).
@@ -404,7 +416,10 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
     const int ld_row = warp * 16 + score_row_token(8 * (mi >> 1) + (lane & 7));
     const int srl[2] = {score_row_token(gid), score_row_token(gid + 8)};  // within the warp's 16 rows
     const int srow[2] = {warp * 16 + srl[0], warp * 16 + srl[1]};
-    float* wsc = reinterpret_cast<float*>(scl + STAGES * SSTAGE) + warp * (NT * 16 * 8);
+    float* kbuf = reinterpret_cast<float*>(scl + STAGES * SSTAGE + warp * NT * kScaleTileBytes);  // [NT][16][4]
+    uint32_t* vbuf = reinterpret_cast<uint32_t*>(kbuf + NT * 16 * 4);                              // [NT][8][NB]
+    const int pv = NB == 4 ? lane >> 2 : (lane >> 1) & 7;  // the token pair whose V scales the lane turns into fp16
+    const int cv = NB == 4 ? lane & 3 : lane & 1;          // and the block
 
     for (int t = 0; t < ntiles; t += NT) {
         int st[NT], rows[NT];
@@ -424,28 +439,43 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
             break;
         }
 
-        // ---- block scales, decoded once per row --------------------------------
-        // Lane l decodes row l / 2 of the warp's 16 (natural token order): the K
-        // scale bytes for even l, the V scale bytes for odd l, as 2^(E - 127)
-        // into the warp's buffer [NT][16 rows][K blocks | V blocks]; rows past
-        // the tile decode to 0.
-        uint32_t vbytes = 0u;  // odd lanes: per-byte maximum of their rows' V scale bytes
+        // ---- block scales --------------------------------------------------------
+        // K: lane l decodes blocks 2(l % 2), 2(l % 2) + 1 (block l % 2 at d = 64) of
+        // row l / 2 of the warp's 16 (natural token order) as 2^(E - 127) into
+        // kbuf[k][row][block].  V: lane l holds the scale words of the token pair
+        // pv = l / 4 (l / 2 mod 8 at d = 64), rows 2 pv and 2 pv + 1; they become
+        // fp16 pairs once the step's reference scale is known.  Rows past the
+        // tile read as scale byte 0 (scale 0).  V scale words are read here for
+        // their maximum and again below.
+        uint32_t vbytes = 0u;  // per-byte maximum of the lane's V scale bytes (a larger byte is a larger scale)
 #pragma unroll
         for (int k = 0; k < NT; ++k) {
+            const unsigned char* ksrc = scl + st[k] * SSTAGE + stage_off[st[k]] * Gm::SB;
+            const unsigned char* vsrc = ksrc + kScaleSlot;
             const int lr = lane >> 1;
-            const unsigned char* src = scl + st[k] * SSTAGE + stage_off[st[k]] * Gm::SB + ((lane & 1) ? kScaleSlot : 0);
-            uint32_t w = 0u;
+            uint32_t kw = 0u;
             if (warp * 16 + lr < rows[k]) {
-                if constexpr (NB == 4) w = *reinterpret_cast<const uint32_t*>(src + 4 * (warp * 16 + lr));
-                else w = *reinterpret_cast<const uint16_t*>(src + 2 * (warp * 16 + lr));
+                if constexpr (NB == 4) kw = *reinterpret_cast<const uint32_t*>(ksrc + 4 * (warp * 16 + lr));
+                else kw = *reinterpret_cast<const uint16_t*>(ksrc + 2 * (warp * 16 + lr));
             }
-            if (lane & 1) vbytes = __vmaxu4(vbytes, w);
-            float* dst = wsc + (k * 16 + lr) * 8 + (lane & 1) * 4;
-            if constexpr (NB == 4)
-                *reinterpret_cast<float4*>(dst) = make_float4(scale_value(w & 0xffu), scale_value((w >> 8) & 0xffu),
-                                                              scale_value((w >> 16) & 0xffu), scale_value(w >> 24));
-            else
-                *reinterpret_cast<float2*>(dst) = make_float2(scale_value(w & 0xffu), scale_value(w >> 8));
+            float* kdst = kbuf + (k * 16 + lr) * 4;
+            if constexpr (NB == 4) {
+                const int c0 = 2 * (lane & 1);
+                *reinterpret_cast<float2*>(kdst + c0) =
+                    make_float2(scale_value((kw >> (8 * c0)) & 0xffu), scale_value((kw >> (8 * c0 + 8)) & 0xffu));
+            } else {
+                kdst[lane & 1] = scale_value((kw >> (8 * (lane & 1))) & 0xffu);
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int r = warp * 16 + 2 * pv + h;
+                uint32_t w = 0u;
+                if (r < rows[k]) {
+                    if constexpr (NB == 4) w = *reinterpret_cast<const uint32_t*>(vsrc + 4 * r);
+                    else w = *reinterpret_cast<const uint16_t*>(vsrc + 2 * r);
+                }
+                vbytes = __vmaxu4(vbytes, w);
+            }
         }
         __syncwarp();
 
@@ -457,7 +487,7 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
             float kf[2][NB];  // the K block scales of rows gid, gid + 8
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
-                const float* src = wsc + (k * 16 + srl[r]) * 8;
+                const float* src = kbuf + (k * 16 + srl[r]) * 4;
                 if constexpr (NB == 4) {
                     const float4 f = *reinterpret_cast<const float4*>(src);
                     kf[r][0] = f.x; kf[r][1] = f.y; kf[r][2] = f.z; kf[r][3] = f.w;
@@ -500,19 +530,33 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
             mx0 = fmaxf(mx0, fmaxf(sc[k][0], sc[k][2]));
             mx1 = fmaxf(mx1, fmaxf(sc[k][1], sc[k][3]));
         }
-        emax = __vmaxu4(emax, __shfl_xor_sync(0xffffffffu, emax, 2));
+        if constexpr (NB == 2) emax = __vmaxu4(emax, __shfl_xor_sync(0xffffffffu, emax, 2));
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {  // over the 16 rows: the lanes of equal tig
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
             emax = __vmaxu4(emax, __shfl_xor_sync(0xffffffffu, emax, off));
         }
-        emax = __vmaxu4(emax, __shfl_xor_sync(0xffffffffu, emax, 1));  // the odd lanes hold the V bytes
         emax = max(max(emax & 0xffu, (emax >> 8) & 0xffu), max((emax >> 16) & 0xffu, emax >> 24));
         const float vref_new = fmaxf(vref, scale_value(emax));
         const float vinv = vref_new > 0.f ? __fdividef(1.f, vref_new) : 0.f;
         const float vf = vref_new > 0.f ? vref * vinv : 1.f;
         vref = vref_new;
+        // V block scales over the reference as fp16 pairs: lane l writes block cv of
+        // its token pair pv, (s(2 pv) / s_ref, s(2 pv + 1) / s_ref), both <= 1
+#pragma unroll
+        for (int k = 0; k < NT; ++k) {
+            const unsigned char* vsrc = scl + st[k] * SSTAGE + stage_off[st[k]] * Gm::SB + kScaleSlot;
+            uint32_t e[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int r = warp * 16 + 2 * pv + h;
+                e[h] = 0u;
+                if (r < rows[k]) e[h] = vsrc[Gm::SB * r + cv];
+            }
+            vbuf[(k * 8 + pv) * NB + cv] = pack_f16(scale_value(e[0]) * vinv, scale_value(e[1]) * vinv);
+        }
+        __syncwarp();
         const float m0 = fmaxf(m_run.x, mx0), m1 = fmaxf(m_run.y, mx1);
         const bool none0 = m0 == -INFINITY, none1 = m1 == -INFINITY;
         const float alpha0 = none0 ? 1.f : exp2_approx(m_run.x - m0);
@@ -550,25 +594,29 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
             // P^T for each V block c: p * 2^e_c(token) / s_ref of accumulator rows gid and
             // gid + 8 (the scale is 0 past the tile, where the codes may be anything
             // finite), each 8x8 block transposed from the score layout
-            float vf[2][NB];  // the V block scales of rows gid, gid + 8 (0 past the tile)
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const float* src = wsc + (k * 16 + srl[r]) * 8 + 4;
-                if constexpr (NB == 4) {
-                    const float4 f = *reinterpret_cast<const float4*>(src);
-                    vf[r][0] = f.x; vf[r][1] = f.y; vf[r][2] = f.z; vf[r][3] = f.w;
-                } else {
-                    const float2 f = *reinterpret_cast<const float2*>(src);
-                    vf[r][0] = f.x; vf[r][1] = f.y;
-                }
+            // P^T of the tile (transposed from the score layout by movmatrix): b0 holds
+            // tokens 4 tig, 4 tig + 1 (pair 2 tig), b1 tokens 4 tig + 2, 4 tig + 3
+            // (pair 2 tig + 1), query gid; block c's operand scales each token by
+            // its block scale over the reference
+            const uint32_t p0 = movmatrix_trans(pack_f16(pr[k][0], pr[k][1]));
+            const uint32_t p1 = movmatrix_trans(pack_f16(pr[k][2], pr[k][3]));
+            uint32_t sv0[NB], sv1[NB];
+            if constexpr (NB == 4) {
+                const uint4 a = *reinterpret_cast<const uint4*>(vbuf + (k * 8 + 2 * tig) * NB);
+                const uint4 c = *reinterpret_cast<const uint4*>(vbuf + (k * 8 + 2 * tig + 1) * NB);
+                sv0[0] = a.x; sv0[1] = a.y; sv0[2] = a.z; sv0[3] = a.w;
+                sv1[0] = c.x; sv1[1] = c.y; sv1[2] = c.z; sv1[3] = c.w;
+            } else {
+                const uint2 a = *reinterpret_cast<const uint2*>(vbuf + (k * 8 + 2 * tig) * NB);
+                const uint2 c = *reinterpret_cast<const uint2*>(vbuf + (k * 8 + 2 * tig + 1) * NB);
+                sv0[0] = a.x; sv0[1] = a.y;
+                sv1[0] = c.x; sv1[1] = c.y;
             }
             uint32_t pb[NB][2];
 #pragma unroll
             for (int c = 0; c < NB; ++c) {
-                const float e0 = vf[0][c] * vinv;
-                const float e1 = vf[1][c] * vinv;
-                pb[c][0] = movmatrix_trans(pack_f16(pr[k][0] * e0, pr[k][1] * e0));
-                pb[c][1] = movmatrix_trans(pack_f16(pr[k][2] * e1, pr[k][3] * e1));
+                pb[c][0] = hmul2_u32(p0, sv0[c]);
+                pb[c][1] = hmul2_u32(p1, sv1[c]);
             }
 #pragma unroll
             for (int x = 0; x < D / 64; ++x) {
