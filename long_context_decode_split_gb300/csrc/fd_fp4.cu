@@ -36,7 +36,9 @@
 //               the fp16 pairs 2^e_b(token) / s_ref of their tokens, s_ref
 //               the largest V block scale the warp has seen.  The block
 //               scales are decoded once per row and step into a per-warp
-//               buffer (K as floats, V as those fp16 pairs).
+//               buffer (K as floats, V as those fp16 pairs), and the query
+//               fragments are read from shared memory where they are used:
+//               the registers they free are worth more at 3 CTAs per SM.
 #include <cmath>
 #include <cstdio>
 
@@ -277,6 +279,8 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
     uint64_t* empty = full + STAGES;
     int* stage_rows = reinterpret_cast<int*>(empty + STAGES);
     int* stage_off = stage_rows + STAGES;
+    uint4* qsm = reinterpret_cast<uint4*>((reinterpret_cast<uintptr_t>(stage_off + STAGES) + 15) &
+                                          ~static_cast<uintptr_t>(15));  // Q fragments [NB][32]
 
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -370,9 +374,9 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
     // fp16 times 2^-e (e the exponent of the query's largest |q|; exact).  The
     // accumulators hold rows (tokens) gid, gid + 8 and columns (queries)
     // 2 tig, 2 tig + 1.
-    uint32_t qa[NB][4];
     float2 qmul;  // columns 2 tig, 2 tig + 1
     {
+        uint32_t qa[NB][4];
         const uint16_t* qrow = p.q + (size_t)(b * p.Hq + hq0 + gid) * D;
         float amax = 0.f;
         uint4 qw[NB];
@@ -401,6 +405,12 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
         }
         const float qm = ldexpf(p.scale_log2, ex);  // query gid's; lane 4q holds query q
         qmul = make_float2(__shfl_sync(0xffffffffu, qm, 8 * tig), __shfl_sync(0xffffffffu, qm, 8 * tig + 4));
+        // every consumer warp holds the same fragments: one copy in shared memory,
+        // [block][lane] so that a warp's 16-byte reads hit distinct banks
+        if (warp == 0)
+#pragma unroll
+            for (int c = 0; c < NB; ++c) qsm[c * 32 + lane] = make_uint4(qa[c][0], qa[c][1], qa[c][2], qa[c][3]);
+        named_barrier(1, CW * 32);
     }
 
     float o[D / 16][4];
@@ -509,8 +519,9 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
                     uint32_t ha[4], hb8[4];
                     e2m1x8_to_f16x8(w[hb], ha);       // row gid: channels 32c + 8 tig ..
                     e2m1x8_to_f16x8(w[2 + hb], hb8);  // row gid + 8
-                    mma_f16(acc, ha[0], hb8[0], ha[1], hb8[1], qa[c][0], qa[c][1]);
-                    mma_f16(acc, ha[2], hb8[2], ha[3], hb8[3], qa[c][2], qa[c][3]);
+                    const uint4 qf = qsm[c * 32 + lane];
+                    mma_f16(acc, ha[0], hb8[0], ha[1], hb8[1], qf.x, qf.y);
+                    mma_f16(acc, ha[2], hb8[2], ha[3], hb8[3], qf.z, qf.w);
                     s0 = __ffma2_rn(make_float2(acc[0], acc[1]), make_float2(kf[0][c], kf[0][c]), s0);
                     s1 = __ffma2_rn(make_float2(acc[2], acc[3]), make_float2(kf[1][c], kf[1][c]), s1);
                 }
@@ -676,7 +687,8 @@ struct Fp4Launcher {
     static constexpr int STAGES = 7;
     static constexpr int STAGE = 2 * F4Geo<D>::CB;
     static constexpr int SMEM =
-        1024 + STAGES * STAGE + STAGES * 2 * kScaleSlot + kScaleBufBytes + STAGES * 16 + STAGES * 8 + 64;
+        1024 + STAGES * STAGE + STAGES * 2 * kScaleSlot + kScaleBufBytes + STAGES * 16 + STAGES * 8 + 16 +
+        F4Geo<D>::NB * 32 * 16 + 64;
     static constexpr int RED = 4 * 8 * D * 4 + 2 * 4 * 8 * 4;
     static_assert(STAGES * STAGE >= RED, "reduction scratch must fit in the ring");
     static constexpr auto kernel = fp4_partial_kernel<D, STAGES, PAGED>;
