@@ -164,7 +164,9 @@ struct TLayout {
     static constexpr int FLAG_OFF = DEC_OFF + DS * CW * 32 * 16;               // need[DS][CW], loaded[DS], scan_rows[SS]
     static constexpr int BAR_OFF = (FLAG_OFF + (DS * CW + DS + SS) * 4 + 15) / 16 * 16;
     static constexpr int MH_OFF = BAR_OFF + (2 * SS + 3 * DS) * 8;             // anchor maxima [CW][8]
-    static constexpr int BYTES = 1024 + MH_OFF + CW * 8 * 4;
+    static constexpr int QV = 3 * Gm::NG;                                      // query vectors per lane
+    static constexpr int Q_OFF = (MH_OFF + CW * 8 * 4 + 15) / 16 * 16;         // [QV][32] x 16 B
+    static constexpr int BYTES = 1024 + Q_OFF + QV * 32 * 16;
     static_assert(DS * Gm::DET_STAGE >= CW * 8 * D * 4 + 2 * CW * 8 * 4, "epilogue scratch must fit in the rings");
     static_assert(Gm::DET_STAGE >= Gm::SCAN_STAGE, "anchor staging must fit in one detail stage");
 };
@@ -225,7 +227,7 @@ struct TDQuery {
 // in group order.
 template <int D>
 __device__ __forceinline__ void scan_tile(const unsigned char* codes, const unsigned char* ms, int warp, int lane,
-                                          const TDQuery<D>& tq, float (&st)[4]) {
+                                          const uint4* qv, float2 scan_scale, float (&st)[4]) {
     using Gm = TGeo<D>;
     const int gid = lane >> 2, tig = lane & 3;
     const int r0 = warp * 16 + gid, r1 = r0 + 8;
@@ -254,30 +256,32 @@ __device__ __forceinline__ void scan_tile(const unsigned char* codes, const unsi
         for (int hg = 0; hg < 2; ++hg) {  // the two 32-channel groups of this 16-byte word
             const int g = 2 * kq + hg;
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint4 qg = qv[g * 32];  // qc0, qc2 of k-steps 2g and 2g + 1
 #pragma unroll
             for (int e2 = 0; e2 < 2; ++e2) {
-                const int kk = 2 * g + e2;
                 const uint32_t ua = wa[2 * hg + e2] >> (4 * tig), ub = wb[2 * hg + e2] >> (4 * tig);
                 // bits 0-1 / 16-17: codes of the even pair as bf16 subnormals code * 2^-133; bits 2-3 /
                 // 18-19: the odd pair as 4 * code * 2^-133 (qc2 carries the 1/4)
-                mma_bf16(acc, ua & 0x00030003u, ub & 0x00030003u, ua & 0x000C000Cu, ub & 0x000C000Cu, tq.qc0[kk],
-                         tq.qc2[kk]);
+                mma_bf16(acc, ua & 0x00030003u, ub & 0x00030003u, ua & 0x000C000Cu, ub & 0x000C000Cu,
+                         e2 ? qg.z : qg.x, e2 ? qg.w : qg.y);
             }
+            const float4 qs4 = *reinterpret_cast<const float4*>(&qv[(2 * Gm::NG + g / 2) * 32]);
+            const float2 qsum = (g & 1) ? make_float2(qs4.z, qs4.w) : make_float2(qs4.x, qs4.y);
             // group g of rows r0 / r1, queries 2 tig and 2 tig + 1: s_g * <q, code>_g + mn_g * sum_g(q),
             // added in g order
             const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&ma[g]));  // (mn, s) of row r0
             const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&mb[g]));  // (mn, s) of row r1
             v0 = __fadd2_rn(v0, __ffma2_rn(make_float2(fa.y, fa.y), make_float2(acc[0], acc[1]),
-                                           __fmul2_rn(make_float2(fa.x, fa.x), tq.qsum[g])));
+                                           __fmul2_rn(make_float2(fa.x, fa.x), qsum)));
             v1 = __fadd2_rn(v1, __ffma2_rn(make_float2(fb.y, fb.y), make_float2(acc[2], acc[3]),
-                                           __fmul2_rn(make_float2(fb.x, fb.x), tq.qsum[g])));
+                                           __fmul2_rn(make_float2(fb.x, fb.x), qsum)));
         }
     }
     // v is the group sum times 2^(sq - 7) exactly; scan_scale undoes the power of two
-    st[0] = __fmul_rn(v0.x, tq.scan_scale.x);
-    st[1] = __fmul_rn(v0.y, tq.scan_scale.y);
-    st[2] = __fmul_rn(v1.x, tq.scan_scale.x);
-    st[3] = __fmul_rn(v1.y, tq.scan_scale.y);
+    st[0] = __fmul_rn(v0.x, scan_scale.x);
+    st[1] = __fmul_rn(v0.y, scan_scale.y);
+    st[2] = __fmul_rn(v1.x, scan_scale.x);
+    st[3] = __fmul_rn(v1.y, scan_scale.y);
 }
 
 // Residual term sum_g rs_g * <q, rq>_g of the warp's 16 rows (same layout as
@@ -290,7 +294,7 @@ __device__ __forceinline__ void scan_tile(const unsigned char* codes, const unsi
 // its two k-steps, in group order.
 template <int D>
 __device__ __forceinline__ void residual_tile(uint32_t res_s, const unsigned char* rs, int warp, int lane,
-                                              const TDQuery<D>& tq, float (&rt)[4]) {
+                                              const uint4* qv, float (&rt)[4]) {
     using Gm = TGeo<D>;
     const int gid = lane >> 2;
     const int mi = lane >> 3;
@@ -319,19 +323,22 @@ __device__ __forceinline__ void residual_tile(uint32_t res_s, const unsigned cha
         uint32_t r[4];
         ldsm_x4(addr, r[0], r[1], r[2], r[3]);  // (row r0, kk 2g), (r0, 2g+1), (r1, 2g), (r1, 2g+1)
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint4 qg = qv[(Gm::NG + g) * 32];  // qr0, qr2 of k-steps 2g and 2g + 1
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             // fp16 0x64uu is 1024 + uu exactly; with uu = x + 128 the operand is 1152 + x and
             // the offset leaves the sum as 1152 * (sum of q over the group), removed below
             const uint32_t ua = r[e] ^ 0x80808080u, ub = r[e + 2] ^ 0x80808080u;
             mma_f16(acc, __byte_perm(ua, 0x64646464u, 0x4140), __byte_perm(ub, 0x64646464u, 0x4140),
-                    __byte_perm(ua, 0x64646464u, 0x4342), __byte_perm(ub, 0x64646464u, 0x4342), tq.qr0[2 * g + e],
-                    tq.qr2[2 * g + e]);
+                    __byte_perm(ua, 0x64646464u, 0x4342), __byte_perm(ub, 0x64646464u, 0x4342), e ? qg.z : qg.x,
+                    e ? qg.w : qg.y);
         }
+        const float4 of4 = *reinterpret_cast<const float4*>(&qv[(2 * Gm::NG + Gm::NG / 2 + g / 2) * 32]);
+        const float2 off = (g & 1) ? make_float2(of4.z, of4.w) : make_float2(of4.x, of4.y);
         const float2 fa = __half22float2(ra[g >> 1]), fb = __half22float2(rb[g >> 1]);
         const float rsa = (g & 1) ? fa.y : fa.x, rsb = (g & 1) ? fb.y : fb.x;
-        v0 = __ffma2_rn(make_float2(rsa, rsa), make_float2(acc[0] - tq.off[g].x, acc[1] - tq.off[g].y), v0);
-        v1 = __ffma2_rn(make_float2(rsb, rsb), make_float2(acc[2] - tq.off[g].x, acc[3] - tq.off[g].y), v1);
+        v0 = __ffma2_rn(make_float2(rsa, rsa), make_float2(acc[0] - off.x, acc[1] - off.y), v0);
+        v1 = __ffma2_rn(make_float2(rsb, rsb), make_float2(acc[2] - off.x, acc[3] - off.y), v1);
     }
     rt[0] = v0.x;
     rt[1] = v0.y;
@@ -476,9 +483,14 @@ topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constan
     const int gid = lane >> 2, tig = lane & 3;
     const bool q_real = gid < p.G;                                // the lane's B-fragment query
     const bool c_real[2] = {2 * tig < p.G, 2 * tig + 1 < p.G};    // its accumulator columns' queries
-    TDQuery<D> tq;
+    // the query fragments of every consumer warp are the same: one copy in
+    // shared memory, [vector][lane], read where they are used (the registers
+    // they would hold are worth more to the dot stages)
+    const uint4* qv = reinterpret_cast<const uint4*>(smem + Ly::Q_OFF) + lane;
+    float2 scan_scale;
     TokAcc<D> ac;
     {
+        TDQuery<D> tq;
         const uint16_t* qrow = p.q + (size_t)(b * p.Hq + hq0 + gid) * D;
         auto qf = [&](int c) { return q_real ? __uint_as_float((uint32_t)qrow[c] << 16) : 0.f; };
         // sq: max |q| * 2^sq in [1, 2) over the query's channels (a quad shares a query)
@@ -513,7 +525,25 @@ topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constan
             tq.off[g] = make_float2(__shfl_sync(0xffffffffu, off, 8 * tig), __shfl_sync(0xffffffffu, off, 8 * tig + 4));
         }
         const float ssc = ldexpf(p.scale, 7 - sq);
-        tq.scan_scale = make_float2(__shfl_sync(0xffffffffu, ssc, 8 * tig), __shfl_sync(0xffffffffu, ssc, 8 * tig + 4));
+        scan_scale = make_float2(__shfl_sync(0xffffffffu, ssc, 8 * tig), __shfl_sync(0xffffffffu, ssc, 8 * tig + 4));
+        if (warp == 0) {
+            // vectors: [g] scan qc0/qc2 of k-steps 2g, 2g+1; [NG + g] residual qr0/qr2 of
+            // the same; [2 NG + i] qsum of groups 2i, 2i+1; [2 NG + NG/2 + i] off of the same
+            uint4* qw = reinterpret_cast<uint4*>(smem + Ly::Q_OFF) + lane;
+#pragma unroll
+            for (int g = 0; g < Gm::NG; ++g) {
+                qw[g * 32] = make_uint4(tq.qc0[2 * g], tq.qc2[2 * g], tq.qc0[2 * g + 1], tq.qc2[2 * g + 1]);
+                qw[(Gm::NG + g) * 32] = make_uint4(tq.qr0[2 * g], tq.qr2[2 * g], tq.qr0[2 * g + 1], tq.qr2[2 * g + 1]);
+            }
+#pragma unroll
+            for (int i = 0; i < Gm::NG / 2; ++i) {
+                *reinterpret_cast<float4*>(&qw[(2 * Gm::NG + i) * 32]) =
+                    make_float4(tq.qsum[2 * i].x, tq.qsum[2 * i].y, tq.qsum[2 * i + 1].x, tq.qsum[2 * i + 1].y);
+                *reinterpret_cast<float4*>(&qw[(2 * Gm::NG + Gm::NG / 2 + i) * 32]) =
+                    make_float4(tq.off[2 * i].x, tq.off[2 * i].y, tq.off[2 * i + 1].x, tq.off[2 * i + 1].y);
+            }
+        }
+        named_barrier(1, CW * 32);  // the query vectors are in place
         tok_acc_init(ac);
     }
 
@@ -552,7 +582,7 @@ topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constan
             }
             named_barrier(1, CW * 32);
             float st[4];
-            scan_tile<D>(stage, stage + kTile * Gm::CODES_ROW, warp, lane, tq, st);
+            scan_tile<D>(stage, stage + kTile * Gm::CODES_ROW, warp, lane, qv, scan_scale, st);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int r = warp * 16 + gid + 8 * (i >> 1);
@@ -592,7 +622,7 @@ topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constan
         const int rows = scan_rows[s];
         const unsigned char* base = smem + Ly::SCAN_OFF + s * Gm::SCAN_STAGE;
         float st[4];
-        scan_tile<D>(base, base + kTile * Gm::CODES_ROW, warp, lane, tq, st);
+        scan_tile<D>(base, base + kTile * Gm::CODES_ROW, warp, lane, qv, scan_scale, st);
         const int ds = k % DS;
         reinterpret_cast<float4*>(dec_s)[(ds * CW + warp) * 32 + lane] = make_float4(st[0], st[1], st[2], st[3]);
         bool any = false;
@@ -627,7 +657,7 @@ topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constan
             const int rows = min(kTile, t1 - tok0);
             unsigned char* st_base = smem + Ly::DET_OFF + ds * Gm::DET_STAGE;
             float rt[4];
-            residual_tile<D>(smem_u32(st_base), st_base + Gm::RES_BYTES + Gm::V_BYTES, warp, lane, tq, rt);
+            residual_tile<D>(smem_u32(st_base), st_base + Gm::RES_BYTES + Gm::V_BYTES, warp, lane, qv, rt);
             const float4 sv = reinterpret_cast<const float4*>(dec_s)[(ds * CW + warp) * 32 + lane];
             const float stv[4] = {sv.x, sv.y, sv.z, sv.w};
             bool selv[4];
