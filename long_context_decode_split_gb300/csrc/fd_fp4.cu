@@ -691,6 +691,8 @@ struct Fp4Launcher {
         F4Geo<D>::NB * 32 * 16 + 64;
     static constexpr int RED = 4 * 8 * D * 4 + 2 * 4 * 8 * 4;
     static_assert(STAGES * STAGE >= RED, "reduction scratch must fit in the ring");
+    // three CTAs per SM: 228 KB of shared memory per SM, 1 KB of it reserved per CTA
+    static_assert(3 * (SMEM + 1024) <= 228 * 1024, "three CTAs per SM must fit in shared memory");
     static constexpr auto kernel = fp4_partial_kernel<D, STAGES, PAGED>;
 
     static cudaError_t prepare() {

@@ -169,6 +169,8 @@ struct TLayout {
     static constexpr int BYTES = 1024 + Q_OFF + QV * 32 * 16;
     static_assert(DS * Gm::DET_STAGE >= CW * 8 * D * 4 + 2 * CW * 8 * 4, "epilogue scratch must fit in the rings");
     static_assert(Gm::DET_STAGE >= Gm::SCAN_STAGE, "anchor staging must fit in one detail stage");
+    // two CTAs per SM: 228 KB of shared memory per SM, 1 KB of it reserved per CTA
+    static_assert(2 * (BYTES + 1024) <= 228 * 1024, "two CTAs per SM must fit in shared memory");
 };
 
 struct TDParams {
