@@ -451,18 +451,21 @@ partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
 }
 
 // ---------------------------------------------------------------------------
-// Merge: one CTA of D threads per (sequence, query head).  The chunks' m
-// values are reduced to M by the whole CTA, D chunk weights are computed at
-// a time (one per thread) into shared memory, and each thread (one output
-// channel) sums its channel over the chunks in chunk order with eight loads
-// in flight, so a long list of chunks costs a few memory latencies, not one
-// per chunk.  Sums run in chunk order: the result does not depend on D.
+// Merge: one CTA of D threads per (sequence, query head).  Each thread (one
+// output channel) starts the loads of its channel's first MB chunk outputs
+// before anything else; meanwhile the chunks' (m, l) pairs are read one per
+// thread, reduced to M by the whole CTA and turned into weights in shared
+// memory.  The channel is then summed over the chunks in chunk order, MB
+// loads in flight at a time, so a long list of chunks costs a few memory
+// latencies, not one per chunk.  Sums run in chunk order: the result does
+// not depend on D or MB.
 template <int D>
 __global__ void __launch_bounds__(D)
 merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
              const int32_t* __restrict__ seq_lens, int Hq, int L_max, int splits, int chunk_fixed,
              void* __restrict__ out, int out_bf16, float* __restrict__ lse) {
     constexpr int NWARP = D / 32;
+    constexpr int MB = 32;  // chunk outputs in flight per thread
     __shared__ float w_s[D];
     __shared__ float red[NWARP];
     pdl_wait_primary();
@@ -473,9 +476,13 @@ merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml
     const int L = clamped_len(seq_lens, b, L_max, nullptr);
     const int chunk = chunk_len(L, splits, chunk_fixed);
     const int n = L > 0 ? min(splits, (L + chunk - 1) / chunk) : 0;
-    const float* ml = part_ml + (size_t)row * splits * 2;
+    const float2* ml = reinterpret_cast<const float2*>(part_ml) + (size_t)row * splits;
+    const float* po = part_o + (size_t)row * splits * D + dim;
+    float v[MB];
+#pragma unroll
+    for (int u = 0; u < MB; ++u) v[u] = u < n ? po[(size_t)u * D] : 0.f;
     float M = -INFINITY;
-    for (int i = dim; i < n; i += D) M = fmaxf(M, ml[2 * i]);
+    for (int i = dim; i < n; i += D) M = fmaxf(M, ml[i].x);
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     if (lane == 0) red[warp] = M;
@@ -485,37 +492,29 @@ merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml
     for (int w = 1; w < NWARP; ++w) M = fmaxf(M, red[w]);
     float wsum = 0.f, acc = 0.f;
     if (M != -INFINITY) {
-        const float* po = part_o + (size_t)row * splits * D + dim;
         for (int base = 0; base < n; base += D) {
             const int i = base + dim;
             float w = 0.f;
             if (i < n) {
-                const float mi = ml[2 * i];
-                if (mi != -INFINITY) w = exp2_approx(mi - M) * ml[2 * i + 1];
+                const float2 mli = ml[i];
+                if (mli.x != -INFINITY) w = exp2_approx(mli.x - M) * mli.y;
             }
             __syncthreads();  // the previous weights are consumed
             w_s[dim] = w;
             __syncthreads();
             const int cnt = min(D, n - base);
-            int j = 0;
-            for (; j + 8 <= cnt; j += 8) {
-                float v[8];
+            for (int j = 0; j < cnt; j += MB) {
+                if (base + j > 0) {  // the first MB outputs were loaded up front
 #pragma unroll
-                for (int u = 0; u < 8; ++u) v[u] = po[(size_t)(base + j + u) * D];
+                    for (int u = 0; u < MB; ++u) v[u] = j + u < cnt ? po[(size_t)(base + j + u) * D] : 0.f;
+                }
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const float wu = w_s[j + u];
+                for (int u = 0; u < MB; ++u) {
+                    const float wu = j + u < cnt ? w_s[j + u] : 0.f;
                     if (wu != 0.f) {
                         wsum += wu;
                         acc += wu * v[u];
                     }
-                }
-            }
-            for (; j < cnt; ++j) {
-                const float wu = w_s[j];
-                if (wu != 0.f) {
-                    wsum += wu;
-                    acc += wu * po[(size_t)(base + j) * D];
                 }
             }
         }
