@@ -95,6 +95,18 @@ def test_split_count_invariance(fd, oracle):
         assert (o - outs[0]).abs().max().item() < 1e-4
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_merge_of_more_chunks_than_threads(fd, oracle, d):
+    # the merge kernel runs d threads per row and takes the chunk weights d at
+    # a time: 157 chunks of 128 tokens (and fewer for the shorter sequence)
+    # cross that block boundary at both head sizes
+    p = W.random_problem(2, 4, 2, 20000, d, seed=12 + d, device=DEV, seq_lens=[20000, 9000])
+    ref, lref = oracle_dense(oracle, p)
+    out, lse = run_dense(fd, p, out_dtype="f32", num_splits=300)
+    assert_out_close(out, ref, F32_TOL)
+    assert_lse_close(lse, lref, 1e-5)
+
+
 def test_deterministic(fd):
     p = W.random_problem(1, 8, 8, 20000, 128, seed=6, device=DEV)
     a, la = run_dense(fd, p, seq_lens=False)
