@@ -97,7 +97,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     return false;
 }
 
-// mbar_wait for all 32 lanes of a warp, with one verdict for the whole warp
+// mbar_wait for all 32 lanes of a warp, with one outcome for the whole warp
 // (so a time-out can never split the warp before its shuffles).
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity,
                                           unsigned long long limit_ns = kWaitLimitNs) {
