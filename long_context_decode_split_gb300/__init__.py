@@ -120,8 +120,9 @@ def _stream(stream):
     belong to that device, or the device's current torch stream."""
     if stream is None:
         return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    _need(stream.device.index == torch.cuda.current_device(),
-          f"stream is on {stream.device}, the tensors on cuda:{torch.cuda.current_device()}")
+    dev = torch.cuda.current_device()
+    if stream.device.index != dev:
+        raise ValueError(f"stream is on {stream.device}, the tensors on cuda:{dev}")
     return ctypes.c_void_p(stream.cuda_stream)
 
 
@@ -131,7 +132,10 @@ def _on_device_of_first_tensor(fn):
     the device that holds the data (every other tensor is checked against it)."""
     @functools.wraps(fn)
     def wrapper(t, *args, **kwargs):
-        _need(isinstance(t, torch.Tensor) and t.is_cuda, f"{fn.__name__}: the first argument must be a CUDA tensor")
+        if not (isinstance(t, torch.Tensor) and t.is_cuda):
+            raise ValueError(f"{fn.__name__}: the first argument must be a CUDA tensor")
+        if t.device.index == torch.cuda.current_device():
+            return fn(t, *args, **kwargs)
         with torch.cuda.device(t.device):
             return fn(t, *args, **kwargs)
     return wrapper
@@ -143,14 +147,18 @@ def _need(cond, what):
 
 
 def _check_cuda(t, name, dtype=None, shape=None):
-    _need(t.is_cuda, f"{name} must be a CUDA tensor")
-    _need(t.device.index == torch.cuda.current_device(),
-          f"{name} is on {t.device}, expected cuda:{torch.cuda.current_device()} (the first tensor's device)")
-    _need(t.is_contiguous(), f"{name} must be contiguous")
-    if dtype is not None:
-        _need(t.dtype == dtype, f"{name} must be {dtype}, got {t.dtype}")
-    if shape is not None:
-        _need(tuple(t.shape) == tuple(shape), f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    # messages are built only on failure: this runs several times per call
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    dev = torch.cuda.current_device()
+    if t.device.index != dev:
+        raise ValueError(f"{name} is on {t.device}, expected cuda:{dev} (the first tensor's device)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
 def _raise(st, where):
