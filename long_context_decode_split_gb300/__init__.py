@@ -112,18 +112,19 @@ def header_symbols(path: str = HEADER):
 
 
 def _p(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # the pointer as a Python int: every pointer parameter is declared c_void_p
+    return None if t is None else t.data_ptr()
 
 
 def _stream(stream):
     """The stream handle for a call on the current device: `stream`, which must
     belong to that device, or the device's current torch stream."""
     if stream is None:
-        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        return torch.cuda.current_stream().cuda_stream
     dev = torch.cuda.current_device()
     if stream.device.index != dev:
         raise ValueError(f"stream is on {stream.device}, the tensors on cuda:{dev}")
-    return ctypes.c_void_p(stream.cuda_stream)
+    return stream.cuda_stream
 
 
 def _on_device_of_first_tensor(fn):
@@ -189,8 +190,18 @@ def fd_num_splits(B, Hq, Hkv, L_max, d, num_splits=0, ragged=False) -> int:
     return r
 
 
+_WS_SIZES = {}
+
+
 def fd_decode_workspace_size(B, Hq, Hkv, L_max, d, num_splits=0, ragged=False) -> int:
-    return int(load().fd_decode_workspace_size(B, Hq, Hkv, L_max, d, num_splits, int(bool(ragged))))
+    # the plan depends on the shape and the current device only: remembered per both
+    key = (torch.cuda.current_device() if torch.cuda.is_available() else -1, B, Hq, Hkv, L_max, d, num_splits,
+           bool(ragged))
+    n = _WS_SIZES.get(key)
+    if n is None:
+        n = int(load().fd_decode_workspace_size(B, Hq, Hkv, L_max, d, num_splits, int(bool(ragged))))
+        _WS_SIZES[key] = n
+    return n
 
 
 def fd_topdelta_workspace_size(B, Hq, Hkv, L_max, d, num_splits=0) -> int:
