@@ -234,6 +234,8 @@ class Workload:
                 self.kv8 = enc(p.k_pages) + venc(p.v_pages)
             else:
                 self.kv8 = enc(p.k) + venc(p.v)
+            n_copies = 1 if self.paged else encoded_copies(name, p.B, p.L_max, p.Hkv, p.d)
+            self.kv8_copies = [self.kv8] + [tuple(t.clone() for t in self.kv8) for _ in range(n_copies - 1)]
             torch.cuda.synchronize()
             if self.fp8:
                 need = fd.fd_decode_fp8_workspace_size(B, Hq, Hkv, p.L_max, d, p.num_splits, self.paged)
@@ -286,13 +288,17 @@ class Workload:
                 "union_tokens": int(ubits.sum()), "tiles_loaded": int(tiles.sum()),
                 "tiles_total": int(tiles.size)}
 
-    def call(self, stream=None, q=None):
+    def call(self, stream=None, q=None, rotate=True):
+        """One decode call; with `rotate` consecutive calls read the cache's
+        copies in turn (the end-to-end step, which writes the newest row into
+        the cache it then reads, passes rotate=False)."""
         fd = self.fd
-        p = self.copies[self._turn % len(self.copies)]
-        self._turn += 1
+        turn = self._turn if rotate else 0
+        self._turn += 1 if rotate else 0
+        p = self.copies[turn % len(self.copies)]
         q = p.q if q is None else q
         if self.fp8 or self.fp4:
-            kc, ks, vc, vs = self.kv8
+            kc, ks, vc, vs = self.kv8_copies[turn % len(self.kv8_copies)]
             if self.paged:
                 paged = fd.fd_decode_paged_fp8 if self.fp8 else fd.fd_decode_paged_fp4
                 paged(q, kc, ks, vc, vs, p.page_table, p.num_pages, p.seq_lens, p.scale, p.num_splits,
@@ -364,6 +370,17 @@ def ladder_copies(B, L, Hkv, d):
     return max(1, -(-3 * L2_BYTES // (B * L * Hkv * d * 4)))
 
 
+def encoded_copies(name, B, L, Hkv, d):
+    """Copies of an fp8/fp4 cache read in turn: a cache less than twice the L2
+    could partly stay resident from one call to the next, so it gets enough
+    copies to exceed three times the L2 together."""
+    if not name.endswith(("_fp8", "_fp4")) or not isinstance(L, int):
+        return 1
+    per_token = 2 * (d + 4) if name.endswith("_fp8") else 2 * (d // 2 + d // 32)
+    nbytes = B * L * Hkv * per_token
+    return 1 if nbytes >= 2 * L2_BYTES else -(-3 * L2_BYTES // nbytes)
+
+
 def workload_config(args):
     """The workload as the command line names it: the same dict in the GPU
     arm and in the reference arm (nothing here depends on the device)."""
@@ -389,6 +406,9 @@ def workload_config(args):
          "l2": "inputs smaller than L2 (no flush)" if base == "tiny" else "inputs larger than L2",
          **({"l2": f"{ladder_copies(B, L, Hkv, d)} copies of the cache read in turn (together larger than L2)"}
             if base == "ladder" and ladder_copies(B, L, Hkv, d) > 1 else {}),
+         **({"l2": f"{encoded_copies(name, B, L, Hkv, d)} copies of the encoded cache read in turn "
+                   f"(together more than three times the L2)"}
+            if encoded_copies(name, B, L, Hkv, d) > 1 else {}),
          "parallelism": f"replicas x{args.gpus}"}
     if base == "tiny":
         c["num_splits"] = args.num_splits or 4
@@ -556,7 +576,7 @@ def time_e2e(wl, steps, warmup, dist_ctx):
         else:
             put(p.k, k_d)
             put(p.v, v_d)
-        wl.call(q=q_d)
+        wl.call(q=q_d, rotate=False)
         result.copy_(wl.io, non_blocking=True)
 
     for _ in range(warmup):
