@@ -704,8 +704,8 @@ class OracleSample:
                 self.enc = oracle.quantize_keys(self.args[1])
             if self.fp8:
                 self.enc = oracle.quantize_kv_fp8(self.args[1]) + oracle.quantize_kv_fp8(self.args[2])
-            if self.fp4:
-                self.enc = oracle.quantize_kv_fp4(self.args[1]) + oracle.quantize_kv_fp4(self.args[2])
+            if self.fp4:  # values in the token-pair layout the fp4 decode reads
+                self.enc = oracle.quantize_kv_fp4(self.args[1]) + oracle.quantize_v_fp4(self.args[2])
             t0 = time.perf_counter()
             self.run()
             dt = time.perf_counter() - t0
@@ -721,20 +721,21 @@ class OracleSample:
                      f"B={B}, d={d}: {self.frac:.4g} of one full call")
         self.threads = oracle.max_threads()
 
-    def run(self):
+    def run(self, n_threads=0):
+        """One pass of the oracle over the sample (n_threads 0: every core)."""
         q, k, v, scale = self.args
         if self.fp8:
             kc, ks, vc, vs = self.enc
-            self.oracle.decode_dense_fp8(q, kc, ks, vc, vs, None, scale)
+            self.oracle.decode_dense_fp8(q, kc, ks, vc, vs, None, scale, n_threads=n_threads)
         elif self.fp4:
             kc, ks, vc, vs = self.enc
-            self.oracle.decode_dense_fp4(q, kc, ks, vc, vs, None, scale)
+            self.oracle.decode_dense_fp4(q, kc, ks, vc, vs, None, scale, n_threads=n_threads)
         elif self.delta is not None:
             c, ms, r, rs = self.enc
             fn = self.oracle.decode_topdelta_group_union if self.union else self.oracle.decode_topdelta
-            fn(q, c, ms, r, rs, v, None, scale, self.delta)
+            fn(q, c, ms, r, rs, v, None, scale, self.delta, n_threads=n_threads)
         else:
-            self.oracle.decode_dense(q, k, v, None, scale)
+            self.oracle.decode_dense(q, k, v, None, scale, n_threads=n_threads)
 
 
 def time_oracle(sample, steps, warmup):
@@ -921,6 +922,13 @@ def main():
         v, s_rep = time_oracle(sample, reps, 1)
         cpu = {"value": v, "unit": "tokens/s", "cores": sample.threads, "kind": "oracle",
                "sample": f"{sample.desc}; {reps} timed runs of {s_rep * 1e3:.1f} ms"}
+        if args.workload in ("tiny", "mha32k"):
+            # the same sample on one core, once
+            t0 = time.perf_counter()
+            sample.run(n_threads=1)
+            dt1 = time.perf_counter() - t0
+            cpu["single_thread"] = {"value": sample.B / (dt1 / sample.frac), "unit": "tokens/s", "cores": 1,
+                                    "seconds": dt1}
     if ctx.rank == 0:
         cfg = workload_config(args)
         line = {
