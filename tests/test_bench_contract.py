@@ -38,6 +38,30 @@ def test_default_workload_is_the_largest_single_gpu_config():
         assert 'ap.add_argument("--workload", default="million"' in f.read()
 
 
+def test_inputs_exceed_l2_or_are_flushed():
+    # every workload's timed calls read HBM: caches under twice the L2 rotate
+    # through copies, the tiny config empties L2 before each call
+    sys.path.insert(0, ROOT)
+    import bench
+    for name, (B, Hq, Hkv, L, d) in bench.FULL_SHAPES.items():
+        c = gpu_arm_config(name)
+        if name == "tiny":
+            assert "512 MiB write before each call" in c["l2"]
+            continue
+        if name.endswith("_fp4"):
+            per_token = 2 * (d // 2 + d // 32)
+        elif name.endswith("_fp8"):
+            per_token = 2 * (d + 4)
+        else:
+            per_token = 4 * d
+        if name == "ladder" or "paged" in name:
+            continue  # the ladder rotates its own copies; the paged pools are > 1 GB
+        nbytes = B * Hkv * L * per_token * bench.encoded_copies(name, B, L, Hkv, d)
+        assert nbytes >= 2 * bench.L2_BYTES or name.startswith("ffd"), (name, nbytes)
+    assert bench.encoded_copies("mha32k_fp4", 1, 32768, 32, 128) == 3
+    assert "3 copies of the encoded cache" in gpu_arm_config("mha32k_fp4")["l2"]
+
+
 @pytest.mark.timeout(600)
 @pytest.mark.parametrize("workload", ["tiny", "mha32k_fp8", "ffd_topdelta5", "ffd_sparse_topdelta5_union"])
 def test_reference_arm_json_line(workload):
