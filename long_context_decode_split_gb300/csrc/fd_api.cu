@@ -52,9 +52,11 @@ struct Plan {
 //   c * max(n, r),
 // r being the number of CTAs whose copy pipelines together saturate HBM
 // (a lone CTA streams at about 1/r of the GPU's bandwidth); CTAs beyond
-// the resident slots form further waves; each wave and each chunk add a
-// small fixed cost.  So: few, long chunks while HBM stays saturated, and no
-// small trailing wave.  Ragged batches (lengths unknown on the host) take
+// the resident slots form further waves; each chunk adds a small fixed cost
+// and so does each wave (wave_tiles > 0: that many tiles of a CTA's time,
+// for the passes whose CTAs are bound by their SM's issue, not by HBM).
+// So: few, long chunks while HBM stays saturated, and no small trailing
+// wave.  Ragged batches (lengths unknown on the host) take
 // chunks such that sequences of length L_max span about four waves, so the
 // hardware block scheduler can even out the load.
 Plan plan(int B, int Hkv, int L_max, int requested, bool ragged, int ctas_per_sm, int sms, double r,
