@@ -562,34 +562,46 @@ topdelta_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constan
         const int tw_beg = win_beg < L ? win_beg / kTile : (L + kTile - 1) / kTile;
         const int tw_end = (L + kTile - 1) / kTile;
         const int tid = warp * 32 + lane;
-        for (int T = 0; T < tw_end; ++T) {
-            if (T >= ts_end && T < tw_beg) T = tw_beg;
-            if (T >= tw_end) break;
-            const int tb = T * kTile;
-            const int rows = min(kTile, L - tb);
+        // the anchor tiles: [0, ts_end) and [tw_lo, tw_end), each once, staged
+        // NBA at a time (one round of loads for all of them on common settings)
+        const int tw_lo = max(ts_end, tw_beg);
+        const int na = ts_end + max(0, tw_end - tw_lo);
+        auto anchor_tile = [&](int i) { return i < ts_end ? i : tw_lo + (i - ts_end); };
+        constexpr int NBA = Gm::DET_STAGE / Gm::SCAN_STAGE;
+        constexpr int CV = kTile * Gm::CODES_ROW / 16, MV = kTile * Gm::MS_ROW / 16;
+        for (int a0 = 0; a0 < na; a0 += NBA) {
+            const int nb = min(NBA, na - a0);
             named_barrier(1, CW * 32);  // the staging area is free
-            constexpr int CV = kTile * Gm::CODES_ROW / 16, MV = kTile * Gm::MS_ROW / 16;
-            for (int i = tid; i < CV + MV; i += CW * 32) {
+            for (int i = tid; i < nb * (CV + MV); i += CW * 32) {
+                const int j = i / (CV + MV), e = i % (CV + MV);
+                const int tb = anchor_tile(a0 + j) * kTile;
+                const int rows = min(kTile, L - tb);
+                unsigned char* sj = stage + j * Gm::SCAN_STAGE;
                 uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                if (i < CV) {
-                    const int r = i * 16 / Gm::CODES_ROW;  // first row this 16-byte vector covers
-                    if (r < rows) v = reinterpret_cast<const uint4*>(p.codes + (size_t)(head_row0 + tb) * Gm::CODES_ROW)[i];
-                    reinterpret_cast<uint4*>(stage)[i] = v;
+                if (e < CV) {
+                    const int r = e * 16 / Gm::CODES_ROW;  // first row this 16-byte vector covers
+                    if (r < rows) v = reinterpret_cast<const uint4*>(p.codes + (size_t)(head_row0 + tb) * Gm::CODES_ROW)[e];
+                    reinterpret_cast<uint4*>(sj)[e] = v;
                 } else {
-                    const int k = i - CV;
+                    const int k = e - CV;
                     const int r = k * 16 / Gm::MS_ROW;  // first row this 16-byte vector covers
                     if (r < rows) v = reinterpret_cast<const uint4*>(p.mn_scale + (size_t)(head_row0 + tb) * Gm::MS_ROW)[k];
-                    reinterpret_cast<uint4*>(stage + kTile * Gm::CODES_ROW)[k] = v;
+                    reinterpret_cast<uint4*>(sj + kTile * Gm::CODES_ROW)[k] = v;
                 }
             }
             named_barrier(1, CW * 32);
-            float st[4];
-            scan_tile<D>(stage, stage + kTile * Gm::CODES_ROW, warp, lane, qv, scan_scale, st);
+            for (int j = 0; j < nb; ++j) {
+                const int tb = anchor_tile(a0 + j) * kTile;
+                const int rows = min(kTile, L - tb);
+                const unsigned char* sj = stage + j * Gm::SCAN_STAGE;
+                float st[4];
+                scan_tile<D>(sj, sj + kTile * Gm::CODES_ROW, warp, lane, qv, scan_scale, st);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int r = warp * 16 + gid + 8 * (i >> 1);
-                const int j = tb + r;
-                if (r < rows && (j < sink_end || j >= win_beg)) mh[i & 1] = fmaxf(mh[i & 1], st[i]);
+                for (int i = 0; i < 4; ++i) {
+                    const int r = warp * 16 + gid + 8 * (i >> 1);
+                    const int jt = tb + r;
+                    if (r < rows && (jt < sink_end || jt >= win_beg)) mh[i & 1] = fmaxf(mh[i & 1], st[i]);
+                }
             }
         }
 #pragma unroll
