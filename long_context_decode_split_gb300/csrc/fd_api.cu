@@ -59,8 +59,36 @@ struct Plan {
 // wave.  Ragged batches (lengths unknown on the host) take
 // chunks such that sequences of length L_max span about four waves, so the
 // hardware block scheduler can even out the load.
+Plan plan_uncached(int B, int Hkv, int L_max, int requested, bool ragged, int ctas_per_sm, int sms, double r,
+                   bool fill_slots, double wave_tiles);
+
+// The cost model walks every chunk count (thousands for a 1M-token cache):
+// its answers are remembered per thread for the last few argument sets.
 Plan plan(int B, int Hkv, int L_max, int requested, bool ragged, int ctas_per_sm, int sms, double r,
           bool fill_slots = false, double wave_tiles = 0.0) {
+    struct Entry {
+        int B, Hkv, L_max, requested, ragged, ctas_per_sm, sms, fill_slots;
+        double r, wave_tiles;
+        Plan pl;
+        bool used;
+    };
+    constexpr int kEntries = 8;
+    thread_local Entry cache[kEntries] = {};
+    thread_local int next = 0;
+    for (const Entry& e : cache)
+        if (e.used && e.B == B && e.Hkv == Hkv && e.L_max == L_max && e.requested == requested &&
+            e.ragged == (int)ragged && e.ctas_per_sm == ctas_per_sm && e.sms == sms &&
+            e.fill_slots == (int)fill_slots && e.r == r && e.wave_tiles == wave_tiles)
+            return e.pl;
+    const Plan pl = plan_uncached(B, Hkv, L_max, requested, ragged, ctas_per_sm, sms, r, fill_slots, wave_tiles);
+    cache[next] = Entry{B, Hkv, L_max, requested, (int)ragged, ctas_per_sm, sms, (int)fill_slots, r, wave_tiles, pl,
+                        true};
+    next = (next + 1) % kEntries;
+    return pl;
+}
+
+Plan plan_uncached(int B, int Hkv, int L_max, int requested, bool ragged, int ctas_per_sm, int sms, double r,
+                   bool fill_slots, double wave_tiles) {
     Plan pl{1, 0};
     if (requested > 0) {
         pl.splits = requested;
