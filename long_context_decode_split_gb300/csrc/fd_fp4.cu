@@ -448,20 +448,17 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
             atomicOr(&g_status_fp4, kStatusTimeout);
             break;
         }
+        // the scale copies start this many rows before the tile (a page starts on a
+        // 64-row boundary: none)
+        auto soff = [&](int s) { return PAGED ? 0 : stage_off[s]; };
 
-        // ---- block scales --------------------------------------------------------
-        // K: lane l decodes blocks 2(l % 2), 2(l % 2) + 1 (block l % 2 at d = 64) of
+        // ---- key block scales ----------------------------------------------------
+        // Lane l decodes blocks 2(l % 2), 2(l % 2) + 1 (block l % 2 at d = 64) of
         // row l / 2 of the warp's 16 (natural token order) as 2^(E - 127) into
-        // kbuf[k][row][block].  V: lane l holds the scale words of the token pair
-        // pv = l / 4 (l / 2 mod 8 at d = 64), rows 2 pv and 2 pv + 1; they become
-        // fp16 pairs once the step's reference scale is known.  Rows past the
-        // tile read as scale byte 0 (scale 0).  V scale words are read here for
-        // their maximum and again below.
-        uint32_t vbytes = 0u;  // per-byte maximum of the lane's V scale bytes (a larger byte is a larger scale)
+        // kbuf[k][row][block].  Rows past the tile read as scale byte 0 (scale 0).
 #pragma unroll
         for (int k = 0; k < NT; ++k) {
-            const unsigned char* ksrc = scl + st[k] * SSTAGE + stage_off[st[k]] * Gm::SB;
-            const unsigned char* vsrc = ksrc + kScaleSlot;
+            const unsigned char* ksrc = scl + st[k] * SSTAGE + soff(st[k]) * Gm::SB;
             const int lr = lane >> 1;
             uint32_t kw = 0u;
             if (warp * 16 + lr < rows[k]) {
@@ -475,16 +472,6 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
                     make_float2(scale_value((kw >> (8 * c0)) & 0xffu), scale_value((kw >> (8 * c0 + 8)) & 0xffu));
             } else {
                 kdst[lane & 1] = scale_value((kw >> (8 * (lane & 1))) & 0xffu);
-            }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int r = warp * 16 + 2 * pv + h;
-                uint32_t w = 0u;
-                if (r < rows[k]) {
-                    if constexpr (NB == 4) w = *reinterpret_cast<const uint32_t*>(vsrc + 4 * r);
-                    else w = *reinterpret_cast<const uint16_t*>(vsrc + 2 * r);
-                }
-                vbytes = __vmaxu4(vbytes, w);
             }
         }
         __syncwarp();
@@ -534,21 +521,31 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
         }
 
         // ---- online softmax per column and the V reference scale ---------------
+        // V: lane l reads the scale bytes of block cv of the token pair pv = l / 4
+        // (l / 2 mod 8 at d = 64), rows 2 pv and 2 pv + 1 (byte 0 past the tile); the
+        // warp's largest byte is the step's largest scale (one redux), and the bytes
+        // become fp16 pairs over the reference below.
         float mx0 = -INFINITY, mx1 = -INFINITY;
-        uint32_t emax = vbytes;  // per-byte maximum of the V scale bytes (a larger byte is a larger scale)
+        uint32_t ev[NT][2];
+        uint32_t emax = 0u;
 #pragma unroll
         for (int k = 0; k < NT; ++k) {
             mx0 = fmaxf(mx0, fmaxf(sc[k][0], sc[k][2]));
             mx1 = fmaxf(mx1, fmaxf(sc[k][1], sc[k][3]));
+            const unsigned char* vsrc = scl + st[k] * SSTAGE + soff(st[k]) * Gm::SB + kScaleSlot;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int r = warp * 16 + 2 * pv + h;
+                ev[k][h] = r < rows[k] ? (uint32_t)vsrc[Gm::SB * r + cv] : 0u;
+                emax = max(emax, ev[k][h]);
+            }
         }
-        if constexpr (NB == 2) emax = __vmaxu4(emax, __shfl_xor_sync(0xffffffffu, emax, 2));
+        emax = __reduce_max_sync(0xffffffffu, emax);
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {  // over the 16 rows: the lanes of equal tig
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-            emax = __vmaxu4(emax, __shfl_xor_sync(0xffffffffu, emax, off));
         }
-        emax = max(max(emax & 0xffu, (emax >> 8) & 0xffu), max((emax >> 16) & 0xffu, emax >> 24));
         const float vref_new = fmaxf(vref, scale_value(emax));
         const float vinv = vref_new > 0.f ? __fdividef(1.f, vref_new) : 0.f;
         const float vf = vref_new > 0.f ? vref * vinv : 1.f;
@@ -556,17 +553,8 @@ fp4_partial_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
         // V block scales over the reference as fp16 pairs: lane l writes block cv of
         // its token pair pv, (s(2 pv) / s_ref, s(2 pv + 1) / s_ref), both <= 1
 #pragma unroll
-        for (int k = 0; k < NT; ++k) {
-            const unsigned char* vsrc = scl + st[k] * SSTAGE + stage_off[st[k]] * Gm::SB + kScaleSlot;
-            uint32_t e[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int r = warp * 16 + 2 * pv + h;
-                e[h] = 0u;
-                if (r < rows[k]) e[h] = vsrc[Gm::SB * r + cv];
-            }
-            vbuf[(k * 8 + pv) * NB + cv] = pack_f16(scale_value(e[0]) * vinv, scale_value(e[1]) * vinv);
-        }
+        for (int k = 0; k < NT; ++k)
+            vbuf[(k * 8 + pv) * NB + cv] = pack_f16(scale_value(ev[k][0]) * vinv, scale_value(ev[k][1]) * vinv);
         __syncwarp();
         const float m0 = fmaxf(m_run.x, mx0), m1 = fmaxf(m_run.y, mx1);
         const bool none0 = m0 == -INFINITY, none1 = m1 == -INFINITY;
