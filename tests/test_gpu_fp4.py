@@ -239,6 +239,23 @@ def test_fp4_paged_parity(fd, oracle, G, d):
     assert fd.fd_device_status(clear=True) == fd.FD_OK
 
 
+def test_fp4_paged_bad_page_is_reported(fd, oracle):
+    # a page id past the pool is reported and not read; the other sequence is unaffected
+    lens = [300, 200]
+    p = W.random_problem(2, 8, 2, 300, 128, seed=9, device=DEV, seq_lens=lens)
+    pp = W.to_paged(p, seed=4, poison_tail=False)
+    kc, ks, vc, vs = paged_codes(oracle, pp, lens)
+    ref, lref = oracle_fp4(oracle, p, *fp4_problem(oracle, p))
+    table = pp.page_table.clone()
+    table[1, 2] = pp.num_pages + 5
+    assert fd.fd_device_status(clear=True) == fd.FD_OK
+    out, lse = fd.fd_decode_paged_fp4(pp.q, kc, ks, vc, vs, table, pp.num_pages, pp.seq_lens, pp.scale)
+    assert fd.fd_device_status(clear=True) == fd.FD_ERR_BAD_PAGE_TABLE
+    assert torch.isfinite(out.float()).all()
+    assert_out_close(out[:1], ref[:1], BF16_TOL)
+    assert_lse_close(lse[:1], lref[:1])
+
+
 # --------------------------------------------------------- full workloads
 
 def test_fp4_full_mha32k_sampled(fd, oracle):
