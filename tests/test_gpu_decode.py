@@ -213,6 +213,16 @@ def test_full_million(fd, oracle):
     assert torch.isfinite(lse).all()
 
 
+@pytest.mark.parametrize("B,L", [(32, 4096), (8, 32768)])
+def test_ladder_batched_rungs_sampled(fd, oracle, B, L):
+    # context-length ladder shapes at batch 8 and 32 (GQA-4, d=128) with the planner's chunking: every
+    # sequence of two KV heads against the oracle
+    p = W.ladder(B=B, L=L, seed=3, device=DEV)
+    out, lse = run_dense(fd, p, seq_lens=False)
+    check_sampled(out, lse, sample_rows_oracle(oracle, p, heads=[0, 7]))
+    assert fd.fd_device_status(clear=True) == fd.FD_OK
+
+
 def test_full_gqa_paged(fd, oracle):
     pp = W.gqa_paged(seed=0, device=DEV)
     out, lse = fd.fd_decode_paged(pp.q, pp.k_pages, pp.v_pages, pp.page_table, pp.num_pages, pp.seq_lens,

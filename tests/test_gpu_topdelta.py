@@ -258,6 +258,31 @@ def test_topdelta_full_ffd_sampled(fd, oracle):
         print(f"delta={delta}: tie tokens with differing membership: {ties}")
 
 
+def test_topdelta_million_tokens_sampled(fd, oracle):
+    """The 1M-token GQA cache (B=1, Hq=32, Hkv=8, d=128, sinks +3 q^) at delta 5: the planner's many
+    chunks per (sequence, head), the anchor window a million tokens past the sinks; oracle on two KV
+    heads."""
+    p = W.million(seed=0, device=DEV)
+    enc_gpu = fd.fd_quantize_keys(p.k, None)
+    G = p.Hq // p.Hkv
+    delta = 5.0
+    out, lse, mask, cnt = fd.fd_decode_topdelta(p.q, *enc_gpu, p.v, None, p.scale, delta, want_selection=True)
+    torch.cuda.synchronize()
+    assert fd.fd_device_status(clear=True) == fd.FD_OK
+    mask = mask.cpu().numpy().view(np.uint32)
+    cnt = cnt.cpu().numpy()
+    for h in (0, 5):
+        sub = W.Problem("million_sub", p.q[:, h * G:(h + 1) * G].contiguous(), p.k[:, h:h + 1].contiguous(),
+                        p.v[:, h:h + 1].contiguous(), p.seq_lens, p.scale, p.L_max)
+        enc = oracle.quantize_keys(bits(sub.k))
+        for rr, g in zip(enc, enc_gpu):
+            gv = g[:, h:h + 1].cpu().numpy()
+            np.testing.assert_array_equal(gv.view(np.uint16) if gv.dtype == np.float16 else gv, rr)
+        ref = oracle.decode_topdelta(bits(sub.q), *enc, bits(sub.v), None, p.scale, delta, 4, 64, want_scores=True)
+        check_topdelta(oracle, sub, enc, ref, out[:, h * G:(h + 1) * G], lse[:, h * G:(h + 1) * G],
+                       mask[:, h * G:(h + 1) * G], cnt[:, h * G:(h + 1) * G], delta, BF16_TOL)
+
+
 # ------------------------------------------------- anchor settings, shared sets
 
 @pytest.mark.parametrize("n_sink", [0, 1, 16, 64])
