@@ -83,20 +83,76 @@ def measured_peaks():
     return None
 
 
+class _Nvml:
+    """Read-only clock queries through the driver's NVML library (ctypes; the
+    call releases the GIL), for sampling inside timed regions shorter than
+    nvidia-smi's period.  Raises OSError when NVML or the device is missing."""
+
+    CLOCK_SM = 1  # NVML_CLOCK_SM
+    # clocks event reason bits (nvml.h): the four the timing rules name
+    REASONS = ((0x8, "hw_slowdown"), (0x40, "hw_thermal_slowdown"), (0x20, "sw_thermal_slowdown"),
+               (0x4, "sw_power_cap"))
+
+    def __init__(self, cuda_index):
+        import ctypes
+        self.ct = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        found = False
+        try:  # the CUDA device's own UUID: immune to CUDA_VISIBLE_DEVICES renumbering
+            import torch
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(cuda_index).uuid)
+            found = lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) == 0
+        except Exception:
+            found = False
+        if not found and lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(cuda_index), ctypes.byref(h)) != 0:
+            raise OSError("no NVML handle")
+        self.lib, self.h = lib, h
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        if self.sample() is None:
+            raise OSError("NVML queries failed")
+
+    def sample(self):
+        ct = self.ct
+        sm, mx, r = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if (self.lib.nvmlDeviceGetClockInfo(self.h, self.CLOCK_SM, ct.byref(sm)) != 0 or
+                self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.CLOCK_SM, ct.byref(mx)) != 0 or
+                self.reasons_fn(self.h, ct.byref(r)) != 0):
+            return None
+        return float(sm.value), float(mx.value), [n for bit, n in self.REASONS if r.value & bit]
+
+
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms in a thread."""
+    """SM clocks and throttle reasons sampled in a thread: every 2 ms through
+    NVML when the driver's library answers (so that even a timed region of a
+    few milliseconds holds samples), else every 200 ms from nvidia-smi."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NVML_PERIOD_S = 0.002
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.samples = []  # (t, sm, max_sm, reasons)
         self.proc = None
         self.thread = None
+        self.source = None
+        self._halt = threading.Event()
 
     def start(self):
+        try:
+            nvml = _Nvml(self.gpu)
+        except Exception:
+            nvml = None
+        if nvml is not None:
+            self.source = "NVML every 2 ms"
+            self.thread = threading.Thread(target=self._poll, args=(nvml,), daemon=True)
+            self.thread.start()
+            return
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
@@ -104,8 +160,16 @@ class ClockSampler:
         except OSError:
             self.proc = None
             return
+        self.source = "nvidia-smi every 200 ms"
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
+
+    def _poll(self, nvml):
+        while not self._halt.is_set():
+            s = nvml.sample()
+            if s is not None:
+                self.samples.append((time.time(),) + s)
+            time.sleep(self.NVML_PERIOD_S)
 
     def _read(self):
         for line in self.proc.stdout:
@@ -121,6 +185,7 @@ class ClockSampler:
             self.samples.append((time.time(), sm, mx, reasons))
 
     def stop(self):
+        self._halt.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -134,14 +199,14 @@ class ClockSampler:
         inside = [s for s in self.samples if t0 <= s[0] <= t1]
         where = "timed region"
         if not inside:
-            inside = self.samples
-            where = "whole run (timed region shorter than the 200 ms sampling period)"
+            inside = list(self.samples)
+            where = "whole run (timed region shorter than the sampling period)"
         if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
-                    "note": "nvidia-smi unavailable"}
+                    "note": "neither NVML nor nvidia-smi answered"}
         reasons = sorted({r for s in inside for r in s[3]})
         return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": max(s[2] for s in inside),
-                "reasons": reasons, "samples": len(inside), "window": where}
+                "reasons": reasons, "samples": len(inside), "window": where, "source": self.source}
 
 
 # --------------------------------------------------------------- workloads
