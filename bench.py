@@ -414,6 +414,20 @@ class Workload:
         detail = union * (d + (d // 32) * 2 + d * 2)
         return scan + detail + io
 
+    def algorithmic_flops(self):
+        """Floating-point operations the method performs per call: 4d per (query
+        head, attended token) for q.k and p.v, plus 2d per (query head, scanned
+        token) for the top-delta 2-bit scan."""
+        p = self.p
+        if self.topdelta is None:
+            return self.kv_tokens * p.Hq * 4 * p.d
+        st = self.sel_stats
+        if self.group_union:
+            attended = st["union_tokens"] * (p.Hq // p.Hkv)
+        else:
+            attended = st["selected_per_query"] * self.kv_tokens * p.Hq
+        return self.kv_tokens * p.Hq * 2 * p.d + attended * 4 * p.d
+
     def plan(self):
         """What this run's inputs and the library's planner made of the workload
         (known only once the inputs exist and the device is queried)."""
@@ -990,6 +1004,7 @@ def main():
     per_call_s = ms / 1e3 / args.steps
     value = n * B * args.steps / (ms / 1e3)
     algo = wl.algorithmic_bytes()
+    flops = wl.algorithmic_flops()
     achieved_gbs = algo / per_call_s / 1e9
     peak = measured_peaks()
     if peak is not None:
@@ -1045,6 +1060,8 @@ def main():
                          "frac": achieved_gbs / peak_gbs, "traffic": traffic, "peak_source": peak_src,
                          "kernel": "split partial pass + merge (whole call)",
                          "algorithmic_bytes_per_launch": algo},
+            "compute": {"algorithmic_flops_per_call": flops, "achieved_tflops": flops / per_call_s / 1e12,
+                        "flop_per_byte": flops / algo},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": args.steps * wl.launches_per_call(),

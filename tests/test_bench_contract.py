@@ -89,3 +89,18 @@ def test_reference_arm_other_ranks_print_nothing():
                   env={"RANK": "1", "WORLD_SIZE": "1", "LOCAL_RANK": "1"})
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+def test_algorithmic_flops():
+    # 4d per (query head, attended token); the top-delta scan adds 2d per (query head, scanned token)
+    from types import SimpleNamespace
+    sys.path.insert(0, ROOT)
+    import bench
+    p = SimpleNamespace(Hq=32, Hkv=8, d=128)
+    dense = SimpleNamespace(p=p, kv_tokens=1 << 20, topdelta=None)
+    assert bench.Workload.algorithmic_flops(dense) == (1 << 20) * 32 * 4 * 128
+    sel = {"selected_per_query": 0.25, "union_tokens": 3 * 1000}
+    td = SimpleNamespace(p=p, kv_tokens=4000, topdelta=5.0, sel_stats=sel, group_union=False)
+    assert bench.Workload.algorithmic_flops(td) == 4000 * 32 * 2 * 128 + 0.25 * 4000 * 32 * 4 * 128
+    tu = SimpleNamespace(p=p, kv_tokens=4000, topdelta=5.0, sel_stats=sel, group_union=True)
+    assert bench.Workload.algorithmic_flops(tu) == 4000 * 32 * 2 * 128 + 3000 * 4 * 4 * 128
