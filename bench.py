@@ -345,10 +345,20 @@ class Workload:
         pad = (-ubits.shape[-1]) % 64
         tiles = np.pad(ubits, ((0, 0), (0, 0), (0, pad))).reshape(B, p.Hkv, -1, 64).any(axis=-1)
         L = p.kv_tokens() / B
+        # the key quantization's share of that deviation: attention with the bf16 keys over the same
+        # candidate sets (KV head 0 and its query heads; plain fp32 torch, informational only)
+        bits_h = np.unpackbits(m[:, :G].view(np.uint8), bitorder="little").reshape(B, G, -1)[:, :, :p.L_max]
+        sel_h = torch.from_numpy(bits_h.astype(bool)).to(p.q.device)
+        s_h = torch.einsum("bgd,bld->bgl", p.q[:, :G].float(), p.k[:, 0].float()) * p.scale
+        s_h = s_h.masked_fill(~sel_h, -math.inf)
+        w_h = torch.softmax(s_h, dim=-1).nan_to_num(0.0)
+        o_h = torch.einsum("bgl,bld->bgd", w_h, p.v[:, 0].float())
+        dev_q = (out_s[:, :G].float() - o_h).abs().max().item()
         return {"selected_per_query": float(cnt.float().mean().item()) / L,
                 "attended": "group union" if self.group_union else "per query head",
                 "captured_mass_min": float(mass.min().item()), "captured_mass_mean": float(mass.mean().item()),
                 "max_abs_dev_vs_dense": dev,
+                "max_abs_dev_vs_bf16_keys_same_selection": dev_q,
                 "union_per_kv_head": float(ubits.sum()) / (B * p.Hkv * L),
                 "union_tokens": int(ubits.sum()), "tiles_loaded": int(tiles.sum()),
                 "tiles_total": int(tiles.size)}
