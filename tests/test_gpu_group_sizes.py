@@ -66,3 +66,19 @@ def test_topdelta_group_sizes(fd, oracle, G):
     for union in (False, True):
         enc, ref, out, lse, mask, cnt = run_both(fd, oracle, p, 5.0, group_union=union)
         check_topdelta(oracle, p, enc, ref, out, lse, mask, cnt, 5.0, BF16_TOL, group_union=union)
+
+
+@pytest.mark.parametrize("G", GROUPS)
+def test_paged_and_unified_group_sizes(fd, oracle, G):
+    # the paged pass (tail rows of the last pages poisoned with NaN) and the fixed-max variant
+    p = problem(G, 128, 80 + G)
+    ref, lref = oracle.decode_dense(bits(p.q), bits(p.k), bits(p.v), p.seq_lens.cpu(), p.scale)
+    pp = W.to_paged(p, seed=G)
+    out, lse = fd.fd_decode_paged(pp.q, pp.k_pages, pp.v_pages, pp.page_table, pp.num_pages, pp.seq_lens, pp.scale)
+    assert_out_close(out, ref, BF16_TOL, what="paged")
+    assert_lse_close(lse, lref)
+    for phi in (6.5, -100.0):
+        out, lse = fd.fd_decode_dense_unified(p.q, p.k, p.v, p.seq_lens, p.scale, phi)
+        assert_out_close(out, ref, BF16_TOL, what=f"unified phi={phi}")
+        assert_lse_close(lse, lref)
+    assert fd.fd_device_status(clear=True) == fd.FD_OK
